@@ -1,0 +1,147 @@
+"""fp64 CPU oracle for causal GQA attention with RoPE on Q/K.
+
+TEST INFRASTRUCTURE ONLY: the test-suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package; the product path
+(the CUDA library and its Python binding) never does, and this package never
+imports the product package.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, double precision, OpenMP
+over rows); this module only compiles it with gcc and marshals numpy arrays.
+See that file's header for the passages of the NanoEuler pages each step
+follows and for the readings taken where the pages are silent.
+
+Every function is pinned by ``tests/test_oracle_pins.py`` (brute force in a
+second formulation, closed forms, invariants and central finite differences);
+no function here is "parity unpinned".
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lib = None
+
+
+def build(force=False):
+    """Compile attn_oracle.c into _build/liboracle.so (gcc, -O2, OpenMP).
+
+    No -ffast-math and no -march flags: the oracle keeps IEEE double
+    semantics and builds the same way on x86-64 and AArch64 hosts.
+    """
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".%d.tmp" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.check_call(cmd)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        dp = ctypes.POINTER(ctypes.c_double)
+        u8p = ctypes.POINTER(ctypes.c_ubyte)
+        i = ctypes.c_int
+        lib.oracle_rope.argtypes = [dp, dp, i, i, i, i, ctypes.c_double, i]
+        lib.oracle_rope.restype = None
+        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i,
+                                        ctypes.c_double, u8p, i]
+        lib.oracle_attn_fwd.restype = None
+        lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, dp,
+                                        i, i, i, i, i, ctypes.c_double, u8p, i]
+        lib.oracle_attn_bwd.restype = None
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = i
+        _lib = lib
+    return _lib
+
+
+def _p(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _sel(B, Hkv, groups):
+    """groups: None (all) or an iterable of (b, kv_head) pairs to compute."""
+    if groups is None:
+        return None
+    s = np.zeros(B * Hkv, dtype=np.uint8)
+    for b, g in groups:
+        s[b * Hkv + g] = 1
+    return s
+
+
+def num_threads():
+    return _load().oracle_num_threads()
+
+
+def rope(x, base, inverse=False):
+    """R_t x for x of shape [B, T, H, D] (interleaved pairs); R_t^T x if inverse."""
+    lib = _load()
+    x = _f64(x)
+    B, T, H, D = x.shape
+    out = np.empty_like(x)
+    lib.oracle_rope(_p(x), _p(out), B, T, H, D, float(base), -1 if inverse else 1)
+    return out
+
+
+def attn_fwd(q, k, v, base=10000.0, groups=None, nthreads=0):
+    """Causal GQA attention forward.  q [B,T,Hq,D], k/v [B,T,Hkv,D] (fp64).
+
+    Returns (o [B,T,Hq,D], lse [B,Hq,T]); entries of groups not selected are NaN.
+    """
+    lib = _load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    assert k.shape == (B, T, Hkv, D) and v.shape == k.shape and Hq % Hkv == 0
+    o = np.full(q.shape, np.nan)
+    lse = np.full((B, Hq, T), np.nan)
+    sel = _sel(B, Hkv, groups)
+    lib.oracle_attn_fwd(_p(q), _p(k), _p(v), _p(o), _p(lse), B, T, Hq, Hkv, D,
+                        float(base),
+                        None if sel is None else sel.ctypes.data_as(
+                            ctypes.POINTER(ctypes.c_ubyte)), int(nthreads))
+    return o, lse
+
+
+def attn_bwd(q, k, v, dout, base=10000.0, groups=None, nthreads=0):
+    """Causal GQA attention backward from the definition.
+
+    Returns dict with dq, dk, dv and the forward by-products o, lse and
+    delta (= sum_j P_tj dP_tj, shape [B,Hq,T]).  Unselected groups are NaN.
+    """
+    lib = _load()
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    assert dout.shape == q.shape and Hq % Hkv == 0
+    dq = np.full(q.shape, np.nan)
+    dk = np.full(k.shape, np.nan)
+    dv = np.full(k.shape, np.nan)
+    o = np.full(q.shape, np.nan)
+    lse = np.full((B, Hq, T), np.nan)
+    delta = np.full((B, Hq, T), np.nan)
+    sel = _sel(B, Hkv, groups)
+    lib.oracle_attn_bwd(_p(q), _p(k), _p(v), _p(dout), _p(dq), _p(dk), _p(dv),
+                        _p(o), _p(lse), _p(delta), B, T, Hq, Hkv, D, float(base),
+                        None if sel is None else sel.ctypes.data_as(
+                            ctypes.POINTER(ctypes.c_ubyte)), int(nthreads))
+    return dict(dq=dq, dk=dk, dv=dv, o=o, lse=lse, delta=delta)
+

@@ -1,0 +1,169 @@
+"""ctypes binding for libneattn.so (C ABI in include/ne_attn.h).
+
+Argument marshalling only: every step of the attention runs in the CUDA
+library.  PyTorch supplies device memory and the current stream.  If the
+library has not been built, or its kernels cannot run on this device, the
+calls raise; there is no other implementation to fall back to.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libneattn.so")
+
+NE_OK = 0
+O_FP32 = 1       # flag bits, see include/ne_attn.h
+GRAD_FP32 = 2
+PRECISE_QK = 4
+_lib = None
+
+
+class NeAttnError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        msg = lib().ne_attn_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__("%s failed with status %d: %s" % (fn, status, msg))
+
+
+def lib():
+    """Loads the in-tree CUDA library (built by __graft_entry__.build())."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libneattn.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.ne_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+        L.ne_attn_fwd.restype = i
+        L.ne_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        L.ne_attn_fwd_ex.restype = i
+        L.ne_attn_bwd_workspace_size.argtypes = [i, i, i, i, i, i]
+        L.ne_attn_bwd_workspace_size.restype = sz
+        L.ne_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
+        L.ne_attn_bwd.restype = i
+        L.ne_attn_check_status.argtypes = [vp]
+        L.ne_attn_check_status.restype = i
+        L.ne_attn_status_string.argtypes = [i]
+        L.ne_attn_status_string.restype = ctypes.c_char_p
+        L.ne_attn_debug_timeout_probe.argtypes = [i, vp]
+        L.ne_attn_debug_timeout_probe.restype = i
+        _lib = L
+    return _lib
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, st):
+    if st != NE_OK:
+        raise NeAttnError(fn, st)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _shape(q, k):
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    return B, T, Hq, Hkv, D
+
+
+def attn_fwd(q, k, v, rope_base=10000.0, o=None, lse=None, o_dtype=torch.bfloat16, precise=False,
+             stream=None):
+    """o, lse = causal GQA attention of q [B,T,Hq,D], k/v [B,T,Hkv,D] (bf16, CUDA).
+
+    o_dtype: bfloat16 or float32.  precise: hi+lo split of the rotated q, k
+    for the logits (NE_ATTN_PRECISE_QK).
+    """
+    B, T, Hq, Hkv, D = _shape(q, k)
+    if o is None:
+        o = torch.empty(q.shape, dtype=o_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    for t in (q, k, v):
+        assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous()
+    assert o.dtype in (torch.bfloat16, torch.float32) and o.is_contiguous()
+    assert lse.dtype == torch.float32 and lse.is_contiguous()
+    flags = (O_FP32 if o.dtype == torch.float32 else 0) | (PRECISE_QK if precise else 0)
+    _check("ne_attn_fwd_ex", lib().ne_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                                  B, T, Hq, Hkv, D, float(rope_base), flags,
+                                                  _stream(stream)))
+    return o, lse
+
+
+def bwd_workspace_size(B, T, Hq, Hkv, D, precise=False):
+    return int(lib().ne_attn_bwd_workspace_size(B, T, Hq, Hkv, D, PRECISE_QK if precise else 0))
+
+
+def alloc_workspace(B, T, Hq, Hkv, D, precise=False, device="cuda"):
+    n = bwd_workspace_size(B, T, Hq, Hkv, D, precise)
+    if n == 0:
+        raise ValueError("unsupported shape")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def attn_bwd(q, k, v, o, lse, dout, rope_base=10000.0, grad_dtype=torch.bfloat16, precise=False,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dq, dk, dv of the causal GQA attention given the forward's o and lse.
+
+    o may be bfloat16 or float32; grad_dtype selects the gradient dtype.
+    """
+    B, T, Hq, Hkv, D = _shape(q, k)
+    if grad_dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("grad_dtype must be bfloat16 or float32")
+    if dq is None:
+        dq = torch.empty(q.shape, dtype=grad_dtype, device=q.device)
+    if dk is None:
+        dk = torch.empty(k.shape, dtype=grad_dtype, device=q.device)
+    if dv is None:
+        dv = torch.empty(k.shape, dtype=grad_dtype, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(B, T, Hq, Hkv, D, precise, q.device)
+    for t in (q, k, v, dout):
+        assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous()
+    assert o.dtype in (torch.bfloat16, torch.float32) and o.is_contiguous()
+    for t in (dq, dk, dv):
+        assert t.dtype == grad_dtype and t.is_contiguous()
+    flags = ((O_FP32 if o.dtype == torch.float32 else 0) | (GRAD_FP32 if grad_dtype == torch.float32 else 0)
+             | (PRECISE_QK if precise else 0))
+    _check("ne_attn_bwd", lib().ne_attn_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+        B, T, Hq, Hkv, D, float(rope_base), flags, _ptr(workspace), workspace.numel(), _stream(stream)))
+    return dq, dk, dv
+
+
+def check_status(stream=None):
+    """Synchronises the stream; raises if a kernel reported a device-side timeout."""
+    _check("ne_attn_check_status", lib().ne_attn_check_status(_stream(stream)))
+
+
+def status_of_last_kernels(stream=None):
+    """Like check_status but returns the raw status code (and clears it)."""
+    return int(lib().ne_attn_check_status(_stream(stream)))
+
+
+def debug_timeout_probe(limit_us, stream=None):
+    _check("ne_attn_debug_timeout_probe", lib().ne_attn_debug_timeout_probe(int(limit_us), _stream(stream)))
+
+
+def fwd_bwd_host(q, k, v, dout, rope_base=10000.0, grad_dtype=torch.bfloat16, o_dtype=torch.bfloat16,
+                 precise=False, device="cuda", stream=None):
+    """End-to-end call on host (CPU) bfloat16 tensors: copies in, forward +
+    backward, copies out.  Pinned host memory makes the copies asynchronous.
+    Returns host tensors (o, lse, dq, dk, dv).
+    """
+    s = torch.cuda.current_stream() if stream is None else stream
+    with torch.cuda.stream(s):
+        qd = q.to(device, non_blocking=True)
+        kd = k.to(device, non_blocking=True)
+        vd = v.to(device, non_blocking=True)
+        dod = dout.to(device, non_blocking=True)
+        o, lse = attn_fwd(qd, kd, vd, rope_base, o_dtype=o_dtype, precise=precise, stream=s)
+        dq, dk, dv = attn_bwd(qd, kd, vd, o, lse, dod, rope_base, grad_dtype, precise=precise, stream=s)
+        out = [t.to("cpu", non_blocking=False) for t in (o, lse, dq, dk, dv)]
+    return tuple(out)

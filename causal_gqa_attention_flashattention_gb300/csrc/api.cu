@@ -1,0 +1,426 @@
+// C-ABI layer of libneattn: argument checks, TMA descriptors, the rotary
+// cos/sin table cache, the device status word, and kernel launches.
+// The operations are defined in include/ne_attn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/ne_attn.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ne {
+
+// ------------------------------------------------------------------ device status word
+__device__ int g_status_word;
+
+// ------------------------------------------------------------------ small kernels
+// cos/sin of t * theta_i in double precision, rounded to fp32.
+__global__ void k_rope_table(float2* tab, int Tcap, int D, double log2_base) {
+  const int half = D / 2;
+  const long long n = (long long)Tcap * half;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(idx / half), i = (int)(idx % half);
+    const double theta = exp2(-2.0 * (double)i / (double)D * log2_base);
+    double s, c;
+    sincos((double)t * theta, &s, &c);
+    tab[idx] = make_float2((float)c, (float)s);
+  }
+}
+
+cudaError_t launch_rope_table(float2* tab, int Tcap, int D, double base, cudaStream_t s) {
+  const long long n = (long long)Tcap * (D / 2);
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 4096) blocks = 4096;
+  k_rope_table<<<blocks, 256, 0, s>>>(tab, Tcap, D, std::log2(base));
+  return cudaGetLastError();
+}
+
+__global__ void k_timeout_probe(int* status, long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Nothing arrives on `bar`: the wait must give up after limit_ns.
+    if (!mbar_wait(&bar, 0, &abort_flag, (unsigned long long)limit_ns)) atomicCAS(status, 0, kStatusTimeout);
+  }
+}
+
+cudaError_t launch_timeout_probe(int* status, long long limit_ns, cudaStream_t s) {
+  k_timeout_probe<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ per-device state
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+struct RopeTable {
+  int D;
+  double base;
+  int Tcap;
+  float2* ptr;
+};
+
+struct DeviceState {
+  bool init = false;
+  bool supported = false;
+  int* status = nullptr;
+  std::vector<RopeTable> tables;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[64];
+EncodeTiledFn g_encode = nullptr;
+
+int current_device(int* dev) { return cudaGetDevice(dev) == cudaSuccess ? NE_OK : NE_ERR_CUDA; }
+
+// Requires g_mu held.
+int device_state(int dev, DeviceState** out) {
+  if (dev < 0 || dev >= 64) return NE_ERR_UNSUPPORTED;
+  DeviceState& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return NE_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    if (d.supported) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return NE_ERR_CUDA;
+      d.status = static_cast<int*>(p);
+    }
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return NE_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.init = true;
+  }
+  if (!d.supported) return NE_ERR_UNSUPPORTED;
+  *out = &d;
+  return NE_OK;
+}
+
+// Returns a table with at least Tneed rows for (D, base) on this device.
+// Requires g_mu held.
+int rope_table(DeviceState& d, int D, double base, int Tneed, cudaStream_t s, const float2** out) {
+  for (auto& t : d.tables)
+    if (t.D == D && t.base == base && t.Tcap >= Tneed) {
+      *out = t.ptr;
+      return NE_OK;
+    }
+  int Tcap = ((Tneed + 1023) / 1024) * 1024;
+  float2* p = nullptr;
+  if (cudaMalloc(&p, sizeof(float2) * (size_t)Tcap * (D / 2)) != cudaSuccess) return NE_ERR_CUDA;
+  if (launch_rope_table(p, Tcap, D, base, s) != cudaSuccess) {
+    cudaFree(p);
+    return NE_ERR_CUDA;
+  }
+  // Older, smaller tables stay allocated: kernels queued on other streams may still read them.
+  d.tables.push_back(RopeTable{D, base, Tcap, p});
+  *out = p;
+  return NE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 4-D map over a [B, T, H, D] bf16 tensor; box = one head, 128 rows, all D.
+int make_map_bthd(CUtensorMap* m, const void* ptr, int B, int T, int H, int D,
+                  CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)T * H * D * 2};
+  cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)kTile, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, dt, 4, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        D == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
+}
+
+// 2-D map over the fp32 dQ accumulator [rows, D]; box = 32 columns x 128 rows.
+int make_map_acc(CUtensorMap* m, void* ptr, long long rows, int D) {
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+  cuuint32_t box[2] = {32, (cuuint32_t)kTile};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
+}
+
+int check_shape(int B, int T, int Hq, int Hkv, int D) {
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return NE_ERR_ARG;
+  if (D != 32 && D != 64) return NE_ERR_UNSUPPORTED;
+  const long long Tp = ((long long)T + kTile - 1) / kTile * kTile;
+  const long long maxH = Hq > Hkv ? Hq : Hkv;
+  if ((long long)B * Tp * maxH * D >= (1LL << 31)) return NE_ERR_UNSUPPORTED;
+  const long long ntiles = Tp / kTile;
+  if (ntiles * B * Hq >= (1LL << 31) - 1) return NE_ERR_UNSUPPORTED;
+  return NE_OK;
+}
+
+int heads_per_cta(int G, int D, bool precise) {
+  for (int hc = fwd_max_heads(D, precise); hc >= 1; hc--)
+    if (G % hc == 0) return hc;
+  return 1;
+}
+
+struct WsLayout {
+  size_t qr, kr, qlo, klo, lse2, delta, dqacc, total;
+};
+
+WsLayout ws_layout(int B, int T, int Hq, int Hkv, int D, bool precise) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t Tp = (size_t)(T + kTile - 1) / kTile * kTile;
+  WsLayout w;
+  size_t off = 0;
+  w.dqacc = off;
+  off += up(sizeof(float) * (size_t)B * Hq * Tp * D);
+  w.qr = off;
+  off += up(2 * (size_t)B * T * Hq * D);
+  w.kr = off;
+  off += up(2 * (size_t)B * T * Hkv * D);
+  w.qlo = w.klo = 0;
+  if (precise) {
+    w.qlo = off;
+    off += up(2 * (size_t)B * T * Hq * D);
+    w.klo = off;
+    off += up(2 * (size_t)B * T * Hkv * D);
+  }
+  w.lse2 = off;
+  off += up(sizeof(float) * (size_t)B * Hq * Tp);
+  w.delta = off;
+  off += up(sizeof(float) * (size_t)B * Hq * Tp);
+  w.total = off;
+  return w;
+}
+
+constexpr int kKnownFlags = kFlagOFp32 | kFlagGradFp32 | kFlagPreciseQK;
+
+}  // namespace
+}  // namespace ne
+
+using namespace ne;
+
+extern "C" {
+
+int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int Hq,
+                   int Hkv, int D, float rope_base, int flags, void* stream) {
+  if (!q || !k || !v || !o || !lse) return NE_ERR_ARG;
+  if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
+  if ((flags & ~(kFlagOFp32 | kFlagPreciseQK)) != 0) return NE_ERR_ARG;
+  int st = check_shape(B, T, Hq, Hkv, D);
+  if (st != NE_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return NE_ERR_ALIGN;
+  const bool precise = (flags & kFlagPreciseQK) != 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev;
+  if ((st = current_device(&dev)) != NE_OK) return st;
+  DeviceState* d;
+  if ((st = device_state(dev, &d)) != NE_OK) return st;
+  FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.nt = (T + kTile - 1) / kTile;
+  if ((st = rope_table(*d, D, (double)rope_base, a.nt * kTile, s, &a.rope)) != NE_OK) return st;
+  if ((st = make_map_bthd(&a.map_q, q, B, T, Hq, D)) != NE_OK) return st;
+  if ((st = make_map_bthd(&a.map_k, k, B, T, Hkv, D)) != NE_OK) return st;
+  if ((st = make_map_bthd(&a.map_v, v, B, T, Hkv, D)) != NE_OK) return st;
+  a.o = o;
+  a.lse = lse;
+  a.status = d->status;
+  a.B = B;
+  a.T = T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.G = Hq / Hkv;
+  a.HC = heads_per_cta(a.G, D, precise);
+  a.o_fp32 = (flags & kFlagOFp32) ? 1 : 0;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  return launch_fwd(a, precise, s) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+int ne_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int Hq, int Hkv,
+                int D, float rope_base, void* stream) {
+  return ne_attn_fwd_ex(q, k, v, o, lse, B, T, Hq, Hkv, D, rope_base, 0, stream);
+}
+
+size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D, int flags) {
+  if (check_shape(B, T, Hq, Hkv, D) != NE_OK || (flags & ~kKnownFlags) != 0) return 0;
+  return ws_layout(B, T, Hq, Hkv, D, (flags & kFlagPreciseQK) != 0).total;
+}
+
+int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D, float rope_base, int flags,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return NE_ERR_ARG;
+  if ((flags & ~kKnownFlags) != 0) return NE_ERR_ARG;
+  if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
+  int st = check_shape(B, T, Hq, Hkv, D);
+  if (st != NE_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return NE_ERR_ALIGN;
+  const bool precise = (flags & kFlagPreciseQK) != 0;
+  const int grad_fp32 = (flags & kFlagGradFp32) ? 1 : 0;
+  const WsLayout w = ws_layout(B, T, Hq, Hkv, D, precise);
+  if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return NE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev;
+  if ((st = current_device(&dev)) != NE_OK) return st;
+  DeviceState* d;
+  if ((st = device_state(dev, &d)) != NE_OK) return st;
+  const int nt = (T + kTile - 1) / kTile;
+  const int Tp = nt * kTile;
+  const float2* rope = nullptr;
+  if ((st = rope_table(*d, D, (double)rope_base, Tp, s, &rope)) != NE_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* dqacc = reinterpret_cast<float*>(ws + w.dqacc);
+  __half* qr = reinterpret_cast<__half*>(ws + w.qr);
+  __half* kr = reinterpret_cast<__half*>(ws + w.kr);
+  __half* qlo = precise ? reinterpret_cast<__half*>(ws + w.qlo) : nullptr;
+  __half* klo = precise ? reinterpret_cast<__half*>(ws + w.klo) : nullptr;
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  float* delta = reinterpret_cast<float*>(ws + w.delta);
+  const double scale = 1.0 / std::sqrt((double)D);
+
+  PrepArgs p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.o = o;
+  p.o_fp32 = (flags & kFlagOFp32) ? 1 : 0;
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.lse = lse;
+  p.qr = qr;
+  p.kr = kr;
+  p.qlo = qlo;
+  p.klo = klo;
+  p.lse2 = lse2;
+  p.delta = delta;
+  p.dqacc = dqacc;
+  p.rope = rope;
+  p.B = B;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.Tp = Tp;
+  if (launch_bwd_prep(p, s) != cudaSuccess) return NE_ERR_CUDA;
+
+  BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  constexpr CUtensorMapDataType kF16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if ((st = make_map_bthd(&a.map_qr, qr, B, T, Hq, D, kF16)) != NE_OK) return st;
+  if ((st = make_map_bthd(&a.map_kr, kr, B, T, Hkv, D, kF16)) != NE_OK) return st;
+  if ((st = make_map_bthd(&a.map_v, v, B, T, Hkv, D)) != NE_OK) return st;
+  if ((st = make_map_bthd(&a.map_do, dout, B, T, Hq, D)) != NE_OK) return st;
+  if (precise) {
+    if ((st = make_map_bthd(&a.map_qlo, qlo, B, T, Hq, D, kF16)) != NE_OK) return st;
+    if ((st = make_map_bthd(&a.map_klo, klo, B, T, Hkv, D, kF16)) != NE_OK) return st;
+  }
+  if ((st = make_map_acc(&a.map_dqacc, dqacc, (long long)B * Hq * Tp, D)) != NE_OK) return st;
+  a.lse2 = lse2;
+  a.delta = delta;
+  a.dk = dk;
+  a.dv = dv;
+  a.rope = rope;
+  a.status = d->status;
+  a.B = B;
+  a.T = T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.G = Hq / Hkv;
+  a.nt = nt;
+  a.Tp = Tp;
+  a.grad_fp32 = grad_fp32;
+  a.scale_log2 = (float)(1.4426950408889634 * scale);
+  a.scale = (float)scale;
+  if (launch_bwd_dkdv(a, precise, s) != cudaSuccess) return NE_ERR_CUDA;
+
+  DqArgs qa;
+  qa.dqacc = dqacc;
+  qa.dq = dq;
+  qa.rope = rope;
+  qa.B = B;
+  qa.T = T;
+  qa.Hq = Hq;
+  qa.D = D;
+  qa.Tp = Tp;
+  qa.grad_fp32 = grad_fp32;
+  qa.scale = (float)scale;
+  if (launch_bwd_dq(qa, s) != cudaSuccess) return NE_ERR_CUDA;
+  return NE_OK;
+}
+
+int ne_attn_check_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return NE_ERR_CUDA;
+  int dev;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NE_ERR_CUDA;
+  DeviceState* d;
+  int st;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if ((st = device_state(dev, &d)) != NE_OK) return st;
+  }
+  int word = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(int)) != cudaSuccess) return NE_ERR_CUDA;
+  if (word != 0 && cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return NE_ERR_CUDA;
+  return word == 0 ? NE_OK : word;
+}
+
+const char* ne_attn_status_string(int status) {
+  switch (status) {
+    case NE_OK: return "ok";
+    case NE_ERR_ARG: return "invalid argument (null pointer, bad size, Hq % Hkv != 0, rope_base or flags)";
+    case NE_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
+    case NE_ERR_UNSUPPORTED: return "unsupported (D not in {32, 64}, size limit, or device is not sm_103)";
+    case NE_ERR_CUDA: return "CUDA runtime or launch error";
+    case NE_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+    case NE_ERR_DEVICE_TIMEOUT: return "a kernel pipeline wait timed out on the device";
+    default: return "unknown status";
+  }
+}
+
+int ne_attn_debug_timeout_probe(int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return NE_ERR_ARG;
+  int dev, st;
+  if ((st = current_device(&dev)) != NE_OK) return st;
+  DeviceState* d;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if ((st = device_state(dev, &d)) != NE_OK) return st;
+  }
+  return launch_timeout_probe(d->status, (long long)limit_us * 1000, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? NE_OK
+             : NE_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,638 @@
+// Backward pass of causal GQA attention with RoPE on Q/K (sm_103a).
+//
+// The NanoEuler pages hand-write the backward of every kernel and check it
+// against central finite differences in double precision, RoPE and GQA
+// included (socker-news README, "Verified backward"; openai-hub article on
+// the hand-written forward/backward).  With P = softmax(S), S = scale Q^ K^T:
+//   dV = P^T dO,  dP = dO V^T,  Delta_t = sum_j P_tj dP_tj = dO_t . O_t,
+//   dS = P o (dP - Delta),  dQ^ = scale dS K^,  dK^ = scale dS^T Q^,
+//   dq = R^T dQ^, dk = R^T dK^ (summed over the query heads of the group).
+//
+// Three kernels:
+//   k_bwd_prep  (HBM-bound, one pass): Delta = rowsum(dO o O), lse*log2(e),
+//               rotated copies q^, k^ (fp16; with precise logits also their
+//               fp16 remainders), zeroed fp32 dQ accumulator.
+//   k_bwd_dkdv  CTA = (key tile j, batch b, kv head g); sweeps query tiles
+//               i >= j and the G query heads of the group:
+//     warp 0    TMA producer (K^_j, V_j once; then Q^_i, dO_i, lse, Delta)
+//     warp 1    tcgen05 issuer: S^T = K^ Q^T, dP^T = V dO^T, dV += P^T dO,
+//               dK += dS^T Q^, dQ_tile = dS K^ (TMEM accumulators)
+//     warps 4-7 one thread per key row: P^T = exp2(S^T scale log2e - lse2),
+//               causal mask on the diagonal tile, dS^T = P^T o (dP^T - Delta)
+//               (fp16, to shared memory in the layout both MMAs read)
+//     warps 8-11 drain dQ_tile from TMEM into swizzled shared memory and add
+//               it to the fp32 accumulator with a TMA tensor reduce-add.
+//     dK and dV accumulate in TMEM across all (i, head) steps, so the GQA
+//     group reduction happens inside the kernel; the epilogue applies scale
+//     and the inverse rotation to dK.
+//   k_bwd_dq    dq = scale R^T dQacc (bf16 or fp32).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "rope.cuh"
+
+namespace ne {
+namespace {
+
+__device__ __forceinline__ void record_timeout(int* status, volatile int* abort) {
+  *abort = 1;
+  atomicCAS(status, 0, kStatusTimeout);
+}
+
+// ====================================================================== pre-pass
+template <int D>
+__global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
+  constexpr int kCPR = D / 8;  // 16-byte chunks (8 bf16) per row
+  const long long gtid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long nthr = (long long)gridDim.x * blockDim.x;  // a multiple of 32
+  const int lane = threadIdx.x & 31;
+
+  // (A) query rows: rotate q, Delta = dO . O, lse2 = lse * log2(e)
+  const long long nA = (long long)a.B * a.T * a.Hq * kCPR;
+  const long long nA32 = (nA + 31) / 32 * 32;
+  for (long long it = gtid; it < nA32; it += nthr) {
+    const bool valid = it < nA;
+    float part = 0.f;
+    long long row = 0;
+    int c = 0;
+    if (valid) {
+      row = it / kCPR;
+      c = (int)(it % kCPR);
+      const int t = (int)((row / a.Hq) % a.T);
+      const uint4 qv = __ldg(reinterpret_cast<const uint4*>(a.q) + it);
+      float4 c0, c1;
+      rope_coeffs<D>(a.rope, t, c, c0, c1);
+      if (a.qlo) {
+        uint4 l;
+        reinterpret_cast<uint4*>(a.qr)[it] = rope_chunk_f16(qv, c0, c1, &l);
+        reinterpret_cast<uint4*>(a.qlo)[it] = l;
+      } else {
+        reinterpret_cast<uint4*>(a.qr)[it] = rope_chunk_f16(qv, c0, c1, nullptr);
+      }
+      const uint4 dv = __ldg(reinterpret_cast<const uint4*>(a.dout) + it);
+      const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+      if (a.o_fp32) {
+        const float4* op = reinterpret_cast<const float4*>(a.o) + 2 * it;
+        const float4 o0 = __ldg(op), o1 = __ldg(op + 1);
+        part = o0.x * bf_lo(dw[0]) + o0.y * bf_hi(dw[0]) + o0.z * bf_lo(dw[1]) + o0.w * bf_hi(dw[1]) +
+               o1.x * bf_lo(dw[2]) + o1.y * bf_hi(dw[2]) + o1.z * bf_lo(dw[3]) + o1.w * bf_hi(dw[3]);
+      } else {
+        const uint4 ov = __ldg(reinterpret_cast<const uint4*>(a.o) + it);
+        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+        for (int p = 0; p < 4; p++) part += bf_lo(ow[p]) * bf_lo(dw[p]) + bf_hi(ow[p]) * bf_hi(dw[p]);
+      }
+    }
+#pragma unroll
+    for (int off = kCPR / 2; off >= 1; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    if (valid && c == 0) {
+      const int h = (int)(row % a.Hq);
+      const long long bt = row / a.Hq;
+      const int t = (int)(bt % a.T), b = (int)(bt / a.T);
+      const size_t o = ((size_t)b * a.Hq + h) * a.Tp + t;
+      a.delta[o] = part;
+      a.lse2[o] = a.lse[((size_t)b * a.Hq + h) * a.T + t] * 1.4426950408889634f;
+    }
+  }
+  (void)lane;
+  // (B) key rows: rotate k
+  const long long nB = (long long)a.B * a.T * a.Hkv * kCPR;
+  for (long long it = gtid; it < nB; it += nthr) {
+    const long long row = it / kCPR;
+    const int c = (int)(it % kCPR);
+    const int t = (int)((row / a.Hkv) % a.T);
+    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(a.k) + it);
+    float4 c0, c1;
+    rope_coeffs<D>(a.rope, t, c, c0, c1);
+    if (a.klo) {
+      uint4 l;
+      reinterpret_cast<uint4*>(a.kr)[it] = rope_chunk_f16(kv, c0, c1, &l);
+      reinterpret_cast<uint4*>(a.klo)[it] = l;
+    } else {
+      reinterpret_cast<uint4*>(a.kr)[it] = rope_chunk_f16(kv, c0, c1, nullptr);
+    }
+  }
+  // (C) zero the dQ accumulator [B, Hq, Tp, D]
+  const long long nC = (long long)a.B * a.Hq * a.Tp * D / 4;
+  for (long long it = gtid; it < nC; it += nthr) reinterpret_cast<float4*>(a.dqacc)[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // (D) padded rows t in [T, Tp): no probability mass (lse2 = +inf), Delta = 0
+  const int npad = a.Tp - a.T;
+  const long long nD = (long long)a.B * a.Hq * npad;
+  for (long long it = gtid; it < nD; it += nthr) {
+    const long long bh = it / npad;
+    const int t = a.T + (int)(it % npad);
+    a.delta[bh * a.Tp + t] = 0.f;
+    a.lse2[bh * a.Tp + t] = __int_as_float(0x7f800000);
+  }
+}
+
+// ====================================================================== dq epilogue
+template <int D>
+__global__ void __launch_bounds__(256) k_bwd_dq(const DqArgs a) {
+  constexpr int kCPR = D / 8;
+  const long long n = (long long)a.B * a.T * a.Hq * kCPR;
+  for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < n;
+       it += (long long)gridDim.x * blockDim.x) {
+    const long long row = it / kCPR;  // (b, t, h)
+    const int c = (int)(it % kCPR);
+    const int h = (int)(row % a.Hq);
+    const long long bt = row / a.Hq;
+    const int t = (int)(bt % a.T), b = (int)(bt / a.T);
+    const float4* src = reinterpret_cast<const float4*>(a.dqacc + (((size_t)b * a.Hq + h) * a.Tp + t) * D + c * 8);
+    const float4 x0 = src[0], x1 = src[1];
+    float4 c0, c1;
+    rope_coeffs<D>(a.rope, t, c, c0, c1);
+    const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    const float cs[4] = {c0.x, c0.z, c1.x, c1.z}, sn[4] = {c0.y, c0.w, c1.y, c1.w};
+    float y[8];
+#pragma unroll
+    for (int p = 0; p < 4; p++) {
+      y[2 * p] = a.scale * (xs[2 * p] * cs[p] + xs[2 * p + 1] * sn[p]);
+      y[2 * p + 1] = a.scale * (xs[2 * p + 1] * cs[p] - xs[2 * p] * sn[p]);
+    }
+    if (a.grad_fp32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.dq) + it * 8);
+      dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+      dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+    } else {
+      reinterpret_cast<uint4*>(a.dq)[it] =
+          make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+    }
+  }
+}
+
+// ====================================================================== dK/dV sweep
+template <int D, bool PRECISE>
+struct BwdCfg {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr uint32_t kSpan = D * 2;
+  static constexpr uint32_t kSwz = D == 64 ? kSw128 : kSw64;
+  static constexpr uint32_t kSBO = 8 * kSpan;
+  static constexpr int kStages = 2;
+  static constexpr int kLo = PRECISE ? 1 : 0;
+  static constexpr int kDsBufs = (PRECISE && D == 64) ? 1 : 2;  // shared-memory budget
+  static constexpr int kVecBytes = kTile * 4;  // lse2 / Delta slice of one tile
+  static constexpr int kDsBytes = kTile * kTile * 2;
+  static constexpr int kStgBytes = kTile * D * 4;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffKlo = kOffK + kTileBytes;
+  static constexpr int kOffV = kOffKlo + kLo * kTileBytes;
+  static constexpr int kOffQ = kOffV + kTileBytes;
+  static constexpr int kOffQlo = kOffQ + kStages * kTileBytes;
+  static constexpr int kOffDO = kOffQlo + kLo * kStages * kTileBytes;
+  static constexpr int kOffDS = kOffDO + kStages * kTileBytes;
+  static constexpr int kOffStg = kOffDS + kDsBufs * kDsBytes;
+  static constexpr int kOffLse = kOffStg + kStgBytes;
+  static constexpr int kOffDel = kOffLse + kStages * kVecBytes;
+  static constexpr int kOffBar = kOffDel + kStages * kVecBytes;
+  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2 * 2 + 2 * 2 + 2;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  // tensor memory columns
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D, kColDQ = 256 + 2 * D;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Named barrier that also returns the AND of `v` over the participating threads.
+__device__ __forceinline__ bool named_sync_and(int id, int nthreads, bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+      : "memory");
+  return out != 0;
+}
+
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, const void* src, int c0, int c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(c0), "r"(c1), "r"(smem_u32(src))
+      : "memory");
+}
+
+template <int D, bool PRECISE>
+__global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ BwdArgs a) {
+  using C = BwdCfg<D, PRECISE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* kv_full = bars;
+  uint64_t* qd_full = kv_full + 1;             // [kStages]
+  uint64_t* qd_empty = qd_full + C::kStages;   // [kStages]
+  uint64_t* s_full = qd_empty + C::kStages;
+  uint64_t* p_ready = s_full + 1;
+  uint64_t* dp_full = p_ready + 1;
+  uint64_t* acc_done = dp_full + 1;
+  uint64_t* ds_ready = acc_done + 1;  // [2]
+  uint64_t* ds_free = ds_ready + 2;   // [2]
+  uint64_t* dq_full = ds_free + 2;    // [2]
+  uint64_t* dq_free = dq_full + 2;    // [2]
+  uint64_t* drain = dq_free + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int per_j = a.B * a.Hkv;
+  const int j = (int)blockIdx.x / per_j;  // smallest j (longest sweep) first
+  const int rem = (int)blockIdx.x % per_j;
+  const int kvh = rem % a.Hkv, b = rem / a.Hkv;
+  const int G = a.G;
+  const int N = (a.nt - j) * G;  // (query tile, head) steps
+
+  if (tid == 0) {
+    *abort = 0;
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < C::kStages; s++) {
+      mbar_init(qd_full + s, 1);
+      mbar_init(qd_empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_ready, 128);
+    mbar_init(dp_full, 1);
+    mbar_init(acc_done, 1);
+    for (int s = 0; s < 2; s++) {
+      mbar_init(ds_ready + s, 128);
+      mbar_init(ds_free + s, 1);
+      mbar_init(dq_full + s, 1);
+      mbar_init(dq_free + s, 128);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const volatile int never = 0;
+  const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
+  const uint32_t sKlo = smem_u32(smem + C::kOffKlo), sQlo = smem_u32(smem + C::kOffQlo);
+  const uint32_t sQ = smem_u32(smem + C::kOffQ), sDO = smem_u32(smem + C::kOffDO);
+  const uint32_t sDS = smem_u32(smem + C::kOffDS);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&a.map_qr);
+      prefetch_tmap(&a.map_do);
+      mbar_arrive_expect_tx(kv_full, (2 + C::kLo) * C::kTileBytes);
+      tma_load_4d(smem + C::kOffK, &a.map_kr, kv_full, 0, kvh, j * kTile, b);
+      if (PRECISE) tma_load_4d(smem + C::kOffKlo, &a.map_klo, kv_full, 0, kvh, j * kTile, b);
+      tma_load_4d(smem + C::kOffV, &a.map_v, kv_full, 0, kvh, j * kTile, b);
+      int loaded = 0;
+      for (int n = 0; n < N; n++) {
+        const int st = n % C::kStages, use = n / C::kStages;
+        if (use > 0 && !mbar_wait(qd_empty + st, (use - 1) & 1, abort)) {
+          record_timeout(a.status, abort);
+          break;
+        }
+        const int i = j + n / G, h = kvh * G + n % G;
+        const size_t vec = ((size_t)b * a.Hq + h) * a.Tp + (size_t)i * kTile;
+        mbar_arrive_expect_tx(qd_full + st, (2 + C::kLo) * C::kTileBytes + 2 * C::kVecBytes);
+        tma_load_4d(smem + C::kOffQ + st * C::kTileBytes, &a.map_qr, qd_full + st, 0, h, i * kTile, b);
+        if (PRECISE)
+          tma_load_4d(smem + C::kOffQlo + st * C::kTileBytes, &a.map_qlo, qd_full + st, 0, h, i * kTile, b);
+        tma_load_4d(smem + C::kOffDO + st * C::kTileBytes, &a.map_do, qd_full + st, 0, h, i * kTile, b);
+        bulk_load(smem + C::kOffLse + st * C::kVecBytes, a.lse2 + vec, C::kVecBytes, qd_full + st);
+        bulk_load(smem + C::kOffDel + st * C::kVecBytes, a.delta + vec, C::kVecBytes, qd_full + st);
+        loaded = n + 1;
+      }
+      mbar_wait(kv_full, 0, &never);
+      for (int n = loaded - C::kStages < 0 ? 0 : loaded - C::kStages; n < loaded; n++)
+        mbar_wait(qd_full + n % C::kStages, (n / C::kStages) & 1, &never);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_fp16(128, 128, false, false);   // K^ Q^T (fp16)
+      constexpr uint32_t idDP = idesc_bf16(128, 128, false, false);  // V dO^T (bf16)
+      constexpr uint32_t idDV = idesc_bf16(128, D, false, true);     // P^T (TMEM) x dO MN-major
+      constexpr uint32_t idDK = idesc_fp16(128, D, false, true);     // dS^T x Q^ MN-major
+      constexpr uint32_t idDQ = idesc_fp16(128, D, true, true);      // dS (MN-major) x K^ MN-major
+      auto issue_kmajor = [&](uint32_t col, uint32_t sa, uint32_t sb, uint32_t id, uint32_t acc) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ks++)
+          mma_ss(tmem + col, smem_desc(sa + ks * 32, 16, C::kSBO, C::kSwz),
+                 smem_desc(sb + ks * 32, 16, C::kSBO, C::kSwz), id, (acc || ks > 0) ? 1u : 0u);
+      };
+      // S^T = Khi Qhi^T (+ Klo Qhi^T + Khi Qlo^T)
+      auto issue_s = [&](int stq) {
+        issue_kmajor(C::kColS, sK, sQ + stq * C::kTileBytes, idS, 0);
+        if (PRECISE) {
+          issue_kmajor(C::kColS, sKlo, sQ + stq * C::kTileBytes, idS, 1);
+          issue_kmajor(C::kColS, sK, sQlo + stq * C::kTileBytes, idS, 1);
+        }
+      };
+      bool ok = mbar_wait(kv_full, 0, abort) && mbar_wait(qd_full, 0, abort);
+      tc_fence_after();
+      if (ok) {
+        issue_s(0);
+        mma_commit(s_full);
+        issue_kmajor(C::kColDP, sV, sDO, idDP, 0);
+        mma_commit(dp_full);
+      }
+      for (int n = 0; ok && n < N; n++) {
+        const int st = n % C::kStages;
+        const uint32_t q_s = sQ + st * C::kTileBytes, do_s = sDO + st * C::kTileBytes;
+        // dV += P^T dO   (A = P^T in TMEM, B = dO MN-major)
+        if (!(ok = mbar_wait(p_ready, n & 1, abort))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ks++)
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + ks * 8,
+                 smem_desc(do_s + ks * 16 * C::kSpan, 16, C::kSBO, C::kSwz), idDV, (n > 0 || ks > 0) ? 1u : 0u);
+        // next S^T (its TMEM region was just read by the dV MMAs issued above)
+        const int st1 = (n + 1) % C::kStages;
+        if (n + 1 < N) {
+          if (!(ok = mbar_wait(qd_full + st1, ((n + 1) / C::kStages) & 1, abort))) break;
+          tc_fence_after();
+          issue_s(st1);
+          mma_commit(s_full);
+        }
+        // dK += dS^T Q^  and  dQ_tile = dS K^
+        const int dsb = n % C::kDsBufs, qb = n & 1;
+        const uint32_t ds = sDS + dsb * C::kDsBytes;
+        if (!(ok = mbar_wait(ds_ready + dsb, (n / C::kDsBufs) & 1, abort))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ks++)
+          mma_ss(tmem + C::kColDK, smem_desc(ds + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024, kSw128),
+                 smem_desc(q_s + ks * 16 * C::kSpan, 16, C::kSBO, C::kSwz), idDK, (n > 0 || ks > 0) ? 1u : 0u);
+        if (n >= 2) {
+          if (!(ok = mbar_wait(dq_free + qb, ((n - 2) >> 1) & 1, abort))) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ks++)
+          mma_ss(tmem + C::kColDQ + qb * D, smem_desc(ds + ks * 2048, 16384, 1024, kSw128),
+                 smem_desc(sK + ks * 16 * C::kSpan, 16, C::kSBO, C::kSwz), idDQ, ks > 0 ? 1u : 0u);
+        mma_commit(dq_full + qb);
+        mma_commit(ds_free + dsb);
+        mma_commit(qd_empty + st);
+        // next dP^T (the compute warps finished reading dP^T before signalling ds_ready)
+        if (n + 1 < N) {
+          issue_kmajor(C::kColDP, sV, sDO + st1 * C::kTileBytes, idDP, 0);
+          mma_commit(dp_full);
+        }
+      }
+      if (!ok) record_timeout(a.status, abort);
+      mma_commit(acc_done);
+      mma_commit(drain);
+      mbar_wait(drain, 0, &never);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ P and dS (one key row per thread)
+    const int r = tid - 128;
+    const uint32_t trow = tmem + ((uint32_t)(warp - 4) * 32u << 16);
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    for (int n = 0; n < N; n++) {
+      const int st = n % C::kStages;
+      const int i = j + n / G;
+      const bool diag = (i == j);
+      const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffLse + st * C::kVecBytes);
+      const float* del = reinterpret_cast<const float*>(smem + C::kOffDel + st * C::kVecBytes);
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full, n & 1, abort)))) break;
+      tc_fence_after();
+      uint32_t pk[kTile / 2];  // P^T row as packed bf16 pairs
+#pragma unroll
+      for (int c = 0; c < kTile / 32; c++) {
+        uint32_t u[32];
+        tmem_ld32(trow + C::kColS + c * 32, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; e++) {
+          const int q0 = c * 32 + 2 * e;
+          float p0 = ex2(fmaf(__uint_as_float(u[2 * e]), sl2, -lse2[q0]));
+          float p1 = ex2(fmaf(__uint_as_float(u[2 * e + 1]), sl2, -lse2[q0 + 1]));
+          if (diag) {
+            if (q0 < r) p0 = 0.f;
+            if (q0 + 1 < r) p1 = 0.f;
+          }
+          pk[c * 16 + e] = pack_bf16(p0, p1);
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; e++) w[e] = pk[c * 16 + e];
+        tmem_st16(trow + C::kColS + c * 16, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+
+      const int dsb = n % C::kDsBufs;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(dp_full, n & 1, abort)))) break;
+      if (n >= C::kDsBufs &&
+          !(ok = __all_sync(0xffffffffu, mbar_wait(ds_free + dsb, ((n - C::kDsBufs) / C::kDsBufs) & 1, abort))))
+        break;
+      tc_fence_after();
+      uint8_t* ds = smem + C::kOffDS + dsb * C::kDsBytes;
+#pragma unroll
+      for (int c = 0; c < kTile / 32; c++) {
+        uint32_t u[32];
+        tmem_ld32(trow + C::kColDP + c * 32, u);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; e++) {
+          const int q0 = c * 32 + 2 * e;
+          const float d0 = (__uint_as_float(u[2 * e]) - del[q0]) * bf_lo(pk[c * 16 + e]);
+          const float d1 = (__uint_as_float(u[2 * e + 1]) - del[q0 + 1]) * bf_hi(pk[c * 16 + e]);
+          w[e] = pack_f16(d0, d1);
+        }
+        // queries c*32 .. c*32+31 of key row r: atom c/2, chunks (c%2)*4 .. +3
+        uint8_t* atom = ds + (c >> 1) * 16384;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; q4++)
+          *reinterpret_cast<uint4*>(atom + swz(r, (c & 1) * 4 + q4, 128)) =
+              make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_ready + dsb);
+    }
+    // dK epilogue: scale, inverse rotation, store
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort));
+    if (ok) {
+      tc_fence_after();
+      const int t = j * kTile + r;
+      float x[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; c++) {
+        uint32_t u[32];
+        tmem_ld32(trow + C::kColDK + c * 32, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e++) x[c * 32 + e] = __uint_as_float(u[e]);
+      }
+      if (t < a.T) {
+        const size_t base = (((size_t)b * a.T + t) * a.Hkv + kvh) * D;
+#pragma unroll
+        for (int c = 0; c < D / 8; c++) {
+          float4 c0, c1;
+          rope_coeffs<D>(a.rope, t, c, c0, c1);
+          const float cs[4] = {c0.x, c0.z, c1.x, c1.z}, sn[4] = {c0.y, c0.w, c1.y, c1.w};
+          float y[8];
+#pragma unroll
+          for (int p = 0; p < 4; p++) {
+            const float x0 = x[c * 8 + 2 * p], x1 = x[c * 8 + 2 * p + 1];
+            y[2 * p] = a.scale * (x0 * cs[p] + x1 * sn[p]);
+            y[2 * p + 1] = a.scale * (x1 * cs[p] - x0 * sn[p]);
+          }
+          if (a.grad_fp32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.dk) + base + c * 8);
+            dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+            dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+          } else {
+            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk) + base)[c] =
+                make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+          }
+        }
+      }
+    }
+    if (!ok) record_timeout(a.status, abort);
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ drain (one query row per thread)
+    const int r = tid - 256;
+    const uint32_t trow = tmem + ((uint32_t)(warp - 8) * 32u << 16);
+    uint8_t* stg = smem + C::kOffStg;
+    bool ok = true;
+    for (int n = 0; n < N; n++) {
+      const int db = n & 1;
+      // Every drain thread reaches both named barriers of an iteration; the
+      // first one agrees on `ok`, so a timeout in one warp stops all four.
+      const bool got = __all_sync(0xffffffffu, mbar_wait(dq_full + db, (n >> 1) & 1, abort));
+      uint32_t u[D];
+      if (got) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; c++) {
+          uint32_t v[32];
+          tmem_ld32(trow + C::kColDQ + db * D + c * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e++) u[c * 32 + e] = v[e];
+        }
+        tc_fence_before();
+        mbar_arrive(dq_free + db);
+      }
+      if (r == 0) bulk_wait_read<0>();  // previous reduction has finished reading the staging tile
+      if (!(ok = named_sync_and(1, 128, got))) break;
+#pragma unroll
+      for (int bx = 0; bx < D / 32; bx++)
+#pragma unroll
+        for (int c = 0; c < 8; c++)
+          *reinterpret_cast<uint4*>(stg + bx * 16384 + swz(r, c, 128)) =
+              make_uint4(u[bx * 32 + 4 * c], u[bx * 32 + 4 * c + 1], u[bx * 32 + 4 * c + 2], u[bx * 32 + 4 * c + 3]);
+      fence_proxy_async_smem();
+      named_sync(1, 128);
+      if (r == 0) {
+        const int i = j + n / G, h = kvh * G + n % G;
+        const int row0 = (int)(((size_t)b * a.Hq + h) * a.Tp + (size_t)i * kTile);
+#pragma unroll
+        for (int bx = 0; bx < D / 32; bx++) tma_reduce_add_2d(&a.map_dqacc, stg + bx * 16384, bx * 32, row0);
+        bulk_commit();
+      }
+    }
+    if (r == 0) bulk_wait<0>();
+    // dV epilogue
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort));
+    if (ok) {
+      tc_fence_after();
+      const int t = j * kTile + r;
+      uint32_t u[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; c++) {
+        uint32_t v[32];
+        tmem_ld32(trow + C::kColDV + c * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e++) u[c * 32 + e] = v[e];
+      }
+      if (t < a.T) {
+        const size_t base = (((size_t)b * a.T + t) * a.Hkv + kvh) * D;
+        if (a.grad_fp32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.dv) + base);
+#pragma unroll
+          for (int c = 0; c < D / 4; c++)
+            dst[c] = make_float4(__uint_as_float(u[4 * c]), __uint_as_float(u[4 * c + 1]), __uint_as_float(u[4 * c + 2]),
+                                 __uint_as_float(u[4 * c + 3]));
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dv) + base);
+#pragma unroll
+          for (int c = 0; c < D / 8; c++)
+            dst[c] = make_uint4(pack_bf16(__uint_as_float(u[8 * c]), __uint_as_float(u[8 * c + 1])),
+                                pack_bf16(__uint_as_float(u[8 * c + 2]), __uint_as_float(u[8 * c + 3])),
+                                pack_bf16(__uint_as_float(u[8 * c + 4]), __uint_as_float(u[8 * c + 5])),
+                                pack_bf16(__uint_as_float(u[8 * c + 6]), __uint_as_float(u[8 * c + 7])));
+        }
+      }
+    }
+    if (!ok) record_timeout(a.status, abort);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    tmem_relinquish();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+int elementwise_blocks(long long items) {
+  long long blocks = (items + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  return (int)blocks;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_prep(const PrepArgs& a, cudaStream_t s) {
+  const long long items = (long long)a.B * a.Tp * a.Hq * a.D / 4;
+  const int blocks = elementwise_blocks(items);
+  if (a.D == 64)
+    k_bwd_prep<64><<<blocks, 256, 0, s>>>(a);
+  else
+    k_bwd_prep<32><<<blocks, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq(const DqArgs& a, cudaStream_t s) {
+  const long long items = (long long)a.B * a.T * a.Hq * a.D / 8;
+  const int blocks = elementwise_blocks(items);
+  if (a.D == 64)
+    k_bwd_dq<64><<<blocks, 256, 0, s>>>(a);
+  else
+    k_bwd_dq<32><<<blocks, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D, bool P>
+cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t s) {
+  using C = BwdCfg<D, P>;
+  const int grid = a.nt * a.B * a.Hkv;
+  cudaError_t e = cudaFuncSetAttribute(k_bwd_dkdv<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  k_bwd_dkdv<D, P><<<grid, 384, C::kSmemBytes, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const BwdArgs& a, bool precise, cudaStream_t s) {
+  if (a.D == 64) return precise ? launch_dkdv_t<64, true>(a, s) : launch_dkdv_t<64, false>(a, s);
+  return precise ? launch_dkdv_t<32, true>(a, s) : launch_dkdv_t<32, false>(a, s);
+}
+
+}  // namespace ne

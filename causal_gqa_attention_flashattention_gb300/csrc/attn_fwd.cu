@@ -1,0 +1,414 @@
+// Forward pass of causal GQA attention with RoPE on Q/K (sm_103a).
+//
+// The NanoEuler GPU engine's FlashAttention is tiled, uses an online softmax
+// and never forms the T x T score matrix (socker-news README, "GPU engine" /
+// "Kernels and acceleration"; ojeo summary); its causal mask skips the upper
+// triangle instead of masking it (openai-hub article, softmax-kernel section).
+// This kernel computes the same result with the GB300 tensor cores:
+//
+//   CTA = (query tile i of 128 rows, batch b, key/value head g, chunk of HC
+//         query heads of g's group).  Tiles are issued largest-i first.
+//   warp 0      TMA producer: the HC query tiles once, then K_j / V_j for
+//               j = 0..i through a ring of kStages stages.  Each K/V tile is
+//               read once and used by all HC heads (GQA sharing).
+//   warp 1      tcgen05 MMA issuer: S = Q_h K_j^T into one of two TMEM score
+//               buffers, then O_h += P V_j with P read from TMEM.
+//   warps 2-3   RoPE: rotate the Q tiles and each K tile in shared memory
+//               (in place, through the swizzled layout) before the MMA reads
+//               them; rotated values never go to HBM.  Rotated operands are
+//               fp16 (three more mantissa bits than bf16).  With PRECISE the
+//               fp16 remainder (rotated - hi) goes to a second buffer and
+//               S = Qhi Khi^T + Qlo Khi^T + Qhi Klo^T, so the logits carry
+//               ~2^-22 relative error even when |s| reaches 10^3.
+//   warps 4-7   softmax, one thread per query row: row max, lazy rescale of
+//               the TMEM accumulator (only when the max grows by > 2^8),
+//               exp2, P (bf16) back into TMEM, row sum of the rounded P (so
+//               O is an exact convex combination of V rows with the weights
+//               the MMA used); epilogue O / l (bf16 or fp32) and
+//               LSE = ln(sum exp).
+// Only the diagonal tile (j == i) is masked; tiles above it are never visited.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "rope.cuh"
+
+namespace ne {
+namespace {
+
+template <int D, bool PRECISE>
+struct FwdCfg {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr uint32_t kSpan = D * 2;  // bytes per row == swizzle span
+  static constexpr uint32_t kSwz = D == 64 ? kSw128 : kSw64;
+  static constexpr uint32_t kSBO = 8 * kSpan;  // one 8-row swizzle atom
+  static constexpr int kMaxHC = D == 64 ? (PRECISE ? 3 : 4) : 8;  // HC*D + 2*128 TMEM columns <= 512
+  static constexpr int kStages = D == 64 ? (PRECISE ? 2 : 3) : (PRECISE ? 3 : 4);
+  static constexpr int kLoTiles = PRECISE ? 1 : 0;
+  // shared memory map (bytes from a 1024-aligned base)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffQlo = kOffQ + kMaxHC * kTileBytes;
+  static constexpr int kOffK = kOffQlo + kLoTiles * kMaxHC * kTileBytes;
+  static constexpr int kOffKlo = kOffK + kStages * kTileBytes;
+  static constexpr int kOffV = kOffKlo + kLoTiles * kStages * kTileBytes;
+  static constexpr int kOffM = kOffV + kStages * kTileBytes;
+  static constexpr int kOffL = kOffM + kMaxHC * kTile * 4;
+  static constexpr int kOffBar = kOffL + kMaxHC * kTile * 4;
+  static constexpr int kNumBars = 2 + 3 * kStages + 4 + kMaxHC + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmemS = 256;  // two 128-column score buffers at 256, 384
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kMaxHC * D <= 256, "tensor memory budget");
+};
+
+__device__ __forceinline__ void record_timeout(int* status, volatile int* abort) {
+  *abort = 1;
+  atomicCAS(status, 0, kStatusTimeout);
+}
+
+// Rotates `ntiles` consecutive 128-row tiles in place (positions pos0 + row),
+// writing fp16 results; with `lo` the fp16 remainders go to the same offsets there.
+template <int D>
+__device__ __forceinline__ void rope_tiles(uint8_t* base, uint8_t* lo, int ntiles, int pos0, const float2* tab,
+                                           int tid, int nthreads) {
+  constexpr uint32_t kSpan = D * 2;
+  constexpr int kCPR = D / 8;  // 16-byte chunks per row
+  const int total = ntiles * kTile * kCPR;
+  for (int idx = tid; idx < total; idx += nthreads) {
+    const int row = (idx / kCPR) % kTile;
+    const int pc = idx % kCPR;
+    const uint32_t phys = (uint32_t)idx * 16u;
+    const int lc = (int)((swz(row, pc, kSpan) - row * kSpan) / 16u);  // logical chunk
+    uint4* p = reinterpret_cast<uint4*>(base + phys);
+    float4 a, b;
+    rope_coeffs<D>(tab, pos0 + row, lc, a, b);
+    if (lo) {
+      uint4 l;
+      *p = rope_chunk_f16(*p, a, b, &l);
+      *reinterpret_cast<uint4*>(lo + phys) = l;
+    } else {
+      *p = rope_chunk_f16(*p, a, b, nullptr);
+    }
+  }
+}
+
+template <int D, bool PRECISE>
+__global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ FwdArgs a) {
+  using C = FwdCfg<D, PRECISE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_ready = bars + 1;
+  uint64_t* kv_full = bars + 2;
+  uint64_t* k_ready = kv_full + C::kStages;
+  uint64_t* kv_empty = k_ready + C::kStages;
+  uint64_t* s_full = kv_empty + C::kStages;  // [2]
+  uint64_t* p_ready = s_full + 2;            // [2]
+  uint64_t* o_done = p_ready + 2;            // [kMaxHC]
+  uint64_t* drain = o_done + C::kMaxHC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  float* sm_m = reinterpret_cast<float*>(smem + C::kOffM);
+  float* sm_l = reinterpret_cast<float*>(smem + C::kOffL);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int HC = a.HC;
+  const int nchunk = a.G / HC;
+  const int per_i = a.B * a.Hkv * nchunk;
+  const int i = a.nt - 1 - (int)blockIdx.x / per_i;
+  int rem = (int)blockIdx.x % per_i;
+  const int hc = rem % nchunk;
+  rem /= nchunk;
+  const int kvh = rem % a.Hkv;
+  const int b = rem / a.Hkv;
+  const int h0 = kvh * a.G + hc * HC;
+  const int nkv = i + 1;
+
+  if (tid == 0) {
+    *abort = 0;
+    mbar_init(q_full, 1);
+    mbar_init(q_ready, 64);
+    for (int s = 0; s < C::kStages; s++) {
+      mbar_init(kv_full + s, 1);
+      mbar_init(k_ready + s, 64);
+      mbar_init(kv_empty + s, 1);
+    }
+    for (int s = 0; s < 2; s++) {
+      mbar_init(s_full + s, 1);
+      mbar_init(p_ready + s, 128);
+    }
+    for (int h = 0; h < C::kMaxHC; h++) mbar_init(o_done + h, 1);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const volatile int never = 0;
+
+  const uint32_t sQ = smem_u32(smem + C::kOffQ);
+  const uint32_t sQlo = smem_u32(smem + C::kOffQlo);
+  const uint32_t sK = smem_u32(smem + C::kOffK);
+  const uint32_t sKlo = smem_u32(smem + C::kOffKlo);
+  const uint32_t sV = smem_u32(smem + C::kOffV);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&a.map_q);
+      prefetch_tmap(&a.map_k);
+      prefetch_tmap(&a.map_v);
+      mbar_arrive_expect_tx(q_full, HC * C::kTileBytes);
+      for (int hh = 0; hh < HC; hh++)
+        tma_load_4d(smem + C::kOffQ + hh * C::kTileBytes, &a.map_q, q_full, 0, h0 + hh, i * kTile, b);
+      int loaded = 0;
+      for (int j = 0; j < nkv; j++) {
+        const int st = j % C::kStages, use = j / C::kStages;
+        if (use > 0 && !mbar_wait(kv_empty + st, (use - 1) & 1, abort)) {
+          record_timeout(a.status, abort);
+          break;
+        }
+        mbar_arrive_expect_tx(kv_full + st, 2 * C::kTileBytes);
+        tma_load_4d(smem + C::kOffK + st * C::kTileBytes, &a.map_k, kv_full + st, 0, kvh, j * kTile, b);
+        tma_load_4d(smem + C::kOffV + st * C::kTileBytes, &a.map_v, kv_full + st, 0, kvh, j * kTile, b);
+        loaded = j + 1;
+      }
+      // Let every copy issued above land before the CTA can exit.
+      mbar_wait(q_full, 0, &never);
+      for (int j = loaded - C::kStages < 0 ? 0 : loaded - C::kStages; j < loaded; j++)
+        mbar_wait(kv_full + j % C::kStages, (j / C::kStages) & 1, &never);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_fp16(128, 128, false, false);
+      constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
+      bool ok = mbar_wait(q_ready, 0, abort);
+      tc_fence_after();
+      auto issue_pv = [&](int m) -> bool {
+        const int hh = m % HC, jm = m / HC, st = jm % C::kStages, sb = m & 1;
+        if (!mbar_wait(p_ready + sb, (m >> 1) & 1, abort)) return false;
+        tc_fence_after();
+        const uint32_t sP = tmem + C::kTmemS + sb * 128;
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ks++)
+          mma_ts(tmem + hh * D, sP + ks * 8,
+                 smem_desc(sV + st * C::kTileBytes + ks * 16 * C::kSpan, 16, C::kSBO, C::kSwz), idPV,
+                 (jm > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(o_done + hh);
+        if (hh == HC - 1) mma_commit(kv_empty + st);
+        return true;
+      };
+      int n = 0;
+      for (int j = 0; ok && j < nkv; j++) {
+        const int st = j % C::kStages;
+        if (!mbar_wait(k_ready + st, (j / C::kStages) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int hh = 0; hh < HC; hh++, n++) {
+          const int sb = n & 1;
+          // S = Qhi Khi^T (+ Qlo Khi^T + Qhi Klo^T)
+          const uint32_t qh = sQ + hh * C::kTileBytes, kh = sK + st * C::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ks++)
+            mma_ss(tmem + C::kTmemS + sb * 128, smem_desc(qh + ks * 32, 16, C::kSBO, C::kSwz),
+                   smem_desc(kh + ks * 32, 16, C::kSBO, C::kSwz), idS, ks > 0 ? 1u : 0u);
+          if (PRECISE) {
+            const uint32_t ql = sQlo + hh * C::kTileBytes, kl = sKlo + st * C::kTileBytes;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ks++) {
+              mma_ss(tmem + C::kTmemS + sb * 128, smem_desc(ql + ks * 32, 16, C::kSBO, C::kSwz),
+                     smem_desc(kh + ks * 32, 16, C::kSBO, C::kSwz), idS, 1u);
+              mma_ss(tmem + C::kTmemS + sb * 128, smem_desc(qh + ks * 32, 16, C::kSBO, C::kSwz),
+                     smem_desc(kl + ks * 32, 16, C::kSBO, C::kSwz), idS, 1u);
+            }
+          }
+          mma_commit(s_full + sb);
+          if (n >= 1 && !issue_pv(n - 1)) {
+            ok = false;
+            break;
+          }
+        }
+      }
+      if (ok && n >= 1) ok = issue_pv(n - 1);
+      if (!ok) record_timeout(a.status, abort);
+      // All issued MMAs must finish before the tensor memory is released.
+      mma_commit(drain);
+      mbar_wait(drain, 0, &never);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ RoPE on Q and K
+    const int rt = tid - 64;
+    bool ok = mbar_wait(q_full, 0, abort);
+    if (ok) {
+      rope_tiles<D>(smem + C::kOffQ, PRECISE ? smem + C::kOffQlo : nullptr, HC, i * kTile, a.rope, rt, 64);
+      fence_proxy_async_smem();
+      mbar_arrive(q_ready);
+    }
+    for (int j = 0; ok && j < nkv; j++) {
+      const int st = j % C::kStages;
+      if (!mbar_wait(kv_full + st, (j / C::kStages) & 1, abort)) {
+        ok = false;
+        break;
+      }
+      rope_tiles<D>(smem + C::kOffK + st * C::kTileBytes, PRECISE ? smem + C::kOffKlo + st * C::kTileBytes : nullptr,
+                    1, j * kTile, a.rope, rt, 64);
+      fence_proxy_async_smem();
+      mbar_arrive(k_ready + st);
+    }
+    if (!ok) record_timeout(a.status, abort);
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int r = tid - 128;               // query row within the tile
+    const uint32_t lane_base = (uint32_t)(warp - 4) * 32u;
+    const uint32_t trow = tmem + (lane_base << 16);
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    int n = 0;
+    for (int j = 0; ok && j < nkv; j++) {
+      const bool diag = (j == i);
+      for (int hh = 0; hh < HC; hh++, n++) {
+        const int sb = n & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort));
+        if (!ok) break;
+        tc_fence_after();
+        float s[kTile];
+        {
+          uint32_t u[32];
+#pragma unroll
+          for (int c = 0; c < kTile / 32; c++) {
+            tmem_ld32(trow + C::kTmemS + sb * 128 + c * 32, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; e++) s[c * 32 + e] = __uint_as_float(u[e]);
+          }
+        }
+        if (diag) {
+#pragma unroll
+          for (int c = 0; c < kTile; c++)
+            if (c > r) s[c] = -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < kTile; c++) mx = fmaxf(mx, s[c]);
+        mx *= sl2;
+        float m_old = j == 0 ? -INFINITY : sm_m[hh * kTile + r];
+        float l_old = j == 0 ? 0.f : sm_l[hh * kTile + r];
+        float m_use = m_old, alpha = 1.f;
+        if (j == 0) {
+          m_use = mx;
+        } else {
+          // The previous O_h += P V must be complete before O_h is read or rescaled.
+          ok = __all_sync(0xffffffffu, mbar_wait(o_done + hh, (j - 1) & 1, abort));
+          if (!ok) break;
+          tc_fence_after();
+          const float m_new = fmaxf(m_old, mx);
+          if (__any_sync(0xffffffffu, m_new > m_old + 8.0f)) {
+            m_use = m_new;
+            alpha = ex2(m_old - m_new);
+#pragma unroll
+            for (int c = 0; c < D / 16; c++) {
+              uint32_t u[16];
+              tmem_ld16(trow + hh * D + c * 16, u);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; e++) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+              tmem_st16(trow + hh * D + c * 16, u);
+            }
+          }
+        }
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < kTile / 32; c++) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; e++) {
+            const float p0 = ex2(fmaf(s[c * 32 + 2 * e], sl2, -m_use));
+            const float p1 = ex2(fmaf(s[c * 32 + 2 * e + 1], sl2, -m_use));
+            pk[e] = pack_bf16(p0, p1);
+            sum += bf_lo(pk[e]) + bf_hi(pk[e]);
+          }
+          tmem_st16(trow + C::kTmemS + sb * 128 + c * 16, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_ready + sb);
+        sm_m[hh * kTile + r] = m_use;
+        sm_l[hh * kTile + r] = l_old * alpha + sum;
+      }
+    }
+    if (ok) {
+      const int t = i * kTile + r;
+      for (int hh = 0; hh < HC; hh++) {
+        ok = __all_sync(0xffffffffu, mbar_wait(o_done + hh, (nkv - 1) & 1, abort));
+        if (!ok) break;
+        tc_fence_after();
+        const float l = sm_l[hh * kTile + r];
+        const float inv = 1.f / l;
+        const int h = h0 + hh;
+        const size_t orow = (((size_t)b * a.T + t) * a.Hq + h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 16; c++) {
+          uint32_t u[16];
+          tmem_ld16(trow + hh * D + c * 16, u);
+          tmem_wait_ld();
+          if (t < a.T) {
+            if (a.o_fp32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o) + orow + c * 16);
+#pragma unroll
+              for (int e = 0; e < 4; e++)
+                dst[e] = make_float4(__uint_as_float(u[4 * e]) * inv, __uint_as_float(u[4 * e + 1]) * inv,
+                                     __uint_as_float(u[4 * e + 2]) * inv, __uint_as_float(u[4 * e + 3]) * inv);
+            } else {
+              uint32_t w[8];
+#pragma unroll
+              for (int e = 0; e < 8; e++)
+                w[e] = pack_bf16(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + orow + c * 16);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+          }
+        }
+        if (t < a.T)
+          a.lse[((size_t)b * a.Hq + h) * a.T + t] = (sm_m[hh * kTile + r] + __log2f(l)) * 0.69314718055994531f;
+      }
+    }
+    if (!ok) record_timeout(a.status, abort);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    tmem_relinquish();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, bool P>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
+  using C = FwdCfg<D, P>;
+  const int grid = a.nt * a.B * a.Hkv * (a.G / a.HC);
+  cudaError_t e = cudaFuncSetAttribute(k_attn_fwd<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  k_attn_fwd<D, P><<<grid, 256, C::kSmemBytes, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, bool precise, cudaStream_t s) {
+  if (a.D == 64) return precise ? launch_fwd_t<64, true>(a, s) : launch_fwd_t<64, false>(a, s);
+  return precise ? launch_fwd_t<32, true>(a, s) : launch_fwd_t<32, false>(a, s);
+}
+
+}  // namespace ne

@@ -1,0 +1,77 @@
+// Internal interfaces between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace ne {
+
+constexpr int kTile = 128;  // query rows / key rows per tile
+
+// Device-side status codes (mirror ne_status in include/ne_attn.h).
+constexpr int kStatusTimeout = -6;
+
+// Flag bits shared with include/ne_attn.h.
+constexpr int kFlagOFp32 = 1;      // o is float32
+constexpr int kFlagGradFp32 = 2;   // dq, dk, dv are float32
+constexpr int kFlagPreciseQK = 4;  // logits from hi + lo fp16 parts of rotated q and k
+
+// Largest number of query heads one forward CTA handles (TMEM/smem budget).
+inline int fwd_max_heads(int D, bool precise) { return D == 64 ? (precise ? 3 : 4) : 8; }
+
+struct FwdArgs {
+  CUtensorMap map_q, map_k, map_v;  // 4-D tiled maps over [B, T, H, D], box D x 1 x 128 x 1
+  void* o;                          // [B, T, Hq, D] bf16 or fp32
+  float* lse;                       // [B, Hq, T]
+  const float2* rope;               // [Tcap][D/2] (cos, sin)
+  int* status;                      // device status word
+  int B, T, Hq, Hkv, D, G, HC;      // HC: query heads per CTA (divides G)
+  int nt;                           // number of 128-row tiles
+  int o_fp32;
+  float scale_log2;                 // log2(e) / sqrt(D)
+};
+
+struct BwdArgs {
+  CUtensorMap map_qr, map_kr, map_v, map_do;  // 4-D maps as above (qr/kr: rotated fp16 copies)
+  CUtensorMap map_qlo, map_klo;               // fp16 remainders (precise logits only)
+  CUtensorMap map_dqacc;                      // 2-D map over [B*Hq*Tp, D] fp32, box 32 x 128
+  const float* lse2;                          // [B, Hq, Tp]  lse * log2(e); +inf on pad rows
+  const float* delta;                         // [B, Hq, Tp]
+  void* dk;                                   // [B, T, Hkv, D] bf16 or fp32
+  void* dv;
+  const float2* rope;
+  int* status;
+  int B, T, Hq, Hkv, D, G, nt, Tp;
+  int grad_fp32;
+  float scale_log2, scale;
+};
+
+struct PrepArgs {
+  const __nv_bfloat16 *q, *k, *dout;
+  const void* o;  // bf16 or fp32
+  const float* lse;
+  __half *qr, *kr, *qlo, *klo;  // qlo/klo null unless precise logits
+  float *lse2, *delta, *dqacc;
+  const float2* rope;
+  int B, T, Hq, Hkv, D, Tp, o_fp32;
+};
+
+struct DqArgs {
+  const float* dqacc;  // [B, Hq, Tp, D]
+  void* dq;            // [B, T, Hq, D]
+  const float2* rope;
+  int B, T, Hq, D, Tp, grad_fp32;
+  float scale;
+};
+
+cudaError_t launch_fwd(const FwdArgs& a, bool precise, cudaStream_t s);
+cudaError_t launch_bwd_prep(const PrepArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_dkdv(const BwdArgs& a, bool precise, cudaStream_t s);
+cudaError_t launch_bwd_dq(const DqArgs& a, cudaStream_t s);
+cudaError_t launch_rope_table(float2* tab, int Tcap, int D, double base, cudaStream_t s);
+cudaError_t launch_timeout_probe(int* status, long long limit_ns, cudaStream_t s);
+
+}  // namespace ne

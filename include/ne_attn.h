@@ -1,0 +1,135 @@
+/*
+ * ne_attn: causal grouped-query attention with rotary position embedding on
+ * Q and K, forward and backward, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the attention block of the NanoEuler decoder-only
+ * transformer (socker-news README, "Architecture": rotary embedding applied
+ * to queries and keys, grouped-query attention in which query heads share a
+ * smaller set of key/value heads; "GPU engine": a tiled FlashAttention with
+ * online softmax that never forms the T x T matrix; mynewscn README, same
+ * items).  For every batch b, query head h (key/value head g = h / (Hq/Hkv))
+ * and position t:
+ *
+ *   q^_t = R_t q[b,t,h],  k^_j = R_j k[b,j,g]       rotary embedding, interleaved
+ *                                                   pairs (2i, 2i+1), angle
+ *                                                   t * base^(-2i/D)
+ *   s_tj = q^_t . k^_j / sqrt(D)  for j <= t        causal: later keys are skipped
+ *   o[b,t,h] = sum_j softmax_j(s_t.) v[b,j,g]
+ *   lse[b,h,t] = ln sum_{j<=t} exp(s_tj)            natural log
+ *
+ * Layouts (row-major, contiguous):
+ *   q, o, dout, dq : [B, T, Hq,  D]   bfloat16 (o and dq may be float32, see flags)
+ *   k, v, dk, dv   : [B, T, Hkv, D]   bfloat16 (dk, dv may be float32)
+ *   lse            : [B, Hq, T]       float32
+ * Supported: D in {32, 64}; Hq % Hkv == 0; 1 <= T; B >= 1; and
+ * B * T * max(Hq, Hkv) * D < 2^31.  All tensor pointers are device pointers,
+ * 16-byte aligned; the caller owns every buffer.
+ *
+ * Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ * default stream): no host synchronisation, no host<->device copies.  Argument
+ * errors are detected on the host and returned before anything is launched.
+ * A kernel whose internal pipeline wait exceeds its time limit stops, frees
+ * its tensor memory and records NE_ERR_DEVICE_TIMEOUT in a device status word
+ * that ne_attn_check_status() reads.
+ *
+ * The library keeps one small table per (device, D, rope_base): fp32
+ * cos/sin of t * theta_i for t below the largest T seen so far, built on the
+ * device in double precision.  The first call that needs a new or larger
+ * table allocates it with cudaMalloc, so make one call with the largest T
+ * before capturing calls in a CUDA graph.  Nothing else is allocated.
+ */
+#ifndef NE_ATTN_H
+#define NE_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NE_OK = 0,
+  NE_ERR_ARG = -1,            /* null pointer, bad size, Hq % Hkv != 0, bad rope_base or flags */
+  NE_ERR_ALIGN = -2,          /* a tensor pointer is not 16-byte aligned */
+  NE_ERR_UNSUPPORTED = -3,    /* D not in {32, 64}, size limits, or device is not sm_103 */
+  NE_ERR_CUDA = -4,           /* a CUDA runtime/driver call or a launch failed */
+  NE_ERR_WORKSPACE = -5,      /* workspace missing, too small or not 256-byte aligned */
+  NE_ERR_DEVICE_TIMEOUT = -6  /* a kernel gave up on a pipeline wait (see above) */
+} ne_status;
+
+/* Flag bits for ne_attn_fwd_ex, ne_attn_bwd and ne_attn_bwd_workspace_size. */
+#define NE_ATTN_O_FP32 1     /* o is float32 [B,T,Hq,D] (forward output, backward input) */
+#define NE_ATTN_GRAD_FP32 2  /* dq, dk, dv are float32 */
+#define NE_ATTN_PRECISE_QK 4 /* logits from hi + lo fp16 parts of the rotated q and k:
+                                S = qhi.khi + qlo.khi + qhi.klo (three tensor-core products)
+                                instead of one; for inputs whose logits reach |s| ~ 10^2..10^3.
+                                Use the same setting for the forward and the backward. */
+
+/*
+ * Forward pass: writes o (bfloat16) and lse.  Same as ne_attn_fwd_ex with
+ * flags = 0.
+ * One kernel: the rotary embedding of Q and K is applied to the tiles in
+ * shared memory (the rotated values never reach HBM) and rounded to fp16
+ * for the tensor cores; K/V tiles are loaded once per key/value head and
+ * shared by the query heads of its group; S = Q K^T and O += P V run on the
+ * tensor cores (fp32 accumulation in tensor memory; P is bf16) with an online
+ * softmax in between.  Returns NE_OK or a negative ne_status.
+ */
+int ne_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
+                int Hq, int Hkv, int D, float rope_base, void* stream);
+
+/* Forward pass with flags (NE_ATTN_O_FP32, NE_ATTN_PRECISE_QK; others rejected). */
+int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
+                   int Hq, int Hkv, int D, float rope_base, int flags, void* stream);
+
+/*
+ * Bytes of device workspace ne_attn_bwd needs for this shape and flags
+ * (pass a 256-byte aligned pointer).  Holds: the rotated q and k (fp16, plus
+ * their fp16 remainders with NE_ATTN_PRECISE_QK), per-row
+ * Delta_t = dO_t . O_t and lse * log2(e) (fp32, rows padded to a multiple of
+ * 128), and the fp32 dQ accumulator [B, Hq, Tpad, D].  Returns 0 for
+ * unsupported shapes or flags.
+ */
+size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D, int flags);
+
+/*
+ * Backward pass: given q, k, v, the forward's o and lse, and the upstream
+ * gradient dout (bfloat16), writes dq, dk, dv: the gradients with respect to
+ * the un-rotated inputs (the inverse rotation R_t^T is applied on the way
+ * out).  flags: NE_ATTN_O_FP32 (o is float32), NE_ATTN_GRAD_FP32 (float32
+ * gradients, else bfloat16), NE_ATTN_PRECISE_QK.
+ * Three kernels: a pre-pass (Delta = rowsum(dO * O), rotated q/k, zeroed dQ
+ * accumulator), a key-tile sweep (dK and dV summed over the query heads of
+ * the group inside the kernel, dQ partial products added into the fp32
+ * accumulator with bulk tensor reductions), and a dQ epilogue.
+ * dQ accumulation order varies between runs, so dq is not bitwise
+ * reproducible run to run; o, lse, dk and dv are.
+ */
+int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                const void* dout, void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv,
+                int D, float rope_base, int flags, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of
+ * the current device: NE_OK, NE_ERR_DEVICE_TIMEOUT, or NE_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+int ne_attn_check_status(void* stream);
+
+/* Static description of a status code. */
+const char* ne_attn_status_string(int status);
+
+/*
+ * Test hook for the timeout path: launches one block that waits on a
+ * barrier nothing will complete, with the given limit in microseconds
+ * (1..1000000), then records NE_ERR_DEVICE_TIMEOUT exactly as the attention
+ * kernels do.  Returns NE_OK if the launch succeeded.
+ */
+int ne_attn_debug_timeout_probe(int limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NE_ATTN_H */

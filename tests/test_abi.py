@@ -1,0 +1,64 @@
+"""CPU checks of the C-ABI library: it builds, loads without a GPU, exports
+every entry point include/ne_attn.h declares, and rejects bad arguments on
+the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def libne():
+    from causal_gqa_attention_flashattention_gb300 import build, binding
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "ne_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ne_attn_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(libne):
+    names = declared_functions()
+    assert "ne_attn_fwd" in names and "ne_attn_bwd" in names
+    for n in names:
+        assert hasattr(libne, n), n
+
+
+def test_workspace_size(libne):
+    B, T, Hq, Hkv, D = 16, 512, 12, 4, 64
+    n = libne.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, D, 0)
+    expect = 4 * B * Hq * T * D + 2 * B * T * (Hq + Hkv) * D + 2 * 4 * B * Hq * T
+    assert expect <= n <= expect + 5 * 256
+    n_precise = libne.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, D, 4)
+    assert n_precise - n >= 2 * B * T * (Hq + Hkv) * D  # fp16 remainders of rotated q and k
+    assert libne.ne_attn_bwd_workspace_size(1, 77, 4, 2, 32, 0) >= 4 * 4 * 128 * 32  # padded to 128 rows
+    assert libne.ne_attn_bwd_workspace_size(1, 16, 3, 2, 64, 0) == 0
+    assert libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 48, 0) == 0
+    assert libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 64, 8) == 0
+
+
+def test_host_argument_checks(libne):
+    buf = ctypes.create_string_buffer(4096 + 64)
+    base = (ctypes.addressof(buf) + 63) // 64 * 64
+    p = ctypes.c_void_p(base)
+    mis = ctypes.c_void_p(base + 2)
+    null = None
+    assert libne.ne_attn_fwd(null, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, null) == -1
+    assert libne.ne_attn_fwd(p, p, p, p, p, 1, 16, 3, 2, 64, 10000.0, null) == -1
+    assert libne.ne_attn_fwd(p, p, p, p, p, 1, 0, 2, 1, 64, 10000.0, null) == -1
+    assert libne.ne_attn_fwd(p, p, p, p, p, 1, 16, 2, 1, 48, 10000.0, null) == -3
+    assert libne.ne_attn_fwd(p, p, p, p, p, 1, 16, 2, 1, 64, 0.5, null) == -1
+    assert libne.ne_attn_fwd(mis, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, null) == -2
+    assert libne.ne_attn_fwd_ex(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 2, null) == -1  # grad flag on fwd
+    assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 8, p, 4096, null) == -1
+    assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 0, p, 16, null) == -5
+    assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 0, mis, 1 << 20, null) == -5
+    assert libne.ne_attn_debug_timeout_probe(0, null) == -1
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert libne.ne_attn_status_string(code)

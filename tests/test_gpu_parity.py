@@ -1,0 +1,219 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Every comparison uses the same seeded bf16 inputs on both sides.  O, dQ, dK
+and dV must reach relative L2 <= 5e-3 and max abs <= 2e-2; LSE max abs <= 1e-2.
+Large workloads are checked on a sample of whole (batch, kv-head) groups,
+which the oracle computes exactly.
+"""
+import numpy as np
+import pytest
+
+import _harness as H
+from causal_gqa_attention_flashattention_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nb():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from causal_gqa_attention_flashattention_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def run_gpu(nb, x, base=inputs.ROPE_BASE, grad_dtype=None, o_dtype=None, precise=False):
+    grad_dtype = grad_dtype or torch.float32
+    o_dtype = o_dtype or torch.bfloat16
+    q, k, v, do = (H.to_device(x[n + "_bits"]) for n in ("q", "k", "v", "dout"))
+    o, lse = nb.attn_fwd(q, k, v, base, o_dtype=o_dtype, precise=precise)
+    dq, dk, dv = nb.attn_bwd(q, k, v, o, lse, do, base, grad_dtype=grad_dtype, precise=precise)
+    nb.check_status()
+    return dict(o=H.to_f64(o), lse=lse.cpu().numpy().astype(np.float64), dq=H.to_f64(dq),
+                dk=H.to_f64(dk), dv=H.to_f64(dv))
+
+
+def compare(oracle_mod, x, gpu, shape, groups, base=inputs.ROPE_BASE, tol_abs=H.MAX_ABS_TOL):
+    B, T, Hq, Hkv, D = shape
+    ref = oracle_mod.attn_bwd(x["q"], x["k"], x["v"], x["dout"], base, groups=groups)
+    qsel, ksel = H.group_slices(B, Hq, Hkv, groups)
+    report = {}
+    for name, gat, sel in (("o", H.gather_q, qsel), ("dq", H.gather_q, qsel),
+                           ("dk", H.gather_k, ksel), ("dv", H.gather_k, ksel)):
+        g, r = gat(gpu[name], sel), gat(ref[name], sel)
+        assert np.isfinite(g).all(), name
+        report[name] = H.errors(g, r)
+    g, r = H.gather_lse(gpu["lse"], qsel), H.gather_lse(ref["lse"], qsel)
+    report["lse"] = H.errors(g, r)
+    bad = [n for n in ("o", "dq", "dk", "dv") if report[n][0] > H.REL_L2_TOL or report[n][1] > tol_abs]
+    assert not bad and report["lse"][1] <= H.LSE_ABS_TOL, report
+    return report
+
+
+WORKLOAD_GROUPS = {
+    "tiny_cpu_model": None,
+    "cpu_small_model_ctx512": None,
+    "gpu_116m_model": None,
+    "scaled_270m_synthetic": [(0, 0), (3, 1), (5, 2), (7, 3)],
+    "long_context_stress": [(1, 2)],
+}
+
+# Output precision per workload.  Gradients are fp32: a bf16 gradient of
+# magnitude >= 4 is already 1/64 away from its neighbours, most of the
+# 2e-2 absolute bound (test_bf16_gradient_outputs covers bf16 gradients).
+# The stress workload (logits ~10^2..10^3, near one-hot rows) also needs the
+# precise logits and an fp32 O, because Delta = dO . O cancels against dP.
+WORKLOAD_MODE = {name: dict(grad_dtype="float32", o_dtype="bfloat16", precise=False)
+                 for name in inputs.WORKLOAD_ORDER}
+WORKLOAD_MODE["long_context_stress"] = dict(grad_dtype="float32", o_dtype="float32", precise=True)
+
+
+def mode_kwargs(name):
+    m = WORKLOAD_MODE[name]
+    return dict(grad_dtype=getattr(torch, m["grad_dtype"]), o_dtype=getattr(torch, m["o_dtype"]),
+                precise=m["precise"])
+
+
+@pytest.mark.parametrize("name", inputs.WORKLOAD_ORDER)
+def test_workload_parity(nb, oracle_mod, name):
+    x = inputs.make_workload_inputs(name)
+    shape = tuple(inputs.WORKLOADS[name][:5])
+    gpu = run_gpu(nb, x, **mode_kwargs(name))
+    rep = compare(oracle_mod, x, gpu, shape, WORKLOAD_GROUPS[name])
+    print(name, rep)
+
+
+def test_bf16_gradient_outputs(nb, oracle_mod):
+    """bf16 gradients on the 116M-model shape: relative L2 within 5e-3 and each
+    element within 2e-2 plus the half-ulp a bf16 value of its size carries."""
+    name = "gpu_116m_model"
+    x = inputs.make_workload_inputs(name)
+    shape = tuple(inputs.WORKLOADS[name][:5])
+    gpu = run_gpu(nb, x, grad_dtype=torch.bfloat16)
+    groups = [(0, 0), (7, 1), (15, 3)]
+    ref = oracle_mod.attn_bwd(x["q"], x["k"], x["v"], x["dout"], groups=groups)
+    qsel, ksel = H.group_slices(shape[0], shape[2], shape[3], groups)
+    for name_, gat, sel in (("dq", H.gather_q, qsel), ("dk", H.gather_k, ksel), ("dv", H.gather_k, ksel)):
+        g, r = gat(gpu[name_], sel), gat(ref[name_], sel)
+        rel, _ = H.errors(g, r)
+        assert rel <= H.REL_L2_TOL, (name_, rel)
+        assert np.all(np.abs(g - r) <= H.MAX_ABS_TOL + np.abs(r) * 2.0 ** -9), name_
+
+
+EDGE_SHAPES = [
+    (1, 1, 2, 1, 64),      # single token
+    (1, 77, 4, 2, 64),     # one ragged tile
+    (2, 1000, 6, 2, 64),   # ragged, many tiles, G = 3
+    (1, 300, 8, 1, 64),    # G = 8: two 4-head chunks per KV head in the forward
+    (1, 200, 8, 1, 32),    # G = 8 at D = 32: one 8-head chunk
+    (2, 129, 3, 3, 32),    # G = 1 (plain MHA), one row past a tile
+    (1, 256, 2, 2, 64),    # G = 1, exact tiles
+    (1, 384, 5, 1, 64),    # G = 5: one head per CTA in the forward
+    (3, 640, 4, 4, 32),
+]
+
+
+@pytest.mark.parametrize("shape", EDGE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_edge_shapes(nb, oracle_mod, shape):
+    x = H.make(*shape, seed=sum(shape))
+    gpu = run_gpu(nb, x)
+    compare(oracle_mod, x, gpu, shape, None)
+
+
+@pytest.mark.parametrize("shape", [(1, 77, 4, 2, 64), (2, 1000, 6, 2, 64), (1, 300, 8, 1, 64),
+                                   (1, 200, 8, 1, 32), (2, 129, 3, 3, 32),
+                                   (1, 128, 16, 1, 64)],  # one KV head shared by 16 query heads
+                         ids=lambda s: "x".join(map(str, s)))
+def test_precise_logits_edge_shapes(nb, oracle_mod, shape):
+    x = H.make(*shape, seed=sum(shape) + 1, recipe="stress")
+    gpu = run_gpu(nb, x, o_dtype=torch.float32, precise=True)
+    compare(oracle_mod, x, gpu, shape, None)
+
+
+def test_other_rope_base(nb, oracle_mod):
+    shape = (2, 333, 6, 2, 64)
+    x = H.make(*shape, seed=7)
+    gpu = run_gpu(nb, x, base=500.0)
+    compare(oracle_mod, x, gpu, shape, None, base=500.0)
+
+
+def test_deterministic_outputs(nb):
+    """o, lse, dk, dv are bitwise reproducible; dq within float reordering."""
+    x = H.make(2, 700, 6, 2, 64, seed=3)
+    a = run_gpu(nb, x)
+    b = run_gpu(nb, x)
+    for n in ("o", "lse", "dk", "dv"):
+        np.testing.assert_array_equal(a[n], b[n])
+    assert np.max(np.abs(a["dq"] - b["dq"])) < 1e-2
+
+
+def test_no_writes_outside_outputs(nb):
+    """Outputs sit between guard bands; nothing outside them may change."""
+    B, T, Hq, Hkv, D = 1, 200, 4, 2, 64
+    x = H.make(B, T, Hq, Hkv, D, seed=11)
+    q, k, v, do = (H.to_device(x[n + "_bits"]) for n in ("q", "k", "v", "dout"))
+    guard = 65536
+    def padded(n, dtype):
+        buf = torch.full((2 * guard + n,), float("nan") if dtype == torch.float32 else 0.0,
+                         dtype=dtype, device="cuda")
+        if dtype == torch.bfloat16:
+            buf.view(torch.int16).fill_(0x5A5A)
+        return buf
+    nq, nk, nl = q.numel(), k.numel(), B * Hq * T
+    ob, lb = padded(nq, torch.bfloat16), padded(nl, torch.float32)
+    dqb, dkb, dvb = padded(nq, torch.bfloat16), padded(nk, torch.bfloat16), padded(nk, torch.bfloat16)
+    snap = [t.clone() for t in (ob, lb, dqb, dkb, dvb)]
+    o = ob[guard:guard + nq].view(q.shape)
+    lse = lb[guard:guard + nl].view(B, Hq, T)
+    nb.attn_fwd(q, k, v, o=o, lse=lse)
+    dq, dk, dv = (t[guard:guard + n].view(s) for t, n, s in
+                  ((dqb, nq, q.shape), (dkb, nk, k.shape), (dvb, nk, k.shape)))
+    nb.attn_bwd(q, k, v, o, lse, do, grad_dtype=torch.bfloat16, dq=dq, dk=dk, dv=dv)
+    nb.check_status()
+    for cur, old, n in zip((ob, lb, dqb, dkb, dvb), snap, (nq, nl, nq, nk, nk)):
+        for part in (slice(0, guard), slice(guard + n, None)):
+            a, b = cur[part], old[part]
+            if a.dtype == torch.float32:
+                assert torch.isnan(a).all()
+            else:
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        assert torch.isfinite(cur[guard:guard + n].float()).all()
+
+
+def test_host_buffer_entry_point(nb, oracle_mod):
+    """The end-to-end call on host tensors matches the oracle too."""
+    shape = (2, 300, 4, 2, 32)
+    x = H.make(*shape, seed=21)
+    hb = [torch.from_numpy(x[n + "_bits"].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+          for n in ("q", "k", "v", "dout")]
+    o, lse, dq, dk, dv = nb.fwd_bwd_host(*hb, grad_dtype=torch.float32)
+    gpu = dict(o=H.to_f64(o), lse=lse.numpy().astype(np.float64), dq=H.to_f64(dq), dk=H.to_f64(dk),
+               dv=H.to_f64(dv))
+    compare(oracle_mod, x, gpu, shape, None)
+
+
+def test_device_timeout_is_reported(nb):
+    """A wait that nothing completes gives up after its limit and reports
+    NE_ERR_DEVICE_TIMEOUT; the context stays usable afterwards."""
+    assert nb.status_of_last_kernels() == 0
+    nb.debug_timeout_probe(2000)
+    assert nb.status_of_last_kernels() == -6
+    assert nb.status_of_last_kernels() == 0  # cleared
+    x = H.make(1, 64, 2, 1, 64, seed=1)
+    run_gpu(nb, x)  # still works
+
+
+def test_bad_arguments_rejected(nb):
+    q = torch.zeros((1, 16, 2, 64), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((1, 16, 1, 64), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((1, 2, 16), dtype=torch.float32, device="cuda")
+    L = nb.lib()
+    s = None
+    p = lambda t: t.data_ptr()
+    assert L.ne_attn_fwd(p(q), p(k), p(k), p(q), p(lse), 1, 16, 2, 1, 48, 10000.0, s) == -3
+    assert L.ne_attn_fwd(p(q) + 2, p(k), p(k), p(q), p(lse), 1, 16, 2, 1, 64, 10000.0, s) == -2
+    assert L.ne_attn_fwd(p(q), p(k), p(k), p(q), p(lse), 1, 16, 3, 2, 64, 10000.0, s) == -1
+    assert L.ne_attn_bwd(p(q), p(k), p(k), p(q), p(lse), p(q), p(q), p(k), p(k), 1, 16, 2, 1, 64,
+                         10000.0, 0, None, 0, s) == -5

@@ -1,0 +1,365 @@
+#!/usr/bin/env python
+"""Throughput of causal GQA attention forward + backward (RoPE on Q/K) on GB300.
+
+One step = ne_attn_fwd + ne_attn_bwd over one batch of the 116M-model
+attention shape (B=16, T=512, Hq=12, Hkv=4, D=64; synthetic N(0,1) bf16
+inputs, seeded).  The metric is algorithmic TFLOP/s: 14 * B * Hq * D *
+T(T+1)/2 matmul flops per fwd+bwd (QK^T and PV forward; recomputed QK^T,
+dP, dV, dK, dQ backward), over the device time of the step.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+With N > 1 (launched by torchrun, one process per GPU) every rank runs its
+own replica of the workload (the attention has no exchange step) and the
+value is the total over ranks divided by the slowest rank's time.
+--impl reference times the fp64 CPU oracle on the host cores instead.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from causal_gqa_attention_flashattention_gb300 import inputs  # noqa: E402
+
+METRIC = "causal GQA attn fwd+bwd TFLOP/s on 1 GB300 (% of bf16 tensor peak)"
+UNIT = "TFLOP/s"
+WORKLOAD = "gpu_116m_model"
+NUM_SETS = 4  # rotating input/output sets so consecutive steps do not hit a warm L2
+
+
+def algo_flops(B, T, Hq, D):
+    pairs = T * (T + 1) / 2.0
+    return dict(fwd=4.0 * B * Hq * D * pairs, bwd=10.0 * B * Hq * D * pairs, total=14.0 * B * Hq * D * pairs)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(bf16_tflops=float(p["bf16_tflops"]), bf16_tflops_sustained=float(p["bf16_tflops_sustained"]),
+                    hbm_gbs=float(p["hbm_gbs"]), source="measured")
+    except Exception:
+        return dict(bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, hbm_gbs=6800.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed loop runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        loaded = [x for x in sm if mx and x >= 0.5 * max(mx)] or sm
+        return dict(sm_mhz=statistics.median(loaded) if loaded else None, sm_max_mhz=max(mx) if mx else None,
+                    reasons=reasons, samples=len(rows))
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def traffic_record(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source as it stands now (hash match); else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except Exception:
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "causal_gqa_attention_flashattention_gb300", "csrc", rec["source"])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if h != rec.get("source_sha256_16"):
+        return None
+    return rec
+
+
+def cpu_oracle_sample(budget_s, shape, x):
+    """Times the fp64 oracle (fwd + bwd) on whole (batch, kv-head) groups of the
+    workload until about budget_s seconds of CPU work have been done."""
+    import oracle
+    B, T, Hq, Hkv, D = shape
+    order = [(b, g) for b in range(B) for g in range(Hkv)]
+    t0 = time.perf_counter()
+    oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], inputs.ROPE_BASE, groups=order[:1])
+    one = time.perf_counter() - t0
+    n = max(1, min(len(order), int(budget_s / max(one, 1e-3))))
+    groups = order[:n]
+    t0 = time.perf_counter()
+    oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], inputs.ROPE_BASE, groups=groups)
+    dt = time.perf_counter() - t0
+    G = Hq // Hkv
+    fl = algo_flops(1, T, G, D)["total"] * n
+    return dict(value=fl / dt / 1e12, unit=UNIT, cores=oracle.num_threads(), kind="oracle",
+                sample="%d of %d (batch, kv-head) groups of %s (fp64 fwd+bwd, %.1f s)" % (n, len(order), WORKLOAD, dt),
+                seconds=dt)
+
+
+def run_reference(args, world, rank):
+    """The fp64 CPU oracle on this host's cores, same metric and workload."""
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    shape = tuple(inputs.WORKLOADS[WORKLOAD][:5])
+    B, T, Hq, Hkv, D = shape
+    x = inputs.make_workload_inputs(WORKLOAD)
+    G = Hq // Hkv
+    order = [(b, g) for b in range(B) for g in range(Hkv)]
+    # size each step so the whole run stays within about two minutes
+    t0 = time.perf_counter()
+    oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], inputs.ROPE_BASE, groups=order[:1])
+    one = time.perf_counter() - t0
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    n = max(1, min(len(order), int(per_step_budget / max(one, 1e-3))))
+    for i in range(args.warmup):
+        oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], inputs.ROPE_BASE, groups=order[:n])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], inputs.ROPE_BASE, groups=order[:n])
+    dt = time.perf_counter() - t0
+    fl = algo_flops(1, T, G, D)["total"] * n
+    value = fl * args.steps / dt / 1e12
+    sample = "%d of %d (batch, kv-head) groups of %s per step (fp64 fwd+bwd)" % (n, len(order), WORKLOAD)
+    line = dict(impl="reference", metric=METRIC, value=value, unit=UNIT, n_gpus=args.gpus, steps=args.steps,
+                warmup=args.warmup, ms_per_step=dt * 1e3 / args.steps, higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype="f64", data="synthetic",
+                config=dict(workload=WORKLOAD, B=B, T=T, Hq=Hq, Hkv=Hkv, D=D, rope_base=inputs.ROPE_BASE),
+                cpu_baseline=dict(value=value, unit=UNIT, cores=oracle.num_threads(), kind="oracle", sample=sample),
+                e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    from causal_gqa_attention_flashattention_gb300 import binding
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    shape = tuple(inputs.WORKLOADS[WORKLOAD][:5])
+    B, T, Hq, Hkv, D = shape
+    fl = algo_flops(B, T, Hq, D)
+    x = inputs.make_workload_inputs(WORKLOAD)
+    base = inputs.ROPE_BASE
+    grad_dtype = torch.float32
+
+    def host_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).view(torch.bfloat16)
+
+    hq, hk, hv, hdo = (host_bf16(x[n + "_bits"]) for n in ("q", "k", "v", "dout"))
+    sets = []
+    for _ in range(NUM_SETS):
+        q, k, v, do = (t.to(dev) for t in (hq, hk, hv, hdo))
+        sets.append(dict(q=q, k=k, v=v, do=do, o=torch.empty_like(q),
+                         lse=torch.empty((B, Hq, T), dtype=torch.float32, device=dev),
+                         dq=torch.empty(q.shape, dtype=grad_dtype, device=dev),
+                         dk=torch.empty(k.shape, dtype=grad_dtype, device=dev),
+                         dv=torch.empty(k.shape, dtype=grad_dtype, device=dev),
+                         ws=binding.alloc_workspace(B, T, Hq, Hkv, D, device=dev)))
+    set_bytes = sum(t.numel() * t.element_size() for t in sets[0].values())
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        s = sets[i % NUM_SETS]
+        binding.attn_fwd(s["q"], s["k"], s["v"], base, o=s["o"], lse=s["lse"], stream=stream)
+        binding.attn_bwd(s["q"], s["k"], s["v"], s["o"], s["lse"], s["do"], base, grad_dtype=grad_dtype,
+                         dq=s["dq"], dk=s["dk"], dv=s["dv"], workspace=s["ws"], stream=stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for i in range(args.warmup):
+        step(i)
+    binding.check_status(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    binding.profile_start(4 * args.steps + 16)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    prof = binding.profile_stop()
+    clk = clocks.stop()
+    binding.check_status(stream)
+    ms_total = e0.elapsed_time(e1)
+    barrier()
+    ms_max = ms_total
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    ms_step = ms_max / args.steps
+    value = world * fl["total"] / (ms_step * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, results out, every step
+    e2e_steps = max(3, min(args.steps, 200))
+    pin = [t.pin_memory() for t in (hq, hk, hv, hdo)]
+    s0 = sets[0]
+    outs = dict(o=torch.empty(s0["o"].shape, dtype=s0["o"].dtype).pin_memory(),
+                lse=torch.empty(s0["lse"].shape, dtype=torch.float32).pin_memory(),
+                dq=torch.empty(s0["dq"].shape, dtype=grad_dtype).pin_memory(),
+                dk=torch.empty(s0["dk"].shape, dtype=grad_dtype).pin_memory(),
+                dv=torch.empty(s0["dv"].shape, dtype=grad_dtype).pin_memory())
+
+    def e2e_step(i):
+        s = sets[i % NUM_SETS]
+        for src, name in zip(pin, ("q", "k", "v", "do")):
+            s[name].copy_(src, non_blocking=True)
+        step(i)
+        for name, dst in outs.items():
+            dst.copy_(s[name], non_blocking=True)
+
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in pin)
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+
+    if rank != 0:
+        return 0
+    peaks = load_peaks()
+    # dominant kernel of the step
+    dom = max(prof, key=lambda k: prof[k][0])
+    ms_dom, n_dom = prof[dom]
+    per_launch_ms = ms_dom / max(1, n_dom)
+    pairs = T * (T + 1) / 2.0
+    if dom in ("fwd", "bwd_dkdv"):
+        work = (4.0 if dom == "fwd" else 10.0) * B * Hq * D * pairs
+        achieved = work / (per_launch_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = dict(bound="tensor", achieved=achieved, peak=peak, unit="TFLOP/s", frac=achieved / peak)
+    else:
+        work = None
+        roof = dict(bound="hbm", achieved=None, peak=peaks["hbm_gbs"], unit="GB/s", frac=None)
+    tr = traffic_record("k_bwd_dkdv" if dom == "bwd_dkdv" else "k_attn_fwd" if dom == "fwd" else dom)
+    roof.update(kernel=dom, traffic=(tr["dram_bytes_per_launch"] if tr else None),
+                peak_source="%s bf16 burst" % peaks["source"] if roof["bound"] == "tensor" else
+                "%s hbm" % peaks["source"], per_launch_us=per_launch_ms * 1e3,
+                kernels={k: dict(us_per_launch=(v[0] / v[1] * 1e3 if v[1] else None), launches=v[1])
+                         for k, v in prof.items()})
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(args.cpu_seconds, shape, x)
+        cpu.pop("seconds", None)
+    line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
+                ms_per_step=ms_step, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
+                data="synthetic",
+                config=dict(workload=WORKLOAD, B=B, T=T, Hq=Hq, Hkv=Hkv, D=D, rope_base=base,
+                            gflop_per_step=fl["total"] / 1e9,
+                            precision="fp16 rotated q/k, bf16 P/V/dO, fp32 accumulate, bf16 o, fp32 dq/dk/dv",
+                            l2="%d rotating buffer sets of %.0f MB (%.0f MB > L2)" % (
+                                NUM_SETS, set_bytes / 1e6, NUM_SETS * set_bytes / 1e6),
+                            parallelism="replicas" if world > 1 else "single GPU"),
+                pct_of_bf16_peak=100.0 * value / world / peaks["bf16_tflops"],
+                roofline=roof, cpu_baseline=cpu,
+                e2e=dict(value=world * fl["total"] / (e2e_ms * 1e-3) / 1e12, unit=UNIT, h2d_bytes_per_step=h2d,
+                         d2h_bytes_per_step=d2h),
+                gpu_launches=int(sum(v[1] for v in prof.values())),
+                clocks=clk)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -49,6 +49,10 @@ def lib():
         L.ne_attn_status_string.restype = ctypes.c_char_p
         L.ne_attn_debug_timeout_probe.argtypes = [i, vp]
         L.ne_attn_debug_timeout_probe.restype = i
+        L.ne_attn_profile_start.argtypes = [i]
+        L.ne_attn_profile_start.restype = i
+        L.ne_attn_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]
+        L.ne_attn_profile_stop.restype = i
         _lib = L
     return _lib
 
@@ -84,7 +88,10 @@ def attn_fwd(q, k, v, rope_base=10000.0, o=None, lse=None, o_dtype=torch.bfloat1
     if o is None:
         o = torch.empty(q.shape, dtype=o_dtype, device=q.device)
     if lse is None:
-        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+        # precise mode stores the LSE and its fp32 remainder: lse[0] is the LSE
+        shape = (2, B, Hq, T) if precise else (B, Hq, T)
+        lse = torch.empty(shape, dtype=torch.float32, device=q.device)
+    assert lse.numel() == (2 if precise else 1) * B * Hq * T
     for t in (q, k, v):
         assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous()
     assert o.dtype in (torch.bfloat16, torch.float32) and o.is_contiguous()
@@ -127,6 +134,7 @@ def attn_bwd(q, k, v, o, lse, dout, rope_base=10000.0, grad_dtype=torch.bfloat16
     for t in (q, k, v, dout):
         assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous()
     assert o.dtype in (torch.bfloat16, torch.float32) and o.is_contiguous()
+    assert lse.dtype == torch.float32 and lse.numel() == (2 if precise else 1) * B * Hq * T
     for t in (dq, dk, dv):
         assert t.dtype == grad_dtype and t.is_contiguous()
     flags = ((O_FP32 if o.dtype == torch.float32 else 0) | (GRAD_FP32 if grad_dtype == torch.float32 else 0)
@@ -145,6 +153,22 @@ def check_status(stream=None):
 def status_of_last_kernels(stream=None):
     """Like check_status but returns the raw status code (and clears it)."""
     return int(lib().ne_attn_check_status(_stream(stream)))
+
+
+KERNEL_KINDS = ("fwd", "bwd_prep", "bwd_dkdv", "bwd_dq")
+
+
+def profile_start(capacity):
+    """Brackets each library kernel launch with CUDA events (see ne_attn_profile_start)."""
+    _check("ne_attn_profile_start", lib().ne_attn_profile_start(int(capacity)))
+
+
+def profile_stop():
+    """Returns {kernel kind: (total device ms, launches)} for the launches since profile_start."""
+    ms = (ctypes.c_double * len(KERNEL_KINDS))()
+    n = (ctypes.c_longlong * len(KERNEL_KINDS))()
+    _check("ne_attn_profile_stop", lib().ne_attn_profile_stop(ms, n))
+    return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(KERNEL_KINDS)}
 
 
 def debug_timeout_probe(limit_us, stream=None):

@@ -188,7 +188,7 @@ int heads_per_cta(int G, int D, bool precise) {
 }
 
 struct WsLayout {
-  size_t qr, kr, qlo, klo, lse2, delta, dqacc, total;
+  size_t qr, kr, qlo, klo, lse2, lse2_lo, delta, dqacc, total;
 };
 
 WsLayout ws_layout(int B, int T, int Hq, int Hkv, int D, bool precise) {
@@ -211,6 +211,11 @@ WsLayout ws_layout(int B, int T, int Hq, int Hkv, int D, bool precise) {
   }
   w.lse2 = off;
   off += up(sizeof(float) * (size_t)B * Hq * Tp);
+  w.lse2_lo = 0;
+  if (precise) {
+    w.lse2_lo = off;
+    off += up(sizeof(float) * (size_t)B * Hq * Tp);
+  }
   w.delta = off;
   off += up(sizeof(float) * (size_t)B * Hq * Tp);
   w.total = off;
@@ -218,6 +223,47 @@ WsLayout ws_layout(int B, int T, int Hq, int Hkv, int D, bool precise) {
 }
 
 constexpr int kKnownFlags = kFlagOFp32 | kFlagGradFp32 | kFlagPreciseQK;
+
+// ------------------------------------------------------------------ kernel timing
+struct Profile {
+  bool on = false;
+  int capacity = 0;
+  int used = 0;
+  std::vector<cudaEvent_t> ev;  // 2 * capacity
+  std::vector<int> kind;        // per timed launch
+  long long launches[NE_ATTN_NUM_KERNEL_KINDS] = {0, 0, 0, 0};
+};
+std::mutex g_prof_mu;
+Profile g_prof;
+
+void prof_reset() {
+  for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
+  g_prof = Profile();
+}
+
+// Records the start event of a launch of `kind`; returns the slot (or -1).
+int prof_begin(int kind, cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (!g_prof.on) return -1;
+  g_prof.launches[kind]++;
+  if (g_prof.used >= g_prof.capacity) return -1;
+  const int slot = g_prof.used++;
+  g_prof.kind[slot] = kind;
+  cudaEventRecord(g_prof.ev[2 * slot], s);
+  return slot;
+}
+void prof_end(int slot, cudaStream_t s) {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (g_prof.on && slot < g_prof.used) cudaEventRecord(g_prof.ev[2 * slot + 1], s);
+}
+
+struct ProfScope {
+  int slot;
+  cudaStream_t s;
+  ProfScope(int kind, cudaStream_t st) : slot(prof_begin(kind, st)), s(st) {}
+  ~ProfScope() { prof_end(slot, s); }
+};
 
 }  // namespace
 }  // namespace ne
@@ -259,7 +305,11 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
   a.G = Hq / Hkv;
   a.HC = heads_per_cta(a.G, D, precise);
   a.o_fp32 = (flags & kFlagOFp32) ? 1 : 0;
-  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  const double sl2 = 1.4426950408889634 / std::sqrt((double)D);
+  a.scale_log2 = (float)sl2;
+  a.scale_log2_lo = (float)(sl2 - (double)a.scale_log2);
+  a.lse_lo = precise ? lse + (size_t)B * Hq * T : nullptr;
+  ProfScope prof(NE_ATTN_KERNEL_FWD, s);
   return launch_fwd(a, precise, s) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
 }
 
@@ -306,6 +356,7 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   __half* qlo = precise ? reinterpret_cast<__half*>(ws + w.qlo) : nullptr;
   __half* klo = precise ? reinterpret_cast<__half*>(ws + w.klo) : nullptr;
   float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  float* lse2_lo = precise ? reinterpret_cast<float*>(ws + w.lse2_lo) : nullptr;
   float* delta = reinterpret_cast<float*>(ws + w.delta);
   const double scale = 1.0 / std::sqrt((double)D);
 
@@ -316,6 +367,8 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   p.o_fp32 = (flags & kFlagOFp32) ? 1 : 0;
   p.dout = static_cast<const __nv_bfloat16*>(dout);
   p.lse = lse;
+  p.lse_lo = precise ? lse + (size_t)B * Hq * T : nullptr;
+  p.lse2_lo = lse2_lo;
   p.qr = qr;
   p.kr = kr;
   p.qlo = qlo;
@@ -330,7 +383,10 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   p.Hkv = Hkv;
   p.D = D;
   p.Tp = Tp;
-  if (launch_bwd_prep(p, s) != cudaSuccess) return NE_ERR_CUDA;
+  {
+    ProfScope prof(NE_ATTN_KERNEL_BWD_PREP, s);
+    if (launch_bwd_prep(p, s) != cudaSuccess) return NE_ERR_CUDA;
+  }
 
   BwdArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -345,6 +401,7 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   }
   if ((st = make_map_acc(&a.map_dqacc, dqacc, (long long)B * Hq * Tp, D)) != NE_OK) return st;
   a.lse2 = lse2;
+  a.lse2_lo = lse2_lo;
   a.delta = delta;
   a.dk = dk;
   a.dv = dv;
@@ -360,8 +417,12 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   a.Tp = Tp;
   a.grad_fp32 = grad_fp32;
   a.scale_log2 = (float)(1.4426950408889634 * scale);
+  a.scale_log2_lo = (float)(1.4426950408889634 * scale - (double)a.scale_log2);
   a.scale = (float)scale;
-  if (launch_bwd_dkdv(a, precise, s) != cudaSuccess) return NE_ERR_CUDA;
+  {
+    ProfScope prof(NE_ATTN_KERNEL_BWD_DKDV, s);
+    if (launch_bwd_dkdv(a, precise, s) != cudaSuccess) return NE_ERR_CUDA;
+  }
 
   DqArgs qa;
   qa.dqacc = dqacc;
@@ -374,7 +435,10 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   qa.Tp = Tp;
   qa.grad_fp32 = grad_fp32;
   qa.scale = (float)scale;
-  if (launch_bwd_dq(qa, s) != cudaSuccess) return NE_ERR_CUDA;
+  {
+    ProfScope prof(NE_ATTN_KERNEL_BWD_DQ, s);
+    if (launch_bwd_dq(qa, s) != cudaSuccess) return NE_ERR_CUDA;
+  }
   return NE_OK;
 }
 
@@ -406,6 +470,46 @@ const char* ne_attn_status_string(int status) {
     case NE_ERR_DEVICE_TIMEOUT: return "a kernel pipeline wait timed out on the device";
     default: return "unknown status";
   }
+}
+
+int ne_attn_profile_start(int capacity) {
+  if (capacity < 0 || capacity > (1 << 22)) return NE_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  prof_reset();
+  g_prof.ev.resize(2 * (size_t)capacity);
+  g_prof.kind.resize(capacity);
+  for (size_t i = 0; i < g_prof.ev.size(); i++) {
+    if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) {
+      g_prof.ev.resize(i);
+      prof_reset();
+      return NE_ERR_CUDA;
+    }
+  }
+  g_prof.capacity = capacity;
+  g_prof.on = true;
+  return NE_OK;
+}
+
+int ne_attn_profile_stop(double* total_ms, long long* launches) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (!g_prof.on) return NE_ERR_ARG;
+  int st = NE_OK;
+  double tot[NE_ATTN_NUM_KERNEL_KINDS] = {0, 0, 0, 0};
+  for (int i = 0; i < g_prof.used; i++) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess) {
+      st = NE_ERR_CUDA;
+      continue;
+    }
+    tot[g_prof.kind[i]] += ms;
+  }
+  for (int k = 0; k < NE_ATTN_NUM_KERNEL_KINDS; k++) {
+    if (total_ms) total_ms[k] = tot[k];
+    if (launches) launches[k] = g_prof.launches[k];
+  }
+  prof_reset();
+  return st;
 }
 
 int ne_attn_debug_timeout_probe(int limit_us, void* stream) {

@@ -92,7 +92,16 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
       const int t = (int)(bt % a.T), b = (int)(bt / a.T);
       const size_t o = ((size_t)b * a.Hq + h) * a.Tp + t;
       a.delta[o] = part;
-      a.lse2[o] = a.lse[((size_t)b * a.Hq + h) * a.T + t] * 1.4426950408889634f;
+      const size_t li = ((size_t)b * a.Hq + h) * a.T + t;
+      if (a.lse_lo) {
+        // (hi + lo) * log2(e) as a two-part value, with a two-part log2(e).
+        const float hi = a.lse[li], lo = a.lse_lo[li];
+        const float h2 = __fmul_rn(hi, kLog2eHi);
+        a.lse2[o] = h2;
+        a.lse2_lo[o] = fmaf(hi, kLog2eHi, -h2) + hi * kLog2eLo + lo * kLog2eHi;
+      } else {
+        a.lse2[o] = a.lse[li] * 1.4426950408889634f;
+      }
     }
   }
   (void)lane;
@@ -124,6 +133,7 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
     const int t = a.T + (int)(it % npad);
     a.delta[bh * a.Tp + t] = 0.f;
     a.lse2[bh * a.Tp + t] = __int_as_float(0x7f800000);
+    if (a.lse2_lo) a.lse2_lo[bh * a.Tp + t] = 0.f;
   }
 }
 
@@ -169,11 +179,16 @@ struct BwdCfg {
   static constexpr uint32_t kSpan = D * 2;
   static constexpr uint32_t kSwz = D == 64 ? kSw128 : kSw64;
   static constexpr uint32_t kSBO = 8 * kSpan;
-  static constexpr int kStages = 2;
+  // PRECISE runs the steps one after another (one stage, one dS and one dQ
+  // buffer): its extra operands (remainder tiles, dS lo, P lo) fill the
+  // shared and tensor memory the overlap would need.
+  static constexpr int kStages = PRECISE ? 1 : 2;
   static constexpr int kLo = PRECISE ? 1 : 0;
-  static constexpr int kDsBufs = (PRECISE && D == 64) ? 1 : 2;  // shared-memory budget
+  static constexpr int kDsBufs = PRECISE ? 1 : 2;
+  static constexpr int kDqBufs = PRECISE ? 1 : 2;
   static constexpr int kVecBytes = kTile * 4;  // lse2 / Delta slice of one tile
   static constexpr int kDsBytes = kTile * kTile * 2;
+  static constexpr int kDsParts = PRECISE ? 2 : 1;  // hi (+ lo) fp16 parts of dS
   static constexpr int kStgBytes = kTile * D * 4;
   static constexpr int kOffK = 0;
   static constexpr int kOffKlo = kOffK + kTileBytes;
@@ -182,17 +197,20 @@ struct BwdCfg {
   static constexpr int kOffQlo = kOffQ + kStages * kTileBytes;
   static constexpr int kOffDO = kOffQlo + kLo * kStages * kTileBytes;
   static constexpr int kOffDS = kOffDO + kStages * kTileBytes;
-  static constexpr int kOffStg = kOffDS + kDsBufs * kDsBytes;
+  static constexpr int kOffStg = kOffDS + kDsBufs * kDsParts * kDsBytes;
   static constexpr int kOffLse = kOffStg + kStgBytes;
-  static constexpr int kOffDel = kOffLse + kStages * kVecBytes;
+  static constexpr int kOffLlo = kOffLse + kStages * kVecBytes;  // lse2 remainder (PRECISE)
+  static constexpr int kOffDel = kOffLlo + kLo * kStages * kVecBytes;
   static constexpr int kOffBar = kOffDel + kStages * kVecBytes;
   static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2 * 2 + 2 * 2 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-  // tensor memory columns
+  // tensor memory columns: S^T/P^T, dP^T, dV, dK, dQ buffers, P^T lo (PRECISE)
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D, kColDQ = 256 + 2 * D;
+  static constexpr uint32_t kColPlo = kColDQ + kDqBufs * D;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kColPlo + (PRECISE ? 64 : 0) <= kTmemCols, "tensor memory budget");
 };
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
@@ -220,6 +238,16 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, const vo
       : "memory");
 }
 
+// Writes 32 fp16 values (packed pairs w[0..15]) for queries c*32..c*32+31 of
+// key row r into a dS^T tile: two 16 KB atoms of 64 queries, 128-byte swizzle.
+__device__ __forceinline__ void store_ds_chunk(uint8_t* ds, int r, int c, const uint32_t (&w)[16]) {
+  uint8_t* atom = ds + (c >> 1) * 16384;
+#pragma unroll
+  for (int q4 = 0; q4 < 4; q4++)
+    *reinterpret_cast<uint4*>(atom + swz(r, (c & 1) * 4 + q4, 128)) =
+        make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+}
+
 template <int D, bool PRECISE>
 __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D, PRECISE>;
@@ -234,10 +262,10 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
   uint64_t* p_ready = s_full + 1;
   uint64_t* dp_full = p_ready + 1;
   uint64_t* acc_done = dp_full + 1;
-  uint64_t* ds_ready = acc_done + 1;  // [2]
-  uint64_t* ds_free = ds_ready + 2;   // [2]
-  uint64_t* dq_full = ds_free + 2;    // [2]
-  uint64_t* dq_free = dq_full + 2;    // [2]
+  uint64_t* ds_ready = acc_done + 1;  // [kDsBufs]
+  uint64_t* ds_free = ds_ready + 2;   // [kDsBufs]
+  uint64_t* dq_full = ds_free + 2;    // [kDqBufs]
+  uint64_t* dq_free = dq_full + 2;    // [kDqBufs]
   uint64_t* drain = dq_free + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -299,12 +327,13 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
         }
         const int i = j + n / G, h = kvh * G + n % G;
         const size_t vec = ((size_t)b * a.Hq + h) * a.Tp + (size_t)i * kTile;
-        mbar_arrive_expect_tx(qd_full + st, (2 + C::kLo) * C::kTileBytes + 2 * C::kVecBytes);
+        mbar_arrive_expect_tx(qd_full + st, (2 + C::kLo) * C::kTileBytes + (2 + C::kLo) * C::kVecBytes);
         tma_load_4d(smem + C::kOffQ + st * C::kTileBytes, &a.map_qr, qd_full + st, 0, h, i * kTile, b);
         if (PRECISE)
           tma_load_4d(smem + C::kOffQlo + st * C::kTileBytes, &a.map_qlo, qd_full + st, 0, h, i * kTile, b);
         tma_load_4d(smem + C::kOffDO + st * C::kTileBytes, &a.map_do, qd_full + st, 0, h, i * kTile, b);
         bulk_load(smem + C::kOffLse + st * C::kVecBytes, a.lse2 + vec, C::kVecBytes, qd_full + st);
+        if (PRECISE) bulk_load(smem + C::kOffLlo + st * C::kVecBytes, a.lse2_lo + vec, C::kVecBytes, qd_full + st);
         bulk_load(smem + C::kOffDel + st * C::kVecBytes, a.delta + vec, C::kVecBytes, qd_full + st);
         loaded = n + 1;
       }
@@ -334,6 +363,19 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
           issue_kmajor(C::kColS, sK, sQlo + stq * C::kTileBytes, idS, 1);
         }
       };
+      // dK += dS^T Q (A = dS^T tile read K-major), dQ = dS K (A = dS^T tile read MN-major)
+      auto issue_dk = [&](uint32_t ds, uint32_t qsm, uint32_t acc) {
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ks++)
+          mma_ss(tmem + C::kColDK, smem_desc(ds + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024, kSw128),
+                 smem_desc(qsm + ks * 16 * C::kSpan, 16, C::kSBO, C::kSwz), idDK, (acc || ks > 0) ? 1u : 0u);
+      };
+      auto issue_dq = [&](uint32_t col, uint32_t ds, uint32_t ksm, uint32_t acc) {
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ks++)
+          mma_ss(tmem + col, smem_desc(ds + ks * 2048, 16384, 1024, kSw128),
+                 smem_desc(ksm + ks * 16 * C::kSpan, 16, C::kSBO, C::kSwz), idDQ, (acc || ks > 0) ? 1u : 0u);
+      };
       bool ok = mbar_wait(kv_full, 0, abort) && mbar_wait(qd_full, 0, abort);
       tc_fence_after();
       if (ok) {
@@ -345,43 +387,60 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
       for (int n = 0; ok && n < N; n++) {
         const int st = n % C::kStages;
         const uint32_t q_s = sQ + st * C::kTileBytes, do_s = sDO + st * C::kTileBytes;
-        // dV += P^T dO   (A = P^T in TMEM, B = dO MN-major)
+        // dV += P^T dO   (A = P^T in TMEM: hi, and lo when PRECISE; B = dO MN-major)
         if (!(ok = mbar_wait(p_ready, n & 1, abort))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ks++)
           mma_ts(tmem + C::kColDV, tmem + C::kColS + ks * 8,
                  smem_desc(do_s + ks * 16 * C::kSpan, 16, C::kSBO, C::kSwz), idDV, (n > 0 || ks > 0) ? 1u : 0u);
-        // next S^T (its TMEM region was just read by the dV MMAs issued above)
+        if (PRECISE) {
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ks++)
+            mma_ts(tmem + C::kColDV, tmem + C::kColPlo + ks * 8,
+                   smem_desc(do_s + ks * 16 * C::kSpan, 16, C::kSBO, C::kSwz), idDV, 1u);
+        }
+        // Overlapped order: the next S^T goes in right after the dV MMAs that
+        // read this step's P^T from the same columns.
         const int st1 = (n + 1) % C::kStages;
-        if (n + 1 < N) {
+        if (!PRECISE && n + 1 < N) {
           if (!(ok = mbar_wait(qd_full + st1, ((n + 1) / C::kStages) & 1, abort))) break;
           tc_fence_after();
           issue_s(st1);
           mma_commit(s_full);
         }
-        // dK += dS^T Q^  and  dQ_tile = dS K^
-        const int dsb = n % C::kDsBufs, qb = n & 1;
-        const uint32_t ds = sDS + dsb * C::kDsBytes;
+        const int dsb = n % C::kDsBufs, qb = n % C::kDqBufs;
+        const uint32_t ds = sDS + dsb * C::kDsParts * C::kDsBytes;
         if (!(ok = mbar_wait(ds_ready + dsb, (n / C::kDsBufs) & 1, abort))) break;
         tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < kTile / 16; ks++)
-          mma_ss(tmem + C::kColDK, smem_desc(ds + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024, kSw128),
-                 smem_desc(q_s + ks * 16 * C::kSpan, 16, C::kSBO, C::kSwz), idDK, (n > 0 || ks > 0) ? 1u : 0u);
-        if (n >= 2) {
-          if (!(ok = mbar_wait(dq_free + qb, ((n - 2) >> 1) & 1, abort))) break;
+        issue_dk(ds, q_s, n > 0);
+        if (PRECISE) {
+          issue_dk(ds + C::kDsBytes, q_s, 1);                          // dS lo x Q hi
+          issue_dk(ds, sQlo + st * C::kTileBytes, 1);                  // dS hi x Q lo
+        }
+        if (n >= C::kDqBufs) {
+          if (!(ok = mbar_wait(dq_free + qb, ((n - C::kDqBufs) / C::kDqBufs) & 1, abort))) break;
           tc_fence_after();
         }
-#pragma unroll
-        for (int ks = 0; ks < kTile / 16; ks++)
-          mma_ss(tmem + C::kColDQ + qb * D, smem_desc(ds + ks * 2048, 16384, 1024, kSw128),
-                 smem_desc(sK + ks * 16 * C::kSpan, 16, C::kSBO, C::kSwz), idDQ, ks > 0 ? 1u : 0u);
+        const uint32_t dqcol = C::kColDQ + qb * D;
+        issue_dq(dqcol, ds, sK, 0);
+        if (PRECISE) {
+          issue_dq(dqcol, ds + C::kDsBytes, sK, 1);                    // dS lo x K hi
+          issue_dq(dqcol, ds, sKlo, 1);                                // dS hi x K lo
+        }
         mma_commit(dq_full + qb);
         mma_commit(ds_free + dsb);
         mma_commit(qd_empty + st);
-        // next dP^T (the compute warps finished reading dP^T before signalling ds_ready)
         if (n + 1 < N) {
+          if (PRECISE) {
+            // Serial order: this step's P^T (read back by the compute warps
+            // for dS) stays in TMEM until ds_ready, so S^T waits until here.
+            if (!(ok = mbar_wait(qd_full + st1, ((n + 1) / C::kStages) & 1, abort))) break;
+            tc_fence_after();
+            issue_s(st1);
+            mma_commit(s_full);
+          }
+          // next dP^T (the compute warps finished reading dP^T before signalling ds_ready)
           issue_kmajor(C::kColDP, sV, sDO + st1 * C::kTileBytes, idDP, 0);
           mma_commit(dp_full);
         }
@@ -402,30 +461,40 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
       const int i = j + n / G;
       const bool diag = (i == j);
       const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffLse + st * C::kVecBytes);
+      const float* lse2lo = reinterpret_cast<const float*>(smem + C::kOffLlo + st * C::kVecBytes);
       const float* del = reinterpret_cast<const float*>(smem + C::kOffDel + st * C::kVecBytes);
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full, n & 1, abort)))) break;
       tc_fence_after();
-      uint32_t pk[kTile / 2];  // P^T row as packed bf16 pairs
+      uint32_t pk[PRECISE ? 1 : kTile / 2];  // P^T row as packed bf16 pairs (default mode)
 #pragma unroll
       for (int c = 0; c < kTile / 32; c++) {
         uint32_t u[32];
         tmem_ld32(trow + C::kColS + c * 32, u);
         tmem_wait_ld();
+        uint32_t w[16], wl[16];
 #pragma unroll
         for (int e = 0; e < 16; e++) {
           const int q0 = c * 32 + 2 * e;
-          float p0 = ex2(fmaf(__uint_as_float(u[2 * e]), sl2, -lse2[q0]));
-          float p1 = ex2(fmaf(__uint_as_float(u[2 * e + 1]), sl2, -lse2[q0 + 1]));
+          const float s0 = __uint_as_float(u[2 * e]), s1 = __uint_as_float(u[2 * e + 1]);
+          float x0 = fmaf(s0, sl2, -lse2[q0]), x1 = fmaf(s1, sl2, -lse2[q0 + 1]);
+          if (PRECISE) {  // logits of 10^3..10^4: add the remainders of scale and LSE
+            x0 += s0 * a.scale_log2_lo - lse2lo[q0];
+            x1 += s1 * a.scale_log2_lo - lse2lo[q0 + 1];
+          }
+          float p0 = ex2(x0);
+          float p1 = ex2(x1);
           if (diag) {
             if (q0 < r) p0 = 0.f;
             if (q0 + 1 < r) p1 = 0.f;
           }
-          pk[c * 16 + e] = pack_bf16(p0, p1);
+          w[e] = pack_bf16(p0, p1);
+          if (PRECISE)
+            wl[e] = pack_bf16(p0 - bf_lo(w[e]), p1 - bf_hi(w[e]));
+          else
+            pk[c * 16 + e] = w[e];
         }
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; e++) w[e] = pk[c * 16 + e];
         tmem_st16(trow + C::kColS + c * 16, w);
+        if (PRECISE) tmem_st16(trow + C::kColPlo + c * 16, wl);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -437,26 +506,37 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
           !(ok = __all_sync(0xffffffffu, mbar_wait(ds_free + dsb, ((n - C::kDsBufs) / C::kDsBufs) & 1, abort))))
         break;
       tc_fence_after();
-      uint8_t* ds = smem + C::kOffDS + dsb * C::kDsBytes;
+      uint8_t* ds = smem + C::kOffDS + dsb * C::kDsParts * C::kDsBytes;
 #pragma unroll
       for (int c = 0; c < kTile / 32; c++) {
         uint32_t u[32];
         tmem_ld32(trow + C::kColDP + c * 32, u);
+        uint32_t ph[16], pl[16];
+        if (PRECISE) {
+          // P^T = hi + lo (bf16 pairs) is still in TMEM: the next S^T is not issued before ds_ready.
+          tmem_ld16(trow + C::kColS + c * 16, ph);
+          tmem_ld16(trow + C::kColPlo + c * 16, pl);
+        }
         tmem_wait_ld();
-        uint32_t w[16];
+        uint32_t w[16], wl[16];
 #pragma unroll
         for (int e = 0; e < 16; e++) {
           const int q0 = c * 32 + 2 * e;
-          const float d0 = (__uint_as_float(u[2 * e]) - del[q0]) * bf_lo(pk[c * 16 + e]);
-          const float d1 = (__uint_as_float(u[2 * e + 1]) - del[q0 + 1]) * bf_hi(pk[c * 16 + e]);
+          float p0, p1;
+          if (PRECISE) {
+            p0 = bf_lo(ph[e]) + bf_lo(pl[e]);
+            p1 = bf_hi(ph[e]) + bf_hi(pl[e]);
+          } else {
+            p0 = bf_lo(pk[c * 16 + e]);
+            p1 = bf_hi(pk[c * 16 + e]);
+          }
+          const float d0 = (__uint_as_float(u[2 * e]) - del[q0]) * p0;
+          const float d1 = (__uint_as_float(u[2 * e + 1]) - del[q0 + 1]) * p1;
           w[e] = pack_f16(d0, d1);
+          if (PRECISE) wl[e] = pack_f16(d0 - f16_lo(w[e]), d1 - f16_hi(w[e]));
         }
-        // queries c*32 .. c*32+31 of key row r: atom c/2, chunks (c%2)*4 .. +3
-        uint8_t* atom = ds + (c >> 1) * 16384;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; q4++)
-          *reinterpret_cast<uint4*>(atom + swz(r, (c & 1) * 4 + q4, 128)) =
-              make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+        store_ds_chunk(ds, r, c, w);
+        if (PRECISE) store_ds_chunk(ds + C::kDsBytes, r, c, wl);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -509,23 +589,23 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
     uint8_t* stg = smem + C::kOffStg;
     bool ok = true;
     for (int n = 0; n < N; n++) {
-      const int db = n & 1;
+      const int qb = n % C::kDqBufs;
       // Every drain thread reaches both named barriers of an iteration; the
       // first one agrees on `ok`, so a timeout in one warp stops all four.
-      const bool got = __all_sync(0xffffffffu, mbar_wait(dq_full + db, (n >> 1) & 1, abort));
+      const bool got = __all_sync(0xffffffffu, mbar_wait(dq_full + qb, (n / C::kDqBufs) & 1, abort));
       uint32_t u[D];
       if (got) {
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; c++) {
           uint32_t v[32];
-          tmem_ld32(trow + C::kColDQ + db * D + c * 32, v);
+          tmem_ld32(trow + C::kColDQ + qb * D + c * 32, v);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; e++) u[c * 32 + e] = v[e];
         }
         tc_fence_before();
-        mbar_arrive(dq_free + db);
+        mbar_arrive(dq_free + qb);
       }
       if (r == 0) bulk_wait_read<0>();  // previous reduction has finished reading the staging tile
       if (!(ok = named_sync_and(1, 128, got))) break;

@@ -24,7 +24,8 @@
 //               the TMEM accumulator (only when the max grows by > 2^8),
 //               exp2, P (bf16) back into TMEM, row sum of the rounded P (so
 //               O is an exact convex combination of V rows with the weights
-//               the MMA used); epilogue O / l (bf16 or fp32) and
+//               the MMA used; with PRECISE, P = hi + lo in two bf16 parts and
+//               O += Phi V + Plo V); epilogue O / l (bf16 or fp32) and
 //               LSE = ln(sum exp).
 // Only the diagonal tile (j == i) is masked; tiles above it are never visited.
 #include <cuda_bf16.h>
@@ -70,26 +71,44 @@ __device__ __forceinline__ void record_timeout(int* status, volatile int* abort)
 
 // Rotates `ntiles` consecutive 128-row tiles in place (positions pos0 + row),
 // writing fp16 results; with `lo` the fp16 remainders go to the same offsets there.
+// Each thread walks 16-byte chunks `nthreads` apart (consecutive threads touch
+// consecutive chunks: conflict-free); the shared-memory chunks and the table
+// entries of a batch of 8 chunks are all loaded before any is rotated, so the
+// table's L2 latency is paid once per batch.
 template <int D>
 __device__ __forceinline__ void rope_tiles(uint8_t* base, uint8_t* lo, int ntiles, int pos0, const float2* tab,
                                            int tid, int nthreads) {
   constexpr uint32_t kSpan = D * 2;
   constexpr int kCPR = D / 8;  // 16-byte chunks per row
+  constexpr int kBatch = 8;
   const int total = ntiles * kTile * kCPR;
-  for (int idx = tid; idx < total; idx += nthreads) {
-    const int row = (idx / kCPR) % kTile;
-    const int pc = idx % kCPR;
-    const uint32_t phys = (uint32_t)idx * 16u;
-    const int lc = (int)((swz(row, pc, kSpan) - row * kSpan) / 16u);  // logical chunk
-    uint4* p = reinterpret_cast<uint4*>(base + phys);
-    float4 a, b;
-    rope_coeffs<D>(tab, pos0 + row, lc, a, b);
-    if (lo) {
-      uint4 l;
-      *p = rope_chunk_f16(*p, a, b, &l);
-      *reinterpret_cast<uint4*>(lo + phys) = l;
-    } else {
-      *p = rope_chunk_f16(*p, a, b, nullptr);
+  for (int first = tid; first < total; first += kBatch * nthreads) {
+    uint4 x[kBatch];
+    float4 ca[kBatch], cb[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; u++) {
+      const int idx = first + u * nthreads;
+      if (idx < total) {
+        const int row = (idx / kCPR) % kTile;
+        const int pc = idx % kCPR;
+        const int lc = (int)((swz(row, pc, kSpan) - row * kSpan) / 16u);  // logical chunk
+        x[u] = *reinterpret_cast<const uint4*>(base + (uint32_t)idx * 16u);
+        rope_coeffs<D>(tab, pos0 + row, lc, ca[u], cb[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; u++) {
+      const int idx = first + u * nthreads;
+      if (idx < total) {
+        const uint32_t phys = (uint32_t)idx * 16u;
+        if (lo) {
+          uint4 l;
+          *reinterpret_cast<uint4*>(base + phys) = rope_chunk_f16(x[u], ca[u], cb[u], &l);
+          *reinterpret_cast<uint4*>(lo + phys) = l;
+        } else {
+          *reinterpret_cast<uint4*>(base + phys) = rope_chunk_f16(x[u], ca[u], cb[u], nullptr);
+        }
+      }
     }
   }
 }
@@ -201,6 +220,12 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
           mma_ts(tmem + hh * D, sP + ks * 8,
                  smem_desc(sV + st * C::kTileBytes + ks * 16 * C::kSpan, 16, C::kSBO, C::kSwz), idPV,
                  (jm > 0 || ks > 0) ? 1u : 0u);
+        if (PRECISE) {  // + P_lo V: the bf16 remainder of P sits in the buffer's upper 64 columns
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ks++)
+            mma_ts(tmem + hh * D, sP + 64 + ks * 8,
+                   smem_desc(sV + st * C::kTileBytes + ks * 16 * C::kSpan, 16, C::kSBO, C::kSwz), idPV, 1u);
+        }
         mma_commit(o_done + hh);
         if (hh == HC - 1) mma_commit(kv_empty + st);
         return true;
@@ -296,23 +321,29 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
           for (int c = 0; c < kTile; c++)
             if (c > r) s[c] = -INFINITY;
         }
-        float mx = s[0];
+        // The row state keeps the raw score r_use that defines the reference
+        // m_use = fp32(r_use * scale_log2); the epilogue needs it for the
+        // double-float LSE.
+        float mxr = s[0];
 #pragma unroll
-        for (int c = 1; c < kTile; c++) mx = fmaxf(mx, s[c]);
-        mx *= sl2;
-        float m_old = j == 0 ? -INFINITY : sm_m[hh * kTile + r];
+        for (int c = 1; c < kTile; c++) mxr = fmaxf(mxr, s[c]);
+        // Every reference value is the correctly rounded product r * scale_log2
+        // (no FMA contraction), so alpha, P and the LSE all use the same m.
+        const float r_old = j == 0 ? -INFINITY : sm_m[hh * kTile + r];
+        const float m_old = __fmul_rn(r_old, sl2);
         float l_old = j == 0 ? 0.f : sm_l[hh * kTile + r];
-        float m_use = m_old, alpha = 1.f;
+        float r_use = r_old, alpha = 1.f;
         if (j == 0) {
-          m_use = mx;
+          r_use = mxr;
         } else {
           // The previous O_h += P V must be complete before O_h is read or rescaled.
           ok = __all_sync(0xffffffffu, mbar_wait(o_done + hh, (j - 1) & 1, abort));
           if (!ok) break;
           tc_fence_after();
-          const float m_new = fmaxf(m_old, mx);
+          const float r_new = fmaxf(r_old, mxr);
+          const float m_new = __fmul_rn(r_new, sl2);
           if (__any_sync(0xffffffffu, m_new > m_old + 8.0f)) {
-            m_use = m_new;
+            r_use = r_new;
             alpha = ex2(m_old - m_new);
 #pragma unroll
             for (int c = 0; c < D / 16; c++) {
@@ -325,23 +356,34 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
             }
           }
         }
+        // Default: P is rounded to bf16 and the row sum adds the rounded values,
+        // so O is the exact average of V rows under the weights the MMA uses.
+        // PRECISE: P = hi + lo (two bf16 parts, ~2^-17 relative) and the row sum
+        // adds the fp32 values, so O and LSE follow the exact softmax.
+        const float m_use = __fmul_rn(r_use, sl2);
         float sum = 0.f;
 #pragma unroll
         for (int c = 0; c < kTile / 32; c++) {
-          uint32_t pk[16];
+          uint32_t pk[16], pl[16];
 #pragma unroll
           for (int e = 0; e < 16; e++) {
             const float p0 = ex2(fmaf(s[c * 32 + 2 * e], sl2, -m_use));
             const float p1 = ex2(fmaf(s[c * 32 + 2 * e + 1], sl2, -m_use));
             pk[e] = pack_bf16(p0, p1);
-            sum += bf_lo(pk[e]) + bf_hi(pk[e]);
+            if (PRECISE) {
+              pl[e] = pack_bf16(p0 - bf_lo(pk[e]), p1 - bf_hi(pk[e]));
+              sum += p0 + p1;
+            } else {
+              sum += bf_lo(pk[e]) + bf_hi(pk[e]);
+            }
           }
           tmem_st16(trow + C::kTmemS + sb * 128 + c * 16, pk);
+          if (PRECISE) tmem_st16(trow + C::kTmemS + sb * 128 + 64 + c * 16, pl);
         }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(p_ready + sb);
-        sm_m[hh * kTile + r] = m_use;
+        sm_m[hh * kTile + r] = r_use;
         sm_l[hh * kTile + r] = l_old * alpha + sum;
       }
     }
@@ -378,8 +420,27 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
             }
           }
         }
-        if (t < a.T)
-          a.lse[((size_t)b * a.Hq + h) * a.T + t] = (sm_m[hh * kTile + r] + __log2f(l)) * 0.69314718055994531f;
+        if (t < a.T) {
+          const size_t li = ((size_t)b * a.Hq + h) * a.T + t;
+          const float r_use = sm_m[hh * kTile + r];
+          const float m_use = __fmul_rn(r_use, sl2);
+          if (PRECISE) {
+            // LSE in log2 units = r_use * scale_log2 + log2(l), carried as hi + lo
+            // (exact product remainder by fma), then converted to natural log with
+            // a two-part ln 2.  The backward rebuilds P from hi + lo.
+            const float m_lo = fmaf(r_use, sl2, -m_use) + r_use * a.scale_log2_lo;
+            float h2, l2;
+            two_sum(m_use, __log2f(l), h2, l2);
+            l2 += m_lo;
+            const float hi = __fmul_rn(h2, kLn2Hi);
+            const float lo = fmaf(h2, kLn2Hi, -hi) + h2 * kLn2Lo + l2 * kLn2Hi;
+            const float H = __fadd_rn(hi, lo);
+            a.lse[li] = H;
+            a.lse_lo[li] = __fsub_rn(lo, __fsub_rn(H, hi));
+          } else {
+            a.lse[li] = (m_use + __log2f(l)) * 0.69314718055994531f;
+          }
+        }
       }
     }
     if (!ok) record_timeout(a.status, abort);

@@ -26,12 +26,14 @@ struct FwdArgs {
   CUtensorMap map_q, map_k, map_v;  // 4-D tiled maps over [B, T, H, D], box D x 1 x 128 x 1
   void* o;                          // [B, T, Hq, D] bf16 or fp32
   float* lse;                       // [B, Hq, T]
+  float* lse_lo;                    // [B, Hq, T] fp32 remainder of lse (precise logits only)
   const float2* rope;               // [Tcap][D/2] (cos, sin)
   int* status;                      // device status word
   int B, T, Hq, Hkv, D, G, HC;      // HC: query heads per CTA (divides G)
   int nt;                           // number of 128-row tiles
   int o_fp32;
-  float scale_log2;                 // log2(e) / sqrt(D)
+  float scale_log2;                 // log2(e) / sqrt(D), rounded to fp32
+  float scale_log2_lo;              // remainder log2(e)/sqrt(D) - scale_log2
 };
 
 struct BwdArgs {
@@ -39,6 +41,7 @@ struct BwdArgs {
   CUtensorMap map_qlo, map_klo;               // fp16 remainders (precise logits only)
   CUtensorMap map_dqacc;                      // 2-D map over [B*Hq*Tp, D] fp32, box 32 x 128
   const float* lse2;                          // [B, Hq, Tp]  lse * log2(e); +inf on pad rows
+  const float* lse2_lo;                       // [B, Hq, Tp]  its fp32 remainder (precise logits only)
   const float* delta;                         // [B, Hq, Tp]
   void* dk;                                   // [B, T, Hkv, D] bf16 or fp32
   void* dv;
@@ -46,15 +49,16 @@ struct BwdArgs {
   int* status;
   int B, T, Hq, Hkv, D, G, nt, Tp;
   int grad_fp32;
-  float scale_log2, scale;
+  float scale_log2, scale_log2_lo, scale;
 };
 
 struct PrepArgs {
   const __nv_bfloat16 *q, *k, *dout;
   const void* o;  // bf16 or fp32
   const float* lse;
+  const float* lse_lo;          // null unless precise logits
   __half *qr, *kr, *qlo, *klo;  // qlo/klo null unless precise logits
-  float *lse2, *delta, *dqacc;
+  float *lse2, *lse2_lo, *delta, *dqacc;
   const float2* rope;
   int B, T, Hq, Hkv, D, Tp, o_fp32;
 };

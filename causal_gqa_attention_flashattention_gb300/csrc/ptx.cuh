@@ -267,6 +267,20 @@ __device__ __forceinline__ float f16_hi(uint32_t w) {
   return f;
 }
 
+// Double-float helpers: a value carried as hi + lo (two fp32 numbers).
+constexpr float kLn2Hi = 0.693147182464599609375f;       // fp32(ln 2)
+constexpr float kLn2Lo = -1.904654299957768e-09f;        // ln 2 - kLn2Hi
+constexpr float kLog2eHi = 1.44269502162933349609375f;   // fp32(log2 e)
+constexpr float kLog2eLo = 1.925963033500011e-08f;       // log2 e - kLog2eHi
+// hi + lo = a + b exactly (Knuth's two-sum).  The _rn intrinsics keep the
+// compiler from fusing these operations into FMAs, which would break the
+// exactness the algorithm relies on.
+__device__ __forceinline__ void two_sum(float a, float b, float& hi, float& lo) {
+  hi = __fadd_rn(a, b);
+  const float bb = __fsub_rn(hi, a);
+  lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(b, bb));
+}
+
 // Byte offset of 16-byte chunk `chunk` of row `row` in a tile whose rows are
 // `span` bytes (32, 64 or 128) and which uses the matching TMA/UMMA swizzle:
 // the chunk index is XORed with address bits 7.. of the unswizzled offset.

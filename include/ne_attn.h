@@ -60,9 +60,14 @@ typedef enum {
 /* Flag bits for ne_attn_fwd_ex, ne_attn_bwd and ne_attn_bwd_workspace_size. */
 #define NE_ATTN_O_FP32 1     /* o is float32 [B,T,Hq,D] (forward output, backward input) */
 #define NE_ATTN_GRAD_FP32 2  /* dq, dk, dv are float32 */
-#define NE_ATTN_PRECISE_QK 4 /* logits from hi + lo fp16 parts of the rotated q and k:
-                                S = qhi.khi + qlo.khi + qhi.klo (three tensor-core products)
-                                instead of one; for inputs whose logits reach |s| ~ 10^2..10^3.
+#define NE_ATTN_PRECISE_QK 4 /* split precision for inputs whose logits reach |s| ~ 10^2..10^4:
+                                S = qhi.khi + qlo.khi + qhi.klo from fp16 hi + lo parts of the
+                                rotated q and k (three tensor-core products instead of one);
+                                P = Phi + Plo (two bf16 parts) in O += P V and dV += P^T dO;
+                                dS = dShi + dSlo (two fp16 parts) in dK and dQ; and lse holds
+                                2*B*Hq*T floats: the fp32 LSE [B,Hq,T] followed by its fp32
+                                remainder [B,Hq,T] (LSE = hi + lo), which the backward uses to
+                                rebuild P where one fp32 ulp of the LSE is already ~1e-3.
                                 Use the same setting for the forward and the backward. */
 
 /*
@@ -119,6 +124,25 @@ int ne_attn_check_status(void* stream);
 
 /* Static description of a status code. */
 const char* ne_attn_status_string(int status);
+
+/*
+ * Kernel timing.  Between ne_attn_profile_start(capacity) and
+ * ne_attn_profile_stop(), each kernel that ne_attn_fwd/_ex and ne_attn_bwd
+ * launch is bracketed by a pair of CUDA timing events recorded on the launch
+ * stream (at most `capacity` launches; later ones are not timed but still
+ * counted).  ne_attn_profile_stop synchronises those events and fills, per
+ * kernel kind (NE_ATTN_KERNEL_*), the summed device time in milliseconds and
+ * the number of launches; arrays must hold NE_ATTN_NUM_KERNEL_KINDS entries.
+ * Starting while a profile is open discards it.  Not for use during stream
+ * capture.  Returns NE_OK or a negative ne_status.
+ */
+#define NE_ATTN_KERNEL_FWD 0
+#define NE_ATTN_KERNEL_BWD_PREP 1
+#define NE_ATTN_KERNEL_BWD_DKDV 2
+#define NE_ATTN_KERNEL_BWD_DQ 3
+#define NE_ATTN_NUM_KERNEL_KINDS 4
+int ne_attn_profile_start(int capacity);
+int ne_attn_profile_stop(double* total_ms, long long* launches);
 
 /*
  * Test hook for the timeout path: launches one block that waits on a

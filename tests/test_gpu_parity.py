@@ -31,6 +31,8 @@ def run_gpu(nb, x, base=inputs.ROPE_BASE, grad_dtype=None, o_dtype=None, precise
     o, lse = nb.attn_fwd(q, k, v, base, o_dtype=o_dtype, precise=precise)
     dq, dk, dv = nb.attn_bwd(q, k, v, o, lse, do, base, grad_dtype=grad_dtype, precise=precise)
     nb.check_status()
+    if precise:
+        lse = lse[0]  # [1] holds the fp32 remainder
     return dict(o=H.to_f64(o), lse=lse.cpu().numpy().astype(np.float64), dq=H.to_f64(dq),
                 dk=H.to_f64(dk), dv=H.to_f64(dv))
 
@@ -48,6 +50,7 @@ def compare(oracle_mod, x, gpu, shape, groups, base=inputs.ROPE_BASE, tol_abs=H.
     g, r = H.gather_lse(gpu["lse"], qsel), H.gather_lse(ref["lse"], qsel)
     report["lse"] = H.errors(g, r)
     bad = [n for n in ("o", "dq", "dk", "dv") if report[n][0] > H.REL_L2_TOL or report[n][1] > tol_abs]
+    print("PARITY", shape, {k: ("%.2e" % v[0], "%.2e" % v[1]) for k, v in report.items()})
     assert not bad and report["lse"][1] <= H.LSE_ABS_TOL, report
     return report
 

@@ -470,16 +470,27 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
       for (int c = 0; c < kTile / 32; c++) {
         uint32_t u[32];
         tmem_ld32(trow + C::kColS + c * 32, u);
+        // the 32 lse2 values of this chunk: broadcast vector loads while the TMEM load is in flight
+        float l2[32], l2lo[PRECISE ? 32 : 1];
+#pragma unroll
+        for (int v4 = 0; v4 < 8; v4++) {
+          const float4 t4 = reinterpret_cast<const float4*>(lse2 + c * 32)[v4];
+          l2[4 * v4] = t4.x, l2[4 * v4 + 1] = t4.y, l2[4 * v4 + 2] = t4.z, l2[4 * v4 + 3] = t4.w;
+          if (PRECISE) {
+            const float4 t5 = reinterpret_cast<const float4*>(lse2lo + c * 32)[v4];
+            l2lo[4 * v4] = t5.x, l2lo[4 * v4 + 1] = t5.y, l2lo[4 * v4 + 2] = t5.z, l2lo[4 * v4 + 3] = t5.w;
+          }
+        }
         tmem_wait_ld();
         uint32_t w[16], wl[16];
 #pragma unroll
         for (int e = 0; e < 16; e++) {
           const int q0 = c * 32 + 2 * e;
           const float s0 = __uint_as_float(u[2 * e]), s1 = __uint_as_float(u[2 * e + 1]);
-          float x0 = fmaf(s0, sl2, -lse2[q0]), x1 = fmaf(s1, sl2, -lse2[q0 + 1]);
+          float x0 = fmaf(s0, sl2, -l2[2 * e]), x1 = fmaf(s1, sl2, -l2[2 * e + 1]);
           if (PRECISE) {  // logits of 10^3..10^4: add the remainders of scale and LSE
-            x0 += s0 * a.scale_log2_lo - lse2lo[q0];
-            x1 += s1 * a.scale_log2_lo - lse2lo[q0 + 1];
+            x0 += s0 * a.scale_log2_lo - l2lo[2 * e];
+            x1 += s1 * a.scale_log2_lo - l2lo[2 * e + 1];
           }
           float p0 = ex2(x0);
           float p1 = ex2(x1);
@@ -517,11 +528,16 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
           tmem_ld16(trow + C::kColS + c * 16, ph);
           tmem_ld16(trow + C::kColPlo + c * 16, pl);
         }
+        float dl[32];
+#pragma unroll
+        for (int v4 = 0; v4 < 8; v4++) {
+          const float4 t4 = reinterpret_cast<const float4*>(del + c * 32)[v4];
+          dl[4 * v4] = t4.x, dl[4 * v4 + 1] = t4.y, dl[4 * v4 + 2] = t4.z, dl[4 * v4 + 3] = t4.w;
+        }
         tmem_wait_ld();
         uint32_t w[16], wl[16];
 #pragma unroll
         for (int e = 0; e < 16; e++) {
-          const int q0 = c * 32 + 2 * e;
           float p0, p1;
           if (PRECISE) {
             p0 = bf_lo(ph[e]) + bf_lo(pl[e]);
@@ -530,8 +546,8 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
             p0 = bf_lo(pk[c * 16 + e]);
             p1 = bf_hi(pk[c * 16 + e]);
           }
-          const float d0 = (__uint_as_float(u[2 * e]) - del[q0]) * p0;
-          const float d1 = (__uint_as_float(u[2 * e + 1]) - del[q0 + 1]) * p1;
+          const float d0 = (__uint_as_float(u[2 * e]) - dl[2 * e]) * p0;
+          const float d1 = (__uint_as_float(u[2 * e + 1]) - dl[2 * e + 1]) * p1;
           w[e] = pack_f16(d0, d1);
           if (PRECISE) wl[e] = pack_f16(d0 - f16_lo(w[e]), d1 - f16_hi(w[e]));
         }

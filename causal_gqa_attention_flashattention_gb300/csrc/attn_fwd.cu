@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
   if (tid == 0) {
     *abort = 0;
     mbar_init(q_full, 1);
-    mbar_init(q_ready, 64);
+    mbar_init(q_ready, 192);
     for (int s = 0; s < C::kStages; s++) {
       mbar_init(kv_full + s, 1);
       mbar_init(k_ready + s, 64);
@@ -269,15 +269,21 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
       mma_commit(drain);
       mbar_wait(drain, 0, &never);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ RoPE on Q and K
-    const int rt = tid - 64;
-    bool ok = mbar_wait(q_full, 0, abort);
-    if (ok) {
-      rope_tiles<D>(smem + C::kOffQ, PRECISE ? smem + C::kOffQlo : nullptr, HC, i * kTile, a.rope, rt, 64);
+  } else {
+    // ------------------------------------------------------------ RoPE on Q (warps 2-7 together)
+    const bool ok_q = mbar_wait(q_full, 0, abort);
+    if (ok_q) {
+      rope_tiles<D>(smem + C::kOffQ, PRECISE ? smem + C::kOffQlo : nullptr, HC, i * kTile, a.rope, tid - 64, 192);
       fence_proxy_async_smem();
       mbar_arrive(q_ready);
+    } else {
+      record_timeout(a.status, abort);
     }
+  }
+  if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ RoPE on K
+    const int rt = tid - 64;
+    bool ok = !*abort;
     for (int j = 0; ok && j < nkv; j++) {
       const int st = j % C::kStages;
       if (!mbar_wait(kv_full + st, (j / C::kStages) & 1, abort)) {
@@ -290,7 +296,7 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
       mbar_arrive(k_ready + st);
     }
     if (!ok) record_timeout(a.status, abort);
-  } else {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int r = tid - 128;               // query row within the tile
     const uint32_t lane_base = (uint32_t)(warp - 4) * 32u;
@@ -307,13 +313,20 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
         tc_fence_after();
         float s[kTile];
         {
-          uint32_t u[32];
+          // all four loads in flight before the single wait
+          uint32_t u0[32], u1[32], u2[32], u3[32];
+          const uint32_t sc = trow + C::kTmemS + sb * 128;
+          tmem_ld32(sc, u0);
+          tmem_ld32(sc + 32, u1);
+          tmem_ld32(sc + 64, u2);
+          tmem_ld32(sc + 96, u3);
+          tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < kTile / 32; c++) {
-            tmem_ld32(trow + C::kTmemS + sb * 128 + c * 32, u);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; e++) s[c * 32 + e] = __uint_as_float(u[e]);
+          for (int e = 0; e < 32; e++) {
+            s[e] = __uint_as_float(u0[e]);
+            s[32 + e] = __uint_as_float(u1[e]);
+            s[64 + e] = __uint_as_float(u2[e]);
+            s[96 + e] = __uint_as_float(u3[e]);
           }
         }
         if (diag) {
@@ -323,10 +336,14 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
         }
         // The row state keeps the raw score r_use that defines the reference
         // m_use = fp32(r_use * scale_log2); the epilogue needs it for the
-        // double-float LSE.
-        float mxr = s[0];
+        // double-float LSE.  Eight partial maxima keep the dependency chain short.
+        float mx8[8];
 #pragma unroll
-        for (int c = 1; c < kTile; c++) mxr = fmaxf(mxr, s[c]);
+        for (int e = 0; e < 8; e++) mx8[e] = s[e];
+#pragma unroll
+        for (int c = 8; c < kTile; c++) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+        const float mxr = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         // Every reference value is the correctly rounded product r * scale_log2
         // (no FMA contraction), so alpha, P and the LSE all use the same m.
         const float r_old = j == 0 ? -INFINITY : sm_m[hh * kTile + r];
@@ -361,7 +378,7 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
         // PRECISE: P = hi + lo (two bf16 parts, ~2^-17 relative) and the row sum
         // adds the fp32 values, so O and LSE follow the exact softmax.
         const float m_use = __fmul_rn(r_use, sl2);
-        float sum = 0.f;
+        float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < kTile / 32; c++) {
           uint32_t pk[16], pl[16];
@@ -372,14 +389,15 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
             pk[e] = pack_bf16(p0, p1);
             if (PRECISE) {
               pl[e] = pack_bf16(p0 - bf_lo(pk[e]), p1 - bf_hi(pk[e]));
-              sum += p0 + p1;
+              sum8[e & 7] += p0 + p1;
             } else {
-              sum += bf_lo(pk[e]) + bf_hi(pk[e]);
+              sum8[e & 7] += bf_lo(pk[e]) + bf_hi(pk[e]);
             }
           }
           tmem_st16(trow + C::kTmemS + sb * 128 + c * 16, pk);
           if (PRECISE) tmem_st16(trow + C::kTmemS + sb * 128 + 64 + c * 16, pl);
         }
+        const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(p_ready + sb);

@@ -19,6 +19,12 @@ namespace ne {
 // ------------------------------------------------------------------ device status word
 __device__ int g_status_word;
 
+// ------------------------------------------------------------------ fixed scratch for ne_attn_bwd_noalloc
+// Every GPU that loads this library holds this array until the process exits.
+// Host code must not use the symbol as an address: ne_attn_bwd_noalloc asks
+// the runtime for its device address (cudaGetSymbolAddress) once per device.
+static __device__ __align__(256) unsigned char g_static_scratch[NE_ATTN_STATIC_SCRATCH_BYTES];
+
 // ------------------------------------------------------------------ small kernels
 // cos/sin of t * theta_i in double precision, rounded to fp32.
 __global__ void k_rope_table(float2* tab, int Tcap, int D, double log2_base) {
@@ -82,6 +88,7 @@ struct DeviceState {
   bool supported = false;
   int* status = nullptr;
   std::vector<RopeTable> tables;
+  unsigned char* static_scratch = nullptr;  // device address of g_static_scratch (set on first use)
 };
 
 std::mutex g_mu;
@@ -468,6 +475,9 @@ const char* ne_attn_status_string(int status) {
     case NE_ERR_CUDA: return "CUDA runtime or launch error";
     case NE_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
     case NE_ERR_DEVICE_TIMEOUT: return "a kernel pipeline wait timed out on the device";
+    case NE_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than the fixed NE_ATTN_STATIC_SCRATCH_BYTES array of "
+             "ne_attn_bwd_noalloc holds; use ne_attn_bwd with a caller workspace";
     default: return "unknown status";
   }
 }
@@ -525,6 +535,127 @@ int ne_attn_debug_timeout_probe(int limit_us, void* stream) {
                  cudaSuccess
              ? NE_OK
              : NE_ERR_CUDA;
+}
+
+// Backward pass that allocates nothing: the same kernels as ne_attn_bwd, with
+// their workspace and rotary table taken from the library's fixed device array
+// instead of caller or library allocations.  See include/ne_attn.h.
+int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D,
+                        float rope_base, int flags, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return NE_ERR_ARG;
+  if ((flags & ~kKnownFlags) != 0) return NE_ERR_ARG;
+  if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
+  int st = check_shape(B, T, Hq, Hkv, D);
+  if (st != NE_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return NE_ERR_ALIGN;
+  const bool precise = (flags & kFlagPreciseQK) != 0;
+  const int grad_fp32 = (flags & kFlagGradFp32) ? 1 : 0;
+  const int nt = (T + kTile - 1) / kTile;
+  const int Tp = nt * kTile;
+  // scratch layout: [rotary table, Tp x D/2 float2][workspace as in ne_attn_bwd]
+  const size_t table_bytes = (sizeof(float2) * (size_t)Tp * (D / 2) + 255) / 256 * 256;
+  const WsLayout w = ws_layout(B, T, Hq, Hkv, D, precise);
+  if (table_bytes + w.total > (size_t)NE_ATTN_STATIC_SCRATCH_BYTES) return NE_ERR_SCRATCH_LIMIT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev;
+  if ((st = current_device(&dev)) != NE_OK) return st;
+  DeviceState* d;
+  if ((st = device_state(dev, &d)) != NE_OK) return st;
+  if (!d->static_scratch) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return NE_ERR_CUDA;
+    d->static_scratch = static_cast<unsigned char*>(p);
+  }
+  float2* rope = reinterpret_cast<float2*>(d->static_scratch);
+  uint8_t* ws = d->static_scratch + table_bytes;
+  // The array keeps the previous call's contents: the table is rebuilt here and
+  // the pre-pass zeroes the dQ accumulator and writes every other field it uses.
+  if (launch_rope_table(rope, Tp, D, (double)rope_base, s) != cudaSuccess) return NE_ERR_CUDA;
+  float* dqacc = reinterpret_cast<float*>(ws + w.dqacc);
+  __half* qr = reinterpret_cast<__half*>(ws + w.qr);
+  __half* kr = reinterpret_cast<__half*>(ws + w.kr);
+  __half* qlo = precise ? reinterpret_cast<__half*>(ws + w.qlo) : nullptr;
+  __half* klo = precise ? reinterpret_cast<__half*>(ws + w.klo) : nullptr;
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  float* lse2_lo = precise ? reinterpret_cast<float*>(ws + w.lse2_lo) : nullptr;
+  float* delta = reinterpret_cast<float*>(ws + w.delta);
+  const double scale = 1.0 / std::sqrt((double)D);
+
+  PrepArgs p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.o = o;
+  p.o_fp32 = (flags & kFlagOFp32) ? 1 : 0;
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.lse = lse;
+  p.lse_lo = precise ? lse + (size_t)B * Hq * T : nullptr;
+  p.lse2_lo = lse2_lo;
+  p.qr = qr;
+  p.kr = kr;
+  p.qlo = qlo;
+  p.klo = klo;
+  p.lse2 = lse2;
+  p.delta = delta;
+  p.dqacc = dqacc;
+  p.rope = rope;
+  p.B = B;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.Tp = Tp;
+  if (launch_bwd_prep(p, s) != cudaSuccess) return NE_ERR_CUDA;
+
+  BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  constexpr CUtensorMapDataType kF16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if ((st = make_map_bthd(&a.map_qr, qr, B, T, Hq, D, kF16)) != NE_OK) return st;
+  if ((st = make_map_bthd(&a.map_kr, kr, B, T, Hkv, D, kF16)) != NE_OK) return st;
+  if ((st = make_map_bthd(&a.map_v, v, B, T, Hkv, D)) != NE_OK) return st;
+  if ((st = make_map_bthd(&a.map_do, dout, B, T, Hq, D)) != NE_OK) return st;
+  if (precise) {
+    if ((st = make_map_bthd(&a.map_qlo, qlo, B, T, Hq, D, kF16)) != NE_OK) return st;
+    if ((st = make_map_bthd(&a.map_klo, klo, B, T, Hkv, D, kF16)) != NE_OK) return st;
+  }
+  if ((st = make_map_acc(&a.map_dqacc, dqacc, (long long)B * Hq * Tp, D)) != NE_OK) return st;
+  a.lse2 = lse2;
+  a.lse2_lo = lse2_lo;
+  a.delta = delta;
+  a.dk = dk;
+  a.dv = dv;
+  a.rope = rope;
+  a.status = d->status;
+  a.B = B;
+  a.T = T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.G = Hq / Hkv;
+  a.nt = nt;
+  a.Tp = Tp;
+  a.grad_fp32 = grad_fp32;
+  a.scale_log2 = (float)(1.4426950408889634 * scale);
+  a.scale_log2_lo = (float)(1.4426950408889634 * scale - (double)a.scale_log2);
+  a.scale = (float)scale;
+  if (launch_bwd_dkdv(a, precise, s) != cudaSuccess) return NE_ERR_CUDA;
+
+  DqArgs qa;
+  qa.dqacc = dqacc;
+  qa.dq = dq;
+  qa.rope = rope;
+  qa.B = B;
+  qa.T = T;
+  qa.Hq = Hq;
+  qa.D = D;
+  qa.Tp = Tp;
+  qa.grad_fp32 = grad_fp32;
+  qa.scale = (float)scale;
+  if (launch_bwd_dq(qa, s) != cudaSuccess) return NE_ERR_CUDA;
+  return NE_OK;
 }
 
 }  // extern "C"

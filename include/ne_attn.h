@@ -54,7 +54,8 @@ typedef enum {
   NE_ERR_UNSUPPORTED = -3,    /* D not in {32, 64}, size limits, or device is not sm_103 */
   NE_ERR_CUDA = -4,           /* a CUDA runtime/driver call or a launch failed */
   NE_ERR_WORKSPACE = -5,      /* workspace missing, too small or not 256-byte aligned */
-  NE_ERR_DEVICE_TIMEOUT = -6  /* a kernel gave up on a pipeline wait (see above) */
+  NE_ERR_DEVICE_TIMEOUT = -6, /* a kernel gave up on a pipeline wait (see above) */
+  NE_ERR_SCRATCH_LIMIT = -7   /* ne_attn_bwd_noalloc: problem too large for its fixed scratch */
 } ne_status;
 
 /* Flag bits for ne_attn_fwd_ex, ne_attn_bwd and ne_attn_bwd_workspace_size. */
@@ -114,6 +115,35 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
                 const void* dout, void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv,
                 int D, float rope_base, int flags, void* workspace, size_t workspace_bytes,
                 void* stream);
+
+/*
+ * Backward pass for callers that cannot allocate device memory: the same
+ * result as ne_attn_bwd (same kernels, same flags) with no workspace argument.
+ * The NanoEuler pages have no counterpart to this entry point; it exists for
+ * callers such as code that runs while a stream is being captured into a CUDA
+ * graph (no cudaMalloc allowed there), plugins whose host process owns every
+ * device allocation, or fixed-memory deployments that forbid allocating after
+ * start-up.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Scratch (the workspace of ne_attn_bwd plus the rotary table) comes from one
+ * fixed device array of NE_ATTN_STATIC_SCRATCH_BYTES that the library defines;
+ * every GPU that loads the library holds it until the process exits.  A
+ * problem whose scratch (the ne_attn_bwd_workspace_size figure plus
+ * Tpad * D * 4 bytes of table, Tpad = T rounded up to 128) does not fit is
+ * rejected with NE_ERR_SCRATCH_LIMIT before anything is launched; the
+ * 116M-model shape (B=16, T=512, Hq=12, Hkv=4, D=64) fits.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture.  Every call uses the same array and it keeps the previous
+ * call's contents; the call rebuilds the table and zeroes the accumulator it
+ * needs.  Calls whose kernels overlap on the GPU (different streams, or
+ * concurrent host threads) race on the array: serialise them.
+ */
+#define NE_ATTN_STATIC_SCRATCH_BYTES (48u * 1024u * 1024u)
+int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv,
+                        int D, float rope_base, int flags, void* stream);
 
 /*
  * Synchronises `stream`, then returns and clears the device status word of

@@ -53,6 +53,10 @@ def lib():
         L.ne_attn_profile_start.restype = i
         L.ne_attn_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]
         L.ne_attn_profile_stop.restype = i
+        L.ne_attn_profile_detach.argtypes = []
+        L.ne_attn_profile_detach.restype = i
+        L.ne_attn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]
+        L.ne_attn_profile_read.restype = i
         _lib = L
     return _lib
 
@@ -168,6 +172,21 @@ def profile_stop():
     ms = (ctypes.c_double * len(KERNEL_KINDS))()
     n = (ctypes.c_longlong * len(KERNEL_KINDS))()
     _check("ne_attn_profile_stop", lib().ne_attn_profile_stop(ms, n))
+    return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def profile_stop_deferred():
+    """Closes a profile whose launches were captured into a CUDA graph: the
+    events run (and are timed) each time the graph replays.  Returns a handle
+    for profile_read, which reads the times of the most recent replay."""
+    _check("ne_attn_profile_detach", lib().ne_attn_profile_detach())
+    return True
+
+
+def profile_read(handle):
+    ms = (ctypes.c_double * len(KERNEL_KINDS))()
+    n = (ctypes.c_longlong * len(KERNEL_KINDS))()
+    _check("ne_attn_profile_read", lib().ne_attn_profile_read(ms, n))
     return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(KERNEL_KINDS)}
 
 

@@ -248,6 +248,16 @@ void prof_reset() {
   g_prof = Profile();
 }
 
+// Under stream capture an event must be recorded as an external event node to be
+// timed when the graph runs; otherwise a plain record.
+void prof_record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+
 // Records the start event of a launch of `kind`; returns the slot (or -1).
 int prof_begin(int kind, cudaStream_t s) {
   std::lock_guard<std::mutex> lock(g_prof_mu);
@@ -256,13 +266,13 @@ int prof_begin(int kind, cudaStream_t s) {
   if (g_prof.used >= g_prof.capacity) return -1;
   const int slot = g_prof.used++;
   g_prof.kind[slot] = kind;
-  cudaEventRecord(g_prof.ev[2 * slot], s);
+  prof_record(g_prof.ev[2 * slot], s);
   return slot;
 }
 void prof_end(int slot, cudaStream_t s) {
   if (slot < 0) return;
   std::lock_guard<std::mutex> lock(g_prof_mu);
-  if (g_prof.on && slot < g_prof.used) cudaEventRecord(g_prof.ev[2 * slot + 1], s);
+  if (g_prof.on && slot < g_prof.used) prof_record(g_prof.ev[2 * slot + 1], s);
 }
 
 struct ProfScope {
@@ -519,6 +529,36 @@ int ne_attn_profile_stop(double* total_ms, long long* launches) {
     if (launches) launches[k] = g_prof.launches[k];
   }
   prof_reset();
+  return st;
+}
+
+int ne_attn_profile_detach(void) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (!g_prof.on) return NE_ERR_ARG;
+  g_prof.on = false;  // no further launches are timed; the recorded events stay valid
+  return NE_OK;
+}
+
+int ne_attn_profile_read(double* total_ms, long long* launches) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (g_prof.ev.empty()) return NE_ERR_ARG;
+  int st = NE_OK;
+  double tot[NE_ATTN_NUM_KERNEL_KINDS] = {0, 0, 0, 0};
+  long long cnt[NE_ATTN_NUM_KERNEL_KINDS] = {0, 0, 0, 0};
+  for (int i = 0; i < g_prof.used; i++) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess) {
+      st = NE_ERR_CUDA;
+      continue;
+    }
+    tot[g_prof.kind[i]] += ms;
+    cnt[g_prof.kind[i]]++;
+  }
+  for (int k = 0; k < NE_ATTN_NUM_KERNEL_KINDS; k++) {
+    if (total_ms) total_ms[k] = tot[k];
+    if (launches) launches[k] = cnt[k];
+  }
   return st;
 }
 

@@ -687,6 +687,412 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
   }
 }
 
+// ---------------------------------------------------------------------- dK/dV sweep, default precision
+// Same computation as k_bwd_dkdv<D, false> with less shared-memory traffic and
+// two compute warpgroups:
+//   * K^ and V are copied once into TMEM and used as the A operands of
+//     S^T = K^ Q^T and dP^T = V dO^T (only Q / dO are read from shared memory);
+//   * dS^T is also written to TMEM (over the dP^T columns it replaces) and is
+//     the A operand of dK += dS^T Q^; the shared-memory copy of dS feeds only
+//     dQ = dS K^, which needs it transposed;
+//   * warps 4-7 handle query columns 0-63 and warps 8-11 columns 64-127 of
+//     every step (P and dS are element-wise once the LSE is known);
+//   * warps 12-15 drain dQ, which has a single TMEM buffer.
+template <int D>
+struct Bwd2Cfg {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr uint32_t kSpan = D * 2;
+  static constexpr uint32_t kSwz = D == 64 ? kSw128 : kSw64;
+  static constexpr uint32_t kSBO = 8 * kSpan;
+  static constexpr int kStages = 2;
+  static constexpr int kDsBufs = 2;
+  static constexpr int kVecBytes = kTile * 4;
+  static constexpr int kDsBytes = kTile * kTile * 2;
+  static constexpr int kStgBytes = kTile * D * 4;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kTileBytes;
+  static constexpr int kOffQ = kOffV + kTileBytes;
+  static constexpr int kOffDO = kOffQ + kStages * kTileBytes;
+  static constexpr int kOffDS = kOffDO + kStages * kTileBytes;
+  static constexpr int kOffStg = kOffDS + kDsBufs * kDsBytes;
+  static constexpr int kOffLse = kOffStg + kStgBytes;
+  static constexpr int kOffDel = kOffLse + kStages * kVecBytes;
+  static constexpr int kOffBar = kOffDel + kStages * kVecBytes;
+  static constexpr int kNumBars = 24;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  // TMEM: S^T/P^T | dP^T (dS^T over it) | dV | dK | dQ | K^ (A operand) | V (A operand)
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D, kColDQ = 256 + 2 * D;
+  static constexpr uint32_t kColK = 256 + 3 * D, kColV = kColK + D / 2;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kColV + D / 2 <= kTmemCols, "tensor memory budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(512, 1) k_bwd_dkdv2(const __grid_constant__ BwdArgs a) {
+  using C = Bwd2Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* kv_full = bars;
+  uint64_t* kv_tmem = bars + 1;
+  uint64_t* qd_full = bars + 2;   // [2]
+  uint64_t* qd_empty = bars + 4;  // [2]
+  uint64_t* s_full = bars + 6;
+  uint64_t* p_ready = bars + 7;
+  uint64_t* dp_full = bars + 8;
+  uint64_t* acc_done = bars + 9;
+  uint64_t* ds_ready = bars + 10;  // [2]
+  uint64_t* ds_free = bars + 12;   // [2]
+  uint64_t* dq_full = bars + 14;
+  uint64_t* dq_free = bars + 15;
+  uint64_t* drain = bars + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int per_j = a.B * a.Hkv;
+  const int j = (int)blockIdx.x / per_j;  // smallest j (longest sweep) first
+  const int rem = (int)blockIdx.x % per_j;
+  const int kvh = rem % a.Hkv, b = rem / a.Hkv;
+  const int G = a.G;
+  const int N = (a.nt - j) * G;
+
+  if (tid == 0) {
+    *abort = 0;
+    mbar_init(kv_full, 1);
+    mbar_init(kv_tmem, 256);
+    for (int s = 0; s < 2; s++) {
+      mbar_init(qd_full + s, 1);
+      mbar_init(qd_empty + s, 1);
+      mbar_init(ds_ready + s, 256);
+      mbar_init(ds_free + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_ready, 256);
+    mbar_init(dp_full, 1);
+    mbar_init(acc_done, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, 128);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const volatile int never = 0;
+  const uint32_t sK = smem_u32(smem + C::kOffK);
+  const uint32_t sQ = smem_u32(smem + C::kOffQ), sDO = smem_u32(smem + C::kOffDO);
+  const uint32_t sDS = smem_u32(smem + C::kOffDS);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&a.map_qr);
+      prefetch_tmap(&a.map_do);
+      mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
+      tma_load_4d(smem + C::kOffK, &a.map_kr, kv_full, 0, kvh, j * kTile, b);
+      tma_load_4d(smem + C::kOffV, &a.map_v, kv_full, 0, kvh, j * kTile, b);
+      int loaded = 0;
+      for (int n = 0; n < N; n++) {
+        const int st = n % C::kStages, use = n / C::kStages;
+        if (use > 0 && !mbar_wait(qd_empty + st, (use - 1) & 1, abort)) {
+          record_timeout(a.status, abort);
+          break;
+        }
+        const int i = j + n / G, h = kvh * G + n % G;
+        const size_t vec = ((size_t)b * a.Hq + h) * a.Tp + (size_t)i * kTile;
+        mbar_arrive_expect_tx(qd_full + st, 2 * C::kTileBytes + 2 * C::kVecBytes);
+        tma_load_4d(smem + C::kOffQ + st * C::kTileBytes, &a.map_qr, qd_full + st, 0, h, i * kTile, b);
+        tma_load_4d(smem + C::kOffDO + st * C::kTileBytes, &a.map_do, qd_full + st, 0, h, i * kTile, b);
+        bulk_load(smem + C::kOffLse + st * C::kVecBytes, a.lse2 + vec, C::kVecBytes, qd_full + st);
+        bulk_load(smem + C::kOffDel + st * C::kVecBytes, a.delta + vec, C::kVecBytes, qd_full + st);
+        loaded = n + 1;
+      }
+      mbar_wait(kv_full, 0, &never);
+      for (int n = loaded - C::kStages < 0 ? 0 : loaded - C::kStages; n < loaded; n++)
+        mbar_wait(qd_full + n % C::kStages, (n / C::kStages) & 1, &never);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_fp16(128, 128, false, false);   // K^ (TMEM) x Q^ (K-major)
+      constexpr uint32_t idDP = idesc_bf16(128, 128, false, false);  // V (TMEM) x dO (K-major)
+      constexpr uint32_t idDV = idesc_bf16(128, D, false, true);     // P^T (TMEM) x dO MN-major
+      constexpr uint32_t idDK = idesc_fp16(128, D, false, true);     // dS^T (TMEM) x Q^ MN-major
+      constexpr uint32_t idDQ = idesc_fp16(128, D, true, true);      // dS (MN-major) x K^ MN-major
+      constexpr int KD = D / 16;                                     // k-steps over the head dimension
+      constexpr uint32_t kStepK = 32 >> 4;                           // K-major: next 16 columns
+      constexpr uint32_t kStepMN = (16 * C::kSpan) >> 4;             // MN-major: next 16 rows
+      // P^T and dS^T halves sit at +0..31 (queries 0..63) and +64..95 (queries 64..127): SPLIT chains
+      // shared-memory descriptors, computed once
+      // (stage / buffer k adds k * bytes / 16 to the start-address field)
+      const uint64_t dQ0 = smem_desc(sQ, 16, C::kSBO, C::kSwz);
+      const uint64_t dDO0 = smem_desc(sDO, 16, C::kSBO, C::kSwz);
+      const uint64_t dDS0 = smem_desc(sDS, 16384, 1024, kSw128);
+      const uint64_t dK = smem_desc(sK, 16, C::kSBO, C::kSwz);
+      auto dQs = [&](int st) { return dQ0 + (uint64_t)(st * (C::kTileBytes >> 4)); };
+      auto dDOs = [&](int st) { return dDO0 + (uint64_t)(st * (C::kTileBytes >> 4)); };
+      auto dDS = [&](int k) { return dDS0 + (uint64_t)(k * (C::kDsBytes >> 4)); };
+      bool ok = mbar_wait(kv_tmem, 0, abort) && mbar_wait(qd_full, 0, abort);
+      tc_fence_after();
+      if (ok) {
+        mma_ts_chain<KD>(tmem + C::kColS, tmem + C::kColK, dQs(0), kStepK, idS, 0);
+        mma_commit(s_full);
+        mma_ts_chain<KD>(tmem + C::kColDP, tmem + C::kColV, dDOs(0), kStepK, idDP, 0);
+        mma_commit(dp_full);
+      }
+      for (int n = 0; ok && n < N; n++) {
+        const int st = n % C::kStages;
+        // dV += P^T dO
+        if (!(ok = mbar_wait(p_ready, n & 1, abort))) break;
+        tc_fence_after();
+        mma_ts_chain<8, true>(tmem + C::kColDV, tmem + C::kColS, dDOs(st), kStepMN, idDV, n > 0 ? 1u : 0u);
+        // next S^T (its TMEM columns were just read by the dV MMAs above)
+        const int st1 = (n + 1) % C::kStages;
+        if (n + 1 < N) {
+          if (!(ok = mbar_wait(qd_full + st1, ((n + 1) / C::kStages) & 1, abort))) break;
+          tc_fence_after();
+          mma_ts_chain<KD>(tmem + C::kColS, tmem + C::kColK, dQs(st1), kStepK, idS, 0);
+          mma_commit(s_full);
+        }
+        // dK += dS^T Q^ (dS^T in TMEM over the dP^T columns), dQ tile = dS K^ (dS from shared memory)
+        const int dsb = n % C::kDsBufs;
+        if (!(ok = mbar_wait(ds_ready + dsb, (n / C::kDsBufs) & 1, abort))) break;
+        tc_fence_after();
+        mma_ts_chain<8, true>(tmem + C::kColDK, tmem + C::kColDP, dQs(st), kStepMN, idDK, n > 0 ? 1u : 0u);
+        if (n >= 1) {
+          if (!(ok = mbar_wait(dq_free, (n - 1) & 1, abort))) break;
+          tc_fence_after();
+        }
+        mma_ss_chain<8>(tmem + C::kColDQ, dDS(dsb), 2048 >> 4, dK, kStepMN, idDQ, 0);
+        mma_commit(dq_full);
+        mma_commit(ds_free + dsb);
+        mma_commit(qd_empty + st);
+        if (n + 1 < N) {  // next dP^T (its columns were read by the compute warps before ds_ready)
+          mma_ts_chain<KD>(tmem + C::kColDP, tmem + C::kColV, dDOs(st1), kStepK, idDP, 0);
+          mma_commit(dp_full);
+        }
+      }
+      if (!ok) record_timeout(a.status, abort);
+      mma_commit(acc_done);
+      mma_commit(drain);
+      mbar_wait(drain, 0, &never);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------ P and dS, half the query columns each
+    const int wg = (warp - 4) >> 2;          // 0: queries 0..63, 1: queries 64..127
+    const int r = tid - 128 - wg * 128;      // key row
+    const int cbase = wg * 64;
+    const uint32_t trow = tmem + ((uint32_t)(warp & 3) * 32u << 16);
+    const float sl2 = a.scale_log2;
+    bool ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, abort));
+    if (ok) {
+      // Copy this thread's row of K^ (warps 4-7) or V (warps 8-11) into TMEM, in logical order.
+      const uint8_t* src = smem + (wg == 0 ? C::kOffK : C::kOffV);
+      uint32_t w[D / 2];
+#pragma unroll
+      for (int c = 0; c < D / 8; c++) {
+        const uint4 x = *reinterpret_cast<const uint4*>(src + swz(r, c, C::kSpan));
+        w[4 * c] = x.x, w[4 * c + 1] = x.y, w[4 * c + 2] = x.z, w[4 * c + 3] = x.w;
+      }
+      if (D == 64) {
+        uint32_t w32[32];
+#pragma unroll
+        for (int e = 0; e < 32; e++) w32[e] = w[e % (D / 2)];
+        tmem_st32(trow + (wg == 0 ? C::kColK : C::kColV), w32);
+      } else {
+        uint32_t w16[16];
+#pragma unroll
+        for (int e = 0; e < 16; e++) w16[e] = w[e % (D / 2)];
+        tmem_st16(trow + (wg == 0 ? C::kColK : C::kColV), w16);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(kv_tmem);
+    }
+    const uint32_t x7 = (uint32_t)(r & 7);  // swizzle of this key row in the dS tile
+    for (int n = 0; ok && n < N; n++) {
+      const int st = n % C::kStages;
+      const int i = j + n / G;
+      const bool diag = (i == j);
+      const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffLse + st * C::kVecBytes) + cbase;
+      const float* del = reinterpret_cast<const float*>(smem + C::kOffDel + st * C::kVecBytes) + cbase;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full, n & 1, abort)))) break;
+      tc_fence_after();
+      uint32_t pk[32];  // P^T for this thread's 64 query columns, packed bf16 pairs
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        uint32_t u[16];
+        tmem_ld16(trow + C::kColS + cbase + c * 16, u);
+        float l2[16];
+#pragma unroll
+        for (int v4 = 0; v4 < 4; v4++) {
+          const float4 t4 = reinterpret_cast<const float4*>(lse2 + c * 16)[v4];
+          l2[4 * v4] = t4.x, l2[4 * v4 + 1] = t4.y, l2[4 * v4 + 2] = t4.z, l2[4 * v4 + 3] = t4.w;
+        }
+        tmem_wait_ld();
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+          const int q0 = cbase + c * 16 + 2 * e;
+          float p0 = ex2(fmaf(__uint_as_float(u[2 * e]), sl2, -l2[2 * e]));
+          float p1 = ex2(fmaf(__uint_as_float(u[2 * e + 1]), sl2, -l2[2 * e + 1]));
+          if (diag) {
+            if (q0 < r) p0 = 0.f;
+            if (q0 + 1 < r) p1 = 0.f;
+          }
+          w[e] = pack_bf16(p0, p1);
+          pk[c * 8 + e] = w[e];
+        }
+        // each warpgroup keeps P^T inside its own score columns (cbase..cbase+63), behind its reads
+        tmem_st8(trow + C::kColS + cbase + c * 8, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+
+      const int dsb = n % C::kDsBufs;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(dp_full, n & 1, abort)))) break;
+      if (n >= C::kDsBufs &&
+          !(ok = __all_sync(0xffffffffu, mbar_wait(ds_free + dsb, ((n - C::kDsBufs) / C::kDsBufs) & 1, abort))))
+        break;
+      tc_fence_after();
+      uint8_t* atom = smem + C::kOffDS + dsb * C::kDsBytes + wg * 16384;
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        uint32_t u[16];
+        tmem_ld16(trow + C::kColDP + cbase + c * 16, u);
+        float dl[16];
+#pragma unroll
+        for (int v4 = 0; v4 < 4; v4++) {
+          const float4 t4 = reinterpret_cast<const float4*>(del + c * 16)[v4];
+          dl[4 * v4] = t4.x, dl[4 * v4 + 1] = t4.y, dl[4 * v4 + 2] = t4.z, dl[4 * v4 + 3] = t4.w;
+        }
+        tmem_wait_ld();
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+          const float d0 = (__uint_as_float(u[2 * e]) - dl[2 * e]) * bf_lo(pk[c * 8 + e]);
+          const float d1 = (__uint_as_float(u[2 * e + 1]) - dl[2 * e + 1]) * bf_hi(pk[c * 8 + e]);
+          w[e] = pack_f16(d0, d1);
+        }
+        // dS^T into TMEM over the dP^T columns already read (for dK), dS into shared memory (for dQ)
+        tmem_st8(trow + C::kColDP + cbase + c * 8, w);
+        *reinterpret_cast<uint4*>(atom + r * 128 + (((uint32_t)(2 * c) ^ x7) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(atom + r * 128 + (((uint32_t)(2 * c + 1) ^ x7) << 4)) =
+            make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_ready + dsb);
+    }
+    // epilogue: warps 4-7 store dK (scale, inverse rotation), warps 8-11 store dV
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort));
+    if (ok) {
+      tc_fence_after();
+      const int t = j * kTile + r;
+      float x[D];
+#pragma unroll
+      for (int c = 0; c < D / 16; c++) {
+        uint32_t u[16];
+        tmem_ld16(trow + (wg == 0 ? C::kColDK : C::kColDV) + c * 16, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; e++) x[c * 16 + e] = __uint_as_float(u[e]);
+      }
+      if (t < a.T) {
+        const size_t base = (((size_t)b * a.T + t) * a.Hkv + kvh) * D;
+        void* out = wg == 0 ? a.dk : a.dv;
+#pragma unroll
+        for (int c = 0; c < D / 8; c++) {
+          float y[8];
+          if (wg == 0) {
+            float4 c0, c1;
+            rope_coeffs<D>(a.rope, t, c, c0, c1);
+            const float cs[4] = {c0.x, c0.z, c1.x, c1.z}, sn[4] = {c0.y, c0.w, c1.y, c1.w};
+#pragma unroll
+            for (int p = 0; p < 4; p++) {
+              const float x0 = x[c * 8 + 2 * p], x1 = x[c * 8 + 2 * p + 1];
+              y[2 * p] = a.scale * (x0 * cs[p] + x1 * sn[p]);
+              y[2 * p + 1] = a.scale * (x1 * cs[p] - x0 * sn[p]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; e++) y[e] = x[c * 8 + e];
+          }
+          if (a.grad_fp32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + base + c * 8);
+            dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+            dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+          } else {
+            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + base)[c] =
+                make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+          }
+        }
+      }
+    }
+    if (!ok) record_timeout(a.status, abort);
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ dQ drain (one query row per thread)
+    const int r = tid - 384;
+    const uint32_t trow = tmem + ((uint32_t)(warp & 3) * 32u << 16);
+    uint8_t* stg = smem + C::kOffStg;
+    bool ok = true;
+    for (int n = 0; n < N; n++) {
+      // Every drain thread reaches both named barriers of an iteration; the
+      // first one agrees on `ok`, so a timeout in one warp stops all four.
+      const bool got = __all_sync(0xffffffffu, mbar_wait(dq_full, n & 1, abort));
+      uint32_t u[D];
+      if (got) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; c++) {
+          uint32_t v[32];
+          tmem_ld32(trow + C::kColDQ + c * 32, v);
+#pragma unroll
+          for (int e = 0; e < 32; e++) u[c * 32 + e] = v[e];
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(dq_free);
+      }
+      if (r == 0) bulk_wait_read<0>();  // previous reduction has finished reading the staging tile
+      if (!(ok = named_sync_and(1, 128, got))) break;
+#pragma unroll
+      for (int bx = 0; bx < D / 32; bx++)
+#pragma unroll
+        for (int c = 0; c < 8; c++)
+          *reinterpret_cast<uint4*>(stg + bx * 16384 + swz(r, c, 128)) =
+              make_uint4(u[bx * 32 + 4 * c], u[bx * 32 + 4 * c + 1], u[bx * 32 + 4 * c + 2], u[bx * 32 + 4 * c + 3]);
+      fence_proxy_async_smem();
+      named_sync(1, 128);
+      if (r == 0) {
+        const int i = j + n / G, h = kvh * G + n % G;
+        const int row0 = (int)(((size_t)b * a.Hq + h) * a.Tp + (size_t)i * kTile);
+#pragma unroll
+        for (int bx = 0; bx < D / 32; bx++) tma_reduce_add_2d(&a.map_dqacc, stg + bx * 16384, bx * 32, row0);
+        bulk_commit();
+      }
+    }
+    if (r == 0) bulk_wait<0>();
+    if (!ok) record_timeout(a.status, abort);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    tmem_relinquish();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
 int elementwise_blocks(long long items) {
   long long blocks = (items + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
@@ -720,15 +1126,39 @@ template <int D, bool P>
 cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t s) {
   using C = BwdCfg<D, P>;
   const int grid = a.nt * a.B * a.Hkv;
-  cudaError_t e = cudaFuncSetAttribute(k_bwd_dkdv<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  if (e != cudaSuccess) return e;
+  // the shared-memory opt-in is a per-device function attribute: set it once per device
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_dkdv<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
   k_bwd_dkdv<D, P><<<grid, 384, C::kSmemBytes, s>>>(a);
   return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_dkdv2_t(const BwdArgs& a, cudaStream_t s) {
+  using C = Bwd2Cfg<D>;
+  const int grid = a.nt * a.B * a.Hkv;
+  // the shared-memory opt-in is a per-device function attribute: set it once per device
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_dkdv2<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  k_bwd_dkdv2<D><<<grid, 512, C::kSmemBytes, s>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, bool precise, cudaStream_t s) {
-  if (a.D == 64) return precise ? launch_dkdv_t<64, true>(a, s) : launch_dkdv_t<64, false>(a, s);
-  return precise ? launch_dkdv_t<32, true>(a, s) : launch_dkdv_t<32, false>(a, s);
+  if (a.D == 64) return precise ? launch_dkdv_t<64, true>(a, s) : launch_dkdv2_t<64>(a, s);
+  return precise ? launch_dkdv_t<32, true>(a, s) : launch_dkdv2_t<32>(a, s);
 }
 
 }  // namespace ne

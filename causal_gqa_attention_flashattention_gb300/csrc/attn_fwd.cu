@@ -208,6 +208,11 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
     if (lane == 0) {
       constexpr uint32_t idS = idesc_fp16(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
+      constexpr uint32_t kStepK = 32 >> 4, kStepMN = (16 * C::kSpan) >> 4, kTileStep = C::kTileBytes >> 4;
+      // shared-memory descriptors, computed once (tile k adds k * bytes / 16 to the start address)
+      const uint64_t dQ0 = smem_desc(sQ, 16, C::kSBO, C::kSwz), dQlo0 = smem_desc(sQlo, 16, C::kSBO, C::kSwz);
+      const uint64_t dK0 = smem_desc(sK, 16, C::kSBO, C::kSwz), dKlo0 = smem_desc(sKlo, 16, C::kSBO, C::kSwz);
+      const uint64_t dV0 = smem_desc(sV, 16, C::kSBO, C::kSwz);
       bool ok = mbar_wait(q_ready, 0, abort);
       tc_fence_after();
       auto issue_pv = [&](int m) -> bool {
@@ -215,17 +220,10 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
         if (!mbar_wait(p_ready + sb, (m >> 1) & 1, abort)) return false;
         tc_fence_after();
         const uint32_t sP = tmem + C::kTmemS + sb * 128;
-#pragma unroll
-        for (int ks = 0; ks < kTile / 16; ks++)
-          mma_ts(tmem + hh * D, sP + ks * 8,
-                 smem_desc(sV + st * C::kTileBytes + ks * 16 * C::kSpan, 16, C::kSBO, C::kSwz), idPV,
-                 (jm > 0 || ks > 0) ? 1u : 0u);
-        if (PRECISE) {  // + P_lo V: the bf16 remainder of P sits in the buffer's upper 64 columns
-#pragma unroll
-          for (int ks = 0; ks < kTile / 16; ks++)
-            mma_ts(tmem + hh * D, sP + 64 + ks * 8,
-                   smem_desc(sV + st * C::kTileBytes + ks * 16 * C::kSpan, 16, C::kSBO, C::kSwz), idPV, 1u);
-        }
+        const uint64_t dV = dV0 + (uint64_t)(st * kTileStep);
+        mma_ts_chain<8>(tmem + hh * D, sP, dV, kStepMN, idPV, jm > 0 ? 1u : 0u);
+        if (PRECISE)  // + P_lo V: the bf16 remainder of P sits in the buffer's upper 64 columns
+          mma_ts_chain<8>(tmem + hh * D, sP + 64, dV, kStepMN, idPV, 1u);
         mma_commit(o_done + hh);
         if (hh == HC - 1) mma_commit(kv_empty + st);
         return true;
@@ -241,20 +239,13 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
         for (int hh = 0; hh < HC; hh++, n++) {
           const int sb = n & 1;
           // S = Qhi Khi^T (+ Qlo Khi^T + Qhi Klo^T)
-          const uint32_t qh = sQ + hh * C::kTileBytes, kh = sK + st * C::kTileBytes;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ks++)
-            mma_ss(tmem + C::kTmemS + sb * 128, smem_desc(qh + ks * 32, 16, C::kSBO, C::kSwz),
-                   smem_desc(kh + ks * 32, 16, C::kSBO, C::kSwz), idS, ks > 0 ? 1u : 0u);
+          const uint64_t qd = dQ0 + (uint64_t)(hh * kTileStep), kd = dK0 + (uint64_t)(st * kTileStep);
+          mma_ss_chain<D / 16>(tmem + C::kTmemS + sb * 128, qd, kStepK, kd, kStepK, idS, 0u);
           if (PRECISE) {
-            const uint32_t ql = sQlo + hh * C::kTileBytes, kl = sKlo + st * C::kTileBytes;
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ks++) {
-              mma_ss(tmem + C::kTmemS + sb * 128, smem_desc(ql + ks * 32, 16, C::kSBO, C::kSwz),
-                     smem_desc(kh + ks * 32, 16, C::kSBO, C::kSwz), idS, 1u);
-              mma_ss(tmem + C::kTmemS + sb * 128, smem_desc(qh + ks * 32, 16, C::kSBO, C::kSwz),
-                     smem_desc(kl + ks * 32, 16, C::kSBO, C::kSwz), idS, 1u);
-            }
+            mma_ss_chain<D / 16>(tmem + C::kTmemS + sb * 128, dQlo0 + (uint64_t)(hh * kTileStep), kStepK, kd,
+                                 kStepK, idS, 1u);
+            mma_ss_chain<D / 16>(tmem + C::kTmemS + sb * 128, qd, kStepK, dKlo0 + (uint64_t)(st * kTileStep),
+                                 kStepK, idS, 1u);
           }
           mma_commit(s_full + sb);
           if (n >= 1 && !issue_pv(n - 1)) {
@@ -477,8 +468,15 @@ template <int D, bool P>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
   using C = FwdCfg<D, P>;
   const int grid = a.nt * a.B * a.Hkv * (a.G / a.HC);
-  cudaError_t e = cudaFuncSetAttribute(k_attn_fwd<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  if (e != cudaSuccess) return e;
+  // the shared-memory opt-in is a per-device function attribute: set it once per device
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_fwd<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
   k_attn_fwd<D, P><<<grid, 256, C::kSmemBytes, s>>>(a);
   return cudaGetLastError();
 }

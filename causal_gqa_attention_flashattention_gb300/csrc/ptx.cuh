@@ -171,6 +171,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+      "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
@@ -232,6 +243,105 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Chains of NK MMAs into one accumulator, operand k at base + k * step (step in
+// 16-byte units, added to the descriptor's start-address field).  The first
+// MMA accumulates if `acc`, the rest always do.  All NK instructions sit in one
+// asm block with their predicates set once, so the issuing thread spends its
+// time on the MMAs themselves.
+template <int NK>
+__device__ __forceinline__ void mma_ss_chain(uint32_t d, uint64_t a, uint32_t a_step, uint64_t b, uint32_t b_step,
+                                             uint32_t idesc, uint32_t acc) {
+  static_assert(NK == 2 || NK == 4 || NK == 8, "chain length");
+  uint64_t ad[NK], bd[NK];
+#pragma unroll
+  for (int k = 0; k < NK; k++) {
+    ad[k] = a + (uint64_t)(k * a_step);
+    bd[k] = b + (uint64_t)(k * b_step);
+  }
+  if constexpr (NK == 2) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 q, %5, %5;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %3, %6, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %4, %6, q;\n\t}" ::"r"(d),
+        "l"(ad[0]), "l"(ad[1]), "l"(bd[0]), "l"(bd[1]), "r"(acc), "r"(idesc)
+        : "memory");
+  } else if constexpr (NK == 4) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %9, 0;\n\tsetp.eq.b32 q, %9, %9;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %10, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %10, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %10, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %10, q;\n\t}" ::"r"(d),
+        "l"(ad[0]), "l"(ad[1]), "l"(ad[2]), "l"(ad[3]), "l"(bd[0]), "l"(bd[1]), "l"(bd[2]), "l"(bd[3]),
+        "r"(acc), "r"(idesc)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %17, 0;\n\tsetp.eq.b32 q, %17, %17;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %18, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %18, q;\n\t}" ::"r"(d),
+        "l"(ad[0]), "l"(ad[1]), "l"(ad[2]), "l"(ad[3]), "l"(ad[4]), "l"(ad[5]), "l"(ad[6]), "l"(ad[7]),
+        "l"(bd[0]), "l"(bd[1]), "l"(bd[2]), "l"(bd[3]), "l"(bd[4]), "l"(bd[5]), "l"(bd[6]), "l"(bd[7]),
+        "r"(acc), "r"(idesc)
+        : "memory");
+  }
+}
+
+// Same with the A operand in tensor memory: A_k at TMEM column a + 8k (16
+// bf16/fp16 values per k-step).  SPLIT places k-steps 4..7 at a + 64 + 8(k-4):
+// an operand whose two 64-wide halves were written into separate column ranges.
+template <int NK, bool SPLIT = false>
+__device__ __forceinline__ void mma_ts_chain(uint32_t d, uint32_t a, uint64_t b, uint32_t b_step, uint32_t idesc,
+                                             uint32_t acc) {
+  static_assert(NK == 2 || NK == 4 || NK == 8, "chain length");
+  uint32_t at[NK];
+  uint64_t bd[NK];
+#pragma unroll
+  for (int k = 0; k < NK; k++) {
+    at[k] = a + ((SPLIT && k >= 4) ? 64u + 8u * (k - 4) : 8u * k);
+    bd[k] = b + (uint64_t)(k * b_step);
+  }
+  if constexpr (NK == 2) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 q, %5, %5;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %3, %6, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %4, %6, q;\n\t}" ::"r"(d),
+        "r"(at[0]), "r"(at[1]), "l"(bd[0]), "l"(bd[1]), "r"(acc), "r"(idesc)
+        : "memory");
+  } else if constexpr (NK == 4) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %9, 0;\n\tsetp.eq.b32 q, %9, %9;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %10, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %10, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %10, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %10, q;\n\t}" ::"r"(d),
+        "r"(at[0]), "r"(at[1]), "r"(at[2]), "r"(at[3]), "l"(bd[0]), "l"(bd[1]), "l"(bd[2]), "l"(bd[3]),
+        "r"(acc), "r"(idesc)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %17, 0;\n\tsetp.eq.b32 q, %17, %17;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %18, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %18, q;\n\t}" ::"r"(d),
+        "r"(at[0]), "r"(at[1]), "r"(at[2]), "r"(at[3]), "r"(at[4]), "r"(at[5]), "r"(at[6]), "r"(at[7]),
+        "l"(bd[0]), "l"(bd[1]), "l"(bd[2]), "l"(bd[3]), "l"(bd[4]), "l"(bd[5]), "l"(bd[6]), "l"(bd[7]),
+        "r"(acc), "r"(idesc)
+        : "memory");
+  }
+}
+
 // Arrive once on `bar` when all previously issued tcgen05 ops of this thread complete.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(

@@ -163,8 +163,15 @@ const char* ne_attn_status_string(int status);
  * counted).  ne_attn_profile_stop synchronises those events and fills, per
  * kernel kind (NE_ATTN_KERNEL_*), the summed device time in milliseconds and
  * the number of launches; arrays must hold NE_ATTN_NUM_KERNEL_KINDS entries.
- * Starting while a profile is open discards it.  Not for use during stream
- * capture.  Returns NE_OK or a negative ne_status.
+ * Starting while a profile is open discards it.  Returns NE_OK or a negative
+ * ne_status.
+ *
+ * Calls made while a stream is captured into a CUDA graph record their events
+ * into the graph, so the events are re-recorded each time the graph runs.  For
+ * that use, ne_attn_profile_detach() ends recording and keeps the events;
+ * ne_attn_profile_read() then returns, per kind, the device time and the count
+ * of timed launches of the most recent run, as often as needed, until the next
+ * ne_attn_profile_start.
  */
 #define NE_ATTN_KERNEL_FWD 0
 #define NE_ATTN_KERNEL_BWD_PREP 1
@@ -173,6 +180,8 @@ const char* ne_attn_status_string(int status);
 #define NE_ATTN_NUM_KERNEL_KINDS 4
 int ne_attn_profile_start(int capacity);
 int ne_attn_profile_stop(double* total_ms, long long* launches);
+int ne_attn_profile_detach(void);
+int ne_attn_profile_read(double* total_ms, long long* launches);
 
 /*
  * Test hook for the timeout path: launches one block that waits on a

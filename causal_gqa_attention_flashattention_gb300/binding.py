@@ -37,8 +37,10 @@ def lib():
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.ne_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         L.ne_attn_fwd.restype = i
-        L.ne_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        L.ne_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
         L.ne_attn_fwd_ex.restype = i
+        L.ne_attn_fwd_workspace_size.argtypes = [i, i, i, i, i, i]
+        L.ne_attn_fwd_workspace_size.restype = sz
         L.ne_attn_bwd_workspace_size.argtypes = [i, i, i, i, i, i]
         L.ne_attn_bwd_workspace_size.restype = sz
         L.ne_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
@@ -81,12 +83,18 @@ def _shape(q, k):
     return B, T, Hq, Hkv, D
 
 
+def fwd_workspace_size(B, T, Hq, Hkv, D, precise=False):
+    return int(lib().ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, PRECISE_QK if precise else 0))
+
+
 def attn_fwd(q, k, v, rope_base=10000.0, o=None, lse=None, o_dtype=torch.bfloat16, precise=False,
-             stream=None):
+             workspace=None, stream=None):
     """o, lse = causal GQA attention of q [B,T,Hq,D], k/v [B,T,Hkv,D] (bf16, CUDA).
 
     o_dtype: bfloat16 or float32.  precise: hi+lo split of the rotated q, k
-    for the logits (NE_ATTN_PRECISE_QK).
+    for the logits (NE_ATTN_PRECISE_QK).  workspace: a uint8 CUDA tensor of at
+    least fwd_workspace_size bytes (the rotated fp16 q, k land there); if None
+    one is allocated for the call.
     """
     B, T, Hq, Hkv, D = _shape(q, k)
     if o is None:
@@ -101,9 +109,13 @@ def attn_fwd(q, k, v, rope_base=10000.0, o=None, lse=None, o_dtype=torch.bfloat1
     assert o.dtype in (torch.bfloat16, torch.float32) and o.is_contiguous()
     assert lse.dtype == torch.float32 and lse.is_contiguous()
     flags = (O_FP32 if o.dtype == torch.float32 else 0) | (PRECISE_QK if precise else 0)
+    if workspace is None:
+        n = fwd_workspace_size(B, T, Hq, Hkv, D, precise)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    assert workspace.dtype == torch.uint8 and workspace.is_cuda
     _check("ne_attn_fwd_ex", lib().ne_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                                   B, T, Hq, Hkv, D, float(rope_base), flags,
-                                                  _stream(stream)))
+                                                  _ptr(workspace), workspace.numel(), _stream(stream)))
     return o, lse
 
 
@@ -159,7 +171,7 @@ def status_of_last_kernels(stream=None):
     return int(lib().ne_attn_check_status(_stream(stream)))
 
 
-KERNEL_KINDS = ("fwd", "bwd_prep", "bwd_dkdv", "bwd_dq")
+KERNEL_KINDS = ("fwd", "bwd_prep", "bwd_dkdv", "bwd_dq", "fwd_rope")
 
 
 def profile_start(capacity):

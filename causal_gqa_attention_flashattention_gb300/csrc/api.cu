@@ -83,11 +83,19 @@ struct RopeTable {
   float2* ptr;
 };
 
+// Library-owned forward workspace of one stream (calls that pass none).
+struct FwdScratch {
+  cudaStream_t stream;
+  void* ptr;
+  size_t bytes;
+};
+
 struct DeviceState {
   bool init = false;
   bool supported = false;
   int* status = nullptr;
   std::vector<RopeTable> tables;
+  std::vector<FwdScratch> fwd_scratch;
   unsigned char* static_scratch = nullptr;  // device address of g_static_scratch (set on first use)
 };
 
@@ -149,6 +157,40 @@ int rope_table(DeviceState& d, int D, double base, int Tneed, cudaStream_t s, co
   return NE_OK;
 }
 
+// Forward workspace owned by the library, one per stream, grown on demand.
+// Never allocates while `s` is being captured into a graph (that would end the
+// capture): a capture needs a workspace that is already large enough.
+// Requires g_mu held.
+int fwd_scratch(DeviceState& d, cudaStream_t s, size_t need, void** out) {
+  FwdScratch* f = nullptr;
+  for (auto& x : d.fwd_scratch)
+    if (x.stream == s) f = &x;
+  if (f && f->bytes >= need) {
+    *out = f->ptr;
+    return NE_OK;
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return NE_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return NE_ERR_WORKSPACE;
+  if (!f) {
+    d.fwd_scratch.push_back(FwdScratch{s, nullptr, 0});
+    f = &d.fwd_scratch.back();
+  }
+  if (f->ptr) {
+    // cudaFree waits for the device to finish the work that may still read it
+    if (cudaFree(f->ptr) != cudaSuccess) return NE_ERR_CUDA;
+    f->ptr = nullptr;
+    f->bytes = 0;
+  }
+  if (cudaMalloc(&f->ptr, need) != cudaSuccess) {
+    f->ptr = nullptr;
+    return NE_ERR_CUDA;
+  }
+  f->bytes = need;
+  *out = f->ptr;
+  return NE_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // 4-D map over a [B, T, H, D] bf16 tensor; box = one head, 128 rows, all D.
@@ -189,7 +231,7 @@ int check_shape(int B, int T, int Hq, int Hkv, int D) {
 }
 
 int heads_per_cta(int G, int D, bool precise) {
-  for (int hc = fwd_max_heads(D, precise); hc >= 1; hc--)
+  for (int hc = precise ? fwd_max_heads(D, true) : fwd2_max_heads(D); hc >= 1; hc--)
     if (G % hc == 0) return hc;
   return 1;
 }
@@ -198,13 +240,18 @@ struct WsLayout {
   size_t qr, kr, qlo, klo, lse2, lse2_lo, delta, dqacc, total;
 };
 
+// Workspace layouts.  Both start with the rotated fp16 q [B,T,Hq,D] and k
+// [B,T,Hkv,D]: the forward's workspace is that prefix alone.
+size_t ws_up(size_t x) { return (x + 255) / 256 * 256; }
+size_t fwd_ws_bytes(int B, int T, int Hq, int Hkv, int D) {
+  return ws_up(2 * (size_t)B * T * Hq * D) + ws_up(2 * (size_t)B * T * Hkv * D);
+}
+
 WsLayout ws_layout(int B, int T, int Hq, int Hkv, int D, bool precise) {
-  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  auto up = ws_up;
   const size_t Tp = (size_t)(T + kTile - 1) / kTile * kTile;
   WsLayout w;
   size_t off = 0;
-  w.dqacc = off;
-  off += up(sizeof(float) * (size_t)B * Hq * Tp * D);
   w.qr = off;
   off += up(2 * (size_t)B * T * Hq * D);
   w.kr = off;
@@ -216,6 +263,8 @@ WsLayout ws_layout(int B, int T, int Hq, int Hkv, int D, bool precise) {
     w.klo = off;
     off += up(2 * (size_t)B * T * Hkv * D);
   }
+  w.dqacc = off;
+  off += up(sizeof(float) * (size_t)B * Hq * Tp * D);
   w.lse2 = off;
   off += up(sizeof(float) * (size_t)B * Hq * Tp);
   w.lse2_lo = 0;
@@ -238,7 +287,7 @@ struct Profile {
   int used = 0;
   std::vector<cudaEvent_t> ev;  // 2 * capacity
   std::vector<int> kind;        // per timed launch
-  long long launches[NE_ATTN_NUM_KERNEL_KINDS] = {0, 0, 0, 0};
+  long long launches[NE_ATTN_NUM_KERNEL_KINDS] = {};
 };
 std::mutex g_prof_mu;
 Profile g_prof;
@@ -289,8 +338,14 @@ using namespace ne;
 
 extern "C" {
 
+size_t ne_attn_fwd_workspace_size(int B, int T, int Hq, int Hkv, int D, int flags) {
+  if (check_shape(B, T, Hq, Hkv, D) != NE_OK || (flags & ~(kFlagOFp32 | kFlagPreciseQK)) != 0) return 0;
+  return (flags & kFlagPreciseQK) ? 0 : fwd_ws_bytes(B, T, Hq, Hkv, D);
+}
+
 int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int Hq,
-                   int Hkv, int D, float rope_base, int flags, void* stream) {
+                   int Hkv, int D, float rope_base, int flags, void* workspace, size_t workspace_bytes,
+                   void* stream) {
   if (!q || !k || !v || !o || !lse) return NE_ERR_ARG;
   if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
   if ((flags & ~(kFlagOFp32 | kFlagPreciseQK)) != 0) return NE_ERR_ARG;
@@ -298,6 +353,9 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
   if (st != NE_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return NE_ERR_ALIGN;
   const bool precise = (flags & kFlagPreciseQK) != 0;
+  const size_t ws_need = precise ? 0 : fwd_ws_bytes(B, T, Hq, Hkv, D);
+  if (workspace && (workspace_bytes < ws_need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return NE_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lock(g_mu);
   int dev;
@@ -308,8 +366,30 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
   std::memset(&a, 0, sizeof(a));
   a.nt = (T + kTile - 1) / kTile;
   if ((st = rope_table(*d, D, (double)rope_base, a.nt * kTile, s, &a.rope)) != NE_OK) return st;
-  if ((st = make_map_bthd(&a.map_q, q, B, T, Hq, D)) != NE_OK) return st;
-  if ((st = make_map_bthd(&a.map_k, k, B, T, Hkv, D)) != NE_OK) return st;
+  if (precise) {
+    if ((st = make_map_bthd(&a.map_q, q, B, T, Hq, D)) != NE_OK) return st;
+    if ((st = make_map_bthd(&a.map_k, k, B, T, Hkv, D)) != NE_OK) return st;
+  } else {
+    void* ws = workspace;
+    if (!ws && (st = fwd_scratch(*d, s, ws_need, &ws)) != NE_OK) return st;
+    RopeArgs ra;
+    ra.q = static_cast<const __nv_bfloat16*>(q);
+    ra.k = static_cast<const __nv_bfloat16*>(k);
+    ra.qr = static_cast<__half*>(ws);
+    ra.kr = reinterpret_cast<__half*>(static_cast<unsigned char*>(ws) + ws_up(2 * (size_t)B * T * Hq * D));
+    ra.rope = a.rope;
+    ra.B = B;
+    ra.T = T;
+    ra.Hq = Hq;
+    ra.Hkv = Hkv;
+    ra.div_hq = make_fastdiv((uint32_t)Hq);
+    ra.div_hkv = make_fastdiv((uint32_t)Hkv);
+    ra.div_t = make_fastdiv((uint32_t)T);
+    if ((st = make_map_bthd(&a.map_q, ra.qr, B, T, Hq, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != NE_OK) return st;
+    if ((st = make_map_bthd(&a.map_k, ra.kr, B, T, Hkv, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != NE_OK) return st;
+    ProfScope prof(NE_ATTN_KERNEL_FWD_ROPE, s);
+    if (launch_rope_qk(ra, D, s) != cudaSuccess) return NE_ERR_CUDA;
+  }
   if ((st = make_map_bthd(&a.map_v, v, B, T, Hkv, D)) != NE_OK) return st;
   a.o = o;
   a.lse = lse;
@@ -321,6 +401,7 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
   a.D = D;
   a.G = Hq / Hkv;
   a.HC = heads_per_cta(a.G, D, precise);
+  a.kv_stages = fwd2_kv_stages(D, a.HC);
   a.o_fp32 = (flags & kFlagOFp32) ? 1 : 0;
   const double sl2 = 1.4426950408889634 / std::sqrt((double)D);
   a.scale_log2 = (float)sl2;
@@ -332,7 +413,7 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
 
 int ne_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int Hq, int Hkv,
                 int D, float rope_base, void* stream) {
-  return ne_attn_fwd_ex(q, k, v, o, lse, B, T, Hq, Hkv, D, rope_base, 0, stream);
+  return ne_attn_fwd_ex(q, k, v, o, lse, B, T, Hq, Hkv, D, rope_base, 0, nullptr, 0, stream);
 }
 
 size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D, int flags) {
@@ -400,6 +481,10 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   p.Hkv = Hkv;
   p.D = D;
   p.Tp = Tp;
+  p.div_hq = make_fastdiv((uint32_t)Hq);
+  p.div_hkv = make_fastdiv((uint32_t)Hkv);
+  p.div_t = make_fastdiv((uint32_t)T);
+  p.div_pad = make_fastdiv((uint32_t)(Tp > T ? Tp - T : 1));
   {
     ProfScope prof(NE_ATTN_KERNEL_BWD_PREP, s);
     if (launch_bwd_prep(p, s) != cudaSuccess) return NE_ERR_CUDA;
@@ -452,6 +537,8 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   qa.Tp = Tp;
   qa.grad_fp32 = grad_fp32;
   qa.scale = (float)scale;
+  qa.div_hq = make_fastdiv((uint32_t)Hq);
+  qa.div_t = make_fastdiv((uint32_t)T);
   {
     ProfScope prof(NE_ATTN_KERNEL_BWD_DQ, s);
     if (launch_bwd_dq(qa, s) != cudaSuccess) return NE_ERR_CUDA;
@@ -514,7 +601,7 @@ int ne_attn_profile_stop(double* total_ms, long long* launches) {
   std::lock_guard<std::mutex> lock(g_prof_mu);
   if (!g_prof.on) return NE_ERR_ARG;
   int st = NE_OK;
-  double tot[NE_ATTN_NUM_KERNEL_KINDS] = {0, 0, 0, 0};
+  double tot[NE_ATTN_NUM_KERNEL_KINDS] = {};
   for (int i = 0; i < g_prof.used; i++) {
     float ms = 0.f;
     if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess ||
@@ -543,8 +630,8 @@ int ne_attn_profile_read(double* total_ms, long long* launches) {
   std::lock_guard<std::mutex> lock(g_prof_mu);
   if (g_prof.ev.empty()) return NE_ERR_ARG;
   int st = NE_OK;
-  double tot[NE_ATTN_NUM_KERNEL_KINDS] = {0, 0, 0, 0};
-  long long cnt[NE_ATTN_NUM_KERNEL_KINDS] = {0, 0, 0, 0};
+  double tot[NE_ATTN_NUM_KERNEL_KINDS] = {};
+  long long cnt[NE_ATTN_NUM_KERNEL_KINDS] = {};
   for (int i = 0; i < g_prof.used; i++) {
     float ms = 0.f;
     if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess ||
@@ -648,6 +735,10 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
   p.Hkv = Hkv;
   p.D = D;
   p.Tp = Tp;
+  p.div_hq = make_fastdiv((uint32_t)Hq);
+  p.div_hkv = make_fastdiv((uint32_t)Hkv);
+  p.div_t = make_fastdiv((uint32_t)T);
+  p.div_pad = make_fastdiv((uint32_t)(Tp > T ? Tp - T : 1));
   if (launch_bwd_prep(p, s) != cudaSuccess) return NE_ERR_CUDA;
 
   BwdArgs a;
@@ -694,6 +785,8 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
   qa.Tp = Tp;
   qa.grad_fp32 = grad_fp32;
   qa.scale = (float)scale;
+  qa.div_hq = make_fastdiv((uint32_t)Hq);
+  qa.div_t = make_fastdiv((uint32_t)T);
   if (launch_bwd_dq(qa, s) != cudaSuccess) return NE_ERR_CUDA;
   return NE_OK;
 }

@@ -44,25 +44,38 @@ __device__ __forceinline__ void record_timeout(int* status, volatile int* abort)
 template <int D>
 __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
   constexpr int kCPR = D / 8;  // 16-byte chunks (8 bf16) per row
-  const long long gtid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  const long long nthr = (long long)gridDim.x * blockDim.x;  // a multiple of 32
-  const int lane = threadIdx.x & 31;
+  constexpr int kShift = D == 64 ? 3 : 2;
+  const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
+  const uint32_t nthr = gridDim.x * blockDim.x;  // a multiple of 32
 
   // (A) query rows: rotate q, Delta = dO . O, lse2 = lse * log2(e)
-  const long long nA = (long long)a.B * a.T * a.Hq * kCPR;
-  const long long nA32 = (nA + 31) / 32 * 32;
-  for (long long it = gtid; it < nA32; it += nthr) {
+  const uint32_t nA = (uint32_t)a.B * a.T * a.Hq * kCPR;
+  const uint32_t nA32 = (nA + 31u) / 32u * 32u;
+  for (uint32_t it = gtid; it < nA32; it += nthr) {
     const bool valid = it < nA;
     float part = 0.f;
-    long long row = 0;
+    uint32_t h = 0, t = 0, b = 0;
     int c = 0;
     if (valid) {
-      row = it / kCPR;
-      c = (int)(it % kCPR);
-      const int t = (int)((row / a.Hq) % a.T);
+      const uint32_t row = it >> kShift;  // (b, t, h)
+      c = (int)(it & (kCPR - 1));
+      const uint32_t bt = fdiv(row, a.div_hq);
+      h = row - bt * a.Hq;
+      b = fdiv(bt, a.div_t);
+      t = bt - b * a.T;
       const uint4 qv = __ldg(reinterpret_cast<const uint4*>(a.q) + it);
+      const uint4 dv = __ldg(reinterpret_cast<const uint4*>(a.dout) + it);
+      float4 o0, o1;
+      uint4 ov;
+      if (a.o_fp32) {
+        const float4* op = reinterpret_cast<const float4*>(a.o) + 2 * (size_t)it;
+        o0 = __ldg(op);
+        o1 = __ldg(op + 1);
+      } else {
+        ov = __ldg(reinterpret_cast<const uint4*>(a.o) + it);
+      }
       float4 c0, c1;
-      rope_coeffs<D>(a.rope, t, c, c0, c1);
+      rope_coeffs<D>(a.rope, (int)t, c, c0, c1);
       if (a.qlo) {
         uint4 l;
         reinterpret_cast<uint4*>(a.qr)[it] = rope_chunk_f16(qv, c0, c1, &l);
@@ -70,15 +83,11 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
       } else {
         reinterpret_cast<uint4*>(a.qr)[it] = rope_chunk_f16(qv, c0, c1, nullptr);
       }
-      const uint4 dv = __ldg(reinterpret_cast<const uint4*>(a.dout) + it);
       const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
       if (a.o_fp32) {
-        const float4* op = reinterpret_cast<const float4*>(a.o) + 2 * it;
-        const float4 o0 = __ldg(op), o1 = __ldg(op + 1);
         part = o0.x * bf_lo(dw[0]) + o0.y * bf_hi(dw[0]) + o0.z * bf_lo(dw[1]) + o0.w * bf_hi(dw[1]) +
                o1.x * bf_lo(dw[2]) + o1.y * bf_hi(dw[2]) + o1.z * bf_lo(dw[3]) + o1.w * bf_hi(dw[3]);
       } else {
-        const uint4 ov = __ldg(reinterpret_cast<const uint4*>(a.o) + it);
         const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
 #pragma unroll
         for (int p = 0; p < 4; p++) part += bf_lo(ow[p]) * bf_lo(dw[p]) + bf_hi(ow[p]) * bf_hi(dw[p]);
@@ -87,9 +96,6 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
 #pragma unroll
     for (int off = kCPR / 2; off >= 1; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
     if (valid && c == 0) {
-      const int h = (int)(row % a.Hq);
-      const long long bt = row / a.Hq;
-      const int t = (int)(bt % a.T), b = (int)(bt / a.T);
       const size_t o = ((size_t)b * a.Hq + h) * a.Tp + t;
       a.delta[o] = part;
       const size_t li = ((size_t)b * a.Hq + h) * a.T + t;
@@ -104,16 +110,16 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
       }
     }
   }
-  (void)lane;
   // (B) key rows: rotate k
-  const long long nB = (long long)a.B * a.T * a.Hkv * kCPR;
-  for (long long it = gtid; it < nB; it += nthr) {
-    const long long row = it / kCPR;
-    const int c = (int)(it % kCPR);
-    const int t = (int)((row / a.Hkv) % a.T);
+  const uint32_t nB = (uint32_t)a.B * a.T * a.Hkv * kCPR;
+  for (uint32_t it = gtid; it < nB; it += nthr) {
+    const uint32_t row = it >> kShift;
+    const int c = (int)(it & (kCPR - 1));
+    const uint32_t bt = fdiv(row, a.div_hkv);
+    const uint32_t t = bt - fdiv(bt, a.div_t) * a.T;
     const uint4 kv = __ldg(reinterpret_cast<const uint4*>(a.k) + it);
     float4 c0, c1;
-    rope_coeffs<D>(a.rope, t, c, c0, c1);
+    rope_coeffs<D>(a.rope, (int)t, c, c0, c1);
     if (a.klo) {
       uint4 l;
       reinterpret_cast<uint4*>(a.kr)[it] = rope_chunk_f16(kv, c0, c1, &l);
@@ -123,17 +129,17 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
     }
   }
   // (C) zero the dQ accumulator [B, Hq, Tp, D]
-  const long long nC = (long long)a.B * a.Hq * a.Tp * D / 4;
-  for (long long it = gtid; it < nC; it += nthr) reinterpret_cast<float4*>(a.dqacc)[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const uint32_t nC = (uint32_t)a.B * a.Hq * a.Tp * (D / 4);
+  for (uint32_t it = gtid; it < nC; it += nthr) reinterpret_cast<float4*>(a.dqacc)[it] = make_float4(0.f, 0.f, 0.f, 0.f);
   // (D) padded rows t in [T, Tp): no probability mass (lse2 = +inf), Delta = 0
-  const int npad = a.Tp - a.T;
-  const long long nD = (long long)a.B * a.Hq * npad;
-  for (long long it = gtid; it < nD; it += nthr) {
-    const long long bh = it / npad;
-    const int t = a.T + (int)(it % npad);
-    a.delta[bh * a.Tp + t] = 0.f;
-    a.lse2[bh * a.Tp + t] = __int_as_float(0x7f800000);
-    if (a.lse2_lo) a.lse2_lo[bh * a.Tp + t] = 0.f;
+  const uint32_t npad = (uint32_t)(a.Tp - a.T);
+  const uint32_t nD = (uint32_t)a.B * a.Hq * npad;
+  for (uint32_t it = gtid; it < nD; it += nthr) {
+    const uint32_t bh = fdiv(it, a.div_pad);
+    const uint32_t t = (uint32_t)a.T + (it - bh * npad);
+    a.delta[(size_t)bh * a.Tp + t] = 0.f;
+    a.lse2[(size_t)bh * a.Tp + t] = __int_as_float(0x7f800000);
+    if (a.lse2_lo) a.lse2_lo[(size_t)bh * a.Tp + t] = 0.f;
   }
 }
 
@@ -141,18 +147,19 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
 template <int D>
 __global__ void __launch_bounds__(256) k_bwd_dq(const DqArgs a) {
   constexpr int kCPR = D / 8;
-  const long long n = (long long)a.B * a.T * a.Hq * kCPR;
-  for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < n;
-       it += (long long)gridDim.x * blockDim.x) {
-    const long long row = it / kCPR;  // (b, t, h)
-    const int c = (int)(it % kCPR);
-    const int h = (int)(row % a.Hq);
-    const long long bt = row / a.Hq;
-    const int t = (int)(bt % a.T), b = (int)(bt / a.T);
+  constexpr int kShift = D == 64 ? 3 : 2;
+  const uint32_t n = (uint32_t)a.B * a.T * a.Hq * kCPR;
+  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < n; it += gridDim.x * blockDim.x) {
+    const uint32_t row = it >> kShift;  // (b, t, h)
+    const int c = (int)(it & (kCPR - 1));
+    const uint32_t bt = fdiv(row, a.div_hq);
+    const uint32_t h = row - bt * a.Hq;
+    const uint32_t b = fdiv(bt, a.div_t);
+    const uint32_t t = bt - b * a.T;
     const float4* src = reinterpret_cast<const float4*>(a.dqacc + (((size_t)b * a.Hq + h) * a.Tp + t) * D + c * 8);
     const float4 x0 = src[0], x1 = src[1];
     float4 c0, c1;
-    rope_coeffs<D>(a.rope, t, c, c0, c1);
+    rope_coeffs<D>(a.rope, (int)t, c, c0, c1);
     const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
     const float cs[4] = {c0.x, c0.z, c1.x, c1.z}, sn[4] = {c0.y, c0.w, c1.y, c1.w};
     float y[8];
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(256) k_bwd_dq(const DqArgs a) {
       y[2 * p + 1] = a.scale * (xs[2 * p + 1] * cs[p] - xs[2 * p] * sn[p]);
     }
     if (a.grad_fp32) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.dq) + it * 8);
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.dq) + (size_t)it * 8);
       dst[0] = make_float4(y[0], y[1], y[2], y[3]);
       dst[1] = make_float4(y[4], y[5], y[6], y[7]);
     } else {

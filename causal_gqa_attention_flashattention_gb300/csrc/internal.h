@@ -23,7 +23,10 @@ constexpr int kFlagPreciseQK = 4;  // logits from hi + lo fp16 parts of rotated 
 inline int fwd_max_heads(int D, bool precise) { return D == 64 ? (precise ? 3 : 4) : 8; }
 
 struct FwdArgs {
-  CUtensorMap map_q, map_k, map_v;  // 4-D tiled maps over [B, T, H, D], box D x 1 x 128 x 1
+  // 4-D tiled maps over [B, T, H, D], box D x 1 x 128 x 1.  Default precision:
+  // map_q / map_k cover the rotated fp16 copies made by the RoPE pre-pass;
+  // precise logits: the bf16 inputs (the kernel rotates them itself).
+  CUtensorMap map_q, map_k, map_v;
   void* o;                          // [B, T, Hq, D] bf16 or fp32
   float* lse;                       // [B, Hq, T]
   float* lse_lo;                    // [B, Hq, T] fp32 remainder of lse (precise logits only)
@@ -34,6 +37,48 @@ struct FwdArgs {
   int o_fp32;
   float scale_log2;                 // log2(e) / sqrt(D), rounded to fp32
   float scale_log2_lo;              // remainder log2(e)/sqrt(D) - scale_log2
+  int kv_stages;                    // K/V ring depth (persistent kernel)
+};
+
+// Persistent forward kernel (default precision): heads per CTA limit and its
+// shared-memory plan for a given HC.  Besides the Q double buffer and the K/V
+// ring: the row statistics (m, l) of every head and the barriers.
+inline int fwd2_max_heads(int D) { return D == 64 ? 4 : 8; }
+inline int fwd2_misc_bytes(int D) { return 2 * fwd2_max_heads(D) * 128 * 4 + 64 * 8 + 16; }
+inline int fwd2_kv_stages(int D, int HC) {
+  const int tile = 128 * D * 2;
+  const int s = (232448 - 1024 - fwd2_misc_bytes(D) - 2 * HC * tile) / (2 * tile);
+  return s > 3 ? 3 : s;
+}
+inline int fwd2_smem_bytes(int D, int HC) {
+  const int tile = 128 * D * 2;
+  return 2 * HC * tile + fwd2_kv_stages(D, HC) * 2 * tile + fwd2_misc_bytes(D) + 1024;
+}
+
+// Division of a non-negative 32-bit n < 2^31 by a runtime divisor d >= 1 with
+// a multiply-high and a shift (round-up magic number):
+//   l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1, n / d = (umulhi(n, m) + n) >> l.
+struct FastDiv {
+  uint32_t d, m, l;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) l++;
+  const uint64_t m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
+  return FastDiv{d, (uint32_t)m, l};
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) { return (__umulhi(n, f.m) + n) >> f.l; }
+#endif
+
+// RoPE pre-pass of the forward: q, k (bf16) -> rotated fp16 copies qr, kr.
+struct RopeArgs {
+  const __nv_bfloat16 *q, *k;
+  __half *qr, *kr;
+  const float2* rope;
+  int B, T, Hq, Hkv;
+  FastDiv div_hq, div_hkv, div_t;
 };
 
 struct BwdArgs {
@@ -61,6 +106,7 @@ struct PrepArgs {
   float *lse2, *lse2_lo, *delta, *dqacc;
   const float2* rope;
   int B, T, Hq, Hkv, D, Tp, o_fp32;
+  FastDiv div_hq, div_hkv, div_t, div_pad;  // by Hq, Hkv, T and Tp - T (pad rows; d = 1 if none)
 };
 
 struct DqArgs {
@@ -69,9 +115,11 @@ struct DqArgs {
   const float2* rope;
   int B, T, Hq, D, Tp, grad_fp32;
   float scale;
+  FastDiv div_hq, div_t;
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, bool precise, cudaStream_t s);
+cudaError_t launch_rope_qk(const RopeArgs& a, int D, cudaStream_t s);
 cudaError_t launch_bwd_prep(const PrepArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, bool precise, cudaStream_t s);
 cudaError_t launch_bwd_dq(const DqArgs& a, cudaStream_t s);

@@ -73,20 +73,40 @@ typedef enum {
 
 /*
  * Forward pass: writes o (bfloat16) and lse.  Same as ne_attn_fwd_ex with
- * flags = 0.
- * One kernel: the rotary embedding of Q and K is applied to the tiles in
- * shared memory (the rotated values never reach HBM) and rounded to fp16
- * for the tensor cores; K/V tiles are loaded once per key/value head and
- * shared by the query heads of its group; S = Q K^T and O += P V run on the
- * tensor cores (fp32 accumulation in tensor memory; P is bf16) with an online
- * softmax in between.  Returns NE_OK or a negative ne_status.
+ * flags = 0 and no workspace.
+ * Two kernels.  A streaming pre-pass applies the rotary embedding to q and k
+ * and stores the rotated values as fp16 (3 more mantissa bits than bf16) in
+ * the workspace.  The attention kernel then runs one CTA per SM over work
+ * items (query tile x query heads of one key/value head): K/V tiles are
+ * loaded once per key/value head and shared by the query heads of its group;
+ * S = Q K^T and O += P V run on the tensor cores (fp32 accumulation in tensor
+ * memory; P is bf16) with an online softmax in between.  Returns NE_OK or a
+ * negative ne_status.
  */
 int ne_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
                 int Hq, int Hkv, int D, float rope_base, void* stream);
 
-/* Forward pass with flags (NE_ATTN_O_FP32, NE_ATTN_PRECISE_QK; others rejected). */
+/*
+ * Bytes of device workspace the forward needs for this shape and flags: the
+ * rotated q [B,T,Hq,D] and k [B,T,Hkv,D] as fp16, each rounded up to 256
+ * bytes (0 with NE_ATTN_PRECISE_QK, whose kernel rotates the tiles in shared
+ * memory).  The same two arrays start the backward's workspace, at the same
+ * offsets.  Returns 0 for unsupported shapes or flags.
+ */
+size_t ne_attn_fwd_workspace_size(int B, int T, int Hq, int Hkv, int D, int flags);
+
+/*
+ * Forward pass with flags (NE_ATTN_O_FP32, NE_ATTN_PRECISE_QK; others
+ * rejected) and an optional caller workspace (256-byte aligned, at least
+ * ne_attn_fwd_workspace_size bytes, else NE_ERR_WORKSPACE; the caller owns it
+ * and must not touch it until the call's work on `stream` is done).  With
+ * workspace = NULL the library uses a buffer of its own per stream, grown
+ * with cudaMalloc when a larger shape arrives; while the stream is captured
+ * into a CUDA graph it cannot grow and the call returns NE_ERR_WORKSPACE.
+ */
 int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
-                   int Hq, int Hkv, int D, float rope_base, int flags, void* stream);
+                   int Hq, int Hkv, int D, float rope_base, int flags, void* workspace,
+                   size_t workspace_bytes, void* stream);
 
 /*
  * Bytes of device workspace ne_attn_bwd needs for this shape and flags
@@ -177,7 +197,8 @@ const char* ne_attn_status_string(int status);
 #define NE_ATTN_KERNEL_BWD_PREP 1
 #define NE_ATTN_KERNEL_BWD_DKDV 2
 #define NE_ATTN_KERNEL_BWD_DQ 3
-#define NE_ATTN_NUM_KERNEL_KINDS 4
+#define NE_ATTN_KERNEL_FWD_ROPE 4 /* the forward's RoPE pre-pass */
+#define NE_ATTN_NUM_KERNEL_KINDS 5
 int ne_attn_profile_start(int capacity);
 int ne_attn_profile_stop(double* total_ms, long long* launches);
 int ne_attn_profile_detach(void);

@@ -43,6 +43,18 @@ def test_workspace_size(libne):
     assert libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 64, 8) == 0
 
 
+def test_fwd_workspace_size(libne):
+    B, T, Hq, Hkv, D = 16, 512, 12, 4, 64
+    n = libne.ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, 0)
+    assert n == 2 * B * T * (Hq + Hkv) * D  # rotated fp16 q and k (both already 256-byte multiples)
+    assert libne.ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, 1) == n  # fp32 o changes nothing
+    assert libne.ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, 4) == 0  # precise kernel rotates in shared memory
+    assert libne.ne_attn_fwd_workspace_size(1, 3, 1, 1, 32, 0) == 2 * 256  # each array rounded to 256 bytes
+    assert libne.ne_attn_fwd_workspace_size(1, 16, 2, 1, 64, 2) == 0  # gradient flag is not a forward flag
+    # the backward's workspace starts with the same two arrays
+    assert libne.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, D, 0) >= n + 4 * B * Hq * T * D
+
+
 def test_host_argument_checks(libne):
     buf = ctypes.create_string_buffer(4096 + 64)
     base = (ctypes.addressof(buf) + 63) // 64 * 64
@@ -55,7 +67,9 @@ def test_host_argument_checks(libne):
     assert libne.ne_attn_fwd(p, p, p, p, p, 1, 16, 2, 1, 48, 10000.0, null) == -3
     assert libne.ne_attn_fwd(p, p, p, p, p, 1, 16, 2, 1, 64, 0.5, null) == -1
     assert libne.ne_attn_fwd(mis, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, null) == -2
-    assert libne.ne_attn_fwd_ex(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 2, null) == -1  # grad flag on fwd
+    assert libne.ne_attn_fwd_ex(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 2, null, 0, null) == -1  # grad flag on fwd
+    assert libne.ne_attn_fwd_ex(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 0, p, 16, null) == -5  # workspace too small
+    assert libne.ne_attn_fwd_ex(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 0, mis, 1 << 20, null) == -5  # misaligned
     assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 8, p, 4096, null) == -1
     assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 0, p, 16, null) == -5
     assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 0, mis, 1 << 20, null) == -5

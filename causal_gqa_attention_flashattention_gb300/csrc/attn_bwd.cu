@@ -755,7 +755,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv2(const __grid_constant__ Bw
   uint64_t* ds_free = bars + 12;   // [2]
   uint64_t* dq_full = bars + 14;
   uint64_t* dq_free = bars + 15;
-  uint64_t* drain = bars + 16;
+  uint64_t* drain = bars + 16;     // [3] one per MMA-issuing thread
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -773,17 +773,17 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv2(const __grid_constant__ Bw
     mbar_init(kv_tmem, 256);
     for (int s = 0; s < 2; s++) {
       mbar_init(qd_full + s, 1);
-      mbar_init(qd_empty + s, 1);
+      mbar_init(qd_empty + s, 2);  // released by the dV/S^T and the dK/dP^T issuers
       mbar_init(ds_ready + s, 256);
       mbar_init(ds_free + s, 1);
     }
     mbar_init(s_full, 1);
     mbar_init(p_ready, 256);
     mbar_init(dp_full, 1);
-    mbar_init(acc_done, 1);
+    mbar_init(acc_done, 2);  // dV and dK issuers
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 128);
-    mbar_init(drain, 1);
+    for (int s = 0; s < 3; s++) mbar_init(drain + s, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
@@ -824,8 +824,14 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv2(const __grid_constant__ Bw
       for (int n = loaded - C::kStages < 0 ? 0 : loaded - C::kStages; n < loaded; n++)
         mbar_wait(qd_full + n % C::kStages, (n / C::kStages) & 1, &never);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= 1 && warp <= 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread issues about one MMA per 70-120 cycles, so the step's 32 MMAs
+    // are spread over three threads (warps 1-3).  Each overwrite of a TMEM
+    // operand stays in the program order of the thread that read it:
+    //   warp 1: dV(n) += P^T(n) dO, then S^T(n+1) over the P^T columns;
+    //   warp 2: dK(n) += dS^T(n) Q, then dP^T(n+1) over the dS^T columns;
+    //   warp 3: the dQ tile = dS(n) K (dS from shared memory).
     if (lane == 0) {
       constexpr uint32_t idS = idesc_fp16(128, 128, false, false);   // K^ (TMEM) x Q^ (K-major)
       constexpr uint32_t idDP = idesc_bf16(128, 128, false, false);  // V (TMEM) x dO (K-major)
@@ -845,50 +851,64 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv2(const __grid_constant__ Bw
       auto dQs = [&](int st) { return dQ0 + (uint64_t)(st * (C::kTileBytes >> 4)); };
       auto dDOs = [&](int st) { return dDO0 + (uint64_t)(st * (C::kTileBytes >> 4)); };
       auto dDS = [&](int k) { return dDS0 + (uint64_t)(k * (C::kDsBytes >> 4)); };
-      bool ok = mbar_wait(kv_tmem, 0, abort) && mbar_wait(qd_full, 0, abort);
-      tc_fence_after();
-      if (ok) {
-        mma_ts_chain<KD>(tmem + C::kColS, tmem + C::kColK, dQs(0), kStepK, idS, 0);
-        mma_commit(s_full);
-        mma_ts_chain<KD>(tmem + C::kColDP, tmem + C::kColV, dDOs(0), kStepK, idDP, 0);
-        mma_commit(dp_full);
-      }
-      for (int n = 0; ok && n < N; n++) {
-        const int st = n % C::kStages;
-        // dV += P^T dO
-        if (!(ok = mbar_wait(p_ready, n & 1, abort))) break;
-        tc_fence_after();
-        mma_ts_chain<8, true>(tmem + C::kColDV, tmem + C::kColS, dDOs(st), kStepMN, idDV, n > 0 ? 1u : 0u);
-        // next S^T (its TMEM columns were just read by the dV MMAs above)
-        const int st1 = (n + 1) % C::kStages;
-        if (n + 1 < N) {
-          if (!(ok = mbar_wait(qd_full + st1, ((n + 1) / C::kStages) & 1, abort))) break;
+      bool ok = true;
+      if (warp == 1) {
+        if ((ok = mbar_wait(kv_tmem, 0, abort) && mbar_wait(qd_full, 0, abort))) {
           tc_fence_after();
-          mma_ts_chain<KD>(tmem + C::kColS, tmem + C::kColK, dQs(st1), kStepK, idS, 0);
+          mma_ts_chain<KD>(tmem + C::kColS, tmem + C::kColK, dQs(0), kStepK, idS, 0);
           mma_commit(s_full);
         }
-        // dK += dS^T Q^ (dS^T in TMEM over the dP^T columns), dQ tile = dS K^ (dS from shared memory)
-        const int dsb = n % C::kDsBufs;
-        if (!(ok = mbar_wait(ds_ready + dsb, (n / C::kDsBufs) & 1, abort))) break;
-        tc_fence_after();
-        mma_ts_chain<8, true>(tmem + C::kColDK, tmem + C::kColDP, dQs(st), kStepMN, idDK, n > 0 ? 1u : 0u);
-        if (n >= 1) {
-          if (!(ok = mbar_wait(dq_free, (n - 1) & 1, abort))) break;
+        for (int n = 0; ok && n < N; n++) {
+          const int st = n % C::kStages, st1 = (n + 1) % C::kStages;
+          if (!(ok = mbar_wait(p_ready, n & 1, abort))) break;
           tc_fence_after();
+          mma_ts_chain<8, true>(tmem + C::kColDV, tmem + C::kColS, dDOs(st), kStepMN, idDV, n > 0 ? 1u : 0u);
+          mma_commit(qd_empty + st);  // this thread's reads of stage st: Q^ by S^T(n), dO by dV(n)
+          if (n + 1 < N) {
+            if (!(ok = mbar_wait(qd_full + st1, ((n + 1) / C::kStages) & 1, abort))) break;
+            tc_fence_after();
+            mma_ts_chain<KD>(tmem + C::kColS, tmem + C::kColK, dQs(st1), kStepK, idS, 0);
+            mma_commit(s_full);
+          }
         }
-        mma_ss_chain<8>(tmem + C::kColDQ, dDS(dsb), 2048 >> 4, dK, kStepMN, idDQ, 0);
-        mma_commit(dq_full);
-        mma_commit(ds_free + dsb);
-        mma_commit(qd_empty + st);
-        if (n + 1 < N) {  // next dP^T (its columns were read by the compute warps before ds_ready)
-          mma_ts_chain<KD>(tmem + C::kColDP, tmem + C::kColV, dDOs(st1), kStepK, idDP, 0);
+        mma_commit(acc_done);
+      } else if (warp == 2) {
+        if ((ok = mbar_wait(kv_tmem, 0, abort) && mbar_wait(qd_full, 0, abort))) {
+          tc_fence_after();
+          mma_ts_chain<KD>(tmem + C::kColDP, tmem + C::kColV, dDOs(0), kStepK, idDP, 0);
           mma_commit(dp_full);
+        }
+        for (int n = 0; ok && n < N; n++) {
+          const int st = n % C::kStages, st1 = (n + 1) % C::kStages;
+          const int dsb = n % C::kDsBufs;
+          if (!(ok = mbar_wait(ds_ready + dsb, (n / C::kDsBufs) & 1, abort))) break;
+          tc_fence_after();
+          mma_ts_chain<8, true>(tmem + C::kColDK, tmem + C::kColDP, dQs(st), kStepMN, idDK, n > 0 ? 1u : 0u);
+          mma_commit(qd_empty + st);  // this thread's reads of stage st: dO by dP^T(n), Q^ by dK(n)
+          if (n + 1 < N) {
+            if (!(ok = mbar_wait(qd_full + st1, ((n + 1) / C::kStages) & 1, abort))) break;
+            tc_fence_after();
+            mma_ts_chain<KD>(tmem + C::kColDP, tmem + C::kColV, dDOs(st1), kStepK, idDP, 0);
+            mma_commit(dp_full);
+          }
+        }
+        mma_commit(acc_done);
+      } else {
+        ok = mbar_wait(kv_full, 0, abort);  // K^ in shared memory
+        for (int n = 0; ok && n < N; n++) {
+          const int dsb = n % C::kDsBufs;
+          if (!(ok = mbar_wait(ds_ready + dsb, (n / C::kDsBufs) & 1, abort))) break;
+          if (n >= 1 && !(ok = mbar_wait(dq_free, (n - 1) & 1, abort))) break;
+          tc_fence_after();
+          mma_ss_chain<8>(tmem + C::kColDQ, dDS(dsb), 2048 >> 4, dK, kStepMN, idDQ, 0);
+          mma_commit(dq_full);
+          mma_commit(ds_free + dsb);
         }
       }
       if (!ok) record_timeout(a.status, abort);
-      mma_commit(acc_done);
-      mma_commit(drain);
-      mbar_wait(drain, 0, &never);
+      uint64_t* my_drain = drain + (warp - 1);
+      mma_commit(my_drain);
+      mbar_wait(my_drain, 0, &never);
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ P and dS, half the query columns each
@@ -933,31 +953,31 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv2(const __grid_constant__ Bw
       tc_fence_after();
       uint32_t pk[32];  // P^T for this thread's 64 query columns, packed bf16 pairs
 #pragma unroll
-      for (int c = 0; c < 4; c++) {
-        uint32_t u[16];
-        tmem_ld16(trow + C::kColS + cbase + c * 16, u);
-        float l2[16];
+      for (int c2 = 0; c2 < 2; c2++) {
+        // two 16-column loads in flight per wait
+        uint32_t u[32];
+        tmem_ld16(trow + C::kColS + cbase + c2 * 32, *reinterpret_cast<uint32_t(*)[16]>(u));
+        tmem_ld16(trow + C::kColS + cbase + c2 * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
+        float l2[32];
 #pragma unroll
-        for (int v4 = 0; v4 < 4; v4++) {
-          const float4 t4 = reinterpret_cast<const float4*>(lse2 + c * 16)[v4];
+        for (int v4 = 0; v4 < 8; v4++) {
+          const float4 t4 = reinterpret_cast<const float4*>(lse2 + c2 * 32)[v4];
           l2[4 * v4] = t4.x, l2[4 * v4 + 1] = t4.y, l2[4 * v4 + 2] = t4.z, l2[4 * v4 + 3] = t4.w;
         }
         tmem_wait_ld();
-        uint32_t w[8];
 #pragma unroll
-        for (int e = 0; e < 8; e++) {
-          const int q0 = cbase + c * 16 + 2 * e;
+        for (int e = 0; e < 16; e++) {
+          const int q0 = cbase + c2 * 32 + 2 * e;
           float p0 = ex2(fmaf(__uint_as_float(u[2 * e]), sl2, -l2[2 * e]));
           float p1 = ex2(fmaf(__uint_as_float(u[2 * e + 1]), sl2, -l2[2 * e + 1]));
           if (diag) {
             if (q0 < r) p0 = 0.f;
             if (q0 + 1 < r) p1 = 0.f;
           }
-          w[e] = pack_bf16(p0, p1);
-          pk[c * 8 + e] = w[e];
+          pk[c2 * 16 + e] = pack_bf16(p0, p1);
         }
         // each warpgroup keeps P^T inside its own score columns (cbase..cbase+63), behind its reads
-        tmem_st8(trow + C::kColS + cbase + c * 8, w);
+        tmem_st16(trow + C::kColS + cbase + c2 * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + c2 * 16));
       }
       tmem_wait_st();
       tc_fence_before();
@@ -971,28 +991,30 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv2(const __grid_constant__ Bw
       tc_fence_after();
       uint8_t* atom = smem + C::kOffDS + dsb * C::kDsBytes + wg * 16384;
 #pragma unroll
-      for (int c = 0; c < 4; c++) {
-        uint32_t u[16];
-        tmem_ld16(trow + C::kColDP + cbase + c * 16, u);
-        float dl[16];
+      for (int c2 = 0; c2 < 2; c2++) {
+        uint32_t u[32];
+        tmem_ld16(trow + C::kColDP + cbase + c2 * 32, *reinterpret_cast<uint32_t(*)[16]>(u));
+        tmem_ld16(trow + C::kColDP + cbase + c2 * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
+        float dl[32];
 #pragma unroll
-        for (int v4 = 0; v4 < 4; v4++) {
-          const float4 t4 = reinterpret_cast<const float4*>(del + c * 16)[v4];
+        for (int v4 = 0; v4 < 8; v4++) {
+          const float4 t4 = reinterpret_cast<const float4*>(del + c2 * 32)[v4];
           dl[4 * v4] = t4.x, dl[4 * v4 + 1] = t4.y, dl[4 * v4 + 2] = t4.z, dl[4 * v4 + 3] = t4.w;
         }
         tmem_wait_ld();
-        uint32_t w[8];
+        uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 8; e++) {
-          const float d0 = (__uint_as_float(u[2 * e]) - dl[2 * e]) * bf_lo(pk[c * 8 + e]);
-          const float d1 = (__uint_as_float(u[2 * e + 1]) - dl[2 * e + 1]) * bf_hi(pk[c * 8 + e]);
+        for (int e = 0; e < 16; e++) {
+          const float d0 = (__uint_as_float(u[2 * e]) - dl[2 * e]) * bf_lo(pk[c2 * 16 + e]);
+          const float d1 = (__uint_as_float(u[2 * e + 1]) - dl[2 * e + 1]) * bf_hi(pk[c2 * 16 + e]);
           w[e] = pack_f16(d0, d1);
         }
         // dS^T into TMEM over the dP^T columns already read (for dK), dS into shared memory (for dQ)
-        tmem_st8(trow + C::kColDP + cbase + c * 8, w);
-        *reinterpret_cast<uint4*>(atom + r * 128 + (((uint32_t)(2 * c) ^ x7) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(atom + r * 128 + (((uint32_t)(2 * c + 1) ^ x7) << 4)) =
-            make_uint4(w[4], w[5], w[6], w[7]);
+        tmem_st16(trow + C::kColDP + cbase + c2 * 16, w);
+#pragma unroll
+        for (int q = 0; q < 4; q++)
+          *reinterpret_cast<uint4*>(atom + r * 128 + (((uint32_t)(4 * c2 + q) ^ x7) << 4)) =
+              make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
       }
       tmem_wait_st();
       fence_proxy_async_smem();

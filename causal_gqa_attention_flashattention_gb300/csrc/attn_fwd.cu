@@ -501,6 +501,10 @@ __global__ void __launch_bounds__(256) k_rope_qk(const RopeArgs a) {
 // shared memory and pass from one warpgroup to the other through the head's
 // `st_ready` barrier.  The warpgroup that finishes a head's last key tile
 // writes that head's O and LSE.
+// Two threads issue the tensor-core work, each from its own warp (one thread
+// issues at most about one MMA per 70-100 cycles, whatever N): warp 1 the
+// S = Q K^T chains, warp 10 the O += P V chains.  S of head-step n reuses the
+// score buffer of head-step n - 2 once that step's PV has completed.
 template <int D>
 struct Fwd2Cfg {
   static constexpr int kTileBytes = kTile * D * 2;
@@ -511,7 +515,7 @@ struct Fwd2Cfg {
   static constexpr int kMaxStages = 3;
   static constexpr uint32_t kTmemS = 256;  // score buffers at columns 256 and 384
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;
   static_assert(kMaxHC * D <= 256, "O accumulators must fit below the score buffers");
 };
 
@@ -535,7 +539,7 @@ __device__ __forceinline__ bool fwd_item(const FwdArgs& a, int tl, FwdItem& it) 
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1) k_attn_fwd2(const __grid_constant__ FwdArgs a) {
+__global__ void __launch_bounds__(352, 1) k_attn_fwd2(const __grid_constant__ FwdArgs a) {
   using C = Fwd2Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -554,9 +558,10 @@ __global__ void __launch_bounds__(320, 1) k_attn_fwd2(const __grid_constant__ Fw
   uint64_t* o_done = bars + 14;    // [kMaxHC]
   uint64_t* o_free = bars + 22;    // [kMaxHC]
   uint64_t* st_ready = bars + 30;  // [kMaxHC]
-  uint64_t* drain = bars + 38;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 40);
-  volatile int* abort = reinterpret_cast<volatile int*>(bars + 40) + 1;
+  uint64_t* drain = bars + 38;     // [2] one per issuing thread
+  uint64_t* buf_free = bars + 41;  // [2] PV of the buffer's last head-step completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 43);
+  volatile int* abort = reinterpret_cast<volatile int*>(bars + 43) + 1;
   // row statistics [head][row]: running maximum (raw logit units) and sum
   float* sm_m = reinterpret_cast<float*>(smem + offStat);
   float* sm_l = sm_m + C::kMaxHC * kTile;
@@ -569,6 +574,8 @@ __global__ void __launch_bounds__(320, 1) k_attn_fwd2(const __grid_constant__ Fw
       mbar_init(q_empty + k, 1);
       mbar_init(s_full + k, 1);
       mbar_init(p_ready + k, 128);
+      mbar_init(buf_free + k, 1);
+      mbar_init(drain + k, 1);
     }
     for (int k = 0; k < C::kMaxStages; k++) {
       mbar_init(kv_full + k, 1);
@@ -579,7 +586,6 @@ __global__ void __launch_bounds__(320, 1) k_attn_fwd2(const __grid_constant__ Fw
       mbar_init(o_free + k, 128);
       mbar_init(st_ready + k, 128);
     }
-    mbar_init(drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
@@ -621,62 +627,68 @@ __global__ void __launch_bounds__(320, 1) k_attn_fwd2(const __grid_constant__ Fw
       for (int x = g - S < 0 ? 0 : g - S; x < g; x++) mbar_wait(kv_full + x % S, (x / S) & 1, &never);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S = Q K^T issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_fp16(128, 128, false, false);
-      constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
-      constexpr uint32_t kStepK = 32 >> 4, kStepMN = (16 * C::kSpan) >> 4;
+      constexpr uint32_t kStepK = 32 >> 4;
       const uint32_t tstep = (uint32_t)TB >> 4;
       const uint64_t dQ0 = smem_desc(smem_u32(smem + offQ), 16, C::kSBO, C::kSwz);
       const uint64_t dK0 = smem_desc(smem_u32(smem + offK), 16, C::kSBO, C::kSwz);
-      const uint64_t dV0 = smem_desc(smem_u32(smem + offV), 16, C::kSBO, C::kSwz);
-      // Head-step n uses score buffer n & 1.  Its O += P V goes out right after
-      // S of head-step n + 1, so the tensor core computes the next scores while
-      // the softmax works on this one.
-      struct Pend {
-        int valid, hh, j, st, n, tl;
-      } pend = {0, 0, 0, 0, 0, 0};
-      int pv_in_stage[C::kMaxStages] = {0, 0, 0};
       bool ok = true;
-      auto issue_pv = [&](const Pend& p) -> bool {
-        if (!mbar_wait(p_ready + (p.n & 1), (p.n >> 1) & 1, abort)) return false;
-        if (p.j == 0 && p.tl > 0 && !mbar_wait(o_free + p.hh, (p.tl - 1) & 1, abort)) return false;
-        tc_fence_after();
-        // P (bf16, 128 keys) in the first 64 columns of the score buffer
-        mma_ts_chain<8, false>(tmem + p.hh * D, tmem + C::kTmemS + (p.n & 1) * 128, dV0 + (uint64_t)(p.st * tstep),
-                               kStepMN, idPV, p.j > 0 ? 1u : 0u);
-        mma_commit(o_done + p.hh);
-        if (++pv_in_stage[p.st] == HC) {
-          pv_in_stage[p.st] = 0;
-          mma_commit(kv_empty + p.st);
-        }
-        return true;
-      };
       int g = 0, n = 0;
       FwdItem it;
       for (int tl = 0; ok && fwd_item(a, tl, it); tl++) {
         const int qb = tl & 1;
         if (!(ok = mbar_wait(q_full + qb, (tl >> 1) & 1, abort))) break;
-        tc_fence_after();
         for (int j = 0; ok && j <= it.i; j++, g++) {
           const int st = g % S;
           if (!(ok = mbar_wait(kv_full + st, (g / S) & 1, abort))) break;
-          tc_fence_after();
           for (int hh = 0; hh < HC; hh++, n++) {
-            // buffer n & 1 last held P of head-step n - 2, whose PV was issued after S(n - 1)
+            // the score buffer's previous head-step (n - 2): its P consumed by its PV
+            if (n >= 2 && !(ok = mbar_wait(buf_free + (n & 1), ((n >> 1) - 1) & 1, abort))) break;
+            tc_fence_after();
             mma_ss_chain<D / 16>(tmem + C::kTmemS + (n & 1) * 128, dQ0 + (uint64_t)((qb * HC + hh) * tstep), kStepK,
                                  dK0 + (uint64_t)(st * tstep), kStepK, idS, 0u);
             mma_commit(s_full + (n & 1));
             if (j == it.i && hh == HC - 1) mma_commit(q_empty + qb);
-            if (pend.valid && !(ok = issue_pv(pend))) break;
-            pend = Pend{1, hh, j, st, n, tl};
           }
         }
       }
-      if (ok && pend.valid) ok = issue_pv(pend);
       if (!ok) record_timeout(a.status, abort);
       mma_commit(drain);
       mbar_wait(drain, 0, &never);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ O += P V issuer
+    if (lane == 0) {
+      constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
+      constexpr uint32_t kStepMN = (16 * C::kSpan) >> 4;
+      const uint32_t tstep = (uint32_t)TB >> 4;
+      const uint64_t dV0 = smem_desc(smem_u32(smem + offV), 16, C::kSBO, C::kSwz);
+      bool ok = true;
+      int g = 0, n = 0;
+      FwdItem it;
+      for (int tl = 0; ok && fwd_item(a, tl, it); tl++) {
+        for (int j = 0; ok && j <= it.i; j++, g++) {
+          const int st = g % S;
+          for (int hh = 0; hh < HC; hh++, n++) {
+            if (!(ok = mbar_wait(p_ready + (n & 1), (n >> 1) & 1, abort))) break;
+            if (j == 0 && tl > 0 && !(ok = mbar_wait(o_free + hh, (tl - 1) & 1, abort))) break;
+            tc_fence_after();
+            // P (bf16, 128 keys) in the first 64 columns of the score buffer
+            mma_ts_chain<8, false>(tmem + hh * D, tmem + C::kTmemS + (n & 1) * 128, dV0 + (uint64_t)(st * tstep),
+                                   kStepMN, idPV, j > 0 ? 1u : 0u);
+            mma_commit(o_done + hh);
+            mma_commit(buf_free + (n & 1));
+          }
+          // K and V of this stage are free: every S that read K completed before
+          // its softmax (hence these PVs) could start
+          if (ok) mma_commit(kv_empty + st);
+        }
+      }
+      if (!ok) record_timeout(a.status, abort);
+      mma_commit(drain + 1);
+      mbar_wait(drain + 1, 0, &never);
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups

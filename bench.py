@@ -227,7 +227,7 @@ def run_ours(args, world, rank, local):
         # the forward's workspace (rotated q, k) is the first part of the backward's
         binding.attn_fwd(s["q"], s["k"], s["v"], base, o=s["o"], lse=s["lse"], workspace=s["ws"], stream=stream)
         binding.attn_bwd(s["q"], s["k"], s["v"], s["o"], s["lse"], s["do"], base, grad_dtype=grad_dtype,
-                         dq=s["dq"], dk=s["dk"], dv=s["dv"], workspace=s["ws"], stream=stream)
+                         dq=s["dq"], dk=s["dk"], dv=s["dv"], workspace=s["ws"], qk_rotated=True, stream=stream)
 
     def barrier():
         if world > 1:

@@ -17,6 +17,7 @@ NE_OK = 0
 O_FP32 = 1       # flag bits, see include/ne_attn.h
 GRAD_FP32 = 2
 PRECISE_QK = 4
+QK_ROTATED = 8
 _lib = None
 
 
@@ -131,11 +132,15 @@ def alloc_workspace(B, T, Hq, Hkv, D, precise=False, device="cuda"):
 
 
 def attn_bwd(q, k, v, o, lse, dout, rope_base=10000.0, grad_dtype=torch.bfloat16, precise=False,
-             dq=None, dk=None, dv=None, workspace=None, stream=None):
+             dq=None, dk=None, dv=None, workspace=None, qk_rotated=False, stream=None):
     """dq, dk, dv of the causal GQA attention given the forward's o and lse.
 
     o may be bfloat16 or float32; grad_dtype selects the gradient dtype.
+    qk_rotated: `workspace` was also the forward's workspace (for these q, k)
+    and still holds its rotated q and k (NE_ATTN_QK_ROTATED).
     """
+    if qk_rotated and workspace is None:
+        raise ValueError("qk_rotated needs the workspace the forward wrote")
     B, T, Hq, Hkv, D = _shape(q, k)
     if grad_dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("grad_dtype must be bfloat16 or float32")
@@ -154,7 +159,7 @@ def attn_bwd(q, k, v, o, lse, dout, rope_base=10000.0, grad_dtype=torch.bfloat16
     for t in (dq, dk, dv):
         assert t.dtype == grad_dtype and t.is_contiguous()
     flags = ((O_FP32 if o.dtype == torch.float32 else 0) | (GRAD_FP32 if grad_dtype == torch.float32 else 0)
-             | (PRECISE_QK if precise else 0))
+             | (PRECISE_QK if precise else 0) | (QK_ROTATED if qk_rotated else 0))
     _check("ne_attn_bwd", lib().ne_attn_bwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
         B, T, Hq, Hkv, D, float(rope_base), flags, _ptr(workspace), workspace.numel(), _stream(stream)))
@@ -218,7 +223,9 @@ def fwd_bwd_host(q, k, v, dout, rope_base=10000.0, grad_dtype=torch.bfloat16, o_
         kd = k.to(device, non_blocking=True)
         vd = v.to(device, non_blocking=True)
         dod = dout.to(device, non_blocking=True)
-        o, lse = attn_fwd(qd, kd, vd, rope_base, o_dtype=o_dtype, precise=precise, stream=s)
-        dq, dk, dv = attn_bwd(qd, kd, vd, o, lse, dod, rope_base, grad_dtype, precise=precise, stream=s)
+        ws = alloc_workspace(*_shape(qd, kd), precise=precise, device=device)
+        o, lse = attn_fwd(qd, kd, vd, rope_base, o_dtype=o_dtype, precise=precise, workspace=ws, stream=s)
+        dq, dk, dv = attn_bwd(qd, kd, vd, o, lse, dod, rope_base, grad_dtype, precise=precise, workspace=ws,
+                              qk_rotated=not precise, stream=s)
         out = [t.to("cpu", non_blocking=False) for t in (o, lse, dq, dk, dv)]
     return tuple(out)

@@ -207,6 +207,23 @@ int make_map_bthd(CUtensorMap* m, const void* ptr, int B, int T, int H, int D,
   return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
 }
 
+// 4-D store map over a gradient [B, T, H, D] (fp32 or bf16); box = 128 bytes of
+// columns (64 bytes when a row is that short) x 1 head x 128 rows x 1, with the
+// swizzle of that span.
+int make_map_grad(CUtensorMap* m, void* ptr, int B, int T, int H, int D, bool fp32) {
+  const int es = fp32 ? 4 : 2;
+  const int span = D * es < 128 ? D * es : 128;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * es, (cuuint64_t)H * D * es, (cuuint64_t)T * H * D * es};
+  cuuint32_t box[4] = {(cuuint32_t)(span / es), 1, (cuuint32_t)kTile, 1};
+  cuuint32_t e1[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims,
+                        strides, box, e1, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
+}
+
 // 2-D map over the fp32 dQ accumulator [rows, D]; box = 32 columns x 128 rows.
 int make_map_acc(CUtensorMap* m, void* ptr, long long rows, int D) {
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
@@ -279,6 +296,7 @@ WsLayout ws_layout(int B, int T, int Hq, int Hkv, int D, bool precise) {
 }
 
 constexpr int kKnownFlags = kFlagOFp32 | kFlagGradFp32 | kFlagPreciseQK;
+constexpr int kBwdFlags = kKnownFlags | kFlagQKRotated;
 
 // ------------------------------------------------------------------ kernel timing
 struct Profile {
@@ -417,7 +435,8 @@ int ne_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse
 }
 
 size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D, int flags) {
-  if (check_shape(B, T, Hq, Hkv, D) != NE_OK || (flags & ~kKnownFlags) != 0) return 0;
+  if (check_shape(B, T, Hq, Hkv, D) != NE_OK || (flags & ~kBwdFlags) != 0) return 0;
+  if ((flags & kFlagQKRotated) && (flags & kFlagPreciseQK)) return 0;
   return ws_layout(B, T, Hq, Hkv, D, (flags & kFlagPreciseQK) != 0).total;
 }
 
@@ -425,7 +444,9 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
                 void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D, float rope_base, int flags,
                 void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return NE_ERR_ARG;
-  if ((flags & ~kKnownFlags) != 0) return NE_ERR_ARG;
+  if ((flags & ~kBwdFlags) != 0) return NE_ERR_ARG;
+  // the forward leaves rotated copies only in default precision
+  if ((flags & kFlagQKRotated) && (flags & kFlagPreciseQK)) return NE_ERR_ARG;
   if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
   int st = check_shape(B, T, Hq, Hkv, D);
   if (st != NE_OK) return st;
@@ -481,6 +502,7 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   p.Hkv = Hkv;
   p.D = D;
   p.Tp = Tp;
+  p.rotate_qk = (flags & kFlagQKRotated) ? 0 : 1;
   p.div_hq = make_fastdiv((uint32_t)Hq);
   p.div_hkv = make_fastdiv((uint32_t)Hkv);
   p.div_t = make_fastdiv((uint32_t)T);
@@ -502,6 +524,8 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
     if ((st = make_map_bthd(&a.map_klo, klo, B, T, Hkv, D, kF16)) != NE_OK) return st;
   }
   if ((st = make_map_acc(&a.map_dqacc, dqacc, (long long)B * Hq * Tp, D)) != NE_OK) return st;
+  if ((st = make_map_grad(&a.map_dk, dk, B, T, Hkv, D, grad_fp32 != 0)) != NE_OK) return st;
+  if ((st = make_map_grad(&a.map_dv, dv, B, T, Hkv, D, grad_fp32 != 0)) != NE_OK) return st;
   a.lse2 = lse2;
   a.lse2_lo = lse2_lo;
   a.delta = delta;
@@ -735,6 +759,7 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
   p.Hkv = Hkv;
   p.D = D;
   p.Tp = Tp;
+  p.rotate_qk = (flags & kFlagQKRotated) ? 0 : 1;
   p.div_hq = make_fastdiv((uint32_t)Hq);
   p.div_hkv = make_fastdiv((uint32_t)Hkv);
   p.div_t = make_fastdiv((uint32_t)T);
@@ -753,6 +778,8 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
     if ((st = make_map_bthd(&a.map_klo, klo, B, T, Hkv, D, kF16)) != NE_OK) return st;
   }
   if ((st = make_map_acc(&a.map_dqacc, dqacc, (long long)B * Hq * Tp, D)) != NE_OK) return st;
+  if ((st = make_map_grad(&a.map_dk, dk, B, T, Hkv, D, grad_fp32 != 0)) != NE_OK) return st;
+  if ((st = make_map_grad(&a.map_dv, dv, B, T, Hkv, D, grad_fp32 != 0)) != NE_OK) return st;
   a.lse2 = lse2;
   a.lse2_lo = lse2_lo;
   a.delta = delta;

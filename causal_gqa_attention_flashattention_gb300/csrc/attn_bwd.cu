@@ -63,7 +63,6 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
       h = row - bt * a.Hq;
       b = fdiv(bt, a.div_t);
       t = bt - b * a.T;
-      const uint4 qv = __ldg(reinterpret_cast<const uint4*>(a.q) + it);
       const uint4 dv = __ldg(reinterpret_cast<const uint4*>(a.dout) + it);
       float4 o0, o1;
       uint4 ov;
@@ -74,14 +73,17 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
       } else {
         ov = __ldg(reinterpret_cast<const uint4*>(a.o) + it);
       }
-      float4 c0, c1;
-      rope_coeffs<D>(a.rope, (int)t, c, c0, c1);
-      if (a.qlo) {
-        uint4 l;
-        reinterpret_cast<uint4*>(a.qr)[it] = rope_chunk_f16(qv, c0, c1, &l);
-        reinterpret_cast<uint4*>(a.qlo)[it] = l;
-      } else {
-        reinterpret_cast<uint4*>(a.qr)[it] = rope_chunk_f16(qv, c0, c1, nullptr);
+      if (a.rotate_qk) {
+        const uint4 qv = __ldg(reinterpret_cast<const uint4*>(a.q) + it);
+        float4 c0, c1;
+        rope_coeffs<D>(a.rope, (int)t, c, c0, c1);
+        if (a.qlo) {
+          uint4 l;
+          reinterpret_cast<uint4*>(a.qr)[it] = rope_chunk_f16(qv, c0, c1, &l);
+          reinterpret_cast<uint4*>(a.qlo)[it] = l;
+        } else {
+          reinterpret_cast<uint4*>(a.qr)[it] = rope_chunk_f16(qv, c0, c1, nullptr);
+        }
       }
       const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
       if (a.o_fp32) {
@@ -110,8 +112,8 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
       }
     }
   }
-  // (B) key rows: rotate k
-  const uint32_t nB = (uint32_t)a.B * a.T * a.Hkv * kCPR;
+  // (B) key rows: rotate k (unless the forward's rotated copy is already there)
+  const uint32_t nB = a.rotate_qk ? (uint32_t)a.B * a.T * a.Hkv * kCPR : 0u;
   for (uint32_t it = gtid; it < nB; it += nthr) {
     const uint32_t row = it >> kShift;
     const int c = (int)(it & (kCPR - 1));
@@ -694,96 +696,166 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
   }
 }
 
-// ---------------------------------------------------------------------- dK/dV sweep, default precision
-// Same computation as k_bwd_dkdv<D, false> with less shared-memory traffic and
-// two compute warpgroups:
-//   * K^ and V are copied once into TMEM and used as the A operands of
-//     S^T = K^ Q^T and dP^T = V dO^T (only Q / dO are read from shared memory);
-//   * dS^T is also written to TMEM (over the dP^T columns it replaces) and is
-//     the A operand of dK += dS^T Q^; the shared-memory copy of dS feeds only
-//     dQ = dS K^, which needs it transposed;
-//   * warps 4-7 handle query columns 0-63 and warps 8-11 columns 64-127 of
-//     every step (P and dS are element-wise once the LSE is known);
-//   * warps 12-15 drain dQ, which has a single TMEM buffer.
+// ====================================================================== persistent dK/dV sweep
+// One CTA per SM loops over work items (key tile j, batch, kv head), longest
+// sweep first in a snake order.  An item accumulates dK and dV of its key
+// tile over the query tiles i >= j of every query head of the group (one
+// step per (i, head)).  S^T = K Q^T and dP^T = V dO^T read K and V from shared
+// memory (double-buffered across items, so the next item's K and V load
+// while this one runs); P^T gets TMEM columns of its own, so S^T of the next
+// step may overwrite the score columns as soon as the compute warps have read
+// them.  The accumulators pass from one item to the next through acc_done
+// (MMAs complete) and acc_free (the compute warps have read them).
+// Warps: 0 TMA producer; 1-3 MMA issuers; 4-11 P and dS (two warpgroups, half
+// the query columns each), then each item's dK / dV store; 12-15 dQ drain.
 template <int D>
-struct Bwd2Cfg {
+struct Bwd3Cfg {
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr uint32_t kSpan = D * 2;
   static constexpr uint32_t kSwz = D == 64 ? kSw128 : kSw64;
   static constexpr uint32_t kSBO = 8 * kSpan;
-  static constexpr int kStages = 2;
-  static constexpr int kDsBufs = 2;
+  static constexpr int kStages = 3;
   static constexpr int kVecBytes = kTile * 4;
   static constexpr int kDsBytes = kTile * kTile * 2;
-  static constexpr int kStgBytes = kTile * D * 4;
-  static constexpr int kOffK = 0;
-  static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffQ = kOffV + kTileBytes;
+  static constexpr int kStgBytes = kTile * 32 * 4;  // one 32-column box of the fp32 dQ tile
+  static constexpr int kOffKV = 0;  // [2] x (K, V)
+  static constexpr int kOffQ = kOffKV + 4 * kTileBytes;
   static constexpr int kOffDO = kOffQ + kStages * kTileBytes;
   static constexpr int kOffDS = kOffDO + kStages * kTileBytes;
-  static constexpr int kOffStg = kOffDS + kDsBufs * kDsBytes;
+  static constexpr int kOffStg = kOffDS + kDsBytes;
   static constexpr int kOffLse = kOffStg + kStgBytes;
   static constexpr int kOffDel = kOffLse + kStages * kVecBytes;
   static constexpr int kOffBar = kOffDel + kStages * kVecBytes;
-  static constexpr int kNumBars = 24;
+  static constexpr int kNumBars = 32;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-  // TMEM: S^T/P^T | dP^T (dS^T over it) | dV | dK | dQ | K^ (A operand) | V (A operand)
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D, kColDQ = 256 + 2 * D;
-  static constexpr uint32_t kColK = 256 + 3 * D, kColV = kColK + D / 2;
+  // TMEM: S^T | dP^T (dS^T over it) | P^T | dV | dK | dQ
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDV = 320, kColDK = 320 + D,
+                            kColDQ = 320 + 2 * D;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kColV + D / 2 <= kTmemCols, "tensor memory budget");
+  static_assert(kColDQ + D <= kTmemCols, "tensor memory budget");
 };
 
+struct BwdItem {
+  int j, b, kvh, N;  // N = (nt - j) * G steps
+};
+
+__device__ __forceinline__ bool bwd_item(const BwdArgs& a, int tl, BwdItem& it) {
+  const int G = (int)gridDim.x, c = (int)blockIdx.x;
+  const int w = (tl & 1) ? (tl + 1) * G - 1 - c : tl * G + c;  // snake over the longest-first order
+  const int per_j = a.B * a.Hkv;
+  if (w >= a.nt * per_j) return false;
+  it.j = w / per_j;
+  const int rem = w % per_j;
+  it.kvh = rem % a.Hkv;
+  it.b = rem / a.Hkv;
+  it.N = (a.nt - it.j) * a.G;
+  return true;
+}
+
+// Stores one 128-row tile of a gradient (row r per thread of a 128-thread
+// group, values x) through shared memory: 128-byte-wide boxes (64 when a row is
+// shorter), swizzled.  Per box: every thread writes its row and arrives on
+// `full`; thread 0 stores the box with TMA (rows past T are not written), waits
+// until the store has read the box and arrives on `free_`; every thread waits
+// for that before the next box.  `e` counts the boxes (barrier phases).
+// Returns false if a wait gave up.
+template <int D, int ES>
+__device__ __forceinline__ bool stage_store(const float (&x)[D], uint8_t* stg, const CUtensorMap* map, int r,
+                                            uint64_t* full, uint64_t* free_, int& e, int h, int row0, int b,
+                                            const volatile int* abort) {
+  constexpr int kSpan = D * ES < 128 ? D * ES : 128;
+  constexpr int kCols = kSpan / ES;
+#pragma unroll
+  for (int c0 = 0; c0 < D; c0 += kCols) {
+#pragma unroll
+    for (int ch = 0; ch < kSpan / 16; ch++) {
+      uint4 w;
+      if constexpr (ES == 4) {
+        const int i = c0 + ch * 4;
+        w = make_uint4(__float_as_uint(x[i]), __float_as_uint(x[i + 1]), __float_as_uint(x[i + 2]),
+                       __float_as_uint(x[i + 3]));
+      } else {
+        const int i = c0 + ch * 8;
+        w = make_uint4(pack_bf16(x[i], x[i + 1]), pack_bf16(x[i + 2], x[i + 3]), pack_bf16(x[i + 4], x[i + 5]),
+                       pack_bf16(x[i + 6], x[i + 7]));
+      }
+      *reinterpret_cast<uint4*>(stg + swz(r, ch, kSpan)) = w;
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(full);
+    if (r == 0) {
+      if (mbar_wait(full, e & 1, abort)) {
+        tma_store_4d(map, stg, c0, h, row0, b);
+        bulk_commit();
+        bulk_wait_read<0>();
+        mbar_arrive(free_);
+      }
+    }
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(free_, e & 1, abort));
+    e++;
+    if (!ok) return false;
+  }
+  return true;
+}
+
 template <int D>
-__global__ void __launch_bounds__(512, 1) k_bwd_dkdv2(const __grid_constant__ BwdArgs a) {
-  using C = Bwd2Cfg<D>;
+__global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ BwdArgs a) {
+  using C = Bwd3Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* kv_full = bars;
-  uint64_t* kv_tmem = bars + 1;
-  uint64_t* qd_full = bars + 2;   // [2]
-  uint64_t* qd_empty = bars + 4;  // [2]
-  uint64_t* s_full = bars + 6;
-  uint64_t* p_ready = bars + 7;
-  uint64_t* dp_full = bars + 8;
-  uint64_t* acc_done = bars + 9;
-  uint64_t* ds_ready = bars + 10;  // [2]
-  uint64_t* ds_free = bars + 12;   // [2]
-  uint64_t* dq_full = bars + 14;
-  uint64_t* dq_free = bars + 15;
-  uint64_t* drain = bars + 16;     // [3] one per MMA-issuing thread
+  uint64_t* kv_full = bars;        // [2]
+  uint64_t* kv_empty = bars + 2;   // [2] released by the three issuers
+  uint64_t* qd_full = bars + 4;    // [kStages]
+  uint64_t* qd_empty = bars + 7;   // [kStages] released by issuers 1 and 2
+  uint64_t* s_full = bars + 10;
+  uint64_t* s_read = bars + 11;    // the compute warps hold S^T in registers
+  uint64_t* p_ready = bars + 12;
+  uint64_t* pbuf_free = bars + 13; // dV read P^T
+  uint64_t* dp_full = bars + 14;
+  uint64_t* ds_ready = bars + 15;
+  uint64_t* ds_free = bars + 16;   // dQ read the dS tile
+  uint64_t* dq_full = bars + 17;
+  uint64_t* dq_free = bars + 18;
+  uint64_t* acc_done = bars + 19;  // an item's last dV and dK complete
+  uint64_t* acc_free = bars + 20;  // the compute warps read dK and dV
+  uint64_t* drain = bars + 21;     // [3]
+  uint64_t* stg_full = bars + 24;  // [2] per compute warpgroup: its rows of a gradient box are staged
+  uint64_t* stg_free = bars + 26;  // [2] the TMA store has read the box
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int per_j = a.B * a.Hkv;
-  const int j = (int)blockIdx.x / per_j;  // smallest j (longest sweep) first
-  const int rem = (int)blockIdx.x % per_j;
-  const int kvh = rem % a.Hkv, b = rem / a.Hkv;
   const int G = a.G;
-  const int N = (a.nt - j) * G;
 
   if (tid == 0) {
     *abort = 0;
-    mbar_init(kv_full, 1);
-    mbar_init(kv_tmem, 256);
     for (int s = 0; s < 2; s++) {
+      mbar_init(kv_full + s, 1);
+      mbar_init(kv_empty + s, 3);
+    }
+    for (int s = 0; s < C::kStages; s++) {
       mbar_init(qd_full + s, 1);
-      mbar_init(qd_empty + s, 2);  // released by the dV/S^T and the dK/dP^T issuers
-      mbar_init(ds_ready + s, 256);
-      mbar_init(ds_free + s, 1);
+      mbar_init(qd_empty + s, 2);
     }
     mbar_init(s_full, 1);
+    mbar_init(s_read, 256);
     mbar_init(p_ready, 256);
+    mbar_init(pbuf_free, 1);
     mbar_init(dp_full, 1);
-    mbar_init(acc_done, 2);  // dV and dK issuers
+    mbar_init(ds_ready, 256);
+    mbar_init(ds_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 128);
+    mbar_init(acc_done, 2);
+    mbar_init(acc_free, 256);
     for (int s = 0; s < 3; s++) mbar_init(drain + s, 1);
+    for (int s = 0; s < 2; s++) {
+      mbar_init(stg_full + s, 128);
+      mbar_init(stg_free + s, 1);
+    }
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
@@ -792,7 +864,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv2(const __grid_constant__ Bw
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const volatile int never = 0;
-  const uint32_t sK = smem_u32(smem + C::kOffK);
+  const uint32_t sKV = smem_u32(smem + C::kOffKV);
   const uint32_t sQ = smem_u32(smem + C::kOffQ), sDO = smem_u32(smem + C::kOffDO);
   const uint32_t sDS = smem_u32(smem + C::kOffDS);
 
@@ -801,108 +873,173 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv2(const __grid_constant__ Bw
     if (lane == 0) {
       prefetch_tmap(&a.map_qr);
       prefetch_tmap(&a.map_do);
-      mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
-      tma_load_4d(smem + C::kOffK, &a.map_kr, kv_full, 0, kvh, j * kTile, b);
-      tma_load_4d(smem + C::kOffV, &a.map_v, kv_full, 0, kvh, j * kTile, b);
-      int loaded = 0;
-      for (int n = 0; n < N; n++) {
-        const int st = n % C::kStages, use = n / C::kStages;
-        if (use > 0 && !mbar_wait(qd_empty + st, (use - 1) & 1, abort)) {
-          record_timeout(a.status, abort);
-          break;
+      prefetch_tmap(&a.map_kr);
+      prefetch_tmap(&a.map_v);
+      bool ok = true;
+      int g = 0, kv_loaded = 0;
+      auto load_kv = [&](int k, const BwdItem& x) -> bool {
+        const int kb = k & 1;
+        if (k >= 2 && !mbar_wait(kv_empty + kb, ((k >> 1) - 1) & 1, abort)) return false;
+        mbar_arrive_expect_tx(kv_full + kb, 2 * C::kTileBytes);
+        tma_load_4d(smem + C::kOffKV + kb * 2 * C::kTileBytes, &a.map_kr, kv_full + kb, 0, x.kvh, x.j * kTile, x.b);
+        tma_load_4d(smem + C::kOffKV + (kb * 2 + 1) * C::kTileBytes, &a.map_v, kv_full + kb, 0, x.kvh, x.j * kTile,
+                    x.b);
+        kv_loaded = k + 1;
+        return true;
+      };
+      BwdItem it, nx;
+      if (bwd_item(a, 0, it)) ok = load_kv(0, it);
+      for (int tl = 0; ok && bwd_item(a, tl, it); tl++) {
+        for (int n = 0; n < it.N; n++, g++) {
+          const int st = g % C::kStages, use = g / C::kStages;
+          if (use > 0 && !(ok = mbar_wait(qd_empty + st, (use - 1) & 1, abort))) break;
+          const int i = it.j + n / G, h = it.kvh * G + n % G;
+          const size_t vec = ((size_t)it.b * a.Hq + h) * a.Tp + (size_t)i * kTile;
+          mbar_arrive_expect_tx(qd_full + st, 2 * C::kTileBytes + 2 * C::kVecBytes);
+          tma_load_4d(smem + C::kOffQ + st * C::kTileBytes, &a.map_qr, qd_full + st, 0, h, i * kTile, it.b);
+          tma_load_4d(smem + C::kOffDO + st * C::kTileBytes, &a.map_do, qd_full + st, 0, h, i * kTile, it.b);
+          bulk_load(smem + C::kOffLse + st * C::kVecBytes, a.lse2 + vec, C::kVecBytes, qd_full + st);
+          bulk_load(smem + C::kOffDel + st * C::kVecBytes, a.delta + vec, C::kVecBytes, qd_full + st);
+          // the next item's K and V, once the previous user of that buffer is done
+          // (after this item's second step is queued, so that wait delays no early step)
+          if (n == (it.N > 1 ? 1 : 0) && bwd_item(a, tl + 1, nx) && !(ok = load_kv(tl + 1, nx))) break;
         }
-        const int i = j + n / G, h = kvh * G + n % G;
-        const size_t vec = ((size_t)b * a.Hq + h) * a.Tp + (size_t)i * kTile;
-        mbar_arrive_expect_tx(qd_full + st, 2 * C::kTileBytes + 2 * C::kVecBytes);
-        tma_load_4d(smem + C::kOffQ + st * C::kTileBytes, &a.map_qr, qd_full + st, 0, h, i * kTile, b);
-        tma_load_4d(smem + C::kOffDO + st * C::kTileBytes, &a.map_do, qd_full + st, 0, h, i * kTile, b);
-        bulk_load(smem + C::kOffLse + st * C::kVecBytes, a.lse2 + vec, C::kVecBytes, qd_full + st);
-        bulk_load(smem + C::kOffDel + st * C::kVecBytes, a.delta + vec, C::kVecBytes, qd_full + st);
-        loaded = n + 1;
       }
-      mbar_wait(kv_full, 0, &never);
-      for (int n = loaded - C::kStages < 0 ? 0 : loaded - C::kStages; n < loaded; n++)
-        mbar_wait(qd_full + n % C::kStages, (n / C::kStages) & 1, &never);
+      if (!ok) record_timeout(a.status, abort);
+      // let every copy issued above land before the CTA can exit
+      for (int k = kv_loaded - 2 < 0 ? 0 : kv_loaded - 2; k < kv_loaded; k++)
+        mbar_wait(kv_full + (k & 1), (k >> 1) & 1, &never);
+      for (int x = g - C::kStages < 0 ? 0 : g - C::kStages; x < g; x++)
+        mbar_wait(qd_full + x % C::kStages, (x / C::kStages) & 1, &never);
     }
   } else if (warp >= 1 && warp <= 3) {
     // ------------------------------------------------------------ MMA issuers
-    // One thread issues about one MMA per 70-120 cycles, so the step's 32 MMAs
-    // are spread over three threads (warps 1-3).  Each overwrite of a TMEM
-    // operand stays in the program order of the thread that read it:
-    //   warp 1: dV(n) += P^T(n) dO, then S^T(n+1) over the P^T columns;
-    //   warp 2: dK(n) += dS^T(n) Q, then dP^T(n+1) over the dS^T columns;
-    //   warp 3: the dQ tile = dS(n) K (dS from shared memory).
+    // One thread issues about one MMA per 70-120 cycles, so each step's 32
+    // MMAs are spread over three threads.  Every overwrite of a TMEM operand
+    // follows the read in the program order of one thread or behind a barrier:
+    //   warp 1: S^T(g+1) once the compute warps read S^T(g), then dV += P^T dO;
+    //   warp 2: dK += dS^T Q, then dP^T(g+1) over the dS^T columns;
+    //   warp 3: the dQ tile = dS K (dS from shared memory).
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_fp16(128, 128, false, false);   // K^ (TMEM) x Q^ (K-major)
-      constexpr uint32_t idDP = idesc_bf16(128, 128, false, false);  // V (TMEM) x dO (K-major)
+      constexpr uint32_t idS = idesc_fp16(128, 128, false, false);   // K^ x Q^ (both K-major)
+      constexpr uint32_t idDP = idesc_bf16(128, 128, false, false);  // V x dO (both K-major)
       constexpr uint32_t idDV = idesc_bf16(128, D, false, true);     // P^T (TMEM) x dO MN-major
       constexpr uint32_t idDK = idesc_fp16(128, D, false, true);     // dS^T (TMEM) x Q^ MN-major
       constexpr uint32_t idDQ = idesc_fp16(128, D, true, true);      // dS (MN-major) x K^ MN-major
       constexpr int KD = D / 16;                                     // k-steps over the head dimension
       constexpr uint32_t kStepK = 32 >> 4;                           // K-major: next 16 columns
       constexpr uint32_t kStepMN = (16 * C::kSpan) >> 4;             // MN-major: next 16 rows
-      // P^T and dS^T halves sit at +0..31 (queries 0..63) and +64..95 (queries 64..127): SPLIT chains
-      // shared-memory descriptors, computed once
-      // (stage / buffer k adds k * bytes / 16 to the start-address field)
+      constexpr uint32_t kTileStep = C::kTileBytes >> 4;
       const uint64_t dQ0 = smem_desc(sQ, 16, C::kSBO, C::kSwz);
       const uint64_t dDO0 = smem_desc(sDO, 16, C::kSBO, C::kSwz);
-      const uint64_t dDS0 = smem_desc(sDS, 16384, 1024, kSw128);
-      const uint64_t dK = smem_desc(sK, 16, C::kSBO, C::kSwz);
-      auto dQs = [&](int st) { return dQ0 + (uint64_t)(st * (C::kTileBytes >> 4)); };
-      auto dDOs = [&](int st) { return dDO0 + (uint64_t)(st * (C::kTileBytes >> 4)); };
-      auto dDS = [&](int k) { return dDS0 + (uint64_t)(k * (C::kDsBytes >> 4)); };
+      const uint64_t dKV0 = smem_desc(sKV, 16, C::kSBO, C::kSwz);
+      const uint64_t dDS = smem_desc(sDS, 16384, 1024, kSw128);
+      auto dK = [&](int kb) { return dKV0 + (uint64_t)(2 * kb * kTileStep); };
+      auto dV = [&](int kb) { return dKV0 + (uint64_t)((2 * kb + 1) * kTileStep); };
+      auto dQs = [&](int st) { return dQ0 + (uint64_t)(st * kTileStep); };
+      auto dDOs = [&](int st) { return dDO0 + (uint64_t)(st * kTileStep); };
       bool ok = true;
+      int g = 0;
+      BwdItem it;
       if (warp == 1) {
-        if ((ok = mbar_wait(kv_tmem, 0, abort) && mbar_wait(qd_full, 0, abort))) {
+        // S^T of the first step
+        BwdItem nx;
+        const bool any = bwd_item(a, 0, it);
+        if (any && (ok = mbar_wait(kv_full, 0, abort) && mbar_wait(qd_full, 0, abort))) {
           tc_fence_after();
-          mma_ts_chain<KD>(tmem + C::kColS, tmem + C::kColK, dQs(0), kStepK, idS, 0);
+          mma_ss_chain<KD>(tmem + C::kColS, dK(0), kStepK, dQs(0), kStepK, idS, 0);
           mma_commit(s_full);
         }
-        for (int n = 0; ok && n < N; n++) {
-          const int st = n % C::kStages, st1 = (n + 1) % C::kStages;
-          if (!(ok = mbar_wait(p_ready, n & 1, abort))) break;
-          tc_fence_after();
-          mma_ts_chain<8, true>(tmem + C::kColDV, tmem + C::kColS, dDOs(st), kStepMN, idDV, n > 0 ? 1u : 0u);
-          mma_commit(qd_empty + st);  // this thread's reads of stage st: Q^ by S^T(n), dO by dV(n)
-          if (n + 1 < N) {
-            if (!(ok = mbar_wait(qd_full + st1, ((n + 1) / C::kStages) & 1, abort))) break;
-            tc_fence_after();
-            mma_ts_chain<KD>(tmem + C::kColS, tmem + C::kColK, dQs(st1), kStepK, idS, 0);
-            mma_commit(s_full);
+        for (int tl = 0; ok && bwd_item(a, tl, it); tl++) {
+          const int kb = tl & 1;
+          for (int n = 0; n < it.N; n++, g++) {
+            const int st = g % C::kStages;
+            // S^T of the next step (this item's or the next item's first) and dV of
+            // this step touch different TMEM columns: issue each as soon as its
+            // inputs are there, so a late Q / dO load does not hold up dV.
+            const bool last = (n + 1 == it.N);
+            bool need_s = !last || bwd_item(a, tl + 1, nx);
+            bool need_dv = true;
+            const int g1 = g + 1, st1 = g1 % C::kStages, kb1 = last ? (kb ^ 1) : kb;
+            const unsigned long long t_start = globaltimer();
+            while (need_s || need_dv) {
+              bool progressed = false;
+              if (need_s && mbar_test(s_read, g & 1) && (!last || mbar_test(kv_full + kb1, ((tl + 1) >> 1) & 1)) &&
+                  mbar_test(qd_full + st1, (g1 / C::kStages) & 1)) {
+                tc_fence_after();
+                mma_ss_chain<KD>(tmem + C::kColS, dK(kb1), kStepK, dQs(st1), kStepK, idS, 0);
+                mma_commit(s_full);
+                need_s = false;
+                progressed = true;
+              }
+              // dV += P^T dO (the first step of an item starts from zero once the
+              // previous item's dV has been read out)
+              if (need_dv && mbar_test(p_ready, g & 1) && (n > 0 || tl == 0 || mbar_test(acc_free, (tl - 1) & 1))) {
+                tc_fence_after();
+                mma_ts_chain<8, false>(tmem + C::kColDV, tmem + C::kColP, dDOs(st), kStepMN, idDV, n > 0 ? 1u : 0u);
+                mma_commit(pbuf_free);
+                mma_commit(qd_empty + st);  // this thread's reads of stage st: Q^ by S^T, dO by dV
+                if (last) {
+                  mma_commit(acc_done);
+                  mma_commit(kv_empty + kb);  // K by S^T
+                }
+                need_dv = false;
+                progressed = true;
+              }
+              if (!progressed && (*abort || globaltimer() - t_start > kWaitLimitNs)) {
+                ok = false;
+                break;
+              }
+            }
+            if (!ok) break;
           }
         }
-        mma_commit(acc_done);
       } else if (warp == 2) {
-        if ((ok = mbar_wait(kv_tmem, 0, abort) && mbar_wait(qd_full, 0, abort))) {
+        const bool any = bwd_item(a, 0, it);
+        if (any && (ok = mbar_wait(kv_full, 0, abort) && mbar_wait(qd_full, 0, abort))) {
           tc_fence_after();
-          mma_ts_chain<KD>(tmem + C::kColDP, tmem + C::kColV, dDOs(0), kStepK, idDP, 0);
+          mma_ss_chain<KD>(tmem + C::kColDP, dV(0), kStepK, dDOs(0), kStepK, idDP, 0);
           mma_commit(dp_full);
         }
-        for (int n = 0; ok && n < N; n++) {
-          const int st = n % C::kStages, st1 = (n + 1) % C::kStages;
-          const int dsb = n % C::kDsBufs;
-          if (!(ok = mbar_wait(ds_ready + dsb, (n / C::kDsBufs) & 1, abort))) break;
-          tc_fence_after();
-          mma_ts_chain<8, true>(tmem + C::kColDK, tmem + C::kColDP, dQs(st), kStepMN, idDK, n > 0 ? 1u : 0u);
-          mma_commit(qd_empty + st);  // this thread's reads of stage st: dO by dP^T(n), Q^ by dK(n)
-          if (n + 1 < N) {
-            if (!(ok = mbar_wait(qd_full + st1, ((n + 1) / C::kStages) & 1, abort))) break;
+        BwdItem nx;
+        for (int tl = 0; ok && bwd_item(a, tl, it); tl++) {
+          const int kb = tl & 1;
+          for (int n = 0; n < it.N; n++, g++) {
+            const int st = g % C::kStages;
+            const bool last = (n + 1 == it.N);
+            if (!(ok = mbar_wait(ds_ready, g & 1, abort))) break;
+            if (n == 0 && tl > 0 && !(ok = mbar_wait(acc_free, (tl - 1) & 1, abort))) break;
             tc_fence_after();
-            mma_ts_chain<KD>(tmem + C::kColDP, tmem + C::kColV, dDOs(st1), kStepK, idDP, 0);
-            mma_commit(dp_full);
+            // dK += dS^T Q^ (dS^T over the dP^T columns: queries 0..63 at +0, 64..127 at +64)
+            mma_ts_chain<8, true>(tmem + C::kColDK, tmem + C::kColDP, dQs(st), kStepMN, idDK, n > 0 ? 1u : 0u);
+            mma_commit(qd_empty + st);  // this thread's reads of stage st: dO by dP^T, Q^ by dK
+            if (last) {
+              mma_commit(acc_done);
+              mma_commit(kv_empty + kb);  // V by dP^T
+            }
+            if (!last || bwd_item(a, tl + 1, nx)) {
+              const int g1 = g + 1, st1 = g1 % C::kStages, kb1 = last ? (kb ^ 1) : kb;
+              if (last && !(ok = mbar_wait(kv_full + kb1, ((tl + 1) >> 1) & 1, abort))) break;
+              if (!(ok = mbar_wait(qd_full + st1, (g1 / C::kStages) & 1, abort))) break;
+              tc_fence_after();
+              mma_ss_chain<KD>(tmem + C::kColDP, dV(kb1), kStepK, dDOs(st1), kStepK, idDP, 0);
+              mma_commit(dp_full);
+            }
           }
         }
-        mma_commit(acc_done);
       } else {
-        ok = mbar_wait(kv_full, 0, abort);  // K^ in shared memory
-        for (int n = 0; ok && n < N; n++) {
-          const int dsb = n % C::kDsBufs;
-          if (!(ok = mbar_wait(ds_ready + dsb, (n / C::kDsBufs) & 1, abort))) break;
-          if (n >= 1 && !(ok = mbar_wait(dq_free, (n - 1) & 1, abort))) break;
-          tc_fence_after();
-          mma_ss_chain<8>(tmem + C::kColDQ, dDS(dsb), 2048 >> 4, dK, kStepMN, idDQ, 0);
-          mma_commit(dq_full);
-          mma_commit(ds_free + dsb);
+        for (int tl = 0; ok && bwd_item(a, tl, it); tl++) {
+          const int kb = tl & 1;
+          if (!(ok = mbar_wait(kv_full + kb, (tl >> 1) & 1, abort))) break;  // K^ in shared memory
+          for (int n = 0; n < it.N; n++, g++) {
+            if (!(ok = mbar_wait(ds_ready, g & 1, abort))) break;
+            if (g >= 1 && !(ok = mbar_wait(dq_free, (g - 1) & 1, abort))) break;
+            tc_fence_after();
+            mma_ss_chain<8>(tmem + C::kColDQ, dDS, 2048 >> 4, dK(kb), kStepMN, idDQ, 0);
+            mma_commit(dq_full);
+            mma_commit(ds_free);
+            if (n + 1 == it.N) mma_commit(kv_empty + kb);  // K by dQ
+          }
         }
       }
       if (!ok) record_timeout(a.status, abort);
@@ -917,115 +1054,89 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv2(const __grid_constant__ Bw
     const int cbase = wg * 64;
     const uint32_t trow = tmem + ((uint32_t)(warp & 3) * 32u << 16);
     const float sl2 = a.scale_log2;
-    bool ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, abort));
-    if (ok) {
-      // Copy this thread's row of K^ (warps 4-7) or V (warps 8-11) into TMEM, in logical order.
-      const uint8_t* src = smem + (wg == 0 ? C::kOffK : C::kOffV);
-      uint32_t w[D / 2];
-#pragma unroll
-      for (int c = 0; c < D / 8; c++) {
-        const uint4 x = *reinterpret_cast<const uint4*>(src + swz(r, c, C::kSpan));
-        w[4 * c] = x.x, w[4 * c + 1] = x.y, w[4 * c + 2] = x.z, w[4 * c + 3] = x.w;
-      }
-      if (D == 64) {
-        uint32_t w32[32];
-#pragma unroll
-        for (int e = 0; e < 32; e++) w32[e] = w[e % (D / 2)];
-        tmem_st32(trow + (wg == 0 ? C::kColK : C::kColV), w32);
-      } else {
-        uint32_t w16[16];
-#pragma unroll
-        for (int e = 0; e < 16; e++) w16[e] = w[e % (D / 2)];
-        tmem_st16(trow + (wg == 0 ? C::kColK : C::kColV), w16);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(kv_tmem);
-    }
     const uint32_t x7 = (uint32_t)(r & 7);  // swizzle of this key row in the dS tile
-    for (int n = 0; ok && n < N; n++) {
-      const int st = n % C::kStages;
-      const int i = j + n / G;
-      const bool diag = (i == j);
-      const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffLse + st * C::kVecBytes) + cbase;
-      const float* del = reinterpret_cast<const float*>(smem + C::kOffDel + st * C::kVecBytes) + cbase;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full, n & 1, abort)))) break;
-      tc_fence_after();
-      uint32_t pk[32];  // P^T for this thread's 64 query columns, packed bf16 pairs
+    uint8_t* atom = smem + C::kOffDS + wg * 16384;
+    bool ok = true;
+    int g = 0, boxes = 0;
+    BwdItem it;
+    for (int tl = 0; ok && bwd_item(a, tl, it); tl++) {
+      for (int n = 0; n < it.N; n++, g++) {
+        const int st = g % C::kStages;
+        const int i = it.j + n / G;
+        const bool diag = (i == it.j);
+        const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffLse + st * C::kVecBytes) + cbase;
+        const float* del = reinterpret_cast<const float*>(smem + C::kOffDel + st * C::kVecBytes) + cbase;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full, g & 1, abort)))) break;
+        tc_fence_after();
+        uint32_t u[64];
 #pragma unroll
-      for (int c2 = 0; c2 < 2; c2++) {
-        // two 16-column loads in flight per wait
-        uint32_t u[32];
-        tmem_ld16(trow + C::kColS + cbase + c2 * 32, *reinterpret_cast<uint32_t(*)[16]>(u));
-        tmem_ld16(trow + C::kColS + cbase + c2 * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
-        float l2[32];
-#pragma unroll
-        for (int v4 = 0; v4 < 8; v4++) {
-          const float4 t4 = reinterpret_cast<const float4*>(lse2 + c2 * 32)[v4];
-          l2[4 * v4] = t4.x, l2[4 * v4 + 1] = t4.y, l2[4 * v4 + 2] = t4.z, l2[4 * v4 + 3] = t4.w;
-        }
+        for (int c = 0; c < 4; c++) tmem_ld16(trow + C::kColS + cbase + c * 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16 * c));
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(s_read);  // S^T of the next step may overwrite the score columns
+        uint32_t pk[32];      // P^T for this thread's 64 query columns, packed bf16 pairs
 #pragma unroll
-        for (int e = 0; e < 16; e++) {
-          const int q0 = cbase + c2 * 32 + 2 * e;
-          float p0 = ex2(fmaf(__uint_as_float(u[2 * e]), sl2, -l2[2 * e]));
-          float p1 = ex2(fmaf(__uint_as_float(u[2 * e + 1]), sl2, -l2[2 * e + 1]));
-          if (diag) {
-            if (q0 < r) p0 = 0.f;
-            if (q0 + 1 < r) p1 = 0.f;
+        for (int v4 = 0; v4 < 16; v4++) {
+          const float4 t4 = reinterpret_cast<const float4*>(lse2)[v4];
+          const float l2[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+          for (int e = 0; e < 2; e++) {
+            const int q0 = cbase + 4 * v4 + 2 * e;
+            float p0 = ex2(fmaf(__uint_as_float(u[4 * v4 + 2 * e]), sl2, -l2[2 * e]));
+            float p1 = ex2(fmaf(__uint_as_float(u[4 * v4 + 2 * e + 1]), sl2, -l2[2 * e + 1]));
+            if (diag) {
+              if (q0 < r) p0 = 0.f;
+              if (q0 + 1 < r) p1 = 0.f;
+            }
+            pk[2 * v4 + e] = pack_bf16(p0, p1);
           }
-          pk[c2 * 16 + e] = pack_bf16(p0, p1);
         }
-        // each warpgroup keeps P^T inside its own score columns (cbase..cbase+63), behind its reads
-        tmem_st16(trow + C::kColS + cbase + c2 * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + c2 * 16));
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_ready);
+        // the P^T columns are free once the previous step's dV has read them
+        if (g > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(pbuf_free, (g - 1) & 1, abort)))) break;
+        tc_fence_after();
+        tmem_st32(trow + C::kColP + wg * 32, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_ready);
 
-      const int dsb = n % C::kDsBufs;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(dp_full, n & 1, abort)))) break;
-      if (n >= C::kDsBufs &&
-          !(ok = __all_sync(0xffffffffu, mbar_wait(ds_free + dsb, ((n - C::kDsBufs) / C::kDsBufs) & 1, abort))))
-        break;
-      tc_fence_after();
-      uint8_t* atom = smem + C::kOffDS + dsb * C::kDsBytes + wg * 16384;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(dp_full, g & 1, abort)))) break;
+        if (g > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (g - 1) & 1, abort)))) break;
+        tc_fence_after();
 #pragma unroll
-      for (int c2 = 0; c2 < 2; c2++) {
-        uint32_t u[32];
-        tmem_ld16(trow + C::kColDP + cbase + c2 * 32, *reinterpret_cast<uint32_t(*)[16]>(u));
-        tmem_ld16(trow + C::kColDP + cbase + c2 * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
-        float dl[32];
+        for (int c2 = 0; c2 < 2; c2++) {
+          uint32_t v[32];
+          tmem_ld16(trow + C::kColDP + cbase + c2 * 32, *reinterpret_cast<uint32_t(*)[16]>(v));
+          tmem_ld16(trow + C::kColDP + cbase + c2 * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+          float dl[32];
 #pragma unroll
-        for (int v4 = 0; v4 < 8; v4++) {
-          const float4 t4 = reinterpret_cast<const float4*>(del + c2 * 32)[v4];
-          dl[4 * v4] = t4.x, dl[4 * v4 + 1] = t4.y, dl[4 * v4 + 2] = t4.z, dl[4 * v4 + 3] = t4.w;
+          for (int v4 = 0; v4 < 8; v4++) {
+            const float4 t4 = reinterpret_cast<const float4*>(del + c2 * 32)[v4];
+            dl[4 * v4] = t4.x, dl[4 * v4 + 1] = t4.y, dl[4 * v4 + 2] = t4.z, dl[4 * v4 + 3] = t4.w;
+          }
+          tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; e++) {
+            const float d0 = (__uint_as_float(v[2 * e]) - dl[2 * e]) * bf_lo(pk[c2 * 16 + e]);
+            const float d1 = (__uint_as_float(v[2 * e + 1]) - dl[2 * e + 1]) * bf_hi(pk[c2 * 16 + e]);
+            w[e] = pack_f16(d0, d1);
+          }
+          // dS^T into TMEM over the dP^T columns already read (for dK), dS into shared memory (for dQ)
+          tmem_st16(trow + C::kColDP + cbase + c2 * 16, w);
+#pragma unroll
+          for (int q = 0; q < 4; q++)
+            *reinterpret_cast<uint4*>(atom + r * 128 + (((uint32_t)(4 * c2 + q) ^ x7) << 4)) =
+                make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
         }
-        tmem_wait_ld();
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; e++) {
-          const float d0 = (__uint_as_float(u[2 * e]) - dl[2 * e]) * bf_lo(pk[c2 * 16 + e]);
-          const float d1 = (__uint_as_float(u[2 * e + 1]) - dl[2 * e + 1]) * bf_hi(pk[c2 * 16 + e]);
-          w[e] = pack_f16(d0, d1);
-        }
-        // dS^T into TMEM over the dP^T columns already read (for dK), dS into shared memory (for dQ)
-        tmem_st16(trow + C::kColDP + cbase + c2 * 16, w);
-#pragma unroll
-        for (int q = 0; q < 4; q++)
-          *reinterpret_cast<uint4*>(atom + r * 128 + (((uint32_t)(4 * c2 + q) ^ x7) << 4)) =
-              make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(ds_ready);
       }
-      tmem_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(ds_ready + dsb);
-    }
-    // epilogue: warps 4-7 store dK (scale, inverse rotation), warps 8-11 store dV
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort));
-    if (ok) {
+      if (!ok) break;
+      // item epilogue: warps 4-7 store dK (scale, inverse rotation), warps 8-11 store dV
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(acc_done, tl & 1, abort)))) break;
       tc_fence_after();
-      const int t = j * kTile + r;
       float x[D];
 #pragma unroll
       for (int c = 0; c < D / 16; c++) {
@@ -1035,37 +1146,37 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv2(const __grid_constant__ Bw
 #pragma unroll
         for (int e = 0; e < 16; e++) x[c * 16 + e] = __uint_as_float(u[e]);
       }
-      if (t < a.T) {
-        const size_t base = (((size_t)b * a.T + t) * a.Hkv + kvh) * D;
-        void* out = wg == 0 ? a.dk : a.dv;
+      tc_fence_before();
+      mbar_arrive(acc_free);  // the next item's first dV / dK may overwrite the accumulators
+      const int t = it.j * kTile + r;
+      if (wg == 0) {
+        // dK = scale * (inverse rotation of the accumulated dK^)
 #pragma unroll
         for (int c = 0; c < D / 8; c++) {
-          float y[8];
-          if (wg == 0) {
-            float4 c0, c1;
-            rope_coeffs<D>(a.rope, t, c, c0, c1);
-            const float cs[4] = {c0.x, c0.z, c1.x, c1.z}, sn[4] = {c0.y, c0.w, c1.y, c1.w};
+          float4 c0, c1;
+          rope_coeffs<D>(a.rope, t, c, c0, c1);
+          const float cs[4] = {c0.x, c0.z, c1.x, c1.z}, sn[4] = {c0.y, c0.w, c1.y, c1.w};
 #pragma unroll
-            for (int p = 0; p < 4; p++) {
-              const float x0 = x[c * 8 + 2 * p], x1 = x[c * 8 + 2 * p + 1];
-              y[2 * p] = a.scale * (x0 * cs[p] + x1 * sn[p]);
-              y[2 * p + 1] = a.scale * (x1 * cs[p] - x0 * sn[p]);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; e++) y[e] = x[c * 8 + e];
-          }
-          if (a.grad_fp32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + base + c * 8);
-            dst[0] = make_float4(y[0], y[1], y[2], y[3]);
-            dst[1] = make_float4(y[4], y[5], y[6], y[7]);
-          } else {
-            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + base)[c] =
-                make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+          for (int p = 0; p < 4; p++) {
+            const float x0 = x[c * 8 + 2 * p], x1 = x[c * 8 + 2 * p + 1];
+            x[c * 8 + 2 * p] = a.scale * (x0 * cs[p] + x1 * sn[p]);
+            x[c * 8 + 2 * p + 1] = a.scale * (x1 * cs[p] - x0 * sn[p]);
           }
         }
       }
+      // Coalesced store: each warpgroup stages its tile (128 rows) in its half of
+      // the dS tile, one 128-byte-wide box at a time, and one thread stores the
+      // box with TMA (rows past T are not written).  The dS tile is free once
+      // the item's last dQ has read it.
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (g - 1) & 1, abort)))) break;
+      // (the next item writes dS into this tile only after the stores have read it)
+      const CUtensorMap* map = wg == 0 ? &a.map_dk : &a.map_dv;
+      ok = a.grad_fp32 ? stage_store<D, 4>(x, atom, map, r, stg_full + wg, stg_free + wg, boxes, it.kvh,
+                                           it.j * kTile, it.b, abort)
+                       : stage_store<D, 2>(x, atom, map, r, stg_full + wg, stg_free + wg, boxes, it.kvh,
+                                           it.j * kTile, it.b, abort);
     }
+    if (ok && r == 0) bulk_wait<0>();
     if (!ok) record_timeout(a.status, abort);
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ drain (one query row per thread)
@@ -1073,40 +1184,45 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv2(const __grid_constant__ Bw
     const uint32_t trow = tmem + ((uint32_t)(warp & 3) * 32u << 16);
     uint8_t* stg = smem + C::kOffStg;
     bool ok = true;
-    for (int n = 0; n < N; n++) {
-      // Every drain thread reaches both named barriers of an iteration; the
-      // first one agrees on `ok`, so a timeout in one warp stops all four.
-      const bool got = __all_sync(0xffffffffu, mbar_wait(dq_full, n & 1, abort));
-      uint32_t u[D];
-      if (got) {
-        tc_fence_after();
+    int g = 0;
+    BwdItem it;
+    for (int tl = 0; ok && bwd_item(a, tl, it); tl++) {
+      for (int n = 0; n < it.N; n++, g++) {
+        // Every drain thread reaches both named barriers of a step; the first
+        // one agrees on `ok`, so a timeout in one warp stops all four.
+        const bool got = __all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, abort));
+        uint32_t u[D];
+        if (got) {
+          tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 32; c++) {
-          uint32_t v[32];
-          tmem_ld32(trow + C::kColDQ + c * 32, v);
+          for (int c = 0; c < D / 32; c++) {
+            uint32_t v[32];
+            tmem_ld32(trow + C::kColDQ + c * 32, v);
 #pragma unroll
-          for (int e = 0; e < 32; e++) u[c * 32 + e] = v[e];
+            for (int e = 0; e < 32; e++) u[c * 32 + e] = v[e];
+          }
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(dq_free);
         }
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(dq_free);
-      }
-      if (r == 0) bulk_wait_read<0>();  // previous reduction has finished reading the staging tile
-      if (!(ok = named_sync_and(1, 128, got))) break;
+        const int i = it.j + n / G, h = it.kvh * G + n % G;
+        const int row0 = (int)(((size_t)it.b * a.Hq + h) * a.Tp + (size_t)i * kTile);
 #pragma unroll
-      for (int bx = 0; bx < D / 32; bx++)
+        for (int bx = 0; bx < D / 32; bx++) {
+          if (r == 0) bulk_wait_read<0>();  // previous reduction has finished reading the staging box
+          if (!(ok = named_sync_and(1, 128, got))) break;
 #pragma unroll
-        for (int c = 0; c < 8; c++)
-          *reinterpret_cast<uint4*>(stg + bx * 16384 + swz(r, c, 128)) =
-              make_uint4(u[bx * 32 + 4 * c], u[bx * 32 + 4 * c + 1], u[bx * 32 + 4 * c + 2], u[bx * 32 + 4 * c + 3]);
-      fence_proxy_async_smem();
-      named_sync(1, 128);
-      if (r == 0) {
-        const int i = j + n / G, h = kvh * G + n % G;
-        const int row0 = (int)(((size_t)b * a.Hq + h) * a.Tp + (size_t)i * kTile);
-#pragma unroll
-        for (int bx = 0; bx < D / 32; bx++) tma_reduce_add_2d(&a.map_dqacc, stg + bx * 16384, bx * 32, row0);
-        bulk_commit();
+          for (int c = 0; c < 8; c++)
+            *reinterpret_cast<uint4*>(stg + swz(r, c, 128)) =
+                make_uint4(u[bx * 32 + 4 * c], u[bx * 32 + 4 * c + 1], u[bx * 32 + 4 * c + 2], u[bx * 32 + 4 * c + 3]);
+          fence_proxy_async_smem();
+          named_sync(1, 128);
+          if (r == 0) {
+            tma_reduce_add_2d(&a.map_dqacc, stg, bx * 32, row0);
+            bulk_commit();
+          }
+        }
+        if (!ok) break;
       }
     }
     if (r == 0) bulk_wait<0>();
@@ -1169,25 +1285,26 @@ cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t s) {
 }
 
 template <int D>
-cudaError_t launch_dkdv2_t(const BwdArgs& a, cudaStream_t s) {
-  using C = Bwd2Cfg<D>;
-  const int grid = a.nt * a.B * a.Hkv;
-  // the shared-memory opt-in is a per-device function attribute: set it once per device
+cudaError_t launch_dkdv3_t(const BwdArgs& a, cudaStream_t s) {
+  using C = Bwd3Cfg<D>;
   static bool attr_set[64] = {};
-  int dev = 0;
+  int dev = 0, nsm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_bwd_dkdv2<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_dkdv3<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  k_bwd_dkdv2<D><<<grid, 512, C::kSmemBytes, s>>>(a);
+  cudaError_t e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int items = a.nt * a.B * a.Hkv;
+  k_bwd_dkdv3<D><<<items < nsm ? items : nsm, 512, C::kSmemBytes, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, bool precise, cudaStream_t s) {
-  if (a.D == 64) return precise ? launch_dkdv_t<64, true>(a, s) : launch_dkdv2_t<64>(a, s);
-  return precise ? launch_dkdv_t<32, true>(a, s) : launch_dkdv2_t<32>(a, s);
+  if (a.D == 64) return precise ? launch_dkdv_t<64, true>(a, s) : launch_dkdv3_t<64>(a, s);
+  return precise ? launch_dkdv_t<32, true>(a, s) : launch_dkdv3_t<32>(a, s);
 }
 
 }  // namespace ne

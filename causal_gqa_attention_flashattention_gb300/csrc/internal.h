@@ -18,6 +18,7 @@ constexpr int kStatusTimeout = -6;
 constexpr int kFlagOFp32 = 1;      // o is float32
 constexpr int kFlagGradFp32 = 2;   // dq, dk, dv are float32
 constexpr int kFlagPreciseQK = 4;  // logits from hi + lo fp16 parts of rotated q and k
+constexpr int kFlagQKRotated = 8;  // backward: the workspace already holds the forward's rotated q and k
 
 // Largest number of query heads one forward CTA handles (TMEM/smem budget).
 inline int fwd_max_heads(int D, bool precise) { return D == 64 ? (precise ? 3 : 4) : 8; }
@@ -85,6 +86,8 @@ struct BwdArgs {
   CUtensorMap map_qr, map_kr, map_v, map_do;  // 4-D maps as above (qr/kr: rotated fp16 copies)
   CUtensorMap map_qlo, map_klo;               // fp16 remainders (precise logits only)
   CUtensorMap map_dqacc;                      // 2-D map over [B*Hq*Tp, D] fp32, box 32 x 128
+  CUtensorMap map_dk, map_dv;                 // 4-D store maps over [B, T, Hkv, D] (fp32 or bf16), box
+                                              // 128 bytes of columns x 1 x 128 rows x 1, same swizzle span
   const float* lse2;                          // [B, Hq, Tp]  lse * log2(e); +inf on pad rows
   const float* lse2_lo;                       // [B, Hq, Tp]  its fp32 remainder (precise logits only)
   const float* delta;                         // [B, Hq, Tp]
@@ -106,6 +109,7 @@ struct PrepArgs {
   float *lse2, *lse2_lo, *delta, *dqacc;
   const float2* rope;
   int B, T, Hq, Hkv, D, Tp, o_fp32;
+  int rotate_qk;                            // 0: qr / kr already hold the rotated q and k
   FastDiv div_hq, div_hkv, div_t, div_pad;  // by Hq, Hkv, T and Tp - T (pad rows; d = 1 if none)
 };
 

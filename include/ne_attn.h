@@ -58,7 +58,7 @@ typedef enum {
   NE_ERR_SCRATCH_LIMIT = -7   /* ne_attn_bwd_noalloc: problem too large for its fixed scratch */
 } ne_status;
 
-/* Flag bits for ne_attn_fwd_ex, ne_attn_bwd and ne_attn_bwd_workspace_size. */
+/* Flag bits for ne_attn_fwd_ex, ne_attn_bwd and the workspace-size queries. */
 #define NE_ATTN_O_FP32 1     /* o is float32 [B,T,Hq,D] (forward output, backward input) */
 #define NE_ATTN_GRAD_FP32 2  /* dq, dk, dv are float32 */
 #define NE_ATTN_PRECISE_QK 4 /* split precision for inputs whose logits reach |s| ~ 10^2..10^4:
@@ -70,6 +70,12 @@ typedef enum {
                                 remainder [B,Hq,T] (LSE = hi + lo), which the backward uses to
                                 rebuild P where one fp32 ulp of the LSE is already ~1e-3.
                                 Use the same setting for the forward and the backward. */
+#define NE_ATTN_QK_ROTATED 8 /* backward only, default precision: the first
+                                ne_attn_fwd_workspace_size bytes of `workspace` still hold the
+                                rotated q and k that ne_attn_fwd_ex wrote there for these q, k and
+                                rope_base, so the backward does not rotate them again (the
+                                forward's workspace is laid out as the start of the backward's).
+                                Rejected with NE_ATTN_PRECISE_QK and by ne_attn_bwd_noalloc. */
 
 /*
  * Forward pass: writes o (bfloat16) and lse.  Same as ne_attn_fwd_ex with

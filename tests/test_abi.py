@@ -40,7 +40,9 @@ def test_workspace_size(libne):
     assert libne.ne_attn_bwd_workspace_size(1, 77, 4, 2, 32, 0) >= 4 * 4 * 128 * 32  # padded to 128 rows
     assert libne.ne_attn_bwd_workspace_size(1, 16, 3, 2, 64, 0) == 0
     assert libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 48, 0) == 0
-    assert libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 64, 8) == 0
+    assert libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 64, 16) == 0  # unknown flag
+    assert libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 64, 8) == libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 64, 0)
+    assert libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 64, 8 | 4) == 0  # reuse needs default precision
 
 
 def test_fwd_workspace_size(libne):
@@ -70,7 +72,8 @@ def test_host_argument_checks(libne):
     assert libne.ne_attn_fwd_ex(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 2, null, 0, null) == -1  # grad flag on fwd
     assert libne.ne_attn_fwd_ex(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 0, p, 16, null) == -5  # workspace too small
     assert libne.ne_attn_fwd_ex(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 0, mis, 1 << 20, null) == -5  # misaligned
-    assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 8, p, 4096, null) == -1
+    assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 16, p, 4096, null) == -1
+    assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 8 | 4, p, 1 << 20, null) == -1
     assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 0, p, 16, null) == -5
     assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 0, mis, 1 << 20, null) == -5
     assert libne.ne_attn_debug_timeout_probe(0, null) == -1

@@ -24,12 +24,17 @@ def nb():
     return binding
 
 
-def run_gpu(nb, x, base=inputs.ROPE_BASE, grad_dtype=None, o_dtype=None, precise=False):
+def run_gpu(nb, x, base=inputs.ROPE_BASE, grad_dtype=None, o_dtype=None, precise=False, qk_rotated=False):
+    """Forward + backward.  qk_rotated: one workspace for both, the backward
+    reusing the rotated q and k the forward left in it."""
     grad_dtype = grad_dtype or torch.float32
     o_dtype = o_dtype or torch.bfloat16
     q, k, v, do = (H.to_device(x[n + "_bits"]) for n in ("q", "k", "v", "dout"))
-    o, lse = nb.attn_fwd(q, k, v, base, o_dtype=o_dtype, precise=precise)
-    dq, dk, dv = nb.attn_bwd(q, k, v, o, lse, do, base, grad_dtype=grad_dtype, precise=precise)
+    ws = nb.alloc_workspace(*x["q_bits"].shape[:3], x["k_bits"].shape[2], x["q_bits"].shape[3],
+                            precise=precise) if qk_rotated else None
+    o, lse = nb.attn_fwd(q, k, v, base, o_dtype=o_dtype, precise=precise, workspace=ws)
+    dq, dk, dv = nb.attn_bwd(q, k, v, o, lse, do, base, grad_dtype=grad_dtype, precise=precise, workspace=ws,
+                             qk_rotated=qk_rotated)
     nb.check_status()
     if precise:
         lse = lse[0]  # [1] holds the fp32 remainder
@@ -83,7 +88,9 @@ def mode_kwargs(name):
 def test_workload_parity(nb, oracle_mod, name):
     x = inputs.make_workload_inputs(name)
     shape = tuple(inputs.WORKLOADS[name][:5])
-    gpu = run_gpu(nb, x, **mode_kwargs(name))
+    kw = mode_kwargs(name)
+    # default precision: one workspace for forward and backward, as bench.py runs it
+    gpu = run_gpu(nb, x, qk_rotated=not kw["precise"], **kw)
     rep = compare(oracle_mod, x, gpu, shape, WORKLOAD_GROUPS[name])
     print(name, rep)
 
@@ -123,6 +130,30 @@ def test_edge_shapes(nb, oracle_mod, shape):
     x = H.make(*shape, seed=sum(shape))
     gpu = run_gpu(nb, x)
     compare(oracle_mod, x, gpu, shape, None)
+
+
+@pytest.mark.parametrize("shape", [(1, 77, 4, 2, 64), (2, 1000, 6, 2, 64), (1, 200, 8, 1, 32), (3, 640, 4, 4, 32)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_backward_reuses_forward_rotation(nb, oracle_mod, shape):
+    """One workspace for forward and backward (NE_ATTN_QK_ROTATED): parity with
+    the oracle, and dk / dv bit-identical to the path that rotates again (both
+    rotations round the same fp32 products to fp16)."""
+    x = H.make(*shape, seed=sum(shape) + 7)
+    shared = run_gpu(nb, x, qk_rotated=True)
+    compare(oracle_mod, x, shared, shape, None)
+    fresh = run_gpu(nb, x)
+    for name in ("o", "lse", "dk", "dv"):
+        assert np.array_equal(shared[name], fresh[name]), name
+
+
+def test_qk_rotated_flag_needs_default_precision(nb):
+    q = torch.zeros((1, 16, 2, 64), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((1, 16, 1, 64), dtype=torch.bfloat16, device="cuda")
+    o, lse = nb.attn_fwd(q, k, k, o_dtype=torch.float32, precise=True)
+    ws = nb.alloc_workspace(1, 16, 2, 1, 64, precise=True)
+    with pytest.raises(nb.NeAttnError) as e:
+        nb.attn_bwd(q, k, k, o, lse, q, precise=True, workspace=ws, qk_rotated=True)
+    assert e.value.status == -1
 
 
 @pytest.mark.parametrize("shape", [(1, 77, 4, 2, 64), (2, 1000, 6, 2, 64), (1, 300, 8, 1, 64),

@@ -350,7 +350,9 @@ def run_ours(args, world, rank, local):
     else:
         work = None
         roof = dict(bound="hbm", achieved=None, peak=peaks["hbm_gbs"], unit="GB/s", frac=None)
-    tr = traffic_record("k_bwd_dkdv" if dom == "bwd_dkdv" else "k_attn_fwd" if dom == "fwd" else dom)
+    kernel_names = dict(fwd="k_attn_fwd2", fwd_rope="k_rope_qk", bwd_prep="k_bwd_prep", bwd_dkdv="k_bwd_dkdv3",
+                        bwd_dq="k_bwd_dq")
+    tr = traffic_record(kernel_names.get(dom, dom))
     roof.update(kernel=dom, traffic=(tr["dram_bytes_per_launch"] if tr else None),
                 peak_source="%s bf16 burst" % peaks["source"] if roof["bound"] == "tensor" else
                 "%s hbm" % peaks["source"], per_launch_us=per_launch_ms * 1e3,

@@ -986,9 +986,12 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
                 need_dv = false;
                 progressed = true;
               }
-              if (!progressed && (*abort || globaltimer() - t_start > kWaitLimitNs)) {
-                ok = false;
-                break;
+              if (!progressed) {
+                if (*abort || globaltimer() - t_start > kWaitLimitNs) {
+                  ok = false;
+                  break;
+                }
+                __nanosleep(64);  // leave the issue slots to the compute warps
               }
             }
             if (!ok) break;

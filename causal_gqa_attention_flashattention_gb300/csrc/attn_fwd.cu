@@ -870,6 +870,402 @@ cudaError_t launch_fwd2_t(const FwdArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ====================================================================== persistent forward, one head per item
+// Default-precision forward over the pre-rotated fp16 q, k.  One CTA per SM
+// loops over work items (query tile i, batch, query head), largest first in a
+// snake order.  Key tile j of an item is step n of the CTA (n counts across
+// items); step n computes S into TMEM score buffer n & 1, is handled by softmax
+// warpgroup n & 1 (warps 2-5 or 6-9, one thread per query row) and writes its
+// P into TMEM P buffer n & 1, from which O += P V reads it.  With separate S
+// and P buffers, S of step n + 2 goes out as soon as step n's scores have been
+// read, and P of step n + 2 waits only for the PV of step n (issued a full
+// step earlier): the warpgroups never wait for the tensor core in the steady
+// state.  The row statistics pass from one step to the next through shared
+// memory: the running maximum after the first pass over the scores (m_ready),
+// the running sum after the second (l_ready).  The warpgroup of an item's last
+// key tile writes O and the LSE.
+// Warps: 0 TMA producer, 1 S = Q K^T issuer, 10 O += P V issuer.
+template <int D>
+struct Fwd3Cfg {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr uint32_t kSpan = D * 2;
+  static constexpr uint32_t kSwz = D == 64 ? kSw128 : kSw64;
+  static constexpr uint32_t kSBO = 8 * kSpan;
+  static constexpr int kStages = 4;  // K/V ring
+  static constexpr uint32_t kColO = 0, kColS = 128, kColP = 384;  // S buffers at 128, 256; P buffers at 384, 448
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kThreads = 352;
+  static constexpr int kOffQ = 0;  // [2]
+  static constexpr int kOffK = 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffStat = kOffV + kStages * kTileBytes;  // m[128], l[128]
+  static constexpr int kOffBar = kOffStat + 2 * kTile * 4;
+  static constexpr int kSmemBytes = kOffBar + 40 * 8 + 16 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct Fwd3Item {
+  int i, b, h;
+};
+
+__device__ __forceinline__ bool fwd3_item(const FwdArgs& a, int tl, Fwd3Item& it) {
+  const int G = (int)gridDim.x, c = (int)blockIdx.x;
+  const int w = (tl & 1) ? (tl + 1) * G - 1 - c : tl * G + c;  // snake over the largest-first order
+  const int per_i = a.B * a.Hq;
+  if (w >= a.nt * per_i) return false;
+  it.i = a.nt - 1 - w / per_i;
+  const int rem = w % per_i;
+  it.h = rem % a.Hq;  // the heads of one kv group sit next to each other: their K/V tiles meet in L2
+  it.b = rem / a.Hq;
+  return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ FwdArgs a) {
+  using C = Fwd3Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  constexpr int S = C::kStages;
+  constexpr int TB = C::kTileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* q_full = bars;         // [2]
+  uint64_t* q_empty = bars + 2;    // [2]
+  uint64_t* kv_full = bars + 4;    // [S]
+  uint64_t* kv_empty = bars + 8;   // [S]
+  uint64_t* s_full = bars + 12;    // [2]
+  uint64_t* s_read = bars + 14;    // [2] the step's warpgroup has read its scores
+  uint64_t* p_ready = bars + 16;   // [2]
+  uint64_t* pv_done = bars + 18;   // [2] PV of the P buffer's last step completed
+  uint64_t* m_ready = bars + 20;   // running maximum of the latest step stored
+  uint64_t* l_ready = bars + 21;   // running sum of the latest step stored
+  uint64_t* o_free = bars + 22;    // the item's O has been read out
+  uint64_t* drain = bars + 23;     // [2] one per issuing thread
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 26);
+  volatile int* abort = reinterpret_cast<volatile int*>(bars + 26) + 1;
+  float* sm_m = reinterpret_cast<float*>(smem + C::kOffStat);
+  float* sm_l = sm_m + kTile;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    *abort = 0;
+    for (int k = 0; k < 2; k++) {
+      mbar_init(q_full + k, 1);
+      mbar_init(q_empty + k, 1);
+      mbar_init(s_full + k, 1);
+      mbar_init(s_read + k, 128);
+      mbar_init(p_ready + k, 128);
+      mbar_init(pv_done + k, 1);
+      mbar_init(drain + k, 1);
+    }
+    for (int k = 0; k < S; k++) {
+      mbar_init(kv_full + k, 1);
+      mbar_init(kv_empty + k, 1);
+    }
+    mbar_init(m_ready, 128);
+    mbar_init(l_ready, 128);
+    mbar_init(o_free, 128);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const volatile int never = 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&a.map_q);
+      prefetch_tmap(&a.map_k);
+      prefetch_tmap(&a.map_v);
+      bool ok = true;
+      int g = 0, loaded_items = 0;
+      Fwd3Item it;
+      for (int tl = 0; ok && fwd3_item(a, tl, it); tl++) {
+        const int qb = tl & 1, kvh = it.h / a.G;
+        if (tl >= 2 && !(ok = mbar_wait(q_empty + qb, ((tl >> 1) - 1) & 1, abort))) break;
+        mbar_arrive_expect_tx(q_full + qb, TB);
+        tma_load_4d(smem + C::kOffQ + qb * TB, &a.map_q, q_full + qb, 0, it.h, it.i * kTile, it.b);
+        loaded_items = tl + 1;
+        for (int j = 0; j <= it.i; j++, g++) {
+          const int st = g % S, use = g / S;
+          if (use > 0 && !(ok = mbar_wait(kv_empty + st, (use - 1) & 1, abort))) break;
+          mbar_arrive_expect_tx(kv_full + st, 2 * TB);
+          tma_load_4d(smem + C::kOffK + st * TB, &a.map_k, kv_full + st, 0, kvh, j * kTile, it.b);
+          tma_load_4d(smem + C::kOffV + st * TB, &a.map_v, kv_full + st, 0, kvh, j * kTile, it.b);
+        }
+      }
+      if (!ok) record_timeout(a.status, abort);
+      // let every copy issued above land before the CTA can exit
+      for (int tl = loaded_items - 2 < 0 ? 0 : loaded_items - 2; tl < loaded_items; tl++)
+        mbar_wait(q_full + (tl & 1), (tl >> 1) & 1, &never);
+      for (int x = g - S < 0 ? 0 : g - S; x < g; x++) mbar_wait(kv_full + x % S, (x / S) & 1, &never);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ S = Q K^T issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_fp16(128, 128, false, false);
+      constexpr uint32_t kStepK = 32 >> 4;
+      constexpr uint32_t tstep = (uint32_t)TB >> 4;
+      const uint64_t dQ0 = smem_desc(smem_u32(smem + C::kOffQ), 16, C::kSBO, C::kSwz);
+      const uint64_t dK0 = smem_desc(smem_u32(smem + C::kOffK), 16, C::kSBO, C::kSwz);
+      bool ok = true;
+      int g = 0;
+      Fwd3Item it;
+      for (int tl = 0; ok && fwd3_item(a, tl, it); tl++) {
+        const int qb = tl & 1;
+        if (!(ok = mbar_wait(q_full + qb, (tl >> 1) & 1, abort))) break;
+        for (int j = 0; j <= it.i; j++, g++) {
+          const int st = g % S;
+          if (!(ok = mbar_wait(kv_full + st, (g / S) & 1, abort))) break;
+          // the score buffer's previous step (g - 2) has read its scores
+          if (g >= 2 && !(ok = mbar_wait(s_read + (g & 1), ((g >> 1) - 1) & 1, abort))) break;
+          tc_fence_after();
+          mma_ss_chain<D / 16>(tmem + C::kColS + (g & 1) * 128, dQ0 + (uint64_t)(qb * tstep), kStepK,
+                               dK0 + (uint64_t)(st * tstep), kStepK, idS, 0u);
+          mma_commit(s_full + (g & 1));
+          if (j == it.i) mma_commit(q_empty + qb);
+        }
+      }
+      if (!ok) record_timeout(a.status, abort);
+      mma_commit(drain);
+      mbar_wait(drain, 0, &never);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ O += P V issuer
+    if (lane == 0) {
+      constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
+      constexpr uint32_t kStepMN = (16 * C::kSpan) >> 4;
+      constexpr uint32_t tstep = (uint32_t)TB >> 4;
+      const uint64_t dV0 = smem_desc(smem_u32(smem + C::kOffV), 16, C::kSBO, C::kSwz);
+      bool ok = true;
+      int g = 0;
+      Fwd3Item it;
+      for (int tl = 0; ok && fwd3_item(a, tl, it); tl++) {
+        for (int j = 0; j <= it.i; j++, g++) {
+          const int st = g % S;
+          if (!(ok = mbar_wait(p_ready + (g & 1), (g >> 1) & 1, abort))) break;
+          if (j == 0 && tl > 0 && !(ok = mbar_wait(o_free, (tl - 1) & 1, abort))) break;
+          tc_fence_after();
+          mma_ts_chain<8, false>(tmem + C::kColO, tmem + C::kColP + (g & 1) * 64, dV0 + (uint64_t)(st * tstep),
+                                 kStepMN, idPV, j > 0 ? 1u : 0u);
+          mma_commit(pv_done + (g & 1));
+          // K was read by S(g), which completed before this step's softmax began
+          mma_commit(kv_empty + st);
+        }
+      }
+      if (!ok) record_timeout(a.status, abort);
+      mma_commit(drain + 1);
+      mbar_wait(drain + 1, 0, &never);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int wg = (warp - 2) >> 2;  // 0: warps 2-5, 1: warps 6-9
+    const int q4 = warp & 3;         // TMEM lane quarter
+    const int r = q4 * 32 + lane;    // query row within the tile
+    const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+    const uint32_t sbuf = trow + C::kColS + wg * 128;
+    const uint32_t pbuf = trow + C::kColP + wg * 64;
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    int g = 0;
+    Fwd3Item it;
+    for (int tl = 0; ok && fwd3_item(a, tl, it); tl++) {
+      const int t = it.i * kTile + r;
+      for (int j = 0; j <= it.i; j++, g++) {
+        if ((g & 1) != wg) continue;
+        const bool diag = (j == it.i);
+        ok = __all_sync(0xffffffffu, mbar_wait(s_full + wg, (g >> 1) & 1, abort));
+        if (!ok) break;
+        tc_fence_after();
+        // pass 1: row maximum over the 128 keys (masked past the diagonal)
+        float mx8[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) mx8[e] = -INFINITY;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; h2++) {
+          uint32_t u[64];
+          tmem_ld32(sbuf + h2 * 64, *reinterpret_cast<uint32_t(*)[32]>(u));
+          tmem_ld32(sbuf + h2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+          tmem_wait_ld();
+          if (diag) {
+#pragma unroll
+            for (int e = 0; e < 64; e++)
+              if (h2 * 64 + e > r) u[e] = 0xff800000u;  // -inf: key after the query
+          }
+#pragma unroll
+          for (int e = 0; e < 64; e += 2)
+            mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(u[e]), __uint_as_float(u[e + 1]));
+        }
+        const float mxr = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        // running maximum (raw logit units) after the previous key tile, from the other
+        // warpgroup; at an item's first tile the wait only orders the two writes of sm_m
+        float r_use = mxr, alpha = 1.f;
+        if (g > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(m_ready, (g - 1) & 1, abort));
+          if (!ok) break;
+        }
+        if (j > 0) {
+          const float r_old = sm_m[r];
+          r_use = r_old;
+          const float m_old = __fmul_rn(r_old, sl2);
+          const float r_new = fmaxf(r_old, mxr);
+          const float m_new = __fmul_rn(r_new, sl2);
+          // lazy rescale: only when some row's maximum grew by more than 2^8; O must
+          // then hold every earlier P V (the latest is step g - 1's)
+          if (__any_sync(0xffffffffu, m_new > m_old + 8.0f)) {
+            ok = __all_sync(0xffffffffu, mbar_wait(pv_done + ((g - 1) & 1), ((g - 1) >> 1) & 1, abort));
+            if (!ok) break;
+            tc_fence_after();
+            r_use = r_new;
+            alpha = ex2(m_old - m_new);
+            uint32_t w[32];
+#pragma unroll
+            for (int c = 0; c < D / 32; c++) {
+              tmem_ld32(trow + C::kColO + c * 32, w);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; e++) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
+              tmem_st32(trow + C::kColO + c * 32, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+          }
+        }
+        sm_m[r] = r_use;
+        mbar_arrive(m_ready);
+        const float m_use = __fmul_rn(r_use, sl2);
+        // P's buffer is free once the PV of step g - 2 has completed
+        if (g >= 2) {
+          ok = __all_sync(0xffffffffu, mbar_wait(pv_done + wg, ((g >> 1) - 1) & 1, abort));
+          if (!ok) break;
+        }
+        tc_fence_after();
+        // pass 2: P = exp2(s * scale_log2 - m) as bf16 into this warpgroup's P buffer;
+        // the next chunk's scores load while this one is exponentiated
+        // (the row sum adds the fp32 values of P; the MMA multiplies their bf16 roundings)
+        uint64_t sum4[4] = {0ull, 0ull, 0ull, 0ull};
+        const uint64_t sl2x2 = f2(sl2, sl2), negm = f2(-m_use, -m_use);
+        uint32_t ua[16], ub[16];
+        tmem_ld16(sbuf, ua);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+          uint32_t(&cur)[16] = (c & 1) ? ub : ua;
+          uint32_t(&nxt)[16] = (c & 1) ? ua : ub;
+          if (c < 7) tmem_ld16(sbuf + (c + 1) * 16, nxt);
+          if (diag) {
+#pragma unroll
+            for (int e = 0; e < 16; e++)
+              if (16 * c + e > r) cur[e] = 0xff800000u;  // exp2(-inf) = 0
+          }
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; e++) {
+            float x0, x1;
+            f2_split(f2_fma(f2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])), sl2x2, negm), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            pk[e] = pack_bf16(p0, p1);
+            sum4[e & 3] = f2_add(sum4[e & 3], f2(p0, p1));
+          }
+          tmem_st8(pbuf + c * 8, pk);
+          if (c < 7) tmem_wait_ld();
+          if (c == 6) {
+            // the last chunk of scores is in registers: S of step g + 2 may overwrite them
+            tc_fence_before();
+            mbar_arrive(s_read + wg);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_ready + wg);
+        float l;
+        {
+          float s0, s1, s2, s3, s4, s5, s6, s7;
+          f2_split(sum4[0], s0, s1);
+          f2_split(sum4[1], s2, s3);
+          f2_split(sum4[2], s4, s5);
+          f2_split(sum4[3], s6, s7);
+          l = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+        }
+        // running sum after the previous key tile; at an item's first tile the wait only
+        // orders this step's write of sm_l after the previous step's read
+        if (g > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(l_ready, (g - 1) & 1, abort));
+          if (!ok) break;
+        }
+        if (j > 0) l += sm_l[r] * alpha;
+        if (!diag) sm_l[r] = l;
+        mbar_arrive(l_ready);
+        if (!diag) continue;
+        // last key tile of the item: O / l and the LSE
+        ok = __all_sync(0xffffffffu, mbar_wait(pv_done + wg, (g >> 1) & 1, abort));
+        if (!ok) break;
+        tc_fence_after();
+        const float inv = 1.f / l;
+        const size_t orow = (((size_t)it.b * a.T + t) * a.Hq + it.h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; c++) {
+          uint32_t w[32];
+          tmem_ld32(trow + C::kColO + c * 32, w);
+          tmem_wait_ld();
+          if (t < a.T) {
+            if (a.o_fp32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o) + orow + c * 32);
+#pragma unroll
+              for (int e = 0; e < 8; e++)
+                dst[e] = make_float4(__uint_as_float(w[4 * e]) * inv, __uint_as_float(w[4 * e + 1]) * inv,
+                                     __uint_as_float(w[4 * e + 2]) * inv, __uint_as_float(w[4 * e + 3]) * inv);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + orow + c * 32);
+#pragma unroll
+              for (int e = 0; e < 4; e++)
+                dst[e] = make_uint4(pack_bf16(__uint_as_float(w[8 * e]) * inv, __uint_as_float(w[8 * e + 1]) * inv),
+                                    pack_bf16(__uint_as_float(w[8 * e + 2]) * inv, __uint_as_float(w[8 * e + 3]) * inv),
+                                    pack_bf16(__uint_as_float(w[8 * e + 4]) * inv, __uint_as_float(w[8 * e + 5]) * inv),
+                                    pack_bf16(__uint_as_float(w[8 * e + 6]) * inv, __uint_as_float(w[8 * e + 7]) * inv));
+            }
+          }
+        }
+        if (t < a.T)
+          a.lse[((size_t)it.b * a.Hq + it.h) * a.T + t] = (__fmul_rn(r_use, sl2) + __log2f(l)) * 0.69314718055994531f;
+        tc_fence_before();
+        mbar_arrive(o_free);  // the next item's first PV may overwrite O
+      }
+    }
+    if (!ok) record_timeout(a.status, abort);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    tmem_relinquish();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd3_t(const FwdArgs& a, cudaStream_t s) {
+  using C = Fwd3Cfg<D>;
+  static bool attr_set[64] = {};
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_fwd3<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  cudaError_t e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int items = a.nt * a.B * a.Hq;
+  k_attn_fwd3<D><<<items < nsm ? items : nsm, C::kThreads, C::kSmemBytes, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int D, bool P>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
   using C = FwdCfg<D, P>;
@@ -890,8 +1286,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, bool precise, cudaStream_t s) {
-  if (a.D == 64) return precise ? launch_fwd_t<64, true>(a, s) : launch_fwd2_t<64>(a, s);
-  return precise ? launch_fwd_t<32, true>(a, s) : launch_fwd2_t<32>(a, s);
+  if (a.D == 64) return precise ? launch_fwd_t<64, true>(a, s) : launch_fwd3_t<64>(a, s);
+  return precise ? launch_fwd_t<32, true>(a, s) : launch_fwd3_t<32>(a, s);
 }
 
 cudaError_t launch_rope_qk(const RopeArgs& a, int D, cudaStream_t s) {

@@ -103,6 +103,24 @@ class ClockSampler:
                     reasons=reasons, samples=len(rows))
 
 
+def slowest_over_ranks(ms, world, device):
+    """The slowest rank's time: every rank passes its own, all get the maximum
+    (the step's wall time when ranks run side by side)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, flops_per_rank_step, ms_per_step):
+    """Throughput of the whole job: every rank runs its own replica of the
+    step, so the work is world x the per-rank work, over the slowest rank's time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_init():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -287,14 +305,8 @@ def run_ours(args, world, rank, local):
     prof = binding.profile_read(prof_cap)
     ms_total = e0.elapsed_time(e1)
     barrier()
-    ms_max = ms_total
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    ms_step = ms_max / args.steps
-    value = world * fl["total"] / (ms_step * 1e-3) / 1e12
+    ms_step = slowest_over_ranks(ms_total, world, dev) / args.steps
+    value = whole_job_tflops(world, fl["total"], ms_step)
 
     # end to end through the public API: pinned host inputs in, results out, every step
     e2e_steps = max(3, min(args.steps, 200))
@@ -323,12 +335,7 @@ def run_ours(args, world, rank, local):
         e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = slowest_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
     h2d = sum(t.numel() * t.element_size() for t in pin)
     d2h = sum(t.numel() * t.element_size() for t in outs.values())
 
@@ -375,7 +382,7 @@ def run_ours(args, world, rank, local):
                                 NUM_SETS, launches_per_step)),
                 pct_of_bf16_peak=100.0 * value / world / peaks["bf16_tflops"],
                 roofline=roof, cpu_baseline=cpu,
-                e2e=dict(value=world * fl["total"] / (e2e_ms * 1e-3) / 1e12, unit=UNIT, h2d_bytes_per_step=h2d,
+                e2e=dict(value=whole_job_tflops(world, fl["total"], e2e_ms), unit=UNIT, h2d_bytes_per_step=h2d,
                          d2h_bytes_per_step=d2h),
                 gpu_launches=launches_per_step * args.steps,
                 clocks=clk)

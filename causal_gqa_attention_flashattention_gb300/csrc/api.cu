@@ -247,8 +247,8 @@ int check_shape(int B, int T, int Hq, int Hkv, int D) {
   return NE_OK;
 }
 
-int heads_per_cta(int G, int D, bool precise) {
-  for (int hc = precise ? fwd_max_heads(D, true) : fwd2_max_heads(D); hc >= 1; hc--)
+int heads_per_cta(int G, int D) {
+  for (int hc = fwd_max_heads(D, true); hc >= 1; hc--)
     if (G % hc == 0) return hc;
   return 1;
 }
@@ -418,8 +418,7 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
   a.Hkv = Hkv;
   a.D = D;
   a.G = Hq / Hkv;
-  a.HC = heads_per_cta(a.G, D, precise);
-  a.kv_stages = fwd2_kv_stages(D, a.HC);
+  a.HC = precise ? heads_per_cta(a.G, D) : 1;
   a.o_fp32 = (flags & kFlagOFp32) ? 1 : 0;
   const double sl2 = 1.4426950408889634 / std::sqrt((double)D);
   a.scale_log2 = (float)sl2;
@@ -503,6 +502,7 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   p.D = D;
   p.Tp = Tp;
   p.rotate_qk = (flags & kFlagQKRotated) ? 0 : 1;
+  p.negate = precise ? 0 : 1;
   p.div_hq = make_fastdiv((uint32_t)Hq);
   p.div_hkv = make_fastdiv((uint32_t)Hkv);
   p.div_t = make_fastdiv((uint32_t)T);
@@ -760,6 +760,7 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
   p.D = D;
   p.Tp = Tp;
   p.rotate_qk = (flags & kFlagQKRotated) ? 0 : 1;
+  p.negate = precise ? 0 : 1;
   p.div_hq = make_fastdiv((uint32_t)Hq);
   p.div_hkv = make_fastdiv((uint32_t)Hkv);
   p.div_t = make_fastdiv((uint32_t)T);

@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
     for (int off = kCPR / 2; off >= 1; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
     if (valid && c == 0) {
       const size_t o = ((size_t)b * a.Hq + h) * a.Tp + t;
-      a.delta[o] = part;
+      a.delta[o] = a.negate ? -part : part;
       const size_t li = ((size_t)b * a.Hq + h) * a.T + t;
       if (a.lse_lo) {
         // (hi + lo) * log2(e) as a two-part value, with a two-part log2(e).
@@ -108,7 +108,8 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
         a.lse2[o] = h2;
         a.lse2_lo[o] = fmaf(hi, kLog2eHi, -h2) + hi * kLog2eLo + lo * kLog2eHi;
       } else {
-        a.lse2[o] = a.lse[li] * 1.4426950408889634f;
+        const float l2 = a.lse[li] * 1.4426950408889634f;
+        a.lse2[o] = a.negate ? -l2 : l2;
       }
     }
   }
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
     const uint32_t bh = fdiv(it, a.div_pad);
     const uint32_t t = (uint32_t)a.T + (it - bh * npad);
     a.delta[(size_t)bh * a.Tp + t] = 0.f;
-    a.lse2[(size_t)bh * a.Tp + t] = __int_as_float(0x7f800000);
+    a.lse2[(size_t)bh * a.Tp + t] = __int_as_float(a.negate ? 0xff800000 : 0x7f800000);
     if (a.lse2_lo) a.lse2_lo[(size_t)bh * a.Tp + t] = 0.f;
   }
 }
@@ -756,8 +757,8 @@ __device__ __forceinline__ bool bwd_item(const BwdArgs& a, int tl, BwdItem& it) 
 
 // Stores one 128-row tile of a gradient (row r per thread of a 128-thread
 // group, values x) through shared memory: 128-byte-wide boxes (64 when a row is
-// shorter), swizzled.  Per box: every thread writes its row and arrives on
-// `full`; thread 0 stores the box with TMA (rows past T are not written), waits
+// shorter), swizzled.  Per box: every warp writes its rows and arrives on
+// `full` (4 arrivals); thread 0 stores the box with TMA (rows past T are not written), waits
 // until the store has read the box and arrives on `free_`; every thread waits
 // for that before the next box.  `e` counts the boxes (barrier phases).
 // Returns false if a wait gave up.
@@ -784,7 +785,7 @@ __device__ __forceinline__ bool stage_store(const float (&x)[D], uint8_t* stg, c
       *reinterpret_cast<uint4*>(stg + swz(r, ch, kSpan)) = w;
     }
     fence_proxy_async_smem();
-    mbar_arrive(full);
+    warp_arrive(full);
     if (r == 0) {
       if (mbar_wait(full, e & 1, abort)) {
         tma_store_4d(map, stg, c0, h, row0, b);
@@ -841,19 +842,19 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
       mbar_init(qd_empty + s, 2);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_read, 256);
-    mbar_init(p_ready, 256);
+    mbar_init(s_read, 8);  // one arrival per warp of the compute warps
+    mbar_init(p_ready, 8);
     mbar_init(pbuf_free, 1);
     mbar_init(dp_full, 1);
-    mbar_init(ds_ready, 256);
+    mbar_init(ds_ready, 8);
     mbar_init(ds_free, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, 128);
+    mbar_init(dq_free, 4);
     mbar_init(acc_done, 2);
-    mbar_init(acc_free, 256);
+    mbar_init(acc_free, 8);
     for (int s = 0; s < 3; s++) mbar_init(drain + s, 1);
     for (int s = 0; s < 2; s++) {
-      mbar_init(stg_full + s, 128);
+      mbar_init(stg_full + s, 4);
       mbar_init(stg_free + s, 1);
     }
     fence_mbar_init();
@@ -1071,70 +1072,88 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
         const float* del = reinterpret_cast<const float*>(smem + C::kOffDel + st * C::kVecBytes) + cbase;
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full, g & 1, abort)))) break;
         tc_fence_after();
-        uint32_t u[64];
+        // P^T = exp2(s * scale_log2 - lse2) for this thread's 64 query columns (the
+        // vectors hold -lse2 and -Delta): the scores arrive with one TMEM round trip
+        // and turn into fp32 P in the same registers, then into bf16 pairs (for dV and dS)
+        float pf[64];
+        uint32_t(&pu)[64] = *reinterpret_cast<uint32_t(*)[64]>(pf);
 #pragma unroll
-        for (int c = 0; c < 4; c++) tmem_ld16(trow + C::kColS + cbase + c * 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16 * c));
+        for (int c = 0; c < 4; c++)
+          tmem_ld16(trow + C::kColS + cbase + c * 16, *reinterpret_cast<uint32_t(*)[16]>(pu + 16 * c));
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(s_read);  // S^T of the next step may overwrite the score columns
-        uint32_t pk[32];      // P^T for this thread's 64 query columns, packed bf16 pairs
+        warp_arrive(s_read);  // S^T of the next step may overwrite the score columns
+        const uint64_t sl2x2 = f2(sl2, sl2);
 #pragma unroll
         for (int v4 = 0; v4 < 16; v4++) {
           const float4 t4 = reinterpret_cast<const float4*>(lse2)[v4];
-          const float l2[4] = {t4.x, t4.y, t4.z, t4.w};
 #pragma unroll
           for (int e = 0; e < 2; e++) {
-            const int q0 = cbase + 4 * v4 + 2 * e;
-            float p0 = ex2(fmaf(__uint_as_float(u[4 * v4 + 2 * e]), sl2, -l2[2 * e]));
-            float p1 = ex2(fmaf(__uint_as_float(u[4 * v4 + 2 * e + 1]), sl2, -l2[2 * e + 1]));
+            const int q = 4 * v4 + 2 * e;
+            float x0, x1;
+            f2_split(f2_fma(f2(pf[q], pf[q + 1]), sl2x2, e == 0 ? f2(t4.x, t4.y) : f2(t4.z, t4.w)), x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
             if (diag) {
-              if (q0 < r) p0 = 0.f;
-              if (q0 + 1 < r) p1 = 0.f;
+              if (cbase + q < r) p0 = 0.f;
+              if (cbase + q + 1 < r) p1 = 0.f;
             }
-            pk[2 * v4 + e] = pack_bf16(p0, p1);
+            pf[q] = p0;
+            pf[q + 1] = p1;
           }
         }
+        uint32_t pk[32];
+#pragma unroll
+        for (int q = 0; q < 32; q++) pk[q] = pack_bf16(pf[2 * q], pf[2 * q + 1]);
         // the P^T columns are free once the previous step's dV has read them
         if (g > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(pbuf_free, (g - 1) & 1, abort)))) break;
         tc_fence_after();
-        tmem_st32(trow + C::kColP + wg * 32, pk);
+#pragma unroll
+        for (int hlf = 0; hlf < 4; hlf++)
+          tmem_st8(trow + C::kColP + wg * 32 + hlf * 8, *reinterpret_cast<const uint32_t(*)[8]>(pk + 8 * hlf));
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(p_ready);
+        warp_arrive(p_ready);
 
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(dp_full, g & 1, abort)))) break;
         if (g > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (g - 1) & 1, abort)))) break;
         tc_fence_after();
+        // dS = P * (dP - Delta), 16 columns at a time; the next chunk of dP^T loads
+        // while this one is computed (its columns are never the ones being stored)
+        uint32_t va[16], vb[16];
+        tmem_ld16(trow + C::kColDP + cbase, va);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c2 = 0; c2 < 2; c2++) {
-          uint32_t v[32];
-          tmem_ld16(trow + C::kColDP + cbase + c2 * 32, *reinterpret_cast<uint32_t(*)[16]>(v));
-          tmem_ld16(trow + C::kColDP + cbase + c2 * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-          float dl[32];
+        for (int c4 = 0; c4 < 4; c4++) {
+          uint32_t(&v)[16] = (c4 & 1) ? vb : va;
+          uint32_t(&nxt)[16] = (c4 & 1) ? va : vb;
+          if (c4 < 3) tmem_ld16(trow + C::kColDP + cbase + (c4 + 1) * 16, nxt);
+          uint32_t w[8];
 #pragma unroll
-          for (int v4 = 0; v4 < 8; v4++) {
-            const float4 t4 = reinterpret_cast<const float4*>(del + c2 * 32)[v4];
-            dl[4 * v4] = t4.x, dl[4 * v4 + 1] = t4.y, dl[4 * v4 + 2] = t4.z, dl[4 * v4 + 3] = t4.w;
-          }
-          tmem_wait_ld();
-          uint32_t w[16];
+          for (int v4 = 0; v4 < 4; v4++) {
+            const float4 t4 = reinterpret_cast<const float4*>(del + c4 * 16)[v4];
 #pragma unroll
-          for (int e = 0; e < 16; e++) {
-            const float d0 = (__uint_as_float(v[2 * e]) - dl[2 * e]) * bf_lo(pk[c2 * 16 + e]);
-            const float d1 = (__uint_as_float(v[2 * e + 1]) - dl[2 * e + 1]) * bf_hi(pk[c2 * 16 + e]);
-            w[e] = pack_f16(d0, d1);
+            for (int e = 0; e < 2; e++) {
+              const int q = 4 * v4 + 2 * e;  // column within this quarter
+              const uint64_t d = f2_mul(f2_add(f2(__uint_as_float(v[q]), __uint_as_float(v[q + 1])),
+                                               e == 0 ? f2(t4.x, t4.y) : f2(t4.z, t4.w)),
+                                        f2(bf_lo(pk[c4 * 8 + (q >> 1)]), bf_hi(pk[c4 * 8 + (q >> 1)])));
+              float d0, d1;
+              f2_split(d, d0, d1);
+              w[q >> 1] = pack_f16(d0, d1);
+            }
           }
           // dS^T into TMEM over the dP^T columns already read (for dK), dS into shared memory (for dQ)
-          tmem_st16(trow + C::kColDP + cbase + c2 * 16, w);
+          tmem_st8(trow + C::kColDP + cbase + c4 * 8, w);
 #pragma unroll
-          for (int q = 0; q < 4; q++)
-            *reinterpret_cast<uint4*>(atom + r * 128 + (((uint32_t)(4 * c2 + q) ^ x7) << 4)) =
+          for (int q = 0; q < 2; q++)
+            *reinterpret_cast<uint4*>(atom + r * 128 + (((uint32_t)(2 * c4 + q) ^ x7) << 4)) =
                 make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          if (c4 < 3) tmem_wait_ld();
         }
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(ds_ready);
+        warp_arrive(ds_ready);
       }
       if (!ok) break;
       // item epilogue: warps 4-7 store dK (scale, inverse rotation), warps 8-11 store dV
@@ -1150,7 +1169,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
         for (int e = 0; e < 16; e++) x[c * 16 + e] = __uint_as_float(u[e]);
       }
       tc_fence_before();
-      mbar_arrive(acc_free);  // the next item's first dV / dK may overwrite the accumulators
+      warp_arrive(acc_free);  // the next item's first dV / dK may overwrite the accumulators
       const int t = it.j * kTile + r;
       if (wg == 0) {
         // dK = scale * (inverse rotation of the accumulated dK^)
@@ -1206,7 +1225,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
           }
           tmem_wait_ld();
           tc_fence_before();
-          mbar_arrive(dq_free);
+          warp_arrive(dq_free);
         }
         const int i = it.j + n / G, h = it.kvh * G + n % G;
         const int row0 = (int)(((size_t)it.b * a.Hq + h) * a.Tp + (size_t)i * kTile);

@@ -471,403 +471,35 @@ template <int D>
 __global__ void __launch_bounds__(256) k_rope_qk(const RopeArgs a) {
   constexpr int kCPR = D / 8;  // 16-byte chunks per row
   constexpr int kShift = D == 64 ? 3 : 2;
+  constexpr int kPer = 4;      // chunks per thread, loaded together
   const uint32_t nq = (uint32_t)a.B * a.T * a.Hq * kCPR;
   const uint32_t n = nq + (uint32_t)a.B * a.T * a.Hkv * kCPR;
-  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < n; it += gridDim.x * blockDim.x) {
-    const bool isq = it < nq;
-    const uint32_t x = isq ? it : it - nq;
-    const uint32_t row = x >> kShift;  // (b, t, h)
-    const int c = (int)(x & (kCPR - 1));
-    const uint32_t bt = fdiv(row, isq ? a.div_hq : a.div_hkv);
-    const uint32_t t = bt - fdiv(bt, a.div_t) * a.T;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(isq ? a.q : a.k) + x);
-    float4 c0, c1;
-    rope_coeffs<D>(a.rope, (int)t, c, c0, c1);
-    reinterpret_cast<uint4*>(isq ? a.qr : a.kr)[x] = rope_chunk_f16(v, c0, c1, nullptr);
-  }
-}
-
-// ====================================================================== persistent forward
-// Default-precision forward over the pre-rotated fp16 q, k: one CTA per SM
-// loops over work items (query tile, batch, kv head, head chunk) taken
-// largest-first in a snake order; its next item's Q tiles load into the
-// second Q buffer while the current item runs.
-// Head-step n (one head of the chunk, one key tile; heads fastest) computes
-// S into TMEM score buffer n & 1 and is handled by softmax warpgroup n & 1
-// (warps 2-5 and 6-9, one thread per query row): the two warpgroups run half
-// a step apart, so one's exponentials overlap the other's wait for its next
-// S.  With an odd number of heads per CTA a head alternates between the
-// warpgroups from one key tile to the next; its row statistics (m, l) live in
-// shared memory and pass from one warpgroup to the other through the head's
-// `st_ready` barrier.  The warpgroup that finishes a head's last key tile
-// writes that head's O and LSE.
-// Two threads issue the tensor-core work, each from its own warp (one thread
-// issues at most about one MMA per 70-100 cycles, whatever N): warp 1 the
-// S = Q K^T chains, warp 10 the O += P V chains.  S of head-step n reuses the
-// score buffer of head-step n - 2 once that step's PV has completed.
-template <int D>
-struct Fwd2Cfg {
-  static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr uint32_t kSpan = D * 2;
-  static constexpr uint32_t kSwz = D == 64 ? kSw128 : kSw64;
-  static constexpr uint32_t kSBO = 8 * kSpan;
-  static constexpr int kMaxHC = D == 64 ? 4 : 8;
-  static constexpr int kMaxStages = 3;
-  static constexpr uint32_t kTmemS = 256;  // score buffers at columns 256 and 384
-  static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kThreads = 352;
-  static_assert(kMaxHC * D <= 256, "O accumulators must fit below the score buffers");
-};
-
-struct FwdItem {
-  int i, b, kvh, hc;
-};
-
-__device__ __forceinline__ bool fwd_item(const FwdArgs& a, int tl, FwdItem& it) {
-  const int G = (int)gridDim.x, c = (int)blockIdx.x;
-  const int w = (tl & 1) ? (tl + 1) * G - 1 - c : tl * G + c;  // snake over the largest-first order
-  const int nchunk = a.G / a.HC;
-  const int per_i = a.B * a.Hkv * nchunk;
-  if (w >= a.nt * per_i) return false;
-  it.i = a.nt - 1 - w / per_i;
-  int rem = w % per_i;
-  it.hc = rem % nchunk;
-  rem /= nchunk;
-  it.kvh = rem % a.Hkv;
-  it.b = rem / a.Hkv;
-  return true;
-}
-
-template <int D>
-__global__ void __launch_bounds__(352, 1) k_attn_fwd2(const __grid_constant__ FwdArgs a) {
-  using C = Fwd2Cfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  const int HC = a.HC, S = a.kv_stages;
-  const int TB = C::kTileBytes;
-  const int offQ = 0, offK = 2 * HC * TB, offV = offK + S * TB, offStat = offV + S * TB;
-  const int offBar = offStat + 2 * C::kMaxHC * kTile * 4;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + offBar);
-  uint64_t* q_full = bars;         // [2]
-  uint64_t* q_empty = bars + 2;    // [2]
-  uint64_t* kv_full = bars + 4;    // [3]
-  uint64_t* kv_empty = bars + 7;   // [3]
-  uint64_t* s_full = bars + 10;    // [2]
-  uint64_t* p_ready = bars + 12;   // [2]
-  uint64_t* o_done = bars + 14;    // [kMaxHC]
-  uint64_t* o_free = bars + 22;    // [kMaxHC]
-  uint64_t* st_ready = bars + 30;  // [kMaxHC]
-  uint64_t* drain = bars + 38;     // [2] one per issuing thread
-  uint64_t* buf_free = bars + 41;  // [2] PV of the buffer's last head-step completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 43);
-  volatile int* abort = reinterpret_cast<volatile int*>(bars + 43) + 1;
-  // row statistics [head][row]: running maximum (raw logit units) and sum
-  float* sm_m = reinterpret_cast<float*>(smem + offStat);
-  float* sm_l = sm_m + C::kMaxHC * kTile;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  if (tid == 0) {
-    *abort = 0;
-    for (int k = 0; k < 2; k++) {
-      mbar_init(q_full + k, 1);
-      mbar_init(q_empty + k, 1);
-      mbar_init(s_full + k, 1);
-      mbar_init(p_ready + k, 128);
-      mbar_init(buf_free + k, 1);
-      mbar_init(drain + k, 1);
-    }
-    for (int k = 0; k < C::kMaxStages; k++) {
-      mbar_init(kv_full + k, 1);
-      mbar_init(kv_empty + k, 1);
-    }
-    for (int k = 0; k < C::kMaxHC; k++) {
-      mbar_init(o_done + k, 1);
-      mbar_init(o_free + k, 128);
-      mbar_init(st_ready + k, 128);
-    }
-    fence_mbar_init();
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const volatile int never = 0;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tmap(&a.map_q);
-      prefetch_tmap(&a.map_k);
-      prefetch_tmap(&a.map_v);
-      bool ok = true;
-      int g = 0, loaded_items = 0;
-      FwdItem it;
-      for (int tl = 0; ok && fwd_item(a, tl, it); tl++) {
-        const int qb = tl & 1;
-        if (tl >= 2 && !(ok = mbar_wait(q_empty + qb, ((tl >> 1) - 1) & 1, abort))) break;
-        mbar_arrive_expect_tx(q_full + qb, HC * TB);
-        const int h0 = it.kvh * a.G + it.hc * HC;
-        for (int hh = 0; hh < HC; hh++)
-          tma_load_4d(smem + offQ + (qb * HC + hh) * TB, &a.map_q, q_full + qb, 0, h0 + hh, it.i * kTile, it.b);
-        loaded_items = tl + 1;
-        for (int j = 0; j <= it.i; j++, g++) {
-          const int st = g % S, use = g / S;
-          if (use > 0 && !(ok = mbar_wait(kv_empty + st, (use - 1) & 1, abort))) break;
-          mbar_arrive_expect_tx(kv_full + st, 2 * TB);
-          tma_load_4d(smem + offK + st * TB, &a.map_k, kv_full + st, 0, it.kvh, j * kTile, it.b);
-          tma_load_4d(smem + offV + st * TB, &a.map_v, kv_full + st, 0, it.kvh, j * kTile, it.b);
-        }
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t base = blockIdx.x * blockDim.x + threadIdx.x; base < n; base += kPer * stride) {
+    uint4 v[kPer];
+    float4 c0[kPer], c1[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; u++) {
+      const uint32_t it = base + u * stride;
+      if (it < n) {
+        const bool isq = it < nq;
+        const uint32_t x = isq ? it : it - nq;
+        const uint32_t row = x >> kShift;  // (b, t, h)
+        const uint32_t bt = fdiv(row, isq ? a.div_hq : a.div_hkv);
+        const uint32_t t = bt - fdiv(bt, a.div_t) * a.T;
+        v[u] = __ldg(reinterpret_cast<const uint4*>(isq ? a.q : a.k) + x);
+        rope_coeffs<D>(a.rope, (int)t, (int)(x & (kCPR - 1)), c0[u], c1[u]);
       }
-      if (!ok) record_timeout(a.status, abort);
-      // let every copy issued above land before the CTA can exit
-      for (int tl = loaded_items - 2 < 0 ? 0 : loaded_items - 2; tl < loaded_items; tl++)
-        mbar_wait(q_full + (tl & 1), (tl >> 1) & 1, &never);
-      for (int x = g - S < 0 ? 0 : g - S; x < g; x++) mbar_wait(kv_full + x % S, (x / S) & 1, &never);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ S = Q K^T issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_fp16(128, 128, false, false);
-      constexpr uint32_t kStepK = 32 >> 4;
-      const uint32_t tstep = (uint32_t)TB >> 4;
-      const uint64_t dQ0 = smem_desc(smem_u32(smem + offQ), 16, C::kSBO, C::kSwz);
-      const uint64_t dK0 = smem_desc(smem_u32(smem + offK), 16, C::kSBO, C::kSwz);
-      bool ok = true;
-      int g = 0, n = 0;
-      FwdItem it;
-      for (int tl = 0; ok && fwd_item(a, tl, it); tl++) {
-        const int qb = tl & 1;
-        if (!(ok = mbar_wait(q_full + qb, (tl >> 1) & 1, abort))) break;
-        for (int j = 0; ok && j <= it.i; j++, g++) {
-          const int st = g % S;
-          if (!(ok = mbar_wait(kv_full + st, (g / S) & 1, abort))) break;
-          for (int hh = 0; hh < HC; hh++, n++) {
-            // the score buffer's previous head-step (n - 2): its P consumed by its PV
-            if (n >= 2 && !(ok = mbar_wait(buf_free + (n & 1), ((n >> 1) - 1) & 1, abort))) break;
-            tc_fence_after();
-            mma_ss_chain<D / 16>(tmem + C::kTmemS + (n & 1) * 128, dQ0 + (uint64_t)((qb * HC + hh) * tstep), kStepK,
-                                 dK0 + (uint64_t)(st * tstep), kStepK, idS, 0u);
-            mma_commit(s_full + (n & 1));
-            if (j == it.i && hh == HC - 1) mma_commit(q_empty + qb);
-          }
-        }
+#pragma unroll
+    for (int u = 0; u < kPer; u++) {
+      const uint32_t it = base + u * stride;
+      if (it < n) {
+        const bool isq = it < nq;
+        reinterpret_cast<uint4*>(isq ? a.qr : a.kr)[isq ? it : it - nq] = rope_chunk_f16(v[u], c0[u], c1[u], nullptr);
       }
-      if (!ok) record_timeout(a.status, abort);
-      mma_commit(drain);
-      mbar_wait(drain, 0, &never);
     }
-  } else if (warp == 10) {
-    // ------------------------------------------------------------ O += P V issuer
-    if (lane == 0) {
-      constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
-      constexpr uint32_t kStepMN = (16 * C::kSpan) >> 4;
-      const uint32_t tstep = (uint32_t)TB >> 4;
-      const uint64_t dV0 = smem_desc(smem_u32(smem + offV), 16, C::kSBO, C::kSwz);
-      bool ok = true;
-      int g = 0, n = 0;
-      FwdItem it;
-      for (int tl = 0; ok && fwd_item(a, tl, it); tl++) {
-        for (int j = 0; ok && j <= it.i; j++, g++) {
-          const int st = g % S;
-          for (int hh = 0; hh < HC; hh++, n++) {
-            if (!(ok = mbar_wait(p_ready + (n & 1), (n >> 1) & 1, abort))) break;
-            if (j == 0 && tl > 0 && !(ok = mbar_wait(o_free + hh, (tl - 1) & 1, abort))) break;
-            tc_fence_after();
-            // P (bf16, 128 keys) in the first 64 columns of the score buffer
-            mma_ts_chain<8, false>(tmem + hh * D, tmem + C::kTmemS + (n & 1) * 128, dV0 + (uint64_t)(st * tstep),
-                                   kStepMN, idPV, j > 0 ? 1u : 0u);
-            mma_commit(o_done + hh);
-            mma_commit(buf_free + (n & 1));
-          }
-          // K and V of this stage are free: every S that read K completed before
-          // its softmax (hence these PVs) could start
-          if (ok) mma_commit(kv_empty + st);
-        }
-      }
-      if (!ok) record_timeout(a.status, abort);
-      mma_commit(drain + 1);
-      mbar_wait(drain + 1, 0, &never);
-    }
-  } else {
-    // ------------------------------------------------------------ softmax warpgroups
-    const int wg = (warp - 2) >> 2;  // 0: warps 2-5, 1: warps 6-9
-    const int q4 = warp & 3;         // TMEM lane quarter
-    const int r = q4 * 32 + lane;    // query row within the tile
-    const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-    const uint32_t sbuf = trow + C::kTmemS + wg * 128;  // this warpgroup's score buffer
-    const float sl2 = a.scale_log2;
-    bool ok = true;
-    int n = 0, pvbase = 0;
-    FwdItem it;
-    for (int tl = 0; ok && fwd_item(a, tl, it); tl++) {
-      const int h0 = it.kvh * a.G + it.hc * HC;
-      const int t = it.i * kTile + r;
-      for (int j = 0; ok && j <= it.i; j++) {
-        const bool diag = (j == it.i);
-        for (int hh = 0; hh < HC; hh++, n++) {
-          if ((n & 1) != wg) continue;
-          ok = __all_sync(0xffffffffu, mbar_wait(s_full + wg, (n >> 1) & 1, abort));
-          if (!ok) break;
-          tc_fence_after();
-          // pass 1: row maximum over the 128 keys (masked past the diagonal)
-          float mx8[8];
-#pragma unroll
-          for (int e = 0; e < 8; e++) mx8[e] = -INFINITY;
-#pragma unroll
-          for (int h2 = 0; h2 < 2; h2++) {
-            uint32_t u[64];
-            tmem_ld32(sbuf + h2 * 64, *reinterpret_cast<uint32_t(*)[32]>(u));
-            tmem_ld32(sbuf + h2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 64; e++) {
-              const float v = (diag && h2 * 64 + e > r) ? -INFINITY : __uint_as_float(u[e]);
-              mx8[e & 7] = fmaxf(mx8[e & 7], v);
-            }
-          }
-          const float mxr = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                  fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-          float r_use = mxr, l_old = 0.f, alpha = 1.f;
-          if (j > 0) {
-            // the head's statistics after key tile j - 1 (possibly from the other
-            // warpgroup), and O_h += P V of that tile complete before O_h is rescaled
-            ok = __all_sync(0xffffffffu, mbar_wait(st_ready + hh, (pvbase + j - 1) & 1, abort) &&
-                                             mbar_wait(o_done + hh, (pvbase + j - 1) & 1, abort));
-            if (!ok) break;
-            tc_fence_after();
-            const float r_old = sm_m[hh * kTile + r];
-            l_old = sm_l[hh * kTile + r];
-            r_use = r_old;
-            const float m_old = __fmul_rn(r_old, sl2);
-            const float r_new = fmaxf(r_old, mxr);
-            const float m_new = __fmul_rn(r_new, sl2);
-            // lazy rescale: only when some row's maximum grew by more than 2^8
-            if (__any_sync(0xffffffffu, m_new > m_old + 8.0f)) {
-              r_use = r_new;
-              alpha = ex2(m_old - m_new);
-              uint32_t w[32];
-#pragma unroll
-              for (int c = 0; c < D / 32; c++) {
-                tmem_ld32(trow + hh * D + c * 32, w);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; e++) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
-                tmem_st32(trow + hh * D + c * 32, w);
-              }
-            }
-          }
-          const float m_use = __fmul_rn(r_use, sl2);
-          // pass 2: P = exp2(s * scale_log2 - m) as bf16 into the buffer's first 64
-          // columns (chunk c's P lands on columns already read); the next chunk's
-          // scores load while this one is exponentiated
-          float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          uint32_t ua[32], ub[32];
-          tmem_ld32(sbuf, ua);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 4; c++) {
-            uint32_t(&cur)[32] = (c & 1) ? ub : ua;
-            uint32_t(&nxt)[32] = (c & 1) ? ua : ub;
-            if (c < 3) tmem_ld32(sbuf + (c + 1) * 32, nxt);
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; e++) {
-              float p0 = ex2(fmaf(__uint_as_float(cur[2 * e]), sl2, -m_use));
-              float p1 = ex2(fmaf(__uint_as_float(cur[2 * e + 1]), sl2, -m_use));
-              if (diag) {
-                if (32 * c + 2 * e > r) p0 = 0.f;
-                if (32 * c + 2 * e + 1 > r) p1 = 0.f;
-              }
-              pk[e] = pack_bf16(p0, p1);
-              sum8[e & 7] += bf_lo(pk[e]) + bf_hi(pk[e]);
-            }
-            tmem_st16(sbuf + c * 16, pk);
-            if (c < 3) tmem_wait_ld();
-          }
-          const float l = l_old * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                                           ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(p_ready + wg);
-          if (!diag) {
-            sm_m[hh * kTile + r] = r_use;
-            sm_l[hh * kTile + r] = l;
-            mbar_arrive(st_ready + hh);
-            continue;
-          }
-          // last key tile of head hh: O_h / l and the LSE
-          ok = __all_sync(0xffffffffu, mbar_wait(o_done + hh, (pvbase + j) & 1, abort));
-          if (!ok) break;
-          tc_fence_after();
-          const float inv = 1.f / l;
-          const size_t orow = (((size_t)it.b * a.T + t) * a.Hq + h0 + hh) * D;
-#pragma unroll
-          for (int c = 0; c < D / 32; c++) {
-            uint32_t w[32];
-            tmem_ld32(trow + hh * D + c * 32, w);
-            tmem_wait_ld();
-            if (t < a.T) {
-              if (a.o_fp32) {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o) + orow + c * 32);
-#pragma unroll
-                for (int e = 0; e < 8; e++)
-                  dst[e] = make_float4(__uint_as_float(w[4 * e]) * inv, __uint_as_float(w[4 * e + 1]) * inv,
-                                       __uint_as_float(w[4 * e + 2]) * inv, __uint_as_float(w[4 * e + 3]) * inv);
-              } else {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + orow + c * 32);
-#pragma unroll
-                for (int e = 0; e < 4; e++)
-                  dst[e] = make_uint4(pack_bf16(__uint_as_float(w[8 * e]) * inv, __uint_as_float(w[8 * e + 1]) * inv),
-                                      pack_bf16(__uint_as_float(w[8 * e + 2]) * inv, __uint_as_float(w[8 * e + 3]) * inv),
-                                      pack_bf16(__uint_as_float(w[8 * e + 4]) * inv, __uint_as_float(w[8 * e + 5]) * inv),
-                                      pack_bf16(__uint_as_float(w[8 * e + 6]) * inv, __uint_as_float(w[8 * e + 7]) * inv));
-              }
-            }
-          }
-          if (t < a.T)
-            a.lse[((size_t)it.b * a.Hq + h0 + hh) * a.T + t] = (__fmul_rn(r_use, sl2) + __log2f(l)) * 0.69314718055994531f;
-          tc_fence_before();
-          mbar_arrive(o_free + hh);    // O_h may now be overwritten by the next item
-          mbar_arrive(st_ready + hh);  // keeps the head's barrier phase in step with its key tiles
-        }
-      }
-      pvbase += it.i + 1;
-    }
-    if (!ok) record_timeout(a.status, abort);
   }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) {
-    tmem_relinquish();
-    tmem_dealloc(tmem, C::kTmemCols);
-  }
-}
-
-template <int D>
-cudaError_t launch_fwd2_t(const FwdArgs& a, cudaStream_t s) {
-  const int smem = fwd2_smem_bytes(D, a.HC);
-  // the K/V ring needs two stages: the load of stage g waits for the PVs of
-  // stage g - kv_stages, the last of which goes out after S of stage g - kv_stages + 1
-  if (a.kv_stages < 2 || a.kv_stages > Fwd2Cfg<D>::kMaxStages || a.HC > Fwd2Cfg<D>::kMaxHC || smem > 232448)
-    return cudaErrorInvalidValue;
-  static bool attr_set[64] = {};
-  int dev = 0, nsm = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_fwd2<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
-  cudaError_t e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  const int items = a.nt * a.B * a.Hkv * (a.G / a.HC);
-  const int grid = items < nsm ? items : nsm;
-  k_attn_fwd2<D><<<grid, Fwd2Cfg<D>::kThreads, smem, s>>>(a);
-  return cudaGetLastError();
 }
 
 // ====================================================================== persistent forward, one head per item
@@ -953,8 +585,8 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
       mbar_init(q_full + k, 1);
       mbar_init(q_empty + k, 1);
       mbar_init(s_full + k, 1);
-      mbar_init(s_read + k, 128);
-      mbar_init(p_ready + k, 128);
+      mbar_init(s_read + k, 4);  // one arrival per warp of the warpgroup
+      mbar_init(p_ready + k, 4);
       mbar_init(pv_done + k, 1);
       mbar_init(drain + k, 1);
     }
@@ -962,9 +594,9 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
       mbar_init(kv_full + k, 1);
       mbar_init(kv_empty + k, 1);
     }
-    mbar_init(m_ready, 128);
-    mbar_init(l_ready, 128);
-    mbar_init(o_free, 128);
+    mbar_init(m_ready, 4);
+    mbar_init(l_ready, 4);
+    mbar_init(o_free, 4);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
@@ -1136,7 +768,7 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
           }
         }
         sm_m[r] = r_use;
-        mbar_arrive(m_ready);
+        warp_arrive(m_ready);
         const float m_use = __fmul_rn(r_use, sl2);
         // P's buffer is free once the PV of step g - 2 has completed
         if (g >= 2) {
@@ -1176,12 +808,12 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
           if (c == 6) {
             // the last chunk of scores is in registers: S of step g + 2 may overwrite them
             tc_fence_before();
-            mbar_arrive(s_read + wg);
+            warp_arrive(s_read + wg);
           }
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(p_ready + wg);
+        warp_arrive(p_ready + wg);
         float l;
         {
           float s0, s1, s2, s3, s4, s5, s6, s7;
@@ -1199,7 +831,7 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
         }
         if (j > 0) l += sm_l[r] * alpha;
         if (!diag) sm_l[r] = l;
-        mbar_arrive(l_ready);
+        warp_arrive(l_ready);
         if (!diag) continue;
         // last key tile of the item: O / l and the LSE
         ok = __all_sync(0xffffffffu, mbar_wait(pv_done + wg, (g >> 1) & 1, abort));
@@ -1233,7 +865,7 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
         if (t < a.T)
           a.lse[((size_t)it.b * a.Hq + it.h) * a.T + t] = (__fmul_rn(r_use, sl2) + __log2f(l)) * 0.69314718055994531f;
         tc_fence_before();
-        mbar_arrive(o_free);  // the next item's first PV may overwrite O
+        warp_arrive(o_free);  // the next item's first PV may overwrite O
       }
     }
     if (!ok) record_timeout(a.status, abort);
@@ -1292,7 +924,7 @@ cudaError_t launch_fwd(const FwdArgs& a, bool precise, cudaStream_t s) {
 
 cudaError_t launch_rope_qk(const RopeArgs& a, int D, cudaStream_t s) {
   const long long n = (long long)a.B * a.T * (a.Hq + a.Hkv) * (D / 8);
-  const long long want = (n + 255) / 256;
+  const long long want = (n + 4 * 256 - 1) / (4 * 256);  // four chunks per thread
   const int blocks = (int)(want < 65536 ? want : 65536);
   if (D == 64)
     k_rope_qk<64><<<blocks, 256, 0, s>>>(a);

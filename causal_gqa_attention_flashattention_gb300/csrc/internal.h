@@ -33,28 +33,12 @@ struct FwdArgs {
   float* lse_lo;                    // [B, Hq, T] fp32 remainder of lse (precise logits only)
   const float2* rope;               // [Tcap][D/2] (cos, sin)
   int* status;                      // device status word
-  int B, T, Hq, Hkv, D, G, HC;      // HC: query heads per CTA (divides G)
+  int B, T, Hq, Hkv, D, G, HC;      // HC: query heads per CTA (divides G; precise-logits kernel)
   int nt;                           // number of 128-row tiles
   int o_fp32;
   float scale_log2;                 // log2(e) / sqrt(D), rounded to fp32
   float scale_log2_lo;              // remainder log2(e)/sqrt(D) - scale_log2
-  int kv_stages;                    // K/V ring depth (persistent kernel)
 };
-
-// Persistent forward kernel (default precision): heads per CTA limit and its
-// shared-memory plan for a given HC.  Besides the Q double buffer and the K/V
-// ring: the row statistics (m, l) of every head and the barriers.
-inline int fwd2_max_heads(int D) { return D == 64 ? 4 : 8; }
-inline int fwd2_misc_bytes(int D) { return 2 * fwd2_max_heads(D) * 128 * 4 + 64 * 8 + 16; }
-inline int fwd2_kv_stages(int D, int HC) {
-  const int tile = 128 * D * 2;
-  const int s = (232448 - 1024 - fwd2_misc_bytes(D) - 2 * HC * tile) / (2 * tile);
-  return s > 3 ? 3 : s;
-}
-inline int fwd2_smem_bytes(int D, int HC) {
-  const int tile = 128 * D * 2;
-  return 2 * HC * tile + fwd2_kv_stages(D, HC) * 2 * tile + fwd2_misc_bytes(D) + 1024;
-}
 
 // Division of a non-negative 32-bit n < 2^31 by a runtime divisor d >= 1 with
 // a multiply-high and a shift (round-up magic number):
@@ -110,6 +94,7 @@ struct PrepArgs {
   const float2* rope;
   int B, T, Hq, Hkv, D, Tp, o_fp32;
   int rotate_qk;                            // 0: qr / kr already hold the rotated q and k
+  int negate;                               // 1: store -lse * log2(e) and -Delta (default-precision sweep)
   FastDiv div_hq, div_hkv, div_t, div_pad;  // by Hq, Hkv, T and Tp - T (pad rows; d = 1 if none)
 };
 

@@ -409,6 +409,7 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
     if (launch_rope_qk(ra, D, s) != cudaSuccess) return NE_ERR_CUDA;
   }
   if ((st = make_map_bthd(&a.map_v, v, B, T, Hkv, D)) != NE_OK) return st;
+  if (!precise && (st = make_map_grad(&a.map_o, o, B, T, Hq, D, (flags & kFlagOFp32) != 0)) != NE_OK) return st;
   a.o = o;
   a.lse = lse;
   a.status = d->status;

@@ -517,6 +517,32 @@ __global__ void __launch_bounds__(256) k_rope_qk(const RopeArgs a) {
 // the running sum after the second (l_ready).  The warpgroup of an item's last
 // key tile writes O and the LSE.
 // Warps: 0 TMA producer, 1 S = Q K^T issuer, 10 O += P V issuer.
+// Writes row r of a 128-row tile (D values, fp32 when ES == 4, else bf16) into a
+// staging area of column boxes: `span` = min(D * ES, 128) bytes per row, box after
+// box, each with the TMA / UMMA swizzle of that span.
+template <int D, int ES>
+__device__ __forceinline__ void stage_rows(const float (&x)[D], uint8_t* stg, int r) {
+  constexpr int kSpan = D * ES < 128 ? D * ES : 128;
+  constexpr int kCols = kSpan / ES;
+#pragma unroll
+  for (int c0 = 0, bx = 0; c0 < D; c0 += kCols, bx++) {
+#pragma unroll
+    for (int ch = 0; ch < kSpan / 16; ch++) {
+      uint4 w;
+      if constexpr (ES == 4) {
+        const int i = c0 + ch * 4;
+        w = make_uint4(__float_as_uint(x[i]), __float_as_uint(x[i + 1]), __float_as_uint(x[i + 2]),
+                       __float_as_uint(x[i + 3]));
+      } else {
+        const int i = c0 + ch * 8;
+        w = make_uint4(pack_bf16(x[i], x[i + 1]), pack_bf16(x[i + 2], x[i + 3]), pack_bf16(x[i + 4], x[i + 5]),
+                       pack_bf16(x[i + 6], x[i + 7]));
+      }
+      *reinterpret_cast<uint4*>(stg + bx * kTile * kSpan + swz(r, ch, kSpan)) = w;
+    }
+  }
+}
+
 template <int D>
 struct Fwd3Cfg {
   static constexpr int kTileBytes = kTile * D * 2;
@@ -530,7 +556,9 @@ struct Fwd3Cfg {
   static constexpr int kOffQ = 0;  // [2]
   static constexpr int kOffK = 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffStat = kOffV + kStages * kTileBytes;  // m[128], l[128]
+  static constexpr int kOstBytes = kTile * D * 4;                // O staging per warpgroup (fp32 rows at most)
+  static constexpr int kOffOst = kOffV + kStages * kTileBytes;    // [2]
+  static constexpr int kOffStat = kOffOst + 2 * kOstBytes;         // m[128], l[128]
   static constexpr int kOffBar = kOffStat + 2 * kTile * 4;
   static constexpr int kSmemBytes = kOffBar + 40 * 8 + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -573,8 +601,10 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
   uint64_t* l_ready = bars + 21;   // running sum of the latest step stored
   uint64_t* o_free = bars + 22;    // the item's O has been read out
   uint64_t* drain = bars + 23;     // [2] one per issuing thread
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 26);
-  volatile int* abort = reinterpret_cast<volatile int*>(bars + 26) + 1;
+  uint64_t* ost_full = bars + 26;  // [2] a warpgroup's rows of O are staged
+  uint64_t* ost_free = bars + 28;  // [2] the previous store from a warpgroup's staging tile has read it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 30);
+  volatile int* abort = reinterpret_cast<volatile int*>(bars + 30) + 1;
   float* sm_m = reinterpret_cast<float*>(smem + C::kOffStat);
   float* sm_l = sm_m + kTile;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -589,6 +619,8 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
       mbar_init(p_ready + k, 4);
       mbar_init(pv_done + k, 1);
       mbar_init(drain + k, 1);
+      mbar_init(ost_full + k, 4);
+      mbar_init(ost_free + k, 1);
     }
     for (int k = 0; k < S; k++) {
       mbar_init(kv_full + k, 1);
@@ -700,9 +732,10 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
     const uint32_t sbuf = trow + C::kColS + wg * 128;
     const uint32_t pbuf = trow + C::kColP + wg * 64;
+    uint8_t* ost = smem + C::kOffOst + wg * C::kOstBytes;
     const float sl2 = a.scale_log2;
     bool ok = true;
-    int g = 0;
+    int g = 0, ne = 0;  // ne: this warpgroup's epilogues so far
     Fwd3Item it;
     for (int tl = 0; ok && fwd3_item(a, tl, it); tl++) {
       const int t = it.i * kTile + r;
@@ -712,13 +745,16 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
         ok = __all_sync(0xffffffffu, mbar_wait(s_full + wg, (g >> 1) & 1, abort));
         if (!ok) break;
         tc_fence_after();
-        // pass 1: row maximum over the 128 keys (masked past the diagonal)
+        // pass 1: row maximum over the 128 keys (masked past the diagonal); the
+        // scores of keys 64..127 stay in registers for pass 2
         float mx8[8];
 #pragma unroll
         for (int e = 0; e < 8; e++) mx8[e] = -INFINITY;
+        uint32_t hi[64];
 #pragma unroll
         for (int h2 = 0; h2 < 2; h2++) {
-          uint32_t u[64];
+          uint32_t lo[64];
+          uint32_t(&u)[64] = h2 ? hi : lo;
           tmem_ld32(sbuf + h2 * 64, *reinterpret_cast<uint32_t(*)[32]>(u));
           tmem_ld32(sbuf + h2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
           tmem_wait_ld();
@@ -776,8 +812,9 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
           if (!ok) break;
         }
         tc_fence_after();
-        // pass 2: P = exp2(s * scale_log2 - m) as bf16 into this warpgroup's P buffer;
-        // the next chunk's scores load while this one is exponentiated
+        // pass 2: P = exp2(s * scale_log2 - m) as bf16 into this warpgroup's P buffer.
+        // Keys 0..63 are read again, 16 at a time (the next chunk loads while this
+        // one is exponentiated); keys 64..127 come from pass 1's registers.
         // (the row sum adds the fp32 values of P; the MMA multiplies their bf16 roundings)
         uint64_t sum4[4] = {0ull, 0ull, 0ull, 0ull};
         const uint64_t sl2x2 = f2(sl2, sl2), negm = f2(-m_use, -m_use);
@@ -786,10 +823,10 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 8; c++) {
-          uint32_t(&cur)[16] = (c & 1) ? ub : ua;
+          uint32_t(&cur)[16] = c >= 4 ? *reinterpret_cast<uint32_t(*)[16]>(hi + 16 * (c - 4)) : ((c & 1) ? ub : ua);
           uint32_t(&nxt)[16] = (c & 1) ? ua : ub;
-          if (c < 7) tmem_ld16(sbuf + (c + 1) * 16, nxt);
-          if (diag) {
+          if (c < 3) tmem_ld16(sbuf + (c + 1) * 16, nxt);
+          if (diag && c < 4) {
 #pragma unroll
             for (int e = 0; e < 16; e++)
               if (16 * c + e > r) cur[e] = 0xff800000u;  // exp2(-inf) = 0
@@ -804,9 +841,9 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
             sum4[e & 3] = f2_add(sum4[e & 3], f2(p0, p1));
           }
           tmem_st8(pbuf + c * 8, pk);
-          if (c < 7) tmem_wait_ld();
-          if (c == 6) {
-            // the last chunk of scores is in registers: S of step g + 2 may overwrite them
+          if (c < 3) tmem_wait_ld();
+          if (c == 2) {
+            // every score is in registers: S of step g + 2 may overwrite them
             tc_fence_before();
             warp_arrive(s_read + wg);
           }
@@ -838,36 +875,52 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
         if (!ok) break;
         tc_fence_after();
         const float inv = 1.f / l;
-        const size_t orow = (((size_t)it.b * a.T + t) * a.Hq + it.h) * D;
+        float x[D];
 #pragma unroll
         for (int c = 0; c < D / 32; c++) {
           uint32_t w[32];
           tmem_ld32(trow + C::kColO + c * 32, w);
           tmem_wait_ld();
-          if (t < a.T) {
-            if (a.o_fp32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o) + orow + c * 32);
 #pragma unroll
-              for (int e = 0; e < 8; e++)
-                dst[e] = make_float4(__uint_as_float(w[4 * e]) * inv, __uint_as_float(w[4 * e + 1]) * inv,
-                                     __uint_as_float(w[4 * e + 2]) * inv, __uint_as_float(w[4 * e + 3]) * inv);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + orow + c * 32);
-#pragma unroll
-              for (int e = 0; e < 4; e++)
-                dst[e] = make_uint4(pack_bf16(__uint_as_float(w[8 * e]) * inv, __uint_as_float(w[8 * e + 1]) * inv),
-                                    pack_bf16(__uint_as_float(w[8 * e + 2]) * inv, __uint_as_float(w[8 * e + 3]) * inv),
-                                    pack_bf16(__uint_as_float(w[8 * e + 4]) * inv, __uint_as_float(w[8 * e + 5]) * inv),
-                                    pack_bf16(__uint_as_float(w[8 * e + 6]) * inv, __uint_as_float(w[8 * e + 7]) * inv));
-            }
+          for (int e = 0; e < 32; e++) x[c * 32 + e] = __uint_as_float(w[e]) * inv;
+        }
+        tc_fence_before();
+        warp_arrive(o_free);  // O is in registers: the next item's first PV may overwrite it
+        // O leaves through the warpgroup's staging tile and a TMA store (rows past T
+        // are not written); the tile is reused once the previous store has read it
+        if (ne > 0) {
+          if (r == 0) {
+            bulk_wait_read<0>();
+            mbar_arrive(ost_free + wg);
+          }
+          ok = __all_sync(0xffffffffu, mbar_wait(ost_free + wg, (ne - 1) & 1, abort));
+          if (!ok) break;
+        }
+        if (a.o_fp32) {
+          stage_rows<D, 4>(x, ost, r);
+        } else {
+          stage_rows<D, 2>(x, ost, r);
+        }
+        fence_proxy_async_smem();
+        warp_arrive(ost_full + wg);
+        if (r == 0) {
+          if (!(ok = mbar_wait(ost_full + wg, ne & 1, abort))) {
+            record_timeout(a.status, abort);
+          } else {
+            const int span = D * (a.o_fp32 ? 4 : 2) < 128 ? D * (a.o_fp32 ? 4 : 2) : 128;
+            const int cols = span / (a.o_fp32 ? 4 : 2);
+            for (int c0 = 0, bx = 0; c0 < D; c0 += cols, bx++)
+              tma_store_4d(&a.map_o, ost + bx * kTile * span, c0, it.h, it.i * kTile, it.b);
+            bulk_commit();
           }
         }
+        ne++;
+        if (!__all_sync(0xffffffffu, ok)) break;
         if (t < a.T)
           a.lse[((size_t)it.b * a.Hq + it.h) * a.T + t] = (__fmul_rn(r_use, sl2) + __log2f(l)) * 0.69314718055994531f;
-        tc_fence_before();
-        warp_arrive(o_free);  // the next item's first PV may overwrite O
       }
     }
+    if (r == 0) bulk_wait<0>();  // the O stores are done with the staging tiles
     if (!ok) record_timeout(a.status, abort);
   }
 

@@ -28,6 +28,7 @@ struct FwdArgs {
   // map_q / map_k cover the rotated fp16 copies made by the RoPE pre-pass;
   // precise logits: the bf16 inputs (the kernel rotates them itself).
   CUtensorMap map_q, map_k, map_v;
+  CUtensorMap map_o;                // store map over o (default precision): 128-byte (or 64-byte) column boxes x 128 rows
   void* o;                          // [B, T, Hq, D] bf16 or fp32
   float* lse;                       // [B, Hq, T]
   float* lse_lo;                    // [B, Hq, T] fp32 remainder of lse (precise logits only)

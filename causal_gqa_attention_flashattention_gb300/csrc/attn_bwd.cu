@@ -705,7 +705,8 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
 // memory (double-buffered across items, so the next item's K and V load
 // while this one runs); P^T gets TMEM columns of its own, so S^T of the next
 // step may overwrite the score columns as soon as the compute warps have read
-// them.  The accumulators pass from one item to the next through acc_done
+// them, and dS^T replaces P^T there once dV has read it, so dP^T of the next
+// step may overwrite its columns as soon as they are read.  The accumulators pass from one item to the next through acc_done
 // (MMAs complete) and acc_free (the compute warps have read them).
 // Warps: 0 TMA producer; 1-3 MMA issuers; 4-11 P and dS (two warpgroups, half
 // the query columns each), then each item's dK / dV store; 12-15 dQ drain.
@@ -730,7 +731,7 @@ struct Bwd3Cfg {
   static constexpr int kNumBars = 32;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-  // TMEM: S^T | dP^T (dS^T over it) | P^T | dV | dK | dQ
+  // TMEM: S^T | dP^T | P^T (dS^T over it) | dV | dK | dQ
   static constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDV = 320, kColDK = 320 + D,
                             kColDQ = 320 + 2 * D;
   static constexpr uint32_t kTmemCols = 512;
@@ -826,6 +827,8 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
   uint64_t* drain = bars + 21;     // [3]
   uint64_t* stg_full = bars + 24;  // [2] per compute warpgroup: its rows of a gradient box are staged
   uint64_t* stg_free = bars + 26;  // [2] the TMA store has read the box
+  uint64_t* dp_read = bars + 28;   // the compute warps hold dP^T(g): dP^T(g+1) may overwrite it
+  uint64_t* dk_done = bars + 29;   // dK(g) read dS^T(g) from the P^T columns
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -857,6 +860,8 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
       mbar_init(stg_full + s, 4);
       mbar_init(stg_free + s, 1);
     }
+    mbar_init(dp_read, 8);
+    mbar_init(dk_done, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
@@ -917,9 +922,9 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
     // ------------------------------------------------------------ MMA issuers
     // One thread issues about one MMA per 70-120 cycles, so each step's 32
     // MMAs are spread over three threads.  Every overwrite of a TMEM operand
-    // follows the read in the program order of one thread or behind a barrier:
-    //   warp 1: S^T(g+1) once the compute warps read S^T(g), then dV += P^T dO;
-    //   warp 2: dK += dS^T Q, then dP^T(g+1) over the dS^T columns;
+    // follows its last read behind a barrier:
+    //   warp 1: S^T(g+1) once the compute warps read S^T(g), and dV += P^T dO;
+    //   warp 2: dP^T(g+1) once the compute warps read dP^T(g), then dK += dS^T Q;
     //   warp 3: the dQ tile = dS K (dS from shared memory).
     if (lane == 0) {
       constexpr uint32_t idS = idesc_fp16(128, 128, false, false);   // K^ x Q^ (both K-major)
@@ -1011,23 +1016,27 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
           for (int n = 0; n < it.N; n++, g++) {
             const int st = g % C::kStages;
             const bool last = (n + 1 == it.N);
-            if (!(ok = mbar_wait(ds_ready, g & 1, abort))) break;
-            if (n == 0 && tl > 0 && !(ok = mbar_wait(acc_free, (tl - 1) & 1, abort))) break;
-            tc_fence_after();
-            // dK += dS^T Q^ (dS^T over the dP^T columns: queries 0..63 at +0, 64..127 at +64)
-            mma_ts_chain<8, true>(tmem + C::kColDK, tmem + C::kColDP, dQs(st), kStepMN, idDK, n > 0 ? 1u : 0u);
-            mma_commit(qd_empty + st);  // this thread's reads of stage st: dO by dP^T, Q^ by dK
-            if (last) {
-              mma_commit(acc_done);
-              mma_commit(kv_empty + kb);  // V by dP^T
-            }
+            // dP^T(g+1) as soon as the compute warps hold dP^T(g) (dS^T(g) goes to
+            // the P^T columns, so dK(g) does not have to run first)
             if (!last || bwd_item(a, tl + 1, nx)) {
               const int g1 = g + 1, st1 = g1 % C::kStages, kb1 = last ? (kb ^ 1) : kb;
+              if (!(ok = mbar_wait(dp_read, g & 1, abort))) break;
               if (last && !(ok = mbar_wait(kv_full + kb1, ((tl + 1) >> 1) & 1, abort))) break;
               if (!(ok = mbar_wait(qd_full + st1, (g1 / C::kStages) & 1, abort))) break;
               tc_fence_after();
               mma_ss_chain<KD>(tmem + C::kColDP, dV(kb1), kStepK, dDOs(st1), kStepK, idDP, 0);
               mma_commit(dp_full);
+            }
+            if (!(ok = mbar_wait(ds_ready, g & 1, abort))) break;
+            if (n == 0 && tl > 0 && !(ok = mbar_wait(acc_free, (tl - 1) & 1, abort))) break;
+            tc_fence_after();
+            // dK += dS^T Q^ (dS^T in the P^T columns, fp16 pairs)
+            mma_ts_chain<8, false>(tmem + C::kColDK, tmem + C::kColP, dQs(st), kStepMN, idDK, n > 0 ? 1u : 0u);
+            mma_commit(dk_done);
+            mma_commit(qd_empty + st);  // this thread's reads of stage st: dO by dP^T, Q^ by dK
+            if (last) {
+              mma_commit(acc_done);
+              mma_commit(kv_empty + kb);  // V by dP^T
             }
           }
         }
@@ -1104,8 +1113,8 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
         uint32_t pk[32];
 #pragma unroll
         for (int q = 0; q < 32; q++) pk[q] = pack_bf16(pf[2 * q], pf[2 * q + 1]);
-        // the P^T columns are free once the previous step's dV has read them
-        if (g > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(pbuf_free, (g - 1) & 1, abort)))) break;
+        // the P^T columns are free once dK(g-1) has read dS^T(g-1) from them
+        if (g > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(dk_done, (g - 1) & 1, abort)))) break;
         tc_fence_after();
 #pragma unroll
         for (int hlf = 0; hlf < 4; hlf++)
@@ -1119,7 +1128,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
         tc_fence_after();
         // dS = P * (dP - Delta), 16 columns at a time; the next chunk of dP^T loads
         // while this one is computed (its columns are never the ones being stored)
-        uint32_t va[16], vb[16];
+        uint32_t va[16], vb[16], dst[32];
         tmem_ld16(trow + C::kColDP + cbase, va);
         tmem_wait_ld();
 #pragma unroll
@@ -1142,14 +1151,25 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
               w[q >> 1] = pack_f16(d0, d1);
             }
           }
-          // dS^T into TMEM over the dP^T columns already read (for dK), dS into shared memory (for dQ)
-          tmem_st8(trow + C::kColDP + cbase + c4 * 8, w);
+          // dS into shared memory (for dQ); dS^T kept for the P^T columns (for dK)
+#pragma unroll
+          for (int q = 0; q < 8; q++) dst[c4 * 8 + q] = w[q];
 #pragma unroll
           for (int q = 0; q < 2; q++)
             *reinterpret_cast<uint4*>(atom + r * 128 + (((uint32_t)(2 * c4 + q) ^ x7) << 4)) =
                 make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
           if (c4 < 3) tmem_wait_ld();
+          if (c4 == 2) {
+            tc_fence_before();
+            warp_arrive(dp_read);  // dP^T(g+1) may overwrite the dP^T columns
+          }
         }
+        // dS^T over P^T once dV(g) has read P^T
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(pbuf_free, g & 1, abort)))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < 4; q++)
+          tmem_st8(trow + C::kColP + wg * 32 + q * 8, *reinterpret_cast<const uint32_t(*)[8]>(dst + 8 * q));
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();

@@ -357,14 +357,14 @@ def run_ours(args, world, rank, local):
     else:
         work = None
         roof = dict(bound="hbm", achieved=None, peak=peaks["hbm_gbs"], unit="GB/s", frac=None)
-    kernel_names = dict(fwd="k_attn_fwd2", fwd_rope="k_rope_qk", bwd_prep="k_bwd_prep", bwd_dkdv="k_bwd_dkdv3",
+    kernel_names = dict(fwd="k_attn_fwd3", fwd_rope="k_rope_qk", bwd_prep="k_bwd_prep", bwd_dkdv="k_bwd_dkdv3",
                         bwd_dq="k_bwd_dq")
     tr = traffic_record(kernel_names.get(dom, dom))
     roof.update(kernel=dom, traffic=(tr["dram_bytes_per_launch"] if tr else None),
                 peak_source="%s bf16 burst" % peaks["source"] if roof["bound"] == "tensor" else
                 "%s hbm" % peaks["source"], per_launch_us=per_launch_ms * 1e3,
-                kernels={k: dict(us_per_launch=(v[0] / v[1] * 1e3 if v[1] else None), launches=v[1])
-                         for k, v in prof.items()})
+                kernels={k: dict(us_per_launch=v[0] / v[1] * 1e3, launches=v[1])
+                         for k, v in prof.items() if v[1]})
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_sample(args.cpu_seconds, shape, x)
@@ -393,6 +393,99 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+# Decode with a KV cache (one new token per sequence): B, Tkv, Tq, Hq, Hkv, D.
+DECODE_WORKLOADS = {
+    "decode_116m_ctx512": (16, 512, 1, 12, 4, 64),    # the 116M model at its full context
+    "decode_116m_ctx8192": (16, 8192, 1, 12, 4, 64),  # the same heads over an 8192-position cache
+}
+
+
+def run_decode(args):
+    """One JSON line per decode workload: KV-cache bytes read per second.
+
+    The caches (rotated fp16 keys, bf16 values) are filled through the public
+    append call from seeded N(0,1) data; enough cache sets rotate through the
+    timed graph that their total exceeds L2 twice over.  The timed region
+    replays a CUDA graph of decode calls (query packing, split sweep, combine).
+    """
+    import torch
+    from causal_gqa_attention_flashattention_gb300 import binding
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(dev)
+    for name, (B, Tkv, Tq, Hq, Hkv, D) in DECODE_WORKLOADS.items():
+        cache_bytes = B * Tkv * Hkv * D * (2 + 2)
+        nsets = max(2, min(64, -(-2 * 129 * 2 ** 20 // cache_bytes)))
+        g = torch.Generator(device=dev).manual_seed(5)
+        sets = []
+        for _ in range(nsets):
+            kc, vc = binding.kv_cache(B, Tkv, Hkv, D, dev)
+            k = torch.randn((B, Tkv, Hkv, D), device=dev, generator=g).bfloat16()
+            v = torch.randn((B, Tkv, Hkv, D), device=dev, generator=g).bfloat16()
+            binding.kv_append(k, v, kc, vc, 0)
+            q = torch.randn((B, Tq, Hq, D), device=dev, generator=g).bfloat16()
+            sets.append(dict(q=q, kc=kc, vc=vc, o=torch.empty_like(q),
+                             lse=torch.empty((B, Hq, Tq), dtype=torch.float32, device=dev)))
+        ws = torch.empty(binding.decode_workspace_size(B, Tq, Tkv, Hq, Hkv, D), dtype=torch.uint8, device=dev)
+
+        def call(s):
+            binding.attn_decode(s["q"], s["kc"], s["vc"], Tkv, o=s["o"], lse=s["lse"], workspace=ws, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                for s in sets:
+                    call(s)
+        binding.check_status(stream)
+        binding.profile_start(3 * nsets + 4)
+        g_prof = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_prof, stream=stream):
+            for s in sets:
+                call(s)
+        prof_cap = binding.profile_stop_deferred()
+        g_all = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_all, stream=stream):
+            for s in sets:
+                call(s)
+        reps = max(1, args.steps // nsets)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):  # graphs replay on the current stream, events time that stream
+            g_all.replay()
+            torch.cuda.synchronize(dev)
+            clocks = ClockSampler(0)
+            clocks.start()
+            e0.record(stream)
+            for _ in range(reps):
+                g_all.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            clk = clocks.stop()
+            binding.check_status(stream)
+            for _ in range(3):
+                g_prof.replay()
+        torch.cuda.synchronize(dev)
+        prof = binding.profile_read(prof_cap)
+        ms_call = e0.elapsed_time(e1) / (reps * nsets)
+        ms_sweep = prof["decode"][0] / max(1, prof["decode"][1])
+        achieved = cache_bytes / (ms_sweep * 1e-3) / 1e9
+        line = dict(metric="decode: KV-cache bytes read per second (one decode step, all sequences)",
+                    value=cache_bytes / (ms_call * 1e-3) / 1e9, unit="GB/s", n_gpus=1, steps=reps * nsets,
+                    warmup=args.warmup, ms_per_step=ms_call, higher_is_better=True, scaling="weak",
+                    vs_baseline=None, dtype="fp16 keys, bf16 values, fp32 accumulate", data="synthetic",
+                    config=dict(workload=name, B=B, Tkv=Tkv, Tq=Tq, Hq=Hq, Hkv=Hkv, D=D, cache_sets=nsets,
+                                l2="%d rotating cache sets of %.1f MB" % (nsets, cache_bytes / 1e6),
+                                launch="CUDA graph replay (3 library kernels per decode call)"),
+                    tokens_per_s=B * Tq / (ms_call * 1e-3),
+                    roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
+                                  frac=achieved / peaks["hbm_gbs"], kernel="decode", traffic=None,
+                                  peak_source="%s hbm" % peaks["source"], per_launch_us=ms_sweep * 1e3,
+                                  kernels={k: dict(us_per_launch=v[0] / v[1] * 1e3, launches=v[1])
+                                           for k, v in prof.items() if v[1]}),
+                    clocks=clk)
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -401,9 +494,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode", action="store_true",
+                    help="measure decode with a KV cache (one JSON line per decode workload) instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.decode:
+        return run_decode(args)
     world, rank, local = dist_init()
     if args.impl == "reference":
         return run_reference(args, world, rank)

@@ -60,6 +60,12 @@ def lib():
         L.ne_attn_profile_detach.restype = i
         L.ne_attn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]
         L.ne_attn_profile_read.restype = i
+        L.ne_attn_kv_append.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+        L.ne_attn_kv_append.restype = i
+        L.ne_attn_decode_workspace_size.argtypes = [i, i, i, i, i, i]
+        L.ne_attn_decode_workspace_size.restype = sz
+        L.ne_attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, sz, vp]
+        L.ne_attn_decode.restype = i
         _lib = L
     return _lib
 
@@ -176,7 +182,7 @@ def status_of_last_kernels(stream=None):
     return int(lib().ne_attn_check_status(_stream(stream)))
 
 
-KERNEL_KINDS = ("fwd", "bwd_prep", "bwd_dkdv", "bwd_dq", "fwd_rope")
+KERNEL_KINDS = ("fwd", "bwd_prep", "bwd_dkdv", "bwd_dq", "fwd_rope", "kv_append", "decode", "decode_aux")
 
 
 def profile_start(capacity):
@@ -229,3 +235,50 @@ def fwd_bwd_host(q, k, v, dout, rope_base=10000.0, grad_dtype=torch.bfloat16, o_
                               qk_rotated=not precise, stream=s)
         out = [t.to("cpu", non_blocking=False) for t in (o, lse, dq, dk, dv)]
     return tuple(out)
+
+
+def kv_cache(B, Tcap, Hkv, D, device):
+    """Empty key (fp16, rotated) and value (bf16) caches [B, Tcap, Hkv, D]."""
+    return (torch.zeros((B, Tcap, Hkv, D), dtype=torch.float16, device=device),
+            torch.zeros((B, Tcap, Hkv, D), dtype=torch.bfloat16, device=device))
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, pos0, rope_base=10000.0, stream=None):
+    """Writes positions pos0 .. pos0 + Tn - 1 of the caches from k_new, v_new [B,Tn,Hkv,D] (bf16)."""
+    B, Tn, Hkv, D = k_new.shape
+    Tcap = k_cache.shape[1]
+    for t in (k_new, v_new):
+        assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous()
+    assert k_cache.dtype == torch.float16 and v_cache.dtype == torch.bfloat16
+    assert k_cache.is_contiguous() and v_cache.is_contiguous() and k_cache.shape == v_cache.shape
+    _check("ne_attn_kv_append", lib().ne_attn_kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                                        B, Tn, pos0, Tcap, Hkv, D, float(rope_base),
+                                                        _stream(stream)))
+
+
+def decode_workspace_size(B, Tq, Tkv, Hq, Hkv, D):
+    return int(lib().ne_attn_decode_workspace_size(B, Tq, Tkv, Hq, Hkv, D))
+
+
+def attn_decode(q, k_cache, v_cache, Tkv, rope_base=10000.0, o=None, lse=None, o_dtype=torch.bfloat16,
+                workspace=None, stream=None):
+    """o, lse for the Tq new queries q [B,Tq,Hq,D] (bf16, positions Tkv-Tq .. Tkv-1)
+    against cache positions 0 .. Tkv-1 (see ne_attn_decode)."""
+    B, Tq, Hq, D = q.shape
+    Tcap, Hkv = k_cache.shape[1], k_cache.shape[2]
+    assert q.dtype == torch.bfloat16 and q.is_cuda and q.is_contiguous()
+    assert k_cache.dtype == torch.float16 and v_cache.dtype == torch.bfloat16
+    if o is None:
+        o = torch.empty(q.shape, dtype=o_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
+    assert o.dtype in (torch.bfloat16, torch.float32) and o.is_contiguous()
+    assert lse.dtype == torch.float32 and lse.is_contiguous() and lse.numel() == B * Hq * Tq
+    if workspace is None:
+        workspace = torch.empty(max(decode_workspace_size(B, Tq, Tkv, Hq, Hkv, D), 1), dtype=torch.uint8,
+                                device=q.device)
+    flags = O_FP32 if o.dtype == torch.float32 else 0
+    _check("ne_attn_decode", lib().ne_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse),
+                                                  B, Tq, Tkv, Tcap, Hq, Hkv, D, float(rope_base), flags,
+                                                  _ptr(workspace), workspace.numel(), _stream(stream)))
+    return o, lse

@@ -207,6 +207,19 @@ int make_map_bthd(CUtensorMap* m, const void* ptr, int B, int T, int H, int D,
   return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
 }
 
+// 4-D map over a key/value cache [B, Tcap, H, D] of which positions 0..Tkv-1 are
+// valid: rows at or past Tkv read as zeros.  Box = one head, 128 rows, all D.
+int make_map_cache(CUtensorMap* m, const void* ptr, int B, int Tkv, int Tcap, int H, int D, CUtensorMapDataType dt) {
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)Tkv, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)Tcap * H * D * 2};
+  cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)kTile, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, dt, 4, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        D == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
+}
+
 // 4-D store map over a gradient [B, T, H, D] (fp32 or bf16); box = 128 bytes of
 // columns (64 bytes when a row is that short) x 1 head x 128 rows x 1, with the
 // swizzle of that span.
@@ -263,6 +276,29 @@ size_t ws_up(size_t x) { return (x + 255) / 256 * 256; }
 size_t fwd_ws_bytes(int B, int T, int Hq, int Hkv, int D) {
   return ws_up(2 * (size_t)B * T * Hq * D) + ws_up(2 * (size_t)B * T * Hkv * D);
 }
+
+// Decode workspace: packed rotated queries, then the splits' partial O and (max, sum).
+struct DecodeWs {
+  size_t qpk, part_o, part_ml, total;
+};
+DecodeWs decode_ws(int B, int Tq, int Tkv, int Hq, int Hkv, int D) {
+  const size_t R = (size_t)(Hq / Hkv) * Tq, ntk = ((size_t)Tkv + kTile - 1) / kTile;
+  DecodeWs w;
+  w.qpk = 0;
+  w.part_o = ws_up((size_t)B * Hkv * kTile * D * 2);
+  w.part_ml = w.part_o + ws_up((size_t)B * Hkv * ntk * R * D * 4);
+  w.total = w.part_ml + ws_up((size_t)B * Hkv * ntk * R * 8);
+  return w;
+}
+
+int check_decode_shape(int B, int Tq, int Tkv, int Tcap, int Hq, int Hkv, int D) {
+  if (Tq < 1 || Tkv < Tq || Tcap < Tkv) return NE_ERR_ARG;
+  int st = check_shape(B, Tcap, Hq, Hkv, D);
+  if (st != NE_OK) return st;
+  if ((Hq / Hkv) * Tq > kTile) return NE_ERR_UNSUPPORTED;
+  return NE_OK;
+}
+
 
 WsLayout ws_layout(int B, int T, int Hq, int Hkv, int D, bool precise) {
   auto up = ws_up;
@@ -672,6 +708,115 @@ int ne_attn_profile_read(double* total_ms, long long* launches) {
     if (launches) launches[k] = cnt[k];
   }
   return st;
+}
+
+int ne_attn_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int B, int Tn,
+                      int pos0, int Tcap, int Hkv, int D, float rope_base, void* stream) {
+  if (!k_new || !v_new || !k_cache || !v_cache) return NE_ERR_ARG;
+  if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
+  if (Tn < 1 || pos0 < 0 || (long long)pos0 + Tn > (long long)Tcap) return NE_ERR_ARG;
+  int st = check_shape(B, Tcap, Hkv, Hkv, D);
+  if (st != NE_OK) return st;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache)) return NE_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev;
+  if ((st = current_device(&dev)) != NE_OK) return st;
+  DeviceState* d;
+  if ((st = device_state(dev, &d)) != NE_OK) return st;
+  KvAppendArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if ((st = rope_table(*d, D, (double)rope_base, pos0 + Tn, s, &a.rope)) != NE_OK) return st;
+  a.k = static_cast<const __nv_bfloat16*>(k_new);
+  a.v = static_cast<const __nv_bfloat16*>(v_new);
+  a.kc = static_cast<__half*>(k_cache);
+  a.vc = static_cast<__nv_bfloat16*>(v_cache);
+  a.B = B;
+  a.Tn = Tn;
+  a.Hkv = Hkv;
+  a.Tcap = Tcap;
+  a.pos0 = pos0;
+  a.div_hkv = make_fastdiv((uint32_t)Hkv);
+  a.div_tn = make_fastdiv((uint32_t)Tn);
+  ProfScope prof(NE_ATTN_KERNEL_KV_APPEND, s);
+  return launch_kv_append(a, D, s) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+size_t ne_attn_decode_workspace_size(int B, int Tq, int Tkv, int Hq, int Hkv, int D) {
+  if (check_decode_shape(B, Tq, Tkv, Tkv, Hq, Hkv, D) != NE_OK) return 0;
+  return decode_ws(B, Tq, Tkv, Hq, Hkv, D).total;
+}
+
+int ne_attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B, int Tq,
+                   int Tkv, int Tcap, int Hq, int Hkv, int D, float rope_base, int flags, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !o || !lse) return NE_ERR_ARG;
+  if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
+  if ((flags & ~kFlagOFp32) != 0) return NE_ERR_ARG;
+  int st = check_decode_shape(B, Tq, Tkv, Tcap, Hq, Hkv, D);
+  if (st != NE_OK) return st;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse))
+    return NE_ERR_ALIGN;
+  const DecodeWs w = decode_ws(B, Tq, Tkv, Hq, Hkv, D);
+  if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return NE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev, nsm = 0;
+  if ((st = current_device(&dev)) != NE_OK) return st;
+  DeviceState* d;
+  if ((st = device_state(dev, &d)) != NE_OK) return st;
+  if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm < 1) return NE_ERR_CUDA;
+  DecodeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if ((st = rope_table(*d, D, (double)rope_base, Tkv, s, &a.rope)) != NE_OK) return st;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.qpk = reinterpret_cast<__half*>(ws + w.qpk);
+  a.part_o = reinterpret_cast<float*>(ws + w.part_o);
+  a.part_ml = reinterpret_cast<float*>(ws + w.part_ml);
+  a.o = o;
+  a.lse = lse;
+  a.status = d->status;
+  a.B = B;
+  a.Tq = Tq;
+  a.Tkv = Tkv;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.G = Hq / Hkv;
+  a.R = a.G * Tq;
+  a.ntk = (Tkv + kTile - 1) / kTile;
+  a.o_fp32 = (flags & kFlagOFp32) ? 1 : 0;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  // Splits of each (batch, key/value head)'s key tiles: the count whose slowest
+  // CTA (work items per CTA x tiles per item, plus about one tile of fixed cost
+  // per item) is shortest.
+  const long long bh = (long long)B * Hkv;
+  long long best = -1;
+  for (int ns = 1; ns <= a.ntk && ns <= 64; ns++) {
+    const long long cost = ((bh * ns + nsm - 1) / nsm) * ((a.ntk + ns - 1) / ns + 1);
+    if (best < 0 || cost < best) {
+      best = cost;
+      a.nsplit = ns;
+    }
+  }
+  if ((st = make_map_bthd(&a.map_q, a.qpk, 1, (int)(bh * kTile), 1, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != NE_OK)
+    return st;
+  if ((st = make_map_cache(&a.map_k, k_cache, B, Tkv, Tcap, Hkv, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != NE_OK)
+    return st;
+  if ((st = make_map_cache(&a.map_v, v_cache, B, Tkv, Tcap, Hkv, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)) != NE_OK)
+    return st;
+  {
+    ProfScope prof(NE_ATTN_KERNEL_DECODE_AUX, s);
+    if (launch_decode_q(a, s) != cudaSuccess) return NE_ERR_CUDA;
+  }
+  {
+    ProfScope prof(NE_ATTN_KERNEL_DECODE, s);
+    if (launch_decode(a, nsm, s) != cudaSuccess) return NE_ERR_CUDA;
+  }
+  ProfScope prof(NE_ATTN_KERNEL_DECODE_AUX, s);
+  return launch_decode_combine(a, s) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
 }
 
 int ne_attn_debug_timeout_probe(int limit_us, void* stream) {

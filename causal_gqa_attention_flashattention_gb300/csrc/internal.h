@@ -108,7 +108,37 @@ struct DqArgs {
   FastDiv div_hq, div_t;
 };
 
+// Key/value cache append: rotated keys (fp16) and values (bf16) of Tn new positions.
+struct KvAppendArgs {
+  const __nv_bfloat16 *k, *v;  // [B, Tn, Hkv, D]
+  __half* kc;                  // [B, Tcap, Hkv, D] rotated keys
+  __nv_bfloat16* vc;           // [B, Tcap, Hkv, D]
+  const float2* rope;
+  int B, Tn, Hkv, Tcap, pos0;
+  FastDiv div_hkv, div_tn;
+};
+
+// Decode over a key/value cache (see attn_decode.cu).
+struct DecodeArgs {
+  CUtensorMap map_q;         // packed rotated queries [B*Hkv*128, D] fp16 (4-D map, box D x 1 x 128 x 1)
+  CUtensorMap map_k, map_v;  // caches [B, Tkv valid of Tcap, Hkv, D] (fp16 keys, bf16 values)
+  const __nv_bfloat16* q;    // [B, Tq, Hq, D]
+  __half* qpk;               // [B, Hkv, 128, D] packed rotated queries (workspace)
+  float* part_o;             // [B, Hkv, nsplit, R, D] unnormalised O per split (workspace)
+  float* part_ml;            // [B, Hkv, nsplit, R] (max in log2 units, sum) pairs (workspace)
+  void* o;                   // [B, Tq, Hq, D] bf16 or fp32
+  float* lse;                // [B, Hq, Tq]
+  const float2* rope;
+  int* status;
+  int B, Tq, Tkv, Hq, Hkv, D, G, R, ntk, nsplit, o_fp32;
+  float scale_log2;
+};
+
 cudaError_t launch_fwd(const FwdArgs& a, bool precise, cudaStream_t s);
+cudaError_t launch_kv_append(const KvAppendArgs& a, int D, cudaStream_t s);
+cudaError_t launch_decode_q(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, int nsm, cudaStream_t s);
+cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_rope_qk(const RopeArgs& a, int D, cudaStream_t s);
 cudaError_t launch_bwd_prep(const PrepArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, bool precise, cudaStream_t s);

@@ -172,6 +172,51 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
                         int D, float rope_base, int flags, void* stream);
 
 /*
+ * Incremental decoding with a key/value cache.  The NanoEuler engine generates
+ * one token at a time with a KV cache (mynewscn README, generation with the
+ * KV cache; socker-news README, GPU generation mode `i`).  A decode step is
+ * the forward pass restricted to its newest positions: with Tkv positions in
+ * the cache, the Tq new queries sit at positions Tkv - Tq .. Tkv - 1 and
+ * o[b,t,h], lse[b,h,t] equal rows Tkv - Tq + t of ne_attn_fwd over T = Tkv.
+ *
+ * Caches (row-major, capacity Tcap positions, the caller owns them):
+ *   k_cache : [B, Tcap, Hkv, D] fp16, the rotated keys k^_j = R_j k_j
+ *   v_cache : [B, Tcap, Hkv, D] bfloat16
+ *
+ * ne_attn_kv_append writes positions pos0 .. pos0 + Tn - 1 of both caches from
+ * the new keys and values k_new, v_new [B, Tn, Hkv, D] (bfloat16): each key is
+ * rotated at its position and stored as fp16, each value copied.  Requires
+ * Tn >= 1, pos0 >= 0, pos0 + Tn <= Tcap.  One streaming kernel.
+ */
+int ne_attn_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int B, int Tn,
+                      int pos0, int Tcap, int Hkv, int D, float rope_base, void* stream);
+
+/*
+ * Bytes of device workspace ne_attn_decode needs (pass a 256-byte aligned
+ * pointer): the rotated queries packed per key/value head ([B, Hkv, 128, D]
+ * fp16) and the partial results of up to ceil(Tkv / 128) splits of the cache
+ * per key/value head.  Returns 0 for unsupported shapes.
+ */
+size_t ne_attn_decode_workspace_size(int B, int Tq, int Tkv, int Hq, int Hkv, int D);
+
+/*
+ * Decode attention: q [B, Tq, Hq, D] (bfloat16, not rotated; rotated here at
+ * positions Tkv - Tq + t) against cache positions 0 .. Tkv - 1.  Writes
+ * o [B, Tq, Hq, D] (bfloat16, or float32 with NE_ATTN_O_FP32, the only flag)
+ * and lse [B, Hq, Tq].  Requires 1 <= Tq <= Tkv <= Tcap and
+ * (Hq / Hkv) * Tq <= 128: the queries of one key/value head fill at most one
+ * 128-row tile, which every K/V tile of the cache serves at once.  The
+ * workspace is required.
+ * Three kernels: query rotation and packing; a sweep over the cache in which
+ * one CTA per SM takes work items (batch, key/value head, split of the key
+ * tiles) and runs S = Q K^T and O += P V on the tensor cores with an online
+ * softmax; and a combine of the splits.  The result is bitwise reproducible.
+ */
+int ne_attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B, int Tq,
+                   int Tkv, int Tcap, int Hq, int Hkv, int D, float rope_base, int flags, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: NE_OK, NE_ERR_DEVICE_TIMEOUT, or NE_ERR_CUDA if the
  * synchronisation itself failed.
@@ -204,7 +249,10 @@ const char* ne_attn_status_string(int status);
 #define NE_ATTN_KERNEL_BWD_DKDV 2
 #define NE_ATTN_KERNEL_BWD_DQ 3
 #define NE_ATTN_KERNEL_FWD_ROPE 4 /* the forward's RoPE pre-pass */
-#define NE_ATTN_NUM_KERNEL_KINDS 5
+#define NE_ATTN_KERNEL_KV_APPEND 5
+#define NE_ATTN_KERNEL_DECODE 6     /* the split sweep over the cache */
+#define NE_ATTN_KERNEL_DECODE_AUX 7 /* query packing and the combine of the splits */
+#define NE_ATTN_NUM_KERNEL_KINDS 8
 int ne_attn_profile_start(int capacity);
 int ne_attn_profile_stop(double* total_ms, long long* launches);
 int ne_attn_profile_detach(void);

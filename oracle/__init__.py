@@ -121,6 +121,25 @@ def attn_fwd(q, k, v, base=10000.0, groups=None, nthreads=0):
     return o, lse
 
 
+def decode_fwd(q_new, k, v, base=10000.0, groups=None, nthreads=0):
+    """Decode step with a key/value cache (the engine's incremental generation
+    with a KV cache: mynewscn README; socker-news README, GPU generation mode).
+
+    The Tq queries q_new [B,Tq,Hq,D] sit at positions T-Tq .. T-1 of
+    k/v [B,T,Hkv,D] and attend causally; the result is rows T-Tq .. T-1 of the
+    forward over T positions.  Earlier query rows cannot reach those rows, so
+    they are zero here.  Returns (o [B,Tq,Hq,D], lse [B,Hq,Tq]).
+    """
+    q_new = _f64(q_new)
+    B, Tq, Hq, D = q_new.shape
+    T = k.shape[1]
+    assert 1 <= Tq <= T
+    q = np.zeros((B, T, Hq, D))
+    q[:, T - Tq:] = q_new
+    o, lse = attn_fwd(q, k, v, base, groups, nthreads)
+    return o[:, T - Tq:].copy(), lse[:, :, T - Tq:].copy()
+
+
 def attn_bwd(q, k, v, dout, base=10000.0, groups=None, nthreads=0):
     """Causal GQA attention backward from the definition.
 

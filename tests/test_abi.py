@@ -79,3 +79,43 @@ def test_host_argument_checks(libne):
     assert libne.ne_attn_debug_timeout_probe(0, null) == -1
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert libne.ne_attn_status_string(code)
+
+
+def test_decode_workspace_size(libne):
+    B, Tq, Tkv, Hq, Hkv, D = 2, 3, 1000, 12, 4, 64
+    n = libne.ne_attn_decode_workspace_size(B, Tq, Tkv, Hq, Hkv, D)
+    R, ntk = (Hq // Hkv) * Tq, (Tkv + 127) // 128
+    # packed queries [B,Hkv,128,D] fp16 + per split: O (fp32 R x D) and (max, sum)
+    assert n >= B * Hkv * 128 * D * 2 + B * Hkv * ntk * R * (D * 4 + 8)
+    assert n % 256 == 0
+    assert libne.ne_attn_decode_workspace_size(1, 129, 129, 1, 1, 64) == 0  # 129 query rows > one tile
+    assert libne.ne_attn_decode_workspace_size(1, 3, 2, 4, 2, 64) == 0      # Tq > Tkv
+    assert libne.ne_attn_decode_workspace_size(1, 1, 10, 3, 2, 64) == 0     # Hq % Hkv
+    assert libne.ne_attn_decode_workspace_size(1, 1, 10, 4, 2, 48) == 0     # D
+
+
+def test_decode_host_argument_checks(libne):
+    buf = ctypes.create_string_buffer(4096 + 512)
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    p = ctypes.c_void_p(base)
+    mis = ctypes.c_void_p(base + 2)
+    null = None
+    # ne_attn_kv_append(k_new, v_new, k_cache, v_cache, B, Tn, pos0, Tcap, Hkv, D, base, stream)
+    assert libne.ne_attn_kv_append(null, p, p, p, 1, 4, 0, 8, 2, 64, 10000.0, null) == -1
+    assert libne.ne_attn_kv_append(p, p, p, p, 1, 4, 5, 8, 2, 64, 10000.0, null) == -1   # past the capacity
+    assert libne.ne_attn_kv_append(p, p, p, p, 1, 0, 0, 8, 2, 64, 10000.0, null) == -1   # nothing to append
+    assert libne.ne_attn_kv_append(p, p, p, p, 1, 4, -1, 8, 2, 64, 10000.0, null) == -1
+    assert libne.ne_attn_kv_append(p, p, mis, p, 1, 4, 0, 8, 2, 64, 10000.0, null) == -2
+    assert libne.ne_attn_kv_append(p, p, p, p, 1, 4, 0, 8, 2, 48, 10000.0, null) == -3
+    # ne_attn_decode(q, kc, vc, o, lse, B, Tq, Tkv, Tcap, Hq, Hkv, D, base, flags, ws, ws_bytes, stream)
+    ok = (1, 1, 10, 16, 4, 2, 64, 10000.0)
+    assert libne.ne_attn_decode(p, p, p, p, p, *ok, 0, p, 4096, null) == -5  # workspace too small
+    assert libne.ne_attn_decode(p, p, p, p, p, *ok, 0, null, 1 << 20, null) == -5  # workspace required
+    assert libne.ne_attn_decode(p, p, p, p, p, *ok, 0, mis, 1 << 20, null) == -5  # misaligned workspace
+    assert libne.ne_attn_decode(p, p, p, p, p, *ok, 2, p, 1 << 20, null) == -1  # gradient flag
+    assert libne.ne_attn_decode(null, p, p, p, p, *ok, 0, p, 1 << 20, null) == -1
+    assert libne.ne_attn_decode(p, p, p, p, p, 1, 11, 10, 16, 4, 2, 64, 10000.0, 0, p, 1 << 20, null) == -1  # Tq > Tkv
+    assert libne.ne_attn_decode(p, p, p, p, p, 1, 1, 10, 9, 4, 2, 64, 10000.0, 0, p, 1 << 20, null) == -1  # Tkv > Tcap
+    assert libne.ne_attn_decode(p, p, p, p, p, 1, 65, 100, 100, 4, 2, 64, 10000.0, 0, p, 1 << 20, null) == -3  # 130 rows
+    assert libne.ne_attn_decode(p, p, p, mis, p, *ok, 0, p, 1 << 20, null) == -2
+

@@ -251,3 +251,73 @@ def test_bad_arguments_rejected(nb):
     assert L.ne_attn_fwd(p(q), p(k), p(k), p(q), p(lse), 1, 16, 3, 2, 64, 10000.0, s) == -1
     assert L.ne_attn_bwd(p(q), p(k), p(k), p(q), p(lse), p(q), p(q), p(k), p(k), 1, 16, 2, 1, 64,
                          10000.0, 0, None, 0, s) == -5
+
+
+# ---------------------------------------------------------------- decode with a KV cache
+DECODE_SHAPES = [
+    # B, Tkv, Tq, Hq, Hkv, D
+    (2, 300, 1, 4, 2, 64),
+    (3, 1000, 4, 12, 4, 64),
+    (1, 129, 7, 8, 8, 32),
+    (2, 128, 128, 4, 4, 64),   # Tq = Tkv and G * Tq = 128: a whole tile of queries
+    (1, 1, 1, 2, 1, 64),       # one cached position
+    (2, 4100, 2, 12, 4, 64),   # many splits, ragged last key tile
+    (1, 257, 16, 16, 2, 32),   # G * Tq = 128 with D = 32
+]
+
+
+def decode_case(nb, oracle_mod, shape, o_dtype=None, seed=700):
+    B, Tkv, Tq, Hq, Hkv, D = shape
+    x = H.make(B, Tkv, Hq, Hkv, D, seed=seed + Tkv)
+    q_new = H.to_device(x["q_bits"][:, Tkv - Tq:])
+    k, v = H.to_device(x["k_bits"]), H.to_device(x["v_bits"])
+    Tcap = Tkv + 37  # the cache's capacity exceeds the valid positions
+    kc, vc = nb.kv_cache(B, Tcap, Hkv, D, "cuda")
+    cut = Tkv - Tq  # the context first, then the new positions
+    if cut > 0:
+        nb.kv_append(k[:, :cut].contiguous(), v[:, :cut].contiguous(), kc, vc, 0)
+    nb.kv_append(k[:, cut:].contiguous(), v[:, cut:].contiguous(), kc, vc, cut)
+    o, lse = nb.attn_decode(q_new, kc, vc, Tkv, o_dtype=o_dtype or torch.bfloat16)
+    o2, lse2 = nb.attn_decode(q_new, kc, vc, Tkv, o_dtype=o_dtype or torch.bfloat16)
+    nb.check_status()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2), "decode is not bitwise reproducible"
+    ro, rl = oracle_mod.decode_fwd(x["q"][:, Tkv - Tq:], x["k"], x["v"], inputs.ROPE_BASE)
+    go = H.to_f64(o)
+    assert np.isfinite(go).all()
+    eo = H.errors(go, ro)
+    el = H.errors(lse.cpu().numpy().astype(np.float64), rl)
+    print("DECODE", shape, "o rel %.2e abs %.2e" % eo, "lse abs %.2e" % el[1])
+    assert eo[0] <= H.REL_L2_TOL and eo[1] <= H.MAX_ABS_TOL and el[1] <= H.LSE_ABS_TOL, (eo, el)
+
+
+@pytest.mark.parametrize("shape", DECODE_SHAPES)
+def test_decode_parity(nb, oracle_mod, shape):
+    decode_case(nb, oracle_mod, shape)
+
+
+def test_decode_fp32_output(nb, oracle_mod):
+    decode_case(nb, oracle_mod, (2, 700, 3, 12, 4, 64), o_dtype=torch.float32)
+
+
+def test_decode_matches_forward_rows(nb):
+    """The decode of the last Tq positions and the training forward agree on those rows."""
+    B, T, Tq, Hq, Hkv, D = 2, 640, 5, 12, 4, 64
+    x = H.make(B, T, Hq, Hkv, D, seed=91)
+    q, k, v = (H.to_device(x[n + "_bits"]) for n in ("q", "k", "v"))
+    o_f, lse_f = nb.attn_fwd(q, k, v)
+    kc, vc = nb.kv_cache(B, T, Hkv, D, "cuda")
+    nb.kv_append(k, v, kc, vc, 0)
+    o_d, lse_d = nb.attn_decode(q[:, T - Tq:].contiguous(), kc, vc, T)
+    nb.check_status()
+    d = (o_d.float() - o_f[:, T - Tq:].float()).abs().max().item()
+    dl = (lse_d - lse_f[:, :, T - Tq:]).abs().max().item()
+    assert d <= 2e-2 and dl <= 1e-3, (d, dl)
+
+
+def test_decode_rejects_oversized_query_tile(nb):
+    q = torch.zeros((1, 33, 8, 64), dtype=torch.bfloat16, device="cuda")  # 4 heads per kv head x 33 tokens
+    kc, vc = nb.kv_cache(1, 64, 2, 64, "cuda")
+    with pytest.raises(nb.NeAttnError) as e:
+        nb.attn_decode(q, kc, vc, 40, workspace=torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == -3
+

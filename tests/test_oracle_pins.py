@@ -147,6 +147,18 @@ def test_central_finite_differences(oracle_mod):
 
 
 # ---------------------------------------------------------------- closed forms
+@pytest.mark.parametrize("shape", [(2, 9, 4, 2, 4, 3), (1, 6, 3, 3, 2, 1), (1, 5, 2, 1, 4, 5)])
+def test_decode_is_the_last_rows(oracle_mod, shape):
+    """decode_fwd equals the last Tq rows of the whole-matrix formulation run on
+    a query tensor whose earlier rows are random (they must not matter)."""
+    B, T, Hq, Hkv, D, Tq = shape
+    q, k, v, do = rnd((B, T, Hq, D), 21), rnd((B, T, Hkv, D), 22), rnd((B, T, Hkv, D), 23), rnd((B, T, Hq, D), 24)
+    o_ref, lse_ref, _, _, _ = bruteforce(q, k, v, do, 10000.0)
+    o, lse = oracle_mod.decode_fwd(q[:, T - Tq:], k, v, 10000.0)
+    close(o, o_ref[:, T - Tq:], 1e-12)
+    close(lse, lse_ref[:, :, T - Tq:], 1e-12)
+
+
 def test_single_token(oracle_mod):
     """T = 1: O = v_0, LSE = s_00, dq = dk = 0, dv_0 = sum over the group of dO."""
     B, T, Hq, Hkv, D = 2, 1, 4, 2, 8

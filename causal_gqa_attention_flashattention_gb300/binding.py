@@ -238,15 +238,15 @@ def fwd_bwd_host(q, k, v, dout, rope_base=10000.0, grad_dtype=torch.bfloat16, o_
 
 
 def kv_cache(B, Tcap, Hkv, D, device):
-    """Empty key (fp16, rotated) and value (bf16) caches [B, Tcap, Hkv, D]."""
-    return (torch.zeros((B, Tcap, Hkv, D), dtype=torch.float16, device=device),
-            torch.zeros((B, Tcap, Hkv, D), dtype=torch.bfloat16, device=device))
+    """Empty head-major key (fp16, rotated) and value (bf16) caches [B, Hkv, Tcap, D]."""
+    return (torch.zeros((B, Hkv, Tcap, D), dtype=torch.float16, device=device),
+            torch.zeros((B, Hkv, Tcap, D), dtype=torch.bfloat16, device=device))
 
 
 def kv_append(k_new, v_new, k_cache, v_cache, pos0, rope_base=10000.0, stream=None):
     """Writes positions pos0 .. pos0 + Tn - 1 of the caches from k_new, v_new [B,Tn,Hkv,D] (bf16)."""
     B, Tn, Hkv, D = k_new.shape
-    Tcap = k_cache.shape[1]
+    Tcap = k_cache.shape[2]
     for t in (k_new, v_new):
         assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous()
     assert k_cache.dtype == torch.float16 and v_cache.dtype == torch.bfloat16
@@ -265,7 +265,7 @@ def attn_decode(q, k_cache, v_cache, Tkv, rope_base=10000.0, o=None, lse=None, o
     """o, lse for the Tq new queries q [B,Tq,Hq,D] (bf16, positions Tkv-Tq .. Tkv-1)
     against cache positions 0 .. Tkv-1 (see ne_attn_decode)."""
     B, Tq, Hq, D = q.shape
-    Tcap, Hkv = k_cache.shape[1], k_cache.shape[2]
+    Hkv, Tcap = k_cache.shape[1], k_cache.shape[2]
     assert q.dtype == torch.bfloat16 and q.is_cuda and q.is_contiguous()
     assert k_cache.dtype == torch.float16 and v_cache.dtype == torch.bfloat16
     if o is None:

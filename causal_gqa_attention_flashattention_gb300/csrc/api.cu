@@ -207,12 +207,13 @@ int make_map_bthd(CUtensorMap* m, const void* ptr, int B, int T, int H, int D,
   return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
 }
 
-// 4-D map over a key/value cache [B, Tcap, H, D] of which positions 0..Tkv-1 are
-// valid: rows at or past Tkv read as zeros.  Box = one head, 128 rows, all D.
+// 4-D map over a head-major key/value cache [B, H, Tcap, D] of which positions
+// 0..Tkv-1 are valid: rows at or past Tkv read as zeros.  Box = 128 rows of one
+// head, all D (one contiguous stretch).
 int make_map_cache(CUtensorMap* m, const void* ptr, int B, int Tkv, int Tcap, int H, int D, CUtensorMapDataType dt) {
-  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)Tkv, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)Tcap * H * D * 2};
-  cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)kTile, 1};
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Tkv, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Tcap * D * 2, (cuuint64_t)H * Tcap * D * 2};
+  cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)kTile, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = g_encode(m, dt, 4, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         D == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
@@ -281,13 +282,15 @@ size_t fwd_ws_bytes(int B, int T, int Hq, int Hkv, int D) {
 struct DecodeWs {
   size_t qpk, part_o, part_ml, total;
 };
+int decode_copies(int R) { return R <= 32 ? 4 : (R <= 64 ? 2 : 1); }
 DecodeWs decode_ws(int B, int Tq, int Tkv, int Hq, int Hkv, int D) {
   const size_t R = (size_t)(Hq / Hkv) * Tq, ntk = ((size_t)Tkv + kTile - 1) / kTile;
+  const size_t F = (size_t)decode_copies((int)R);
   DecodeWs w;
   w.qpk = 0;
   w.part_o = ws_up((size_t)B * Hkv * kTile * D * 2);
-  w.part_ml = w.part_o + ws_up((size_t)B * Hkv * ntk * R * D * 4);
-  w.total = w.part_ml + ws_up((size_t)B * Hkv * ntk * R * 8);
+  w.part_ml = w.part_o + ws_up((size_t)B * Hkv * ntk * F * R * D * 4);
+  w.total = w.part_ml + ws_up((size_t)B * Hkv * ntk * F * R * 8);
   return w;
 }
 
@@ -786,12 +789,14 @@ int ne_attn_decode(const void* q, const void* k_cache, const void* v_cache, void
   a.D = D;
   a.G = Hq / Hkv;
   a.R = a.G * Tq;
+  a.F = decode_copies(a.R);
   a.ntk = (Tkv + kTile - 1) / kTile;
   a.o_fp32 = (flags & kFlagOFp32) ? 1 : 0;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   // Splits of each (batch, key/value head)'s key tiles: the count whose slowest
   // CTA (work items per CTA x tiles per item, plus about one tile of fixed cost
-  // per item) is shortest.
+  // per item) is shortest; among equals the smaller count, which leaves fewer
+  // partial results for the combine to merge.
   const long long bh = (long long)B * Hkv;
   long long best = -1;
   for (int ns = 1; ns <= a.ntk && ns <= 64; ns++) {

@@ -9,7 +9,10 @@
 //
 //   k_kv_append       new keys rotated (fp16) and new values copied into the caches
 //   k_decode_q        the Tq x G query rows of each key/value head rotated and
-//                     packed into one 128-row tile (row t * G + g; zero rows after)
+//                     packed into one 128-row tile (row t * G + g; zero rows after);
+//                     with at most 32 (64) rows the tile holds 4 (2) copies of them
+//                     and copy f takes key columns f * 128 / F .. of every key tile,
+//                     so the exponentials of a tile are spread over four warps
 //   k_decode          split sweep over the cache: one CTA per SM loops over work
 //                     items (batch, key/value head, split of the key tiles);
 //                     S = Q K^T and O += P V on the tensor cores, an online softmax
@@ -19,7 +22,9 @@
 //
 // Decode streams the cache once and does little arithmetic per byte, so the
 // sweep is bound by HBM; the G query heads of a key/value head (and the Tq
-// tokens) share every K/V tile through the M dimension of the MMAs.
+// tokens) share every K/V tile through the M dimension of the MMAs.  The
+// caches are head-major ([B, Hkv, Tcap, D]): a work item reads one contiguous
+// stretch of each.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -54,7 +59,7 @@ __global__ void __launch_bounds__(256) k_kv_append(const KvAppendArgs a) {
     const uint4 vv = __ldg(reinterpret_cast<const uint4*>(a.v) + it);
     float4 c0, c1;
     rope_coeffs<D>(a.rope, pos, c, c0, c1);
-    const size_t dst = (((size_t)b * a.Tcap + pos) * a.Hkv + g) * kCPR + c;
+    const size_t dst = (((size_t)b * a.Hkv + g) * a.Tcap + pos) * kCPR + c;  // head-major cache
     reinterpret_cast<uint4*>(a.kc)[dst] = rope_chunk_f16(kv, c0, c1, nullptr);
     reinterpret_cast<uint4*>(a.vc)[dst] = vv;
   }
@@ -69,7 +74,7 @@ __global__ void __launch_bounds__(256) k_decode_q(const DecodeArgs a) {
     const uint32_t row = it / kCPR;  // (b * Hkv + g) * 128 + r
     const int c = (int)(it % kCPR);
     const uint32_t bk = row / kTile;
-    const int r = (int)(row % kTile);
+    const int r = (int)(row % kTile) % (kTile / a.F);  // copy (row % 128) / (128 / F) of query row r
     uint4 out = make_uint4(0, 0, 0, 0);
     if (r < a.R) {
       const int t = r / a.G, gg = r - t * a.G;
@@ -117,6 +122,146 @@ __device__ __forceinline__ bool dec_item(const DecodeArgs& a, int tl, DecItem& i
   return true;
 }
 
+// Softmax role of the decode sweep for one warp: rows of its TMEM lane quarter
+// (copy f of the query rows), key columns f * W .. f * W + W - 1 of every tile.
+// Returns false if a wait gave up.
+template <int D, int W>
+__device__ __forceinline__ bool decode_softmax(const DecodeArgs& a, uint32_t tmem, int warp, int lane, uint64_t* s_full,
+                                               uint64_t* s_read, uint64_t* p_ready, uint64_t* pv_done,
+                                               uint64_t* o_free, volatile int* abort) {
+  using C = DecCfg<D>;
+  const int q4 = warp & 3;        // TMEM lane quarter
+  const int rr = q4 * 32 + lane;  // row of the packed tile
+  const int span = kTile / a.F;
+  const int f = rr / span, r = rr % span;  // copy, query row (token r / G, head r % G of the group)
+  const int c0 = f * W;                    // this copy's first key column of a tile
+  const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+  const float sl2 = a.scale_log2;
+  // this row's last visible key position (-1: a padding row sees none)
+  const int qpos = r < a.R ? a.Tkv - a.Tq + r / a.G : -1;
+  if (W < 128) {
+    // the P columns of the other copies stay zero in this warp's lanes
+    uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int c = 0; c < 8; c++) tmem_st8(trow + C::kColP + c * 8, z);
+    tmem_wait_st();
+  }
+  bool ok = true;
+  int g = 0;
+  DecItem it;
+  for (int tl = 0; ok && dec_item(a, tl, it); tl++) {
+    float r_max = -INFINITY, l = 0.f;  // raw-logit running maximum (as used) and sum
+    for (int n = it.n0; n < it.n1; n++, g++) {
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full, g & 1, abort));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[W];
+#pragma unroll
+      for (int c = 0; c < W / 32; c++)
+        tmem_ld32(trow + C::kColS + c0 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c));
+      tmem_wait_ld();
+      tc_fence_before();
+      warp_arrive(s_read);  // S of the next step may overwrite the score columns
+      // keys after this row's position (and past the cache) are masked
+      const int lim = qpos - n * kTile - c0;  // columns 0..lim of the slice are visible
+      if (lim < W - 1) {
+#pragma unroll
+        for (int c = 0; c < W; c++)
+          if (c > lim) s[c] = 0xff800000u;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < W; c += 2) mx = fmax3(mx, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+      const float r_new = fmaxf(r_max, mx);
+      // lazy rescale of O and l when the maximum grows by more than 2^8
+      float r_use = r_max;
+      if (r_max == -INFINITY) {
+        r_use = r_new;  // first visible keys of this item (O holds zeros so far)
+      } else if (__fmul_rn(r_new, sl2) > __fmul_rn(r_max, sl2) + 8.0f) {
+        r_use = r_new;
+      }
+      const bool resc = r_max != -INFINITY && r_use != r_max;
+      if (__any_sync(0xffffffffu, resc)) {
+        // O must hold every earlier P V
+        ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (g - 1) & 1, abort));
+        if (!ok) break;
+        tc_fence_after();
+        const float alpha = resc ? ex2(__fmul_rn(r_max, sl2) - __fmul_rn(r_use, sl2)) : 1.f;
+        l *= alpha;
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < D / 32; c++) {
+          tmem_ld32(trow + C::kColO + c * 32, w);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e++) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
+          tmem_st32(trow + C::kColO + c * 32, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+      }
+      r_max = r_use;
+      // P = exp2(s * scale_log2 - m) (0 while the row has seen no visible key)
+      const float m_use = r_use == -INFINITY ? 0.f : __fmul_rn(r_use, sl2);
+      const uint64_t sl2x2 = f2(sl2, sl2), negm = f2(-m_use, -m_use);
+      uint64_t sum4[4] = {0ull, 0ull, 0ull, 0ull};
+      uint32_t pk[W / 2];
+#pragma unroll
+      for (int e = 0; e < W / 2; e++) {
+        float x0, x1;
+        f2_split(f2_fma(f2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sl2x2, negm), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        pk[e] = pack_bf16(p0, p1);
+        sum4[e & 3] = f2_add(sum4[e & 3], f2(p0, p1));
+      }
+      {
+        float s0, s1, s2, s3, s4, s5, s6, s7;
+        f2_split(sum4[0], s0, s1);
+        f2_split(sum4[1], s2, s3);
+        f2_split(sum4[2], s4, s5);
+        f2_split(sum4[3], s6, s7);
+        l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+      }
+      // one P buffer: the previous step's P V has read it
+      if (g >= 1) {
+        ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (g - 1) & 1, abort));
+        if (!ok) break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < W / 16; c++)
+        tmem_st8(trow + C::kColP + c0 / 2 + c * 8, *reinterpret_cast<const uint32_t(*)[8]>(pk + 8 * c));
+      tmem_wait_st();
+      tc_fence_before();
+      warp_arrive(p_ready);
+    }
+    if (!ok) break;
+    // the copy's partial result: unnormalised O, the max (log2 units) and the sum
+    ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (g - 1) & 1, abort));
+    if (!ok) break;
+    tc_fence_after();
+    const size_t prow = (((size_t)it.bk * a.nsplit + it.s) * a.F + f) * a.R + r;
+#pragma unroll
+    for (int c = 0; c < D / 32; c++) {
+      uint32_t w[32];
+      tmem_ld32(trow + C::kColO + c * 32, w);
+      tmem_wait_ld();
+      if (r < a.R) {
+        float4* dst = reinterpret_cast<float4*>(a.part_o + prow * D + c * 32);
+#pragma unroll
+        for (int e = 0; e < 8; e++)
+          dst[e] = make_float4(__uint_as_float(w[4 * e]), __uint_as_float(w[4 * e + 1]), __uint_as_float(w[4 * e + 2]),
+                               __uint_as_float(w[4 * e + 3]));
+      }
+    }
+    if (r < a.R)
+      reinterpret_cast<float2*>(a.part_ml)[prow] = make_float2(r_max == -INFINITY ? -INFINITY : __fmul_rn(r_max, sl2), l);
+    tc_fence_before();
+    warp_arrive(o_free);  // the next item's first P V may overwrite O
+  }
+  return ok;
+}
+
 template <int D>
 __global__ void __launch_bounds__(224, 1) k_decode(const __grid_constant__ DecodeArgs a) {
   using C = DecCfg<D>;
@@ -140,7 +285,8 @@ __global__ void __launch_bounds__(224, 1) k_decode(const __grid_constant__ Decod
   volatile int* abort = reinterpret_cast<volatile int*>(s_full + 7) + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // softmax warps whose TMEM lane quarter holds query rows (the others sit out)
-  const int nact = (a.R + 31) / 32;
+  int nact = 0;
+  for (int q = 0; q < 4; q++) nact += ((q * 32) % (kTile / a.F)) < a.R ? 1 : 0;
 
   if (tid == 0) {
     *abort = 0;
@@ -186,8 +332,8 @@ __global__ void __launch_bounds__(224, 1) k_decode(const __grid_constant__ Decod
           const int st = g % S, use = g / S;
           if (use > 0 && !(ok = mbar_wait(kv_empty + st, (use - 1) & 1, abort))) break;
           mbar_arrive_expect_tx(kv_full + st, 2 * TB);
-          tma_load_4d(smem + C::kOffK + st * TB, &a.map_k, kv_full + st, 0, kvh, n * kTile, b);
-          tma_load_4d(smem + C::kOffV + st * TB, &a.map_v, kv_full + st, 0, kvh, n * kTile, b);
+          tma_load_4d(smem + C::kOffK + st * TB, &a.map_k, kv_full + st, 0, n * kTile, kvh, b);
+          tma_load_4d(smem + C::kOffV + st * TB, &a.map_v, kv_full + st, 0, n * kTile, kvh, b);
         }
       }
       if (!ok) record_timeout(a.status, abort);
@@ -252,127 +398,15 @@ __global__ void __launch_bounds__(224, 1) k_decode(const __grid_constant__ Decod
       mma_commit(drain + 1);
       mbar_wait(drain + 1, 0, &never);
     }
-  } else if (((warp & 3) < nact)) {
+  } else if ((((warp & 3) * 32) % (kTile / a.F)) < a.R) {
     // ------------------------------------------------------------ softmax, one row per thread
-    // (rows past R of a quarter in use are padding; their P rows are zero)
-    const int q4 = warp & 3;       // TMEM lane quarter
-    const int r = q4 * 32 + lane;  // row of the packed tile: token r / G, head r % G of the group
-    const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-    const float sl2 = a.scale_log2;
-    // this row's last visible key position (-1: a padding row sees none)
-    const int qpos = r < a.R ? a.Tkv - a.Tq + r / a.G : -1;
-    bool ok = true;
-    int g = 0;
-    DecItem it;
-    for (int tl = 0; ok && dec_item(a, tl, it); tl++) {
-      float r_max = -INFINITY, l = 0.f;  // raw-logit running maximum (as used) and sum
-      for (int n = it.n0; n < it.n1; n++, g++) {
-        ok = __all_sync(0xffffffffu, mbar_wait(s_full, g & 1, abort));
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t s[128];
-#pragma unroll
-        for (int c = 0; c < 4; c++) tmem_ld32(trow + C::kColS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c));
-        tmem_wait_ld();
-        tc_fence_before();
-        warp_arrive(s_read);  // S of the next step may overwrite the score columns
-        // keys after this row's position (and past the cache) are masked
-        const int lim = qpos - n * kTile;  // columns 0..lim are visible
-        if (lim < 127) {
-#pragma unroll
-          for (int c = 0; c < 128; c++)
-            if (c > lim) s[c] = 0xff800000u;
-        }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 128; c += 2) mx = fmax3(mx, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
-        const float r_new = fmaxf(r_max, mx);
-        // lazy rescale of O and l when the maximum grows by more than 2^8
-        float r_use = r_max;
-        if (r_max == -INFINITY) {
-          r_use = r_new;  // first visible keys of this item (O holds zeros so far)
-        } else if (__fmul_rn(r_new, sl2) > __fmul_rn(r_max, sl2) + 8.0f) {
-          r_use = r_new;
-        }
-        const bool resc = r_max != -INFINITY && r_use != r_max;
-        if (__any_sync(0xffffffffu, resc)) {
-          // O must hold every earlier P V
-          ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (g - 1) & 1, abort));
-          if (!ok) break;
-          tc_fence_after();
-          const float alpha = resc ? ex2(__fmul_rn(r_max, sl2) - __fmul_rn(r_use, sl2)) : 1.f;
-          l *= alpha;
-          uint32_t w[32];
-#pragma unroll
-          for (int c = 0; c < D / 32; c++) {
-            tmem_ld32(trow + C::kColO + c * 32, w);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; e++) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
-            tmem_st32(trow + C::kColO + c * 32, w);
-          }
-          tmem_wait_st();
-          tc_fence_before();
-        }
-        r_max = r_use;
-        // P = exp2(s * scale_log2 - m) (0 while the row has seen no visible key)
-        const float m_use = r_use == -INFINITY ? 0.f : __fmul_rn(r_use, sl2);
-        const uint64_t sl2x2 = f2(sl2, sl2), negm = f2(-m_use, -m_use);
-        uint64_t sum4[4] = {0ull, 0ull, 0ull, 0ull};
-        uint32_t pk[64];
-#pragma unroll
-        for (int e = 0; e < 64; e++) {
-          float x0, x1;
-          f2_split(f2_fma(f2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sl2x2, negm), x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          pk[e] = pack_bf16(p0, p1);
-          sum4[e & 3] = f2_add(sum4[e & 3], f2(p0, p1));
-        }
-        {
-          float s0, s1, s2, s3, s4, s5, s6, s7;
-          f2_split(sum4[0], s0, s1);
-          f2_split(sum4[1], s2, s3);
-          f2_split(sum4[2], s4, s5);
-          f2_split(sum4[3], s6, s7);
-          l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
-        }
-        // one P buffer: the previous step's P V has read it
-        if (g >= 1) {
-          ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (g - 1) & 1, abort));
-          if (!ok) break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 8; c++) tmem_st8(trow + C::kColP + c * 8, *reinterpret_cast<const uint32_t(*)[8]>(pk + 8 * c));
-        tmem_wait_st();
-        tc_fence_before();
-        warp_arrive(p_ready);
-      }
-      if (!ok) break;
-      // the item's partial result: unnormalised O, the max (log2 units) and the sum
-      ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (g - 1) & 1, abort));
-      if (!ok) break;
-      tc_fence_after();
-      const size_t prow = ((size_t)it.bk * a.nsplit + it.s) * a.R + r;
-#pragma unroll
-      for (int c = 0; c < D / 32; c++) {
-        uint32_t w[32];
-        tmem_ld32(trow + C::kColO + c * 32, w);
-        tmem_wait_ld();
-        if (r < a.R) {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + prow * D + c * 32);
-#pragma unroll
-          for (int e = 0; e < 8; e++)
-            dst[e] = make_float4(__uint_as_float(w[4 * e]), __uint_as_float(w[4 * e + 1]),
-                                 __uint_as_float(w[4 * e + 2]), __uint_as_float(w[4 * e + 3]));
-        }
-      }
-      if (r < a.R)
-        reinterpret_cast<float2*>(a.part_ml)[prow] =
-            make_float2(r_max == -INFINITY ? -INFINITY : __fmul_rn(r_max, sl2), l);
-      tc_fence_before();
-      warp_arrive(o_free);  // the next item's first P V may overwrite O
-    }
+    bool ok;
+    if (a.F == 4)
+      ok = decode_softmax<D, 32>(a, tmem, warp, lane, s_full, s_read, p_ready, pv_done, o_free, abort);
+    else if (a.F == 2)
+      ok = decode_softmax<D, 64>(a, tmem, warp, lane, s_full, s_read, p_ready, pv_done, o_free, abort);
+    else
+      ok = decode_softmax<D, 128>(a, tmem, warp, lane, s_full, s_read, p_ready, pv_done, o_free, abort);
     if (!ok) record_timeout(a.status, abort);
   }
 
@@ -398,14 +432,15 @@ __global__ void __launch_bounds__(256) k_decode_combine(const DecodeArgs a) {
     const uint32_t b = bt / a.Tq, t = bt - b * a.Tq;
     const uint32_t g = h / a.G, gg = h - g * a.G;
     const int r = (int)(t * a.G + gg);
-    const size_t base = ((size_t)b * a.Hkv + g) * a.nsplit;
+    const int npart = a.nsplit * a.F;  // splits x copies of the query rows
+    const size_t base = ((size_t)b * a.Hkv + g) * npart;
     const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
     float m = -INFINITY;
-    for (int s = 0; s < a.nsplit; s++) m = fmaxf(m, ml[(base + s) * a.R + r].x);
+    for (int s = 0; s < npart; s++) m = fmaxf(m, ml[(base + s) * a.R + r].x);
     float acc[kPer], L = 0.f;
 #pragma unroll
     for (int e = 0; e < kPer; e++) acc[e] = 0.f;
-    for (int s = 0; s < a.nsplit; s++) {
+    for (int s = 0; s < npart; s++) {
       const size_t pr = (base + s) * a.R + r;
       const float2 v = ml[pr];
       if (v.y == 0.f) continue;  // no visible key in this split

@@ -111,8 +111,8 @@ struct DqArgs {
 // Key/value cache append: rotated keys (fp16) and values (bf16) of Tn new positions.
 struct KvAppendArgs {
   const __nv_bfloat16 *k, *v;  // [B, Tn, Hkv, D]
-  __half* kc;                  // [B, Tcap, Hkv, D] rotated keys
-  __nv_bfloat16* vc;           // [B, Tcap, Hkv, D]
+  __half* kc;                  // [B, Hkv, Tcap, D] rotated keys
+  __nv_bfloat16* vc;           // [B, Hkv, Tcap, D]
   const float2* rope;
   int B, Tn, Hkv, Tcap, pos0;
   FastDiv div_hkv, div_tn;
@@ -121,16 +121,17 @@ struct KvAppendArgs {
 // Decode over a key/value cache (see attn_decode.cu).
 struct DecodeArgs {
   CUtensorMap map_q;         // packed rotated queries [B*Hkv*128, D] fp16 (4-D map, box D x 1 x 128 x 1)
-  CUtensorMap map_k, map_v;  // caches [B, Tkv valid of Tcap, Hkv, D] (fp16 keys, bf16 values)
+  CUtensorMap map_k, map_v;  // caches [B, Hkv, Tkv valid of Tcap, D] (fp16 keys, bf16 values)
   const __nv_bfloat16* q;    // [B, Tq, Hq, D]
   __half* qpk;               // [B, Hkv, 128, D] packed rotated queries (workspace)
-  float* part_o;             // [B, Hkv, nsplit, R, D] unnormalised O per split (workspace)
-  float* part_ml;            // [B, Hkv, nsplit, R] (max in log2 units, sum) pairs (workspace)
+  float* part_o;             // [B, Hkv, nsplit, F, R, D] unnormalised O per split and copy (workspace)
+  float* part_ml;            // [B, Hkv, nsplit, F, R] (max in log2 units, sum) pairs (workspace)
   void* o;                   // [B, Tq, Hq, D] bf16 or fp32
   float* lse;                // [B, Hq, Tq]
   const float2* rope;
   int* status;
   int B, Tq, Tkv, Hq, Hkv, D, G, R, ntk, nsplit, o_fp32;
+  int F;                     // copies of the R query rows in the 128-row tile: 4 if R <= 32, 2 if R <= 64, else 1
   float scale_log2;
 };
 

@@ -179,9 +179,10 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
  * the cache, the Tq new queries sit at positions Tkv - Tq .. Tkv - 1 and
  * o[b,t,h], lse[b,h,t] equal rows Tkv - Tq + t of ne_attn_fwd over T = Tkv.
  *
- * Caches (row-major, capacity Tcap positions, the caller owns them):
- *   k_cache : [B, Tcap, Hkv, D] fp16, the rotated keys k^_j = R_j k_j
- *   v_cache : [B, Tcap, Hkv, D] bfloat16
+ * Caches (row-major, head-major, capacity Tcap positions, the caller owns them):
+ *   k_cache : [B, Hkv, Tcap, D] fp16, the rotated keys k^_j = R_j k_j
+ *   v_cache : [B, Hkv, Tcap, D] bfloat16
+ * (head-major so that a decode step reads each head's cache as one stretch)
  *
  * ne_attn_kv_append writes positions pos0 .. pos0 + Tn - 1 of both caches from
  * the new keys and values k_new, v_new [B, Tn, Hkv, D] (bfloat16): each key is

@@ -415,6 +415,8 @@ def run_decode(args):
     peaks = load_peaks()
     stream = torch.cuda.Stream(dev)
     for name, (B, Tkv, Tq, Hq, Hkv, D) in DECODE_WORKLOADS.items():
+        if args.decode_workload and name != args.decode_workload:
+            continue
         cache_bytes = B * Tkv * Hkv * D * (2 + 2)
         nsets = max(2, min(64, -(-2 * 129 * 2 ** 20 // cache_bytes)))
         g = torch.Generator(device=dev).manual_seed(5)
@@ -496,6 +498,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode", action="store_true",
                     help="measure decode with a KV cache (one JSON line per decode workload) instead")
+    ap.add_argument("--decode-workload", default=None, choices=sorted(DECODE_WORKLOADS),
+                    help="with --decode: only this workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

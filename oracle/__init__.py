@@ -53,13 +53,13 @@ def _load():
         dp = ctypes.POINTER(ctypes.c_double)
         u8p = ctypes.POINTER(ctypes.c_ubyte)
         i = ctypes.c_int
-        lib.oracle_rope.argtypes = [dp, dp, i, i, i, i, ctypes.c_double, i]
+        lib.oracle_rope.argtypes = [dp, dp, i, i, i, i, ctypes.c_double, i, i]
         lib.oracle_rope.restype = None
         lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i,
-                                        ctypes.c_double, u8p, i]
+                                        ctypes.c_double, i, u8p, i]
         lib.oracle_attn_fwd.restype = None
         lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, dp,
-                                        i, i, i, i, i, ctypes.c_double, u8p, i]
+                                        i, i, i, i, i, ctypes.c_double, i, u8p, i]
         lib.oracle_attn_bwd.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i
@@ -91,17 +91,17 @@ def num_threads():
     return _load().oracle_num_threads()
 
 
-def rope(x, base, inverse=False):
+def rope(x, base, inverse=False, half=False):
     """R_t x for x of shape [B, T, H, D] (interleaved pairs); R_t^T x if inverse."""
     lib = _load()
     x = _f64(x)
     B, T, H, D = x.shape
     out = np.empty_like(x)
-    lib.oracle_rope(_p(x), _p(out), B, T, H, D, float(base), -1 if inverse else 1)
+    lib.oracle_rope(_p(x), _p(out), B, T, H, D, float(base), -1 if inverse else 1, int(bool(half)))
     return out
 
 
-def attn_fwd(q, k, v, base=10000.0, groups=None, nthreads=0):
+def attn_fwd(q, k, v, base=10000.0, groups=None, nthreads=0, half=False):
     """Causal GQA attention forward.  q [B,T,Hq,D], k/v [B,T,Hkv,D] (fp64).
 
     Returns (o [B,T,Hq,D], lse [B,Hq,T]); entries of groups not selected are NaN.
@@ -115,13 +115,13 @@ def attn_fwd(q, k, v, base=10000.0, groups=None, nthreads=0):
     lse = np.full((B, Hq, T), np.nan)
     sel = _sel(B, Hkv, groups)
     lib.oracle_attn_fwd(_p(q), _p(k), _p(v), _p(o), _p(lse), B, T, Hq, Hkv, D,
-                        float(base),
+                        float(base), int(bool(half)),
                         None if sel is None else sel.ctypes.data_as(
                             ctypes.POINTER(ctypes.c_ubyte)), int(nthreads))
     return o, lse
 
 
-def decode_fwd(q_new, k, v, base=10000.0, groups=None, nthreads=0):
+def decode_fwd(q_new, k, v, base=10000.0, groups=None, nthreads=0, half=False):
     """Decode step with a key/value cache (the engine's incremental generation
     with a KV cache: mynewscn README; socker-news README, GPU generation mode).
 
@@ -136,11 +136,11 @@ def decode_fwd(q_new, k, v, base=10000.0, groups=None, nthreads=0):
     assert 1 <= Tq <= T
     q = np.zeros((B, T, Hq, D))
     q[:, T - Tq:] = q_new
-    o, lse = attn_fwd(q, k, v, base, groups, nthreads)
+    o, lse = attn_fwd(q, k, v, base, groups, nthreads, half)
     return o[:, T - Tq:].copy(), lse[:, :, T - Tq:].copy()
 
 
-def attn_bwd(q, k, v, dout, base=10000.0, groups=None, nthreads=0):
+def attn_bwd(q, k, v, dout, base=10000.0, groups=None, nthreads=0, half=False):
     """Causal GQA attention backward from the definition.
 
     Returns dict with dq, dk, dv and the forward by-products o, lse and
@@ -159,7 +159,7 @@ def attn_bwd(q, k, v, dout, base=10000.0, groups=None, nthreads=0):
     delta = np.full((B, Hq, T), np.nan)
     sel = _sel(B, Hkv, groups)
     lib.oracle_attn_bwd(_p(q), _p(k), _p(v), _p(dout), _p(dq), _p(dk), _p(dv),
-                        _p(o), _p(lse), _p(delta), B, T, Hq, Hkv, D, float(base),
+                        _p(o), _p(lse), _p(delta), B, T, Hq, Hkv, D, float(base), int(bool(half)),
                         None if sel is None else sel.ctypes.data_as(
                             ctypes.POINTER(ctypes.c_ubyte)), int(nthreads))
     return dict(dq=dq, dk=dk, dv=dv, o=o, lse=lse, delta=delta)

@@ -23,7 +23,9 @@
  * Readings where the pages are silent (each also listed in the design notes):
  *   - RoPE pairs are interleaved (x[2i], x[2i+1]), angle t * theta_i with
  *     theta_i = base^(-2i/D), rotation [[cos, -sin], [sin, cos]], positions
- *     t = 0..T-1 for both queries and keys.
+ *     t = 0..T-1 for both queries and keys.  The pages name no pair layout;
+ *     `half` selects the other common reading, pairs (x[i], x[i + D/2]) with
+ *     the same angles (the half-split layout).
  *   - softmax scale is 1/sqrt(D), applied to the dot product of the rotated
  *     vectors; key j is visible to query t iff j <= t.
  *   - LSE is the natural log of sum_j exp(s_tj) of the scaled scores.
@@ -45,29 +47,31 @@
 
 #define IDX4(b, t, h, d, T, H, D) ((((size_t)(b) * (T) + (t)) * (H) + (h)) * (D) + (d))
 
-/* Rotation of one D-vector at position t (interleaved pairs), in place.
+/* Rotation of one D-vector at position t, in place: pair i is (x[2i], x[2i+1])
+ * (interleaved) or, with half != 0, (x[i], x[i + D/2]) (half-split).
  * dir = +1 applies R_t, dir = -1 applies R_t^T = R_{-t} (the adjoint used by
  * the backward pass: the rotation is orthogonal). */
-static void rope_vec(double* x, int D, long t, double base, int dir) {
+static void rope_vec(double* x, int D, long t, double base, int dir, int half) {
   for (int i = 0; i < D / 2; i++) {
     double theta = pow(base, -2.0 * (double)i / (double)D);
     double ang = (double)t * theta;
     double c = cos(ang), s = sin(ang) * (double)dir;
-    double x0 = x[2 * i], x1 = x[2 * i + 1];
-    x[2 * i] = x0 * c - x1 * s;
-    x[2 * i + 1] = x0 * s + x1 * c;
+    int i0 = half ? i : 2 * i, i1 = half ? i + D / 2 : 2 * i + 1;
+    double x0 = x[i0], x1 = x[i1];
+    x[i0] = x0 * c - x1 * s;
+    x[i1] = x0 * s + x1 * c;
   }
 }
 
 /* out[b,t,h,:] = R_t x[b,t,h,:]  (dir=+1)  or  R_t^T x  (dir=-1). */
 void oracle_rope(const double* x, double* out, int B, int T, int H, int D,
-                 double base, int dir) {
+                 double base, int dir, int half) {
   size_t n = (size_t)B * T * H * D;
   memcpy(out, x, n * sizeof(double));
   for (int b = 0; b < B; b++)
     for (int t = 0; t < T; t++)
       for (int h = 0; h < H; h++)
-        rope_vec(out + IDX4(b, t, h, 0, T, H, D), D, t, base, dir);
+        rope_vec(out + IDX4(b, t, h, 0, T, H, D), D, t, base, dir, half);
 }
 
 static double dot(const double* a, const double* b, int D) {
@@ -81,7 +85,7 @@ static double dot(const double* a, const double* b, int D) {
  * gradient rows are gathered the same way for contiguous access. */
 static void gather_group(const double* q, const double* k, const double* v,
                          const double* dout, int b, int g, int T, int Hq,
-                         int Hkv, int D, double base, double* qh, double* kh,
+                         int Hkv, int D, double base, int half, double* qh, double* kh,
                          double* vh, double* doh) {
   int G = Hq / Hkv;
   for (int hh = 0; hh < G; hh++) {
@@ -89,7 +93,7 @@ static void gather_group(const double* q, const double* k, const double* v,
     for (int t = 0; t < T; t++) {
       double* dst = qh + ((size_t)hh * T + t) * D;
       memcpy(dst, q + IDX4(b, t, h, 0, T, Hq, D), D * sizeof(double));
-      rope_vec(dst, D, t, base, +1);
+      rope_vec(dst, D, t, base, +1, half);
       if (doh)
         memcpy(doh + ((size_t)hh * T + t) * D, dout + IDX4(b, t, h, 0, T, Hq, D),
                D * sizeof(double));
@@ -98,7 +102,7 @@ static void gather_group(const double* q, const double* k, const double* v,
   for (int t = 0; t < T; t++) {
     double* dk = kh + (size_t)t * D;
     memcpy(dk, k + IDX4(b, t, g, 0, T, Hkv, D), D * sizeof(double));
-    rope_vec(dk, D, t, base, +1);
+    rope_vec(dk, D, t, base, +1, half);
     memcpy(vh + (size_t)t * D, v + IDX4(b, t, g, 0, T, Hkv, D), D * sizeof(double));
   }
 }
@@ -142,7 +146,7 @@ static int default_threads(int nthreads) {
 /* Forward: o [B,T,Hq,D], lse [B,Hq,T]. */
 void oracle_attn_fwd(const double* q, const double* k, const double* v,
                      double* o, double* lse, int B, int T, int Hq, int Hkv,
-                     int D, double base, const unsigned char* sel,
+                     int D, double base, int half, const unsigned char* sel,
                      int nthreads) {
   int G = Hq / Hkv;
   double scale = 1.0 / sqrt((double)D);
@@ -153,7 +157,7 @@ void oracle_attn_fwd(const double* q, const double* k, const double* v,
   for (int b = 0; b < B; b++)
     for (int g = 0; g < Hkv; g++) {
       if (sel && !sel[b * Hkv + g]) continue;
-      gather_group(q, k, v, NULL, b, g, T, Hq, Hkv, D, base, qh, kh, vh, NULL);
+      gather_group(q, k, v, NULL, b, g, T, Hq, Hkv, D, base, half, qh, kh, vh, NULL);
 #pragma omp parallel num_threads(nt)
       {
         double* s = malloc(sizeof(double) * T);
@@ -190,7 +194,7 @@ void oracle_attn_fwd(const double* q, const double* k, const double* v,
 void oracle_attn_bwd(const double* q, const double* k, const double* v,
                      const double* dout, double* dq, double* dk, double* dv,
                      double* o, double* lse, double* delta, int B, int T,
-                     int Hq, int Hkv, int D, double base,
+                     int Hq, int Hkv, int D, double base, int half,
                      const unsigned char* sel, int nthreads) {
   int G = Hq / Hkv;
   double scale = 1.0 / sqrt((double)D);
@@ -204,7 +208,7 @@ void oracle_attn_bwd(const double* q, const double* k, const double* v,
   for (int b = 0; b < B; b++)
     for (int g = 0; g < Hkv; g++) {
       if (sel && !sel[b * Hkv + g]) continue;
-      gather_group(q, k, v, dout, b, g, T, Hq, Hkv, D, base, qh, kh, vh, doh);
+      gather_group(q, k, v, dout, b, g, T, Hq, Hkv, D, base, half, qh, kh, vh, doh);
       /* pass 1: query rows */
 #pragma omp parallel num_threads(nt)
       {
@@ -230,7 +234,7 @@ void oracle_attn_bwd(const double* q, const double* k, const double* v,
             for (int d = 0; d < D; d++) acc[d] += dsj * kj[d];
           }
           for (int d = 0; d < D; d++) acc[d] *= scale;
-          rope_vec(acc, D, t, base, -1);
+          rope_vec(acc, D, t, base, -1, half);
           memcpy(dq + IDX4(b, t, h, 0, T, Hq, D), acc, D * sizeof(double));
           rl[r] = l;
           rd[r] = dt;
@@ -266,7 +270,7 @@ void oracle_attn_bwd(const double* q, const double* k, const double* v,
               }
             }
           for (int d = 0; d < D; d++) ak[d] *= scale;
-          rope_vec(ak, D, j, base, -1);
+          rope_vec(ak, D, j, base, -1, half);
           memcpy(dk + IDX4(b, j, g, 0, T, Hkv, D), ak, D * sizeof(double));
           memcpy(dv + IDX4(b, j, g, 0, T, Hkv, D), av, D * sizeof(double));
         }

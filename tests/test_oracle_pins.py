@@ -30,26 +30,28 @@ def rnd(shape, seed):
 
 
 # ---------------------------------------------------------------- second formulation
-def _rot_complex(x, base, sign=1.0):
-    """Rotary embedding as a complex phase: (x0 + i x1) * exp(i t theta)."""
+def _rot_complex(x, base, sign=1.0, half=False):
+    """Rotary embedding as a complex phase: (x0 + i x1) * exp(i t theta), with
+    pairs (x[2i], x[2i+1]) or, half-split, (x[i], x[i + D/2])."""
     B, T, H, D = x.shape
     theta = base ** (-np.arange(0, D, 2) / D)
     ang = np.arange(T)[:, None] * theta[None, :]
     ph = np.exp(1j * sign * ang)[None, :, None, :]
-    z = (x[..., 0::2] + 1j * x[..., 1::2]) * ph
+    lo, hi = (slice(0, D // 2), slice(D // 2, D)) if half else (slice(0, D, 2), slice(1, D, 2))
+    z = (x[..., lo] + 1j * x[..., hi]) * ph
     out = np.empty_like(x)
-    out[..., 0::2] = z.real
-    out[..., 1::2] = z.imag
+    out[..., lo] = z.real
+    out[..., hi] = z.imag
     return out
 
 
-def bruteforce(q, k, v, do, base):
+def bruteforce(q, k, v, do, base, half=False):
     """Whole-matrix causal GQA attention and its matrix-calculus gradients."""
     B, T, Hq, D = q.shape
     Hkv = k.shape[2]
     G = Hq // Hkv
     scale = 1.0 / math.sqrt(D)
-    qr, kr = _rot_complex(q, base), _rot_complex(k, base)
+    qr, kr = _rot_complex(q, base, half=half), _rot_complex(k, base, half=half)
     mask = np.triu(np.ones((T, T), dtype=bool), 1)  # True where key > query
     o = np.zeros_like(q)
     lse = np.zeros((B, Hq, T))
@@ -72,8 +74,8 @@ def bruteforce(q, k, v, do, base):
             dqr[b, :, h] = scale * dS @ kr[b, :, g]
             dkr[b, :, g] += scale * dS.T @ qr[b, :, h]
             dv[b, :, g] += P.T @ do[b, :, h]
-    dq = _rot_complex(dqr, base, -1.0)
-    dk = _rot_complex(dkr, base, -1.0)
+    dq = _rot_complex(dqr, base, -1.0, half)
+    dk = _rot_complex(dkr, base, -1.0, half)
     return o, lse, dq, dk, dv
 
 
@@ -157,6 +159,40 @@ def test_decode_is_the_last_rows(oracle_mod, shape):
     o, lse = oracle_mod.decode_fwd(q[:, T - Tq:], k, v, 10000.0)
     close(o, o_ref[:, T - Tq:], 1e-12)
     close(lse, lse_ref[:, :, T - Tq:], 1e-12)
+
+
+@pytest.mark.parametrize("shape", [(1, 5, 2, 1, 4), (2, 7, 4, 2, 8), (1, 9, 3, 3, 6)])
+def test_half_split_layout_matrix_form(oracle_mod, shape):
+    """The half-split pair layout (x[i], x[i + D/2]) against the whole-matrix
+    formulation with the same layout."""
+    B, T, Hq, Hkv, D = shape
+    q, k, v, do = rnd((B, T, Hq, D), 31), rnd((B, T, Hkv, D), 32), rnd((B, T, Hkv, D), 33), rnd((B, T, Hq, D), 34)
+    o_r, lse_r, dq_r, dk_r, dv_r = bruteforce(q, k, v, do, 500.0, half=True)
+    ref = oracle_mod.attn_bwd(q, k, v, do, 500.0, half=True)
+    for name, r in (("o", o_r), ("lse", lse_r), ("dq", dq_r), ("dk", dk_r), ("dv", dv_r)):
+        close(ref[name], r, 1e-12)
+
+
+def test_half_split_is_a_feature_permutation(oracle_mod):
+    """Half-split RoPE of x equals interleaved RoPE of P x read back through P,
+    with (P x)[2i] = x[i] and (P x)[2i+1] = x[i + D/2]; the scores use both
+    q and k in the same order, so o and lse agree and dq, dk map back by P."""
+    B, T, Hq, Hkv, D = 2, 8, 4, 2, 8
+    q, k, v, do = rnd((B, T, Hq, D), 41), rnd((B, T, Hkv, D), 42), rnd((B, T, Hkv, D), 43), rnd((B, T, Hq, D), 44)
+    perm = np.empty(D, dtype=int)
+    perm[0::2], perm[1::2] = np.arange(D // 2), np.arange(D // 2, D)  # P x = x[..., perm]
+    half = oracle_mod.attn_bwd(q, k, v, do, 10000.0, half=True)
+    inter = oracle_mod.attn_bwd(q[..., perm], k[..., perm], v, do, 10000.0)
+    inv = np.argsort(perm)
+    close(half["o"], inter["o"], 1e-12)
+    close(half["lse"], inter["lse"], 1e-12)
+    close(half["dq"], inter["dq"][..., inv], 1e-12)
+    close(half["dk"], inter["dk"][..., inv], 1e-12)
+    close(half["dv"], inter["dv"], 1e-12)
+    x = rnd((B, T, Hq, D), 45)
+    close(oracle_mod.rope(x, 10000.0, half=True), oracle_mod.rope(x[..., perm], 10000.0)[..., inv], 1e-12)
+    y = rnd((B, T, Hq, 2), 46)  # with D = 2 the two layouts are the same rotation
+    close(oracle_mod.rope(y, 10000.0, half=True), oracle_mod.rope(y, 10000.0), 1e-15)
 
 
 def test_single_token(oracle_mod):

@@ -18,6 +18,7 @@ O_FP32 = 1       # flag bits, see include/ne_attn.h
 GRAD_FP32 = 2
 PRECISE_QK = 4
 QK_ROTATED = 8
+ROPE_HALF = 16
 _lib = None
 
 
@@ -60,7 +61,7 @@ def lib():
         L.ne_attn_profile_detach.restype = i
         L.ne_attn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]
         L.ne_attn_profile_read.restype = i
-        L.ne_attn_kv_append.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+        L.ne_attn_kv_append.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
         L.ne_attn_kv_append.restype = i
         L.ne_attn_decode_workspace_size.argtypes = [i, i, i, i, i, i]
         L.ne_attn_decode_workspace_size.restype = sz
@@ -95,7 +96,7 @@ def fwd_workspace_size(B, T, Hq, Hkv, D, precise=False):
 
 
 def attn_fwd(q, k, v, rope_base=10000.0, o=None, lse=None, o_dtype=torch.bfloat16, precise=False,
-             workspace=None, stream=None):
+             workspace=None, rope_half=False, stream=None):
     """o, lse = causal GQA attention of q [B,T,Hq,D], k/v [B,T,Hkv,D] (bf16, CUDA).
 
     o_dtype: bfloat16 or float32.  precise: hi+lo split of the rotated q, k
@@ -115,7 +116,7 @@ def attn_fwd(q, k, v, rope_base=10000.0, o=None, lse=None, o_dtype=torch.bfloat1
         assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous()
     assert o.dtype in (torch.bfloat16, torch.float32) and o.is_contiguous()
     assert lse.dtype == torch.float32 and lse.is_contiguous()
-    flags = (O_FP32 if o.dtype == torch.float32 else 0) | (PRECISE_QK if precise else 0)
+    flags = (O_FP32 if o.dtype == torch.float32 else 0) | (PRECISE_QK if precise else 0) | (ROPE_HALF if rope_half else 0)
     if workspace is None:
         n = fwd_workspace_size(B, T, Hq, Hkv, D, precise)
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
@@ -138,7 +139,7 @@ def alloc_workspace(B, T, Hq, Hkv, D, precise=False, device="cuda"):
 
 
 def attn_bwd(q, k, v, o, lse, dout, rope_base=10000.0, grad_dtype=torch.bfloat16, precise=False,
-             dq=None, dk=None, dv=None, workspace=None, qk_rotated=False, stream=None):
+             dq=None, dk=None, dv=None, workspace=None, qk_rotated=False, rope_half=False, stream=None):
     """dq, dk, dv of the causal GQA attention given the forward's o and lse.
 
     o may be bfloat16 or float32; grad_dtype selects the gradient dtype.
@@ -165,7 +166,7 @@ def attn_bwd(q, k, v, o, lse, dout, rope_base=10000.0, grad_dtype=torch.bfloat16
     for t in (dq, dk, dv):
         assert t.dtype == grad_dtype and t.is_contiguous()
     flags = ((O_FP32 if o.dtype == torch.float32 else 0) | (GRAD_FP32 if grad_dtype == torch.float32 else 0)
-             | (PRECISE_QK if precise else 0) | (QK_ROTATED if qk_rotated else 0))
+             | (PRECISE_QK if precise else 0) | (QK_ROTATED if qk_rotated else 0) | (ROPE_HALF if rope_half else 0))
     _check("ne_attn_bwd", lib().ne_attn_bwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
         B, T, Hq, Hkv, D, float(rope_base), flags, _ptr(workspace), workspace.numel(), _stream(stream)))
@@ -243,7 +244,7 @@ def kv_cache(B, Tcap, Hkv, D, device):
             torch.zeros((B, Hkv, Tcap, D), dtype=torch.bfloat16, device=device))
 
 
-def kv_append(k_new, v_new, k_cache, v_cache, pos0, rope_base=10000.0, stream=None):
+def kv_append(k_new, v_new, k_cache, v_cache, pos0, rope_base=10000.0, rope_half=False, stream=None):
     """Writes positions pos0 .. pos0 + Tn - 1 of the caches from k_new, v_new [B,Tn,Hkv,D] (bf16)."""
     B, Tn, Hkv, D = k_new.shape
     Tcap = k_cache.shape[2]
@@ -253,7 +254,7 @@ def kv_append(k_new, v_new, k_cache, v_cache, pos0, rope_base=10000.0, stream=No
     assert k_cache.is_contiguous() and v_cache.is_contiguous() and k_cache.shape == v_cache.shape
     _check("ne_attn_kv_append", lib().ne_attn_kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
                                                         B, Tn, pos0, Tcap, Hkv, D, float(rope_base),
-                                                        _stream(stream)))
+                                                        ROPE_HALF if rope_half else 0, _stream(stream)))
 
 
 def decode_workspace_size(B, Tq, Tkv, Hq, Hkv, D):
@@ -261,7 +262,7 @@ def decode_workspace_size(B, Tq, Tkv, Hq, Hkv, D):
 
 
 def attn_decode(q, k_cache, v_cache, Tkv, rope_base=10000.0, o=None, lse=None, o_dtype=torch.bfloat16,
-                workspace=None, stream=None):
+                workspace=None, rope_half=False, stream=None):
     """o, lse for the Tq new queries q [B,Tq,Hq,D] (bf16, positions Tkv-Tq .. Tkv-1)
     against cache positions 0 .. Tkv-1 (see ne_attn_decode)."""
     B, Tq, Hq, D = q.shape
@@ -277,7 +278,7 @@ def attn_decode(q, k_cache, v_cache, Tkv, rope_base=10000.0, o=None, lse=None, o
     if workspace is None:
         workspace = torch.empty(max(decode_workspace_size(B, Tq, Tkv, Hq, Hkv, D), 1), dtype=torch.uint8,
                                 device=q.device)
-    flags = O_FP32 if o.dtype == torch.float32 else 0
+    flags = (O_FP32 if o.dtype == torch.float32 else 0) | (ROPE_HALF if rope_half else 0)
     _check("ne_attn_decode", lib().ne_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse),
                                                   B, Tq, Tkv, Tcap, Hq, Hkv, D, float(rope_base), flags,
                                                   _ptr(workspace), workspace.numel(), _stream(stream)))

@@ -334,7 +334,9 @@ WsLayout ws_layout(int B, int T, int Hq, int Hkv, int D, bool precise) {
   return w;
 }
 
-constexpr int kKnownFlags = kFlagOFp32 | kFlagGradFp32 | kFlagPreciseQK;
+constexpr int kKnownFlags = kFlagOFp32 | kFlagGradFp32 | kFlagPreciseQK | kFlagRopeHalf;
+// the split-precision kernels rotate tiles in shared memory in the interleaved layout only
+bool half_with_precise(int flags) { return (flags & kFlagRopeHalf) && (flags & kFlagPreciseQK); }
 constexpr int kBwdFlags = kKnownFlags | kFlagQKRotated;
 
 // ------------------------------------------------------------------ kernel timing
@@ -396,7 +398,8 @@ using namespace ne;
 extern "C" {
 
 size_t ne_attn_fwd_workspace_size(int B, int T, int Hq, int Hkv, int D, int flags) {
-  if (check_shape(B, T, Hq, Hkv, D) != NE_OK || (flags & ~(kFlagOFp32 | kFlagPreciseQK)) != 0) return 0;
+  if (check_shape(B, T, Hq, Hkv, D) != NE_OK || (flags & ~(kFlagOFp32 | kFlagPreciseQK | kFlagRopeHalf)) != 0) return 0;
+  if (half_with_precise(flags)) return 0;
   return (flags & kFlagPreciseQK) ? 0 : fwd_ws_bytes(B, T, Hq, Hkv, D);
 }
 
@@ -405,7 +408,8 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
                    void* stream) {
   if (!q || !k || !v || !o || !lse) return NE_ERR_ARG;
   if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
-  if ((flags & ~(kFlagOFp32 | kFlagPreciseQK)) != 0) return NE_ERR_ARG;
+  if ((flags & ~(kFlagOFp32 | kFlagPreciseQK | kFlagRopeHalf)) != 0) return NE_ERR_ARG;
+  if (half_with_precise(flags)) return NE_ERR_UNSUPPORTED;
   int st = check_shape(B, T, Hq, Hkv, D);
   if (st != NE_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return NE_ERR_ALIGN;
@@ -442,6 +446,7 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
     ra.div_hq = make_fastdiv((uint32_t)Hq);
     ra.div_hkv = make_fastdiv((uint32_t)Hkv);
     ra.div_t = make_fastdiv((uint32_t)T);
+    ra.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
     if ((st = make_map_bthd(&a.map_q, ra.qr, B, T, Hq, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != NE_OK) return st;
     if ((st = make_map_bthd(&a.map_k, ra.kr, B, T, Hkv, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != NE_OK) return st;
     ProfScope prof(NE_ATTN_KERNEL_FWD_ROPE, s);
@@ -476,6 +481,7 @@ int ne_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse
 size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D, int flags) {
   if (check_shape(B, T, Hq, Hkv, D) != NE_OK || (flags & ~kBwdFlags) != 0) return 0;
   if ((flags & kFlagQKRotated) && (flags & kFlagPreciseQK)) return 0;
+  if (half_with_precise(flags)) return 0;
   return ws_layout(B, T, Hq, Hkv, D, (flags & kFlagPreciseQK) != 0).total;
 }
 
@@ -486,6 +492,7 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   if ((flags & ~kBwdFlags) != 0) return NE_ERR_ARG;
   // the forward leaves rotated copies only in default precision
   if ((flags & kFlagQKRotated) && (flags & kFlagPreciseQK)) return NE_ERR_ARG;
+  if (half_with_precise(flags)) return NE_ERR_UNSUPPORTED;
   if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
   int st = check_shape(B, T, Hq, Hkv, D);
   if (st != NE_OK) return st;
@@ -543,6 +550,7 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   p.Tp = Tp;
   p.rotate_qk = (flags & kFlagQKRotated) ? 0 : 1;
   p.negate = precise ? 0 : 1;
+  p.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
   p.div_hq = make_fastdiv((uint32_t)Hq);
   p.div_hkv = make_fastdiv((uint32_t)Hkv);
   p.div_t = make_fastdiv((uint32_t)T);
@@ -582,6 +590,7 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   a.nt = nt;
   a.Tp = Tp;
   a.grad_fp32 = grad_fp32;
+  a.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
   a.scale_log2 = (float)(1.4426950408889634 * scale);
   a.scale_log2_lo = (float)(1.4426950408889634 * scale - (double)a.scale_log2);
   a.scale = (float)scale;
@@ -600,6 +609,7 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   qa.D = D;
   qa.Tp = Tp;
   qa.grad_fp32 = grad_fp32;
+  qa.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
   qa.scale = (float)scale;
   qa.div_hq = make_fastdiv((uint32_t)Hq);
   qa.div_t = make_fastdiv((uint32_t)T);
@@ -714,8 +724,9 @@ int ne_attn_profile_read(double* total_ms, long long* launches) {
 }
 
 int ne_attn_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int B, int Tn,
-                      int pos0, int Tcap, int Hkv, int D, float rope_base, void* stream) {
+                      int pos0, int Tcap, int Hkv, int D, float rope_base, int flags, void* stream) {
   if (!k_new || !v_new || !k_cache || !v_cache) return NE_ERR_ARG;
+  if ((flags & ~kFlagRopeHalf) != 0) return NE_ERR_ARG;
   if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
   if (Tn < 1 || pos0 < 0 || (long long)pos0 + Tn > (long long)Tcap) return NE_ERR_ARG;
   int st = check_shape(B, Tcap, Hkv, Hkv, D);
@@ -741,6 +752,7 @@ int ne_attn_kv_append(const void* k_new, const void* v_new, void* k_cache, void*
   a.pos0 = pos0;
   a.div_hkv = make_fastdiv((uint32_t)Hkv);
   a.div_tn = make_fastdiv((uint32_t)Tn);
+  a.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
   ProfScope prof(NE_ATTN_KERNEL_KV_APPEND, s);
   return launch_kv_append(a, D, s) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
 }
@@ -755,7 +767,7 @@ int ne_attn_decode(const void* q, const void* k_cache, const void* v_cache, void
                    size_t workspace_bytes, void* stream) {
   if (!q || !k_cache || !v_cache || !o || !lse) return NE_ERR_ARG;
   if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
-  if ((flags & ~kFlagOFp32) != 0) return NE_ERR_ARG;
+  if ((flags & ~(kFlagOFp32 | kFlagRopeHalf)) != 0) return NE_ERR_ARG;
   int st = check_decode_shape(B, Tq, Tkv, Tcap, Hq, Hkv, D);
   if (st != NE_OK) return st;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse))
@@ -790,6 +802,7 @@ int ne_attn_decode(const void* q, const void* k_cache, const void* v_cache, void
   a.G = Hq / Hkv;
   a.R = a.G * Tq;
   a.F = decode_copies(a.R);
+  a.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
   a.ntk = (Tkv + kTile - 1) / kTile;
   a.o_fp32 = (flags & kFlagOFp32) ? 1 : 0;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
@@ -847,6 +860,7 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
                         float rope_base, int flags, void* stream) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return NE_ERR_ARG;
   if ((flags & ~kKnownFlags) != 0) return NE_ERR_ARG;
+  if (half_with_precise(flags)) return NE_ERR_UNSUPPORTED;
   if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
   int st = check_shape(B, T, Hq, Hkv, D);
   if (st != NE_OK) return st;
@@ -912,6 +926,7 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
   p.Tp = Tp;
   p.rotate_qk = (flags & kFlagQKRotated) ? 0 : 1;
   p.negate = precise ? 0 : 1;
+  p.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
   p.div_hq = make_fastdiv((uint32_t)Hq);
   p.div_hkv = make_fastdiv((uint32_t)Hkv);
   p.div_t = make_fastdiv((uint32_t)T);
@@ -948,6 +963,7 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
   a.nt = nt;
   a.Tp = Tp;
   a.grad_fp32 = grad_fp32;
+  a.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
   a.scale_log2 = (float)(1.4426950408889634 * scale);
   a.scale_log2_lo = (float)(1.4426950408889634 * scale - (double)a.scale_log2);
   a.scale = (float)scale;
@@ -963,6 +979,7 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
   qa.D = D;
   qa.Tp = Tp;
   qa.grad_fp32 = grad_fp32;
+  qa.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
   qa.scale = (float)scale;
   qa.div_hq = make_fastdiv((uint32_t)Hq);
   qa.div_t = make_fastdiv((uint32_t)T);

@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
         ov = __ldg(reinterpret_cast<const uint4*>(a.o) + it);
       }
       if (a.rotate_qk) {
-        const uint4 qv = __ldg(reinterpret_cast<const uint4*>(a.q) + it);
+        const uint4 qv = load_rope_chunk<D>(a.q + (size_t)row * D, c, a.rope_half != 0);
         float4 c0, c1;
         rope_coeffs<D>(a.rope, (int)t, c, c0, c1);
         if (a.qlo) {
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
     const int c = (int)(it & (kCPR - 1));
     const uint32_t bt = fdiv(row, a.div_hkv);
     const uint32_t t = bt - fdiv(bt, a.div_t) * a.T;
-    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(a.k) + it);
+    const uint4 kv = load_rope_chunk<D>(a.k + (size_t)row * D, c, a.rope_half != 0);
     float4 c0, c1;
     rope_coeffs<D>(a.rope, (int)t, c, c0, c1);
     if (a.klo) {
@@ -171,7 +171,19 @@ __global__ void __launch_bounds__(256) k_bwd_dq(const DqArgs a) {
       y[2 * p] = a.scale * (xs[2 * p] * cs[p] + xs[2 * p + 1] * sn[p]);
       y[2 * p + 1] = a.scale * (xs[2 * p + 1] * cs[p] - xs[2 * p] * sn[p]);
     }
-    if (a.grad_fp32) {
+    if (a.rope_half) {
+      // pair p of the chunk is (x[4c + p], x[D/2 + 4c + p]) of the row
+      const size_t r0 = (size_t)row * D + 4 * c, r1 = r0 + D / 2;
+      if (a.grad_fp32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(a.dq) + r0) = make_float4(y[0], y[2], y[4], y[6]);
+        *reinterpret_cast<float4*>(static_cast<float*>(a.dq) + r1) = make_float4(y[1], y[3], y[5], y[7]);
+      } else {
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.dq) + r0) =
+            make_uint2(pack_bf16(y[0], y[2]), pack_bf16(y[4], y[6]));
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.dq) + r1) =
+            make_uint2(pack_bf16(y[1], y[3]), pack_bf16(y[5], y[7]));
+      }
+    } else if (a.grad_fp32) {
       float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.dq) + (size_t)it * 8);
       dst[0] = make_float4(y[0], y[1], y[2], y[3]);
       dst[1] = make_float4(y[4], y[5], y[6], y[7]);
@@ -763,7 +775,7 @@ __device__ __forceinline__ bool bwd_item(const BwdArgs& a, int tl, BwdItem& it) 
 // until the store has read the box and arrives on `free_`; every thread waits
 // for that before the next box.  `e` counts the boxes (barrier phases).
 // Returns false if a wait gave up.
-template <int D, int ES>
+template <int D, int ES, bool HALF = false>
 __device__ __forceinline__ bool stage_store(const float (&x)[D], uint8_t* stg, const CUtensorMap* map, int r,
                                             uint64_t* full, uint64_t* free_, int& e, int h, int row0, int b,
                                             const volatile int* abort) {
@@ -774,14 +786,17 @@ __device__ __forceinline__ bool stage_store(const float (&x)[D], uint8_t* stg, c
 #pragma unroll
     for (int ch = 0; ch < kSpan / 16; ch++) {
       uint4 w;
+      // column j of the row; with HALF, x holds the rotated (interleaved) order of
+      // a half-split row, whose column j is x[2j] (j < D/2) or x[2(j - D/2) + 1]
+      auto col = [&](int j) { return HALF ? x[j < D / 2 ? 2 * j : 2 * (j - D / 2) + 1] : x[j]; };
       if constexpr (ES == 4) {
         const int i = c0 + ch * 4;
-        w = make_uint4(__float_as_uint(x[i]), __float_as_uint(x[i + 1]), __float_as_uint(x[i + 2]),
-                       __float_as_uint(x[i + 3]));
+        w = make_uint4(__float_as_uint(col(i)), __float_as_uint(col(i + 1)), __float_as_uint(col(i + 2)),
+                       __float_as_uint(col(i + 3)));
       } else {
         const int i = c0 + ch * 8;
-        w = make_uint4(pack_bf16(x[i], x[i + 1]), pack_bf16(x[i + 2], x[i + 3]), pack_bf16(x[i + 4], x[i + 5]),
-                       pack_bf16(x[i + 6], x[i + 7]));
+        w = make_uint4(pack_bf16(col(i), col(i + 1)), pack_bf16(col(i + 2), col(i + 3)),
+                       pack_bf16(col(i + 4), col(i + 5)), pack_bf16(col(i + 6), col(i + 7)));
       }
       *reinterpret_cast<uint4*>(stg + swz(r, ch, kSpan)) = w;
     }
@@ -1213,10 +1228,17 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (g - 1) & 1, abort)))) break;
       // (the next item writes dS into this tile only after the stores have read it)
       const CUtensorMap* map = wg == 0 ? &a.map_dk : &a.map_dv;
-      ok = a.grad_fp32 ? stage_store<D, 4>(x, atom, map, r, stg_full + wg, stg_free + wg, boxes, it.kvh,
-                                           it.j * kTile, it.b, abort)
-                       : stage_store<D, 2>(x, atom, map, r, stg_full + wg, stg_free + wg, boxes, it.kvh,
-                                           it.j * kTile, it.b, abort);
+      // dK in the half-split layout: rotated pair i goes back to columns i, i + D/2
+      if (wg == 0 && a.rope_half)
+        ok = a.grad_fp32 ? stage_store<D, 4, true>(x, atom, map, r, stg_full + wg, stg_free + wg, boxes, it.kvh,
+                                                   it.j * kTile, it.b, abort)
+                         : stage_store<D, 2, true>(x, atom, map, r, stg_full + wg, stg_free + wg, boxes, it.kvh,
+                                                   it.j * kTile, it.b, abort);
+      else
+        ok = a.grad_fp32 ? stage_store<D, 4>(x, atom, map, r, stg_full + wg, stg_free + wg, boxes, it.kvh,
+                                             it.j * kTile, it.b, abort)
+                         : stage_store<D, 2>(x, atom, map, r, stg_full + wg, stg_free + wg, boxes, it.kvh,
+                                             it.j * kTile, it.b, abort);
     }
     if (ok && r == 0) bulk_wait<0>();
     if (!ok) record_timeout(a.status, abort);

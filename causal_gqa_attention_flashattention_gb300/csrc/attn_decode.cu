@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(256) k_kv_append(const KvAppendArgs a) {
     const uint32_t b = fdiv(bt, a.div_tn);
     const uint32_t t = bt - b * a.Tn;
     const int pos = a.pos0 + (int)t;
-    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(a.k) + it);
+    const uint4 kv = load_rope_chunk<D>(a.k + (size_t)row * D, c, a.rope_half != 0);
     const uint4 vv = __ldg(reinterpret_cast<const uint4*>(a.v) + it);
     float4 c0, c1;
     rope_coeffs<D>(a.rope, pos, c, c0, c1);
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(256) k_decode_q(const DecodeArgs a) {
       const int t = r / a.G, gg = r - t * a.G;
       const uint32_t b = bk / a.Hkv, g = bk - b * a.Hkv;
       const int h = (int)g * a.G + gg;
-      const uint4 qv = __ldg(reinterpret_cast<const uint4*>(a.q) + (((size_t)b * a.Tq + t) * a.Hq + h) * kCPR + c);
+      const uint4 qv = load_rope_chunk<D>(a.q + (((size_t)b * a.Tq + t) * a.Hq + h) * D, c, a.rope_half != 0);
       float4 c0, c1;
       rope_coeffs<D>(a.rope, a.Tkv - a.Tq + t, c, c0, c1);
       out = rope_chunk_f16(qv, c0, c1, nullptr);

@@ -487,7 +487,7 @@ __global__ void __launch_bounds__(256) k_rope_qk(const RopeArgs a) {
         const uint32_t row = x >> kShift;  // (b, t, h)
         const uint32_t bt = fdiv(row, isq ? a.div_hq : a.div_hkv);
         const uint32_t t = bt - fdiv(bt, a.div_t) * a.T;
-        v[u] = __ldg(reinterpret_cast<const uint4*>(isq ? a.q : a.k) + x);
+        v[u] = load_rope_chunk<D>((isq ? a.q : a.k) + (size_t)row * D, (int)(x & (kCPR - 1)), a.rope_half != 0);
         rope_coeffs<D>(a.rope, (int)t, (int)(x & (kCPR - 1)), c0[u], c1[u]);
       }
     }

@@ -19,6 +19,7 @@ constexpr int kFlagOFp32 = 1;      // o is float32
 constexpr int kFlagGradFp32 = 2;   // dq, dk, dv are float32
 constexpr int kFlagPreciseQK = 4;  // logits from hi + lo fp16 parts of rotated q and k
 constexpr int kFlagQKRotated = 8;  // backward: the workspace already holds the forward's rotated q and k
+constexpr int kFlagRopeHalf = 16;  // RoPE pairs (x[i], x[i + D/2]) instead of (x[2i], x[2i+1])
 
 // Largest number of query heads one forward CTA handles (TMEM/smem budget).
 inline int fwd_max_heads(int D, bool precise) { return D == 64 ? (precise ? 3 : 4) : 8; }
@@ -64,6 +65,7 @@ struct RopeArgs {
   __half *qr, *kr;
   const float2* rope;
   int B, T, Hq, Hkv;
+  int rope_half;  // half-split pair layout of q and k
   FastDiv div_hq, div_hkv, div_t;
 };
 
@@ -82,6 +84,7 @@ struct BwdArgs {
   int* status;
   int B, T, Hq, Hkv, D, G, nt, Tp;
   int grad_fp32;
+  int rope_half;  // dk leaves in the half-split pair layout
   float scale_log2, scale_log2_lo, scale;
 };
 
@@ -95,6 +98,7 @@ struct PrepArgs {
   const float2* rope;
   int B, T, Hq, Hkv, D, Tp, o_fp32;
   int rotate_qk;                            // 0: qr / kr already hold the rotated q and k
+  int rope_half;                            // half-split pair layout of q and k
   int negate;                               // 1: store -lse * log2(e) and -Delta (default-precision sweep)
   FastDiv div_hq, div_hkv, div_t, div_pad;  // by Hq, Hkv, T and Tp - T (pad rows; d = 1 if none)
 };
@@ -104,6 +108,7 @@ struct DqArgs {
   void* dq;            // [B, T, Hq, D]
   const float2* rope;
   int B, T, Hq, D, Tp, grad_fp32;
+  int rope_half;  // dq leaves in the half-split pair layout
   float scale;
   FastDiv div_hq, div_t;
 };
@@ -115,6 +120,7 @@ struct KvAppendArgs {
   __nv_bfloat16* vc;           // [B, Hkv, Tcap, D]
   const float2* rope;
   int B, Tn, Hkv, Tcap, pos0;
+  int rope_half;  // half-split pair layout of the new keys
   FastDiv div_hkv, div_tn;
 };
 
@@ -132,6 +138,7 @@ struct DecodeArgs {
   int* status;
   int B, Tq, Tkv, Hq, Hkv, D, G, R, ntk, nsplit, o_fp32;
   int F;                     // copies of the R query rows in the 128-row tile: 4 if R <= 32, 2 if R <= 64, else 1
+  int rope_half;             // half-split pair layout of q (and of the cached keys)
   float scale_log2;
 };
 

@@ -48,6 +48,21 @@ __device__ __forceinline__ uint4 rope_chunk_f16(uint4 x, const float4 cs01, cons
   return make_uint4(hi[0], hi[1], hi[2], hi[3]);
 }
 
+// Chunk c (pairs 4c..4c+3) of a bf16 row of D values, in the interleaved order
+// the rotation works on.  Interleaved rows store it as is.  In the half-split
+// layout pair i is (x[i], x[i + D/2]): the chunk gathers x[4c..4c+3] and
+// x[D/2 + 4c .. D/2 + 4c + 3] next to each other, so the rotated values come out
+// in the interleaved order of a feature permutation, which leaves every q . k
+// dot product unchanged.
+template <int D>
+__device__ __forceinline__ uint4 load_rope_chunk(const __nv_bfloat16* row, int c, bool half) {
+  if (!half) return __ldg(reinterpret_cast<const uint4*>(row) + c);
+  const uint2 x = __ldg(reinterpret_cast<const uint2*>(row + 4 * c));
+  const uint2 y = __ldg(reinterpret_cast<const uint2*>(row + D / 2 + 4 * c));
+  return make_uint4(__byte_perm(x.x, y.x, 0x5410), __byte_perm(x.x, y.x, 0x7632), __byte_perm(x.y, y.y, 0x5410),
+                    __byte_perm(x.y, y.y, 0x7632));
+}
+
 // Loads the (cos, sin) entries for pairs 4c..4c+3 of position `pos`.
 template <int D>
 __device__ __forceinline__ void rope_coeffs(const float2* tab, int pos, int chunk, float4& a, float4& b) {

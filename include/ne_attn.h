@@ -76,6 +76,13 @@ typedef enum {
                                 rope_base, so the backward does not rotate them again (the
                                 forward's workspace is laid out as the start of the backward's).
                                 Rejected with NE_ATTN_PRECISE_QK and by ne_attn_bwd_noalloc. */
+#define NE_ATTN_ROPE_HALF 16 /* rotary pairs (x[i], x[i + D/2]) (the half-split layout) instead
+                                of the interleaved (x[2i], x[2i+1]); same angles t * base^(-2i/D)
+                                for pair i.  The pages name no pair layout.  Accepted by the
+                                forward, the backward (both calls of a step must agree, as with
+                                NE_ATTN_QK_ROTATED), ne_attn_kv_append and ne_attn_decode (the
+                                cache and the queries must agree); not with NE_ATTN_PRECISE_QK
+                                (NE_ERR_UNSUPPORTED). */
 
 /*
  * Forward pass: writes o (bfloat16) and lse.  Same as ne_attn_fwd_ex with
@@ -187,10 +194,13 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
  * ne_attn_kv_append writes positions pos0 .. pos0 + Tn - 1 of both caches from
  * the new keys and values k_new, v_new [B, Tn, Hkv, D] (bfloat16): each key is
  * rotated at its position and stored as fp16, each value copied.  Requires
- * Tn >= 1, pos0 >= 0, pos0 + Tn <= Tcap.  One streaming kernel.
+ * Tn >= 1, pos0 >= 0, pos0 + Tn <= Tcap.  flags: NE_ATTN_ROPE_HALF or 0.  With
+ * NE_ATTN_ROPE_HALF the cached keys hold the rotation in a feature order of the
+ * library's own, which only ne_attn_decode with the same flag reads.  One
+ * streaming kernel.
  */
 int ne_attn_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache, int B, int Tn,
-                      int pos0, int Tcap, int Hkv, int D, float rope_base, void* stream);
+                      int pos0, int Tcap, int Hkv, int D, float rope_base, int flags, void* stream);
 
 /*
  * Bytes of device workspace ne_attn_decode needs (pass a 256-byte aligned
@@ -203,8 +213,9 @@ size_t ne_attn_decode_workspace_size(int B, int Tq, int Tkv, int Hq, int Hkv, in
 /*
  * Decode attention: q [B, Tq, Hq, D] (bfloat16, not rotated; rotated here at
  * positions Tkv - Tq + t) against cache positions 0 .. Tkv - 1.  Writes
- * o [B, Tq, Hq, D] (bfloat16, or float32 with NE_ATTN_O_FP32, the only flag)
- * and lse [B, Hq, Tq].  Requires 1 <= Tq <= Tkv <= Tcap and
+ * o [B, Tq, Hq, D] (bfloat16, or float32 with NE_ATTN_O_FP32)
+ * and lse [B, Hq, Tq] (flags: NE_ATTN_O_FP32, NE_ATTN_ROPE_HALF as given to
+ * ne_attn_kv_append).  Requires 1 <= Tq <= Tkv <= Tcap and
  * (Hq / Hkv) * Tq <= 128: the queries of one key/value head fill at most one
  * 128-row tile, which every K/V tile of the cache serves at once.  The
  * workspace is required.

@@ -40,7 +40,7 @@ def test_workspace_size(libne):
     assert libne.ne_attn_bwd_workspace_size(1, 77, 4, 2, 32, 0) >= 4 * 4 * 128 * 32  # padded to 128 rows
     assert libne.ne_attn_bwd_workspace_size(1, 16, 3, 2, 64, 0) == 0
     assert libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 48, 0) == 0
-    assert libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 64, 16) == 0  # unknown flag
+    assert libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 64, 32) == 0  # unknown flag
     assert libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 64, 8) == libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 64, 0)
     assert libne.ne_attn_bwd_workspace_size(1, 16, 2, 1, 64, 8 | 4) == 0  # reuse needs default precision
 
@@ -72,7 +72,7 @@ def test_host_argument_checks(libne):
     assert libne.ne_attn_fwd_ex(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 2, null, 0, null) == -1  # grad flag on fwd
     assert libne.ne_attn_fwd_ex(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 0, p, 16, null) == -5  # workspace too small
     assert libne.ne_attn_fwd_ex(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 0, mis, 1 << 20, null) == -5  # misaligned
-    assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 16, p, 4096, null) == -1
+    assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 32, p, 4096, null) == -1  # unknown flag
     assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 8 | 4, p, 1 << 20, null) == -1
     assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 0, p, 16, null) == -5
     assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 0, mis, 1 << 20, null) == -5
@@ -100,13 +100,13 @@ def test_decode_host_argument_checks(libne):
     p = ctypes.c_void_p(base)
     mis = ctypes.c_void_p(base + 2)
     null = None
-    # ne_attn_kv_append(k_new, v_new, k_cache, v_cache, B, Tn, pos0, Tcap, Hkv, D, base, stream)
-    assert libne.ne_attn_kv_append(null, p, p, p, 1, 4, 0, 8, 2, 64, 10000.0, null) == -1
-    assert libne.ne_attn_kv_append(p, p, p, p, 1, 4, 5, 8, 2, 64, 10000.0, null) == -1   # past the capacity
-    assert libne.ne_attn_kv_append(p, p, p, p, 1, 0, 0, 8, 2, 64, 10000.0, null) == -1   # nothing to append
-    assert libne.ne_attn_kv_append(p, p, p, p, 1, 4, -1, 8, 2, 64, 10000.0, null) == -1
-    assert libne.ne_attn_kv_append(p, p, mis, p, 1, 4, 0, 8, 2, 64, 10000.0, null) == -2
-    assert libne.ne_attn_kv_append(p, p, p, p, 1, 4, 0, 8, 2, 48, 10000.0, null) == -3
+    # ne_attn_kv_append(k_new, v_new, k_cache, v_cache, B, Tn, pos0, Tcap, Hkv, D, base, flags, stream)
+    assert libne.ne_attn_kv_append(null, p, p, p, 1, 4, 0, 8, 2, 64, 10000.0, 0, null) == -1
+    assert libne.ne_attn_kv_append(p, p, p, p, 1, 4, 5, 8, 2, 64, 10000.0, 0, null) == -1   # past the capacity
+    assert libne.ne_attn_kv_append(p, p, p, p, 1, 0, 0, 8, 2, 64, 10000.0, 0, null) == -1   # nothing to append
+    assert libne.ne_attn_kv_append(p, p, p, p, 1, 4, -1, 8, 2, 64, 10000.0, 0, null) == -1
+    assert libne.ne_attn_kv_append(p, p, mis, p, 1, 4, 0, 8, 2, 64, 10000.0, 0, null) == -2
+    assert libne.ne_attn_kv_append(p, p, p, p, 1, 4, 0, 8, 2, 48, 10000.0, 0, null) == -3
     # ne_attn_decode(q, kc, vc, o, lse, B, Tq, Tkv, Tcap, Hq, Hkv, D, base, flags, ws, ws_bytes, stream)
     ok = (1, 1, 10, 16, 4, 2, 64, 10000.0)
     assert libne.ne_attn_decode(p, p, p, p, p, *ok, 0, p, 4096, null) == -5  # workspace too small
@@ -118,4 +118,23 @@ def test_decode_host_argument_checks(libne):
     assert libne.ne_attn_decode(p, p, p, p, p, 1, 1, 10, 9, 4, 2, 64, 10000.0, 0, p, 1 << 20, null) == -1  # Tkv > Tcap
     assert libne.ne_attn_decode(p, p, p, p, p, 1, 65, 100, 100, 4, 2, 64, 10000.0, 0, p, 1 << 20, null) == -3  # 130 rows
     assert libne.ne_attn_decode(p, p, p, mis, p, *ok, 0, p, 1 << 20, null) == -2
+    assert libne.ne_attn_kv_append(p, p, p, p, 1, 4, 0, 8, 2, 64, 10000.0, 1, null) == -1  # only the layout flag
+    assert libne.ne_attn_decode(p, p, p, p, p, *ok, 16, p, 4096, null) == -5  # layout flag accepted (then workspace)
+
+
+def test_half_split_flag_rules(libne):
+    buf = ctypes.create_string_buffer(4096 + 512)
+    p = ctypes.c_void_p((ctypes.addressof(buf) + 255) // 256 * 256)
+    null = None
+    B, T, Hq, Hkv, D = 2, 200, 4, 2, 64
+    assert libne.ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, 16) == libne.ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, 0)
+    assert libne.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, D, 16) == libne.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, D, 0)
+    assert libne.ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, 16 | 4) == 0  # not with split precision
+    assert libne.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, D, 16 | 4) == 0
+    assert libne.ne_attn_fwd_ex(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 16 | 4, null, 0, null) == -3
+    assert libne.ne_attn_bwd(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 16 | 4, p, 1 << 20, null) == -3
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    libne.ne_attn_bwd_noalloc.argtypes = [vp] * 9 + [i] * 5 + [f, i, vp]
+    libne.ne_attn_bwd_noalloc.restype = i
+    assert libne.ne_attn_bwd_noalloc(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 16 | 4, null) == -3
 

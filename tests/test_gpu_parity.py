@@ -266,7 +266,7 @@ DECODE_SHAPES = [
 ]
 
 
-def decode_case(nb, oracle_mod, shape, o_dtype=None, seed=700):
+def decode_case(nb, oracle_mod, shape, o_dtype=None, seed=700, half=False):
     B, Tkv, Tq, Hq, Hkv, D = shape
     x = H.make(B, Tkv, Hq, Hkv, D, seed=seed + Tkv)
     q_new = H.to_device(x["q_bits"][:, Tkv - Tq:])
@@ -275,13 +275,13 @@ def decode_case(nb, oracle_mod, shape, o_dtype=None, seed=700):
     kc, vc = nb.kv_cache(B, Tcap, Hkv, D, "cuda")
     cut = Tkv - Tq  # the context first, then the new positions
     if cut > 0:
-        nb.kv_append(k[:, :cut].contiguous(), v[:, :cut].contiguous(), kc, vc, 0)
-    nb.kv_append(k[:, cut:].contiguous(), v[:, cut:].contiguous(), kc, vc, cut)
-    o, lse = nb.attn_decode(q_new, kc, vc, Tkv, o_dtype=o_dtype or torch.bfloat16)
-    o2, lse2 = nb.attn_decode(q_new, kc, vc, Tkv, o_dtype=o_dtype or torch.bfloat16)
+        nb.kv_append(k[:, :cut].contiguous(), v[:, :cut].contiguous(), kc, vc, 0, rope_half=half)
+    nb.kv_append(k[:, cut:].contiguous(), v[:, cut:].contiguous(), kc, vc, cut, rope_half=half)
+    o, lse = nb.attn_decode(q_new, kc, vc, Tkv, o_dtype=o_dtype or torch.bfloat16, rope_half=half)
+    o2, lse2 = nb.attn_decode(q_new, kc, vc, Tkv, o_dtype=o_dtype or torch.bfloat16, rope_half=half)
     nb.check_status()
     assert torch.equal(o, o2) and torch.equal(lse, lse2), "decode is not bitwise reproducible"
-    ro, rl = oracle_mod.decode_fwd(x["q"][:, Tkv - Tq:], x["k"], x["v"], inputs.ROPE_BASE)
+    ro, rl = oracle_mod.decode_fwd(x["q"][:, Tkv - Tq:], x["k"], x["v"], inputs.ROPE_BASE, half=half)
     go = H.to_f64(o)
     assert np.isfinite(go).all()
     eo = H.errors(go, ro)
@@ -320,4 +320,45 @@ def test_decode_rejects_oversized_query_tile(nb):
     with pytest.raises(nb.NeAttnError) as e:
         nb.attn_decode(q, kc, vc, 40, workspace=torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
     assert e.value.status == -3
+
+
+# ---------------------------------------------------------------- half-split RoPE pair layout
+HALF_SHAPES = [(2, 200, 4, 2, 64), (1, 130, 6, 3, 32), (2, 384, 12, 4, 64)]
+
+
+@pytest.mark.parametrize("shape", HALF_SHAPES)
+@pytest.mark.parametrize("reuse", [False, True])
+def test_half_split_layout_parity(nb, oracle_mod, shape, reuse):
+    """NE_ATTN_ROPE_HALF: pairs (x[i], x[i + D/2]) through the forward and the
+    backward (with and without the backward reusing the forward's rotation)."""
+    B, T, Hq, Hkv, D = shape
+    x = H.make(B, T, Hq, Hkv, D, seed=811 + T)
+    q, k, v, do = (H.to_device(x[n + "_bits"]) for n in ("q", "k", "v", "dout"))
+    ws = nb.alloc_workspace(B, T, Hq, Hkv, D) if reuse else None
+    o, lse = nb.attn_fwd(q, k, v, inputs.ROPE_BASE, workspace=ws, rope_half=True)
+    dq, dk, dv = nb.attn_bwd(q, k, v, o, lse, do, inputs.ROPE_BASE, grad_dtype=torch.float32, workspace=ws,
+                             qk_rotated=reuse, rope_half=True)
+    nb.check_status()
+    ref = oracle_mod.attn_bwd(x["q"], x["k"], x["v"], x["dout"], inputs.ROPE_BASE, half=True)
+    gpu = dict(o=H.to_f64(o), dq=H.to_f64(dq), dk=H.to_f64(dk), dv=H.to_f64(dv))
+    rep = {n: H.errors(gpu[n], ref[n]) for n in gpu}
+    rep["lse"] = H.errors(lse.cpu().numpy().astype(np.float64), ref["lse"])
+    print("HALF", shape, reuse, {n: ("%.2e" % a, "%.2e" % b) for n, (a, b) in rep.items()})
+    bad = [n for n in ("o", "dq", "dk", "dv") if rep[n][0] > H.REL_L2_TOL or rep[n][1] > H.MAX_ABS_TOL]
+    assert not bad and rep["lse"][1] <= H.LSE_ABS_TOL, rep
+
+
+def test_half_split_layout_changes_the_result(nb):
+    """The flag is not a no-op: the two layouts give different attention for D > 2."""
+    B, T, Hq, Hkv, D = 1, 256, 2, 1, 64
+    x = H.make(B, T, Hq, Hkv, D, seed=5)
+    q, k, v = (H.to_device(x[n + "_bits"]) for n in ("q", "k", "v"))
+    o1, _ = nb.attn_fwd(q, k, v)
+    o2, _ = nb.attn_fwd(q, k, v, rope_half=True)
+    assert (o1.float() - o2.float()).abs().max().item() > 1e-2
+
+
+@pytest.mark.parametrize("shape", [(2, 300, 1, 4, 2, 64), (1, 257, 16, 16, 2, 32)])
+def test_decode_half_split_layout(nb, oracle_mod, shape):
+    decode_case(nb, oracle_mod, shape, half=True)
 

@@ -86,3 +86,33 @@ def make_workload_inputs(name, seed=None):
 def workload_shape(name):
     B, T, Hq, Hkv, D, _ = WORKLOADS[name]
     return dict(B=B, T=T, Hq=Hq, Hkv=Hkv, D=D)
+
+
+# name -> (B, T, C, Hq, Hkv, D): the step in front of attention (RMSNorm and the
+# Q/K/V projection) at the models' widths (socker-news README, "Configuration").
+PROLOGUE_WORKLOADS = {
+    "tiny_cpu_model": (2, 128, 128, 4, 2, 32),
+    "gpu_116m_model": (16, 512, 768, 12, 4, 64),
+}
+
+
+def make_prologue_inputs(B, T, C, Hq, Hkv, D, seed):
+    """Draw the inputs of RMSNorm + the fused Q/K/V projection.
+
+    x ~ N(0, 1) [B, T, C] (a residual stream of unit scale); the norm weight
+    ~ 1 + 0.1 N(0, 1) [C] (near its initial value of one); the projection
+    w_qkv ~ N(0, 1) / sqrt(C) [(Hq + 2 Hkv) D, C], so the projected q, k, v
+    are of unit scale like the attention workloads' inputs.  All rounded to
+    bf16.  Returns "<name>_bits" and "<name>" (exact fp64) for x, norm_w, w_qkv.
+    """
+    rng = np.random.default_rng(seed)
+    N = (Hq + 2 * Hkv) * D
+    x = rng.standard_normal((B, T, C), dtype=np.float32)
+    w = (1.0 + 0.1 * rng.standard_normal(C)).astype(np.float32)
+    W = (rng.standard_normal((N, C), dtype=np.float32) / np.float32(np.sqrt(C))).astype(np.float32)
+    out = {}
+    for name, arr in (("x", x), ("norm_w", w), ("w_qkv", W)):
+        bits = bf16_round_bits(arr)
+        out[name + "_bits"] = bits
+        out[name] = bf16_bits_to_f64(bits)
+    return out

@@ -1,14 +1,17 @@
-"""fp64 CPU oracle for causal GQA attention with RoPE on Q/K.
+"""fp64 CPU oracle for causal GQA attention with RoPE on Q/K, and for the
+RMSNorm + Q/K/V projection step that feeds it.
 
 TEST INFRASTRUCTURE ONLY: the test-suite, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package; the product path
 (the CUDA library and its Python binding) never does, and this package never
 imports the product package.
 
-The arithmetic lives in ``attn_oracle.c`` (plain C, double precision, OpenMP
-over rows); this module only compiles it with gcc and marshals numpy arrays.
-See that file's header for the passages of the NanoEuler pages each step
-follows and for the readings taken where the pages are silent.
+The attention arithmetic lives in ``attn_oracle.c`` (plain C, double
+precision, OpenMP over rows); this module compiles it with gcc and marshals
+numpy arrays.  The RMSNorm + projection step (``qkv_rmsnorm``) is written here
+in float64 numpy, with one library matrix product.  The header of
+``attn_oracle.c`` and the docstrings below name the passages of the NanoEuler
+pages each step follows and the readings taken where the pages are silent.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` (brute force in a
 second formulation, closed forms, invariants and central finite differences);
@@ -164,3 +167,33 @@ def attn_bwd(q, k, v, dout, base=10000.0, groups=None, nthreads=0, half=False):
                             ctypes.POINTER(ctypes.c_ubyte)), int(nthreads))
     return dict(dq=dq, dk=dk, dv=dv, o=o, lse=lse, delta=delta)
 
+
+
+def qkv_rmsnorm(x, norm_w, w_qkv, Hq, Hkv, D, eps=1e-5):
+    """The step in front of attention: RMSNorm, then the fused Q/K/V projection.
+
+    Each NanoEuler block computes x + attn(rmsnorm(x)) with a pre-norm
+    RMSNorm and no bias anywhere (socker-news README, "Architecture" and
+    "Block structure order"; mynewscn README, architecture list).  The pages
+    name RMSNorm without writing it out; its definition (Zhang and Sennrich,
+    "Root Mean Square Layer Normalization", 2019) is
+        rstd_r = 1 / sqrt(mean_c x[r, c]^2 + eps),   xn[r, c] = x[r, c] * rstd_r * w[c].
+    The projection is one matrix for all three (read here as rows
+    [Hq*D query features | Hkv*D key features | Hkv*D value features] of
+    w_qkv [N, C], the output-by-input layout), qkv = xn W^T, without bias.
+    The rotary embedding is not part of this step: attn_fwd applies it.
+
+    x [B, T, C], norm_w [C], w_qkv [(Hq + 2 Hkv) D, C], all taken exactly as
+    float64.  Returns (q [B,T,Hq,D], k [B,T,Hkv,D], v [B,T,Hkv,D], rstd [B,T]).
+    """
+    x, w, W = _f64(x), _f64(norm_w), _f64(w_qkv)
+    B, T, C = x.shape
+    N = (Hq + 2 * Hkv) * D
+    assert w.shape == (C,) and W.shape == (N, C)
+    rstd = 1.0 / np.sqrt(np.mean(x * x, axis=-1) + float(eps))
+    xn = x * rstd[..., None] * w
+    qkv = xn.reshape(B * T, C) @ W.T
+    q = qkv[:, :Hq * D].reshape(B, T, Hq, D)
+    k = qkv[:, Hq * D:(Hq + Hkv) * D].reshape(B, T, Hkv, D)
+    v = qkv[:, (Hq + Hkv) * D:].reshape(B, T, Hkv, D)
+    return q.copy(), k.copy(), v.copy(), rstd

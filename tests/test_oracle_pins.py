@@ -351,3 +351,79 @@ def test_bf16_rounding_and_recipe():
     b = inputs.make_shape_inputs(1, 64, 2, 1, 16, seed=5, recipe="stress")
     np.testing.assert_array_equal(a["q_bits"], b["q_bits"])
     assert np.max(np.abs(a["q"])) > 16.0  # outlier rows present at this size
+
+
+# ---------------------------------------------------------------- RMSNorm + Q/K/V projection
+def _stack_proj(*blocks):
+    return np.concatenate(blocks, axis=0)
+
+
+def test_rmsnorm_worked_example(oracle_mod):
+    # x = (3, 4): mean of squares (9 + 16) / 2 = 12.5, so with w = 1 and eps = 0
+    # the normalised row is (3, 4) / sqrt(12.5) = (0.848528137423857, 1.131370849898476).
+    # Projection rows [I; 2 I; -I] read it back as q = xn, k = 2 xn, v = -xn.
+    x = np.array([[[3.0, 4.0]]])
+    I = np.eye(2)
+    W = _stack_proj(I, 2 * I, -I)
+    q, k, v, rstd = oracle_mod.qkv_rmsnorm(x, np.ones(2), W, Hq=1, Hkv=1, D=2, eps=0.0)
+    xn = np.array([0.8485281374238571, 1.1313708498984762])
+    np.testing.assert_allclose(rstd[0, 0], 0.28284271247461906, rtol=1e-15)  # 1 / sqrt(12.5)
+    np.testing.assert_allclose(q[0, 0, 0], xn, rtol=1e-15)
+    np.testing.assert_allclose(k[0, 0, 0], 2 * xn, rtol=1e-15)
+    np.testing.assert_allclose(v[0, 0, 0], -xn, rtol=1e-15)
+    # eps adds to the mean of squares: 1 / sqrt(12.5 + 0.5) = 1 / sqrt(13)
+    _, _, _, r2 = oracle_mod.qkv_rmsnorm(x, np.ones(2), W, Hq=1, Hkv=1, D=2, eps=0.5)
+    np.testing.assert_allclose(r2[0, 0], 0.2773500981126146, rtol=1e-15)
+    # the norm weight scales feature c before the projection: w = (2, -1)
+    q3, _, _, _ = oracle_mod.qkv_rmsnorm(x, np.array([2.0, -1.0]), W, Hq=1, Hkv=1, D=2, eps=0.0)
+    np.testing.assert_allclose(q3[0, 0, 0], [2 * xn[0], -xn[1]], rtol=1e-15)
+
+
+def test_rmsnorm_unit_rms_and_scale_invariance(oracle_mod):
+    # with w = 1, eps = 0 and the identity projection (N = C = 16), the
+    # concatenated q | k | v of a row is the normalised row: mean square 1,
+    # and scaling the row by any positive factor changes nothing.
+    B, T, C, Hq, Hkv, D = 2, 5, 16, 2, 1, 4
+    x = rnd((B, T, C), 31)
+    q, k, v, _ = oracle_mod.qkv_rmsnorm(x, np.ones(C), np.eye(C), Hq, Hkv, D, eps=0.0)
+    cat = np.concatenate([q.reshape(B, T, -1), k.reshape(B, T, -1), v.reshape(B, T, -1)], axis=-1)
+    np.testing.assert_allclose(np.mean(cat * cat, axis=-1), 1.0, rtol=1e-14)
+    q2, k2, v2, _ = oracle_mod.qkv_rmsnorm(7.25 * x, np.ones(C), np.eye(C), Hq, Hkv, D, eps=0.0)
+    np.testing.assert_allclose(q2, q, rtol=1e-13)
+    np.testing.assert_allclose(v2, v, rtol=1e-13)
+    # a zero row stays zero and its rstd is 1 / sqrt(eps)
+    x[0, 0] = 0.0
+    q3, _, _, r3 = oracle_mod.qkv_rmsnorm(x, np.ones(C), np.eye(C), Hq, Hkv, D, eps=1e-4)
+    assert np.all(q3[0, 0] == 0.0) and abs(r3[0, 0] - 100.0) < 1e-12
+
+
+def test_projection_one_hot_rows_and_head_order(oracle_mod):
+    # A row with one non-zero entry s at column c has mean square s^2 / C, so
+    # (eps = 0) it normalises to sign(s) sqrt(C) w_c e_c and projects onto
+    # sign(s) sqrt(C) w_c W[:, c]; the first Hq*D rows of W are the query
+    # features (head h at rows h*D ..), then Hkv*D key rows, then the values.
+    B, T, C, Hq, Hkv, D = 1, 3, 12, 3, 1, 2
+    N = (Hq + 2 * Hkv) * D
+    W = rnd((N, C), 32)
+    w = 1.0 + 0.1 * rnd((C,), 33)
+    x = np.zeros((B, T, C))
+    cols, vals = [4, 0, 11], [-2.5, 0.75, 3.0]
+    for t in range(T):
+        x[0, t, cols[t]] = vals[t]
+    q, k, v, rstd = oracle_mod.qkv_rmsnorm(x, w, W, Hq, Hkv, D, eps=0.0)
+    for t in range(T):
+        c, s = cols[t], vals[t]
+        col = np.sign(s) * np.sqrt(C) * w[c] * W[:, c]
+        np.testing.assert_allclose(rstd[0, t], np.sqrt(C) / abs(s), rtol=1e-15)
+        for h in range(Hq):
+            np.testing.assert_allclose(q[0, t, h], col[h * D:(h + 1) * D], rtol=1e-13)
+        np.testing.assert_allclose(k[0, t, 0], col[Hq * D:(Hq + 1) * D], rtol=1e-13)
+        np.testing.assert_allclose(v[0, t, 0], col[(Hq + 1) * D:], rtol=1e-13)
+
+
+def test_prologue_inputs_recipe():
+    a = inputs.make_prologue_inputs(2, 16, 64, 4, 2, 8, seed=3)
+    b = inputs.make_prologue_inputs(2, 16, 64, 4, 2, 8, seed=3)
+    np.testing.assert_array_equal(a["w_qkv_bits"], b["w_qkv_bits"])
+    assert a["w_qkv"].shape == ((4 + 2 * 2) * 8, 64) and a["norm_w"].shape == (64,)
+    assert 0.5 < np.std(a["w_qkv"]) * np.sqrt(64) < 1.5 and abs(np.mean(a["norm_w"]) - 1.0) < 0.1

@@ -488,6 +488,112 @@ def run_decode(args):
     return 0
 
 
+def run_prologue(args):
+    """One JSON line for the step in front of attention: RMSNorm + the fused
+    Q/K/V projection at the 116M model's width (ne_attn_qkv_rmsnorm writing
+    v and the rotated q, k into the attention workspace, as a block runs it).
+
+    Metric: projection TFLOP/s (2 * B*T * C * N per call).  Seeded inputs
+    (x ~ N(0,1), norm weight ~ 1 + 0.1 N(0,1), projection ~ N(0,1)/sqrt(C))
+    rotate through enough sets that their total exceeds L2; the timed region
+    replays a CUDA graph of calls.
+    """
+    import numpy as np
+    import torch
+    import oracle
+    from causal_gqa_attention_flashattention_gb300 import binding
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(dev)
+    name = "gpu_116m_model"
+    B, T, C, Hq, Hkv, D = inputs.PROLOGUE_WORKLOADS[name]
+    M, N = B * T, (Hq + 2 * Hkv) * D
+    flops = 2.0 * M * C * N
+    x = inputs.make_prologue_inputs(B, T, C, Hq, Hkv, D, seed=21)
+
+    def dev_bf16(bits):
+        return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+
+    ws_bytes = binding.qkv_workspace_size(B, T, C, Hq, Hkv, D, rotated=True)
+    set_bytes = 2 * (M * C + C + N * C) + ws_bytes + 2 * M * Hkv * D + 4 * M
+    nsets = max(2, min(16, -(-2 * 129 * 2 ** 20 // set_bytes)))
+    sets = []
+    for i in range(nsets):
+        sets.append(dict(x=dev_bf16(x["x_bits"]), w=dev_bf16(x["norm_w_bits"]), W=dev_bf16(x["w_qkv_bits"]),
+                         v=torch.empty((B, T, Hkv, D), dtype=torch.bfloat16, device=dev),
+                         rstd=torch.empty((B, T), dtype=torch.float32, device=dev),
+                         ws=torch.empty(ws_bytes, dtype=torch.uint8, device=dev)))
+
+    def call(st):
+        binding.qkv_rmsnorm(st["x"], st["w"], st["W"], Hq, Hkv, D, rotated=True, write_qk=False, v=st["v"],
+                            rstd=st["rstd"], workspace=st["ws"], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for st in sets:
+                call(st)
+    binding.check_status(stream)
+    binding.profile_start(2 * nsets + 4)
+    g_prof = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_prof, stream=stream):
+        for st in sets:
+            call(st)
+    prof_cap = binding.profile_stop_deferred()
+    g_all = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_all, stream=stream):
+        for st in sets:
+            call(st)
+    reps = max(1, args.steps // nsets)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g_all.replay()
+        torch.cuda.synchronize(dev)
+        clocks = ClockSampler(0)
+        clocks.start()
+        e0.record(stream)
+        for _ in range(reps):
+            g_all.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        clk = clocks.stop()
+        binding.check_status(stream)
+        for _ in range(3):
+            g_prof.replay()
+    torch.cuda.synchronize(dev)
+    prof = binding.profile_read(prof_cap)
+    ms_call = e0.elapsed_time(e1) / (reps * nsets)
+    ms_gemm = prof["qkv"][0] / max(1, prof["qkv"][1])
+    achieved = flops / (ms_gemm * 1e-3) / 1e12
+    tr = traffic_record("k_qkv_gemm")
+    cpu = None
+    if not args.no_cpu_baseline:
+        rows = 2048
+        t0 = time.perf_counter()
+        oracle.qkv_rmsnorm(x["x"].reshape(M, 1, C)[:rows], x["norm_w"], x["w_qkv"], Hq, Hkv, D)
+        dt = time.perf_counter() - t0
+        cpu = dict(value=2.0 * rows * C * N / dt / 1e12, unit="TFLOP/s", cores=os.cpu_count(), kind="oracle",
+                   sample="%d of %d rows (fp64 numpy RMSNorm + projection, %.2f s)" % (rows, M, dt))
+    line = dict(metric="RMSNorm + fused Q/K/V projection with the rotary epilogue: projection TFLOP/s",
+                value=flops / (ms_call * 1e-3) / 1e12, unit="TFLOP/s", n_gpus=1, steps=reps * nsets,
+                warmup=args.warmup, ms_per_step=ms_call, higher_is_better=True, scaling="weak", vs_baseline=None,
+                dtype="bf16 operands, fp32 accumulate", data="synthetic",
+                config=dict(workload=name, B=B, T=T, C=C, Hq=Hq, Hkv=Hkv, D=D, N=N, input_sets=nsets,
+                            l2="%d rotating input/output sets of %.1f MB" % (nsets, set_bytes / 1e6),
+                            outputs="v (bf16) and the rotated q, k (fp16) in the attention workspace",
+                            launch="CUDA graph replay (2 library kernels per call)"),
+                tokens_per_s=M / (ms_call * 1e-3),
+                roofline=dict(bound="tensor", achieved=achieved, peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                              frac=achieved / peaks["bf16_tflops"], kernel="qkv",
+                              traffic=(tr["dram_bytes_per_launch"] if tr else None),
+                              peak_source="%s bf16 (burst)" % peaks["source"], per_launch_us=ms_gemm * 1e3,
+                              kernels={k: dict(us_per_launch=v[0] / v[1] * 1e3, launches=v[1])
+                                       for k, v in prof.items() if v[1]}),
+                cpu_baseline=cpu, gpu_launches=2 * reps * nsets, clocks=clk)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -500,11 +606,15 @@ def main():
                     help="measure decode with a KV cache (one JSON line per decode workload) instead")
     ap.add_argument("--decode-workload", default=None, choices=sorted(DECODE_WORKLOADS),
                     help="with --decode: only this workload")
+    ap.add_argument("--prologue", action="store_true",
+                    help="measure RMSNorm + the fused Q/K/V projection (one JSON line) instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.decode:
         return run_decode(args)
+    if args.prologue:
+        return run_prologue(args)
     world, rank, local = dist_init()
     if args.impl == "reference":
         return run_reference(args, world, rank)

@@ -67,6 +67,10 @@ def lib():
         L.ne_attn_decode_workspace_size.restype = sz
         L.ne_attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, sz, vp]
         L.ne_attn_decode.restype = i
+        L.ne_attn_qkv_workspace_size.argtypes = [i, i, i, i, i, i, i]
+        L.ne_attn_qkv_workspace_size.restype = sz
+        L.ne_attn_qkv_rmsnorm.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, i, vp, sz, vp]
+        L.ne_attn_qkv_rmsnorm.restype = i
         _lib = L
     return _lib
 
@@ -82,7 +86,7 @@ def _check(fn, st):
 
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr())
+    return ctypes.c_void_p(None if t is None else t.data_ptr())
 
 
 def _shape(q, k):
@@ -96,30 +100,40 @@ def fwd_workspace_size(B, T, Hq, Hkv, D, precise=False):
 
 
 def attn_fwd(q, k, v, rope_base=10000.0, o=None, lse=None, o_dtype=torch.bfloat16, precise=False,
-             workspace=None, rope_half=False, stream=None):
+             workspace=None, rope_half=False, qk_rotated=False, Hq=None, stream=None):
     """o, lse = causal GQA attention of q [B,T,Hq,D], k/v [B,T,Hkv,D] (bf16, CUDA).
 
     o_dtype: bfloat16 or float32.  precise: hi+lo split of the rotated q, k
     for the logits (NE_ATTN_PRECISE_QK).  workspace: a uint8 CUDA tensor of at
     least fwd_workspace_size bytes (the rotated fp16 q, k land there); if None
-    one is allocated for the call.
+    one is allocated for the call.  qk_rotated: `workspace` already holds the
+    rotated q and k (written by qkv_rmsnorm with rotated=True); q and k may
+    then be None, with the number of query heads given as Hq.
     """
-    B, T, Hq, Hkv, D = _shape(q, k)
+    if qk_rotated and workspace is None:
+        raise ValueError("qk_rotated needs the workspace that holds the rotated q and k")
+    if q is None:
+        if not qk_rotated or Hq is None:
+            raise ValueError("q may be None only with qk_rotated and Hq")
+        B, T, Hkv, D = v.shape
+    else:
+        B, T, Hq, Hkv, D = _shape(q, k)
     if o is None:
-        o = torch.empty(q.shape, dtype=o_dtype, device=q.device)
+        o = torch.empty((B, T, Hq, D), dtype=o_dtype, device=v.device)
     if lse is None:
         # precise mode stores the LSE and its fp32 remainder: lse[0] is the LSE
         shape = (2, B, Hq, T) if precise else (B, Hq, T)
-        lse = torch.empty(shape, dtype=torch.float32, device=q.device)
-    assert lse.numel() == (2 if precise else 1) * B * Hq * T
+        lse = torch.empty(shape, dtype=torch.float32, device=v.device)
+    assert lse.numel() == (2 if precise else 1) * B * Hq * T and o.shape == (B, T, Hq, D)
     for t in (q, k, v):
-        assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous()
+        assert t is None or (t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous())
     assert o.dtype in (torch.bfloat16, torch.float32) and o.is_contiguous()
     assert lse.dtype == torch.float32 and lse.is_contiguous()
-    flags = (O_FP32 if o.dtype == torch.float32 else 0) | (PRECISE_QK if precise else 0) | (ROPE_HALF if rope_half else 0)
+    flags = ((O_FP32 if o.dtype == torch.float32 else 0) | (PRECISE_QK if precise else 0)
+             | (ROPE_HALF if rope_half else 0) | (QK_ROTATED if qk_rotated else 0))
     if workspace is None:
         n = fwd_workspace_size(B, T, Hq, Hkv, D, precise)
-        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=v.device)
     assert workspace.dtype == torch.uint8 and workspace.is_cuda
     _check("ne_attn_fwd_ex", lib().ne_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                                   B, T, Hq, Hkv, D, float(rope_base), flags,
@@ -148,19 +162,22 @@ def attn_bwd(q, k, v, o, lse, dout, rope_base=10000.0, grad_dtype=torch.bfloat16
     """
     if qk_rotated and workspace is None:
         raise ValueError("qk_rotated needs the workspace the forward wrote")
-    B, T, Hq, Hkv, D = _shape(q, k)
+    if (q is None or k is None) and not qk_rotated:
+        raise ValueError("q and k may be None only with qk_rotated")
+    B, T, Hq, D = dout.shape
+    Hkv = v.shape[2]
     if grad_dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("grad_dtype must be bfloat16 or float32")
     if dq is None:
-        dq = torch.empty(q.shape, dtype=grad_dtype, device=q.device)
+        dq = torch.empty(dout.shape, dtype=grad_dtype, device=v.device)
     if dk is None:
-        dk = torch.empty(k.shape, dtype=grad_dtype, device=q.device)
+        dk = torch.empty(v.shape, dtype=grad_dtype, device=v.device)
     if dv is None:
-        dv = torch.empty(k.shape, dtype=grad_dtype, device=q.device)
+        dv = torch.empty(v.shape, dtype=grad_dtype, device=v.device)
     if workspace is None:
-        workspace = alloc_workspace(B, T, Hq, Hkv, D, precise, q.device)
+        workspace = alloc_workspace(B, T, Hq, Hkv, D, precise, v.device)
     for t in (q, k, v, dout):
-        assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous()
+        assert t is None or (t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous())
     assert o.dtype in (torch.bfloat16, torch.float32) and o.is_contiguous()
     assert lse.dtype == torch.float32 and lse.numel() == (2 if precise else 1) * B * Hq * T
     for t in (dq, dk, dv):
@@ -183,7 +200,8 @@ def status_of_last_kernels(stream=None):
     return int(lib().ne_attn_check_status(_stream(stream)))
 
 
-KERNEL_KINDS = ("fwd", "bwd_prep", "bwd_dkdv", "bwd_dq", "fwd_rope", "kv_append", "decode", "decode_aux")
+KERNEL_KINDS = ("fwd", "bwd_prep", "bwd_dkdv", "bwd_dq", "fwd_rope", "kv_append", "decode", "decode_aux",
+                "qkv_prep", "qkv")
 
 
 def profile_start(capacity):
@@ -283,3 +301,59 @@ def attn_decode(q, k_cache, v_cache, Tkv, rope_base=10000.0, o=None, lse=None, o
                                                   B, Tq, Tkv, Tcap, Hq, Hkv, D, float(rope_base), flags,
                                                   _ptr(workspace), workspace.numel(), _stream(stream)))
     return o, lse
+
+
+def qkv_workspace_size(B, T, C, Hq, Hkv, D, rotated=False, rope_half=False):
+    flags = (QK_ROTATED if rotated else 0) | (ROPE_HALF if rope_half else 0)
+    return int(lib().ne_attn_qkv_workspace_size(B, T, C, Hq, Hkv, D, flags))
+
+
+def qkv_rmsnorm(x, norm_w, w_qkv, Hq, Hkv, D, eps=1e-5, rope_base=10000.0, rotated=False, rope_half=False,
+                write_qk=True, q=None, k=None, v=None, rstd=None, workspace=None, stream=None):
+    """RMSNorm of x [B,T,C] and the fused projection w_qkv [(Hq+2Hkv)D, C] (bf16, CUDA).
+
+    Returns (q, k, v, rstd, workspace): q [B,T,Hq,D], k and v [B,T,Hkv,D]
+    (bf16; q and k are None when write_qk is False), rstd [B,T] fp32.
+    rotated: also write the rotated q, k (fp16) at the start of `workspace`
+    (allocated here if None; at least qkv_workspace_size bytes), where
+    attn_fwd / attn_bwd with qk_rotated=True take them.
+    """
+    B, T, C = x.shape
+    N = (Hq + 2 * Hkv) * D
+    assert norm_w.shape == (C,) and w_qkv.shape == (N, C)
+    for t in (x, norm_w, w_qkv):
+        assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous()
+    if not write_qk and not rotated:
+        raise ValueError("write_qk=False needs rotated=True")
+    dev = x.device
+    if write_qk:
+        q = torch.empty((B, T, Hq, D), dtype=torch.bfloat16, device=dev) if q is None else q
+        k = torch.empty((B, T, Hkv, D), dtype=torch.bfloat16, device=dev) if k is None else k
+    else:
+        q = k = None
+    v = torch.empty((B, T, Hkv, D), dtype=torch.bfloat16, device=dev) if v is None else v
+    rstd = torch.empty((B, T), dtype=torch.float32, device=dev) if rstd is None else rstd
+    for t in (q, k, v):
+        assert t is None or (t.dtype == torch.bfloat16 and t.is_contiguous())
+    assert rstd.dtype == torch.float32 and rstd.numel() == B * T
+    if workspace is None:
+        n = qkv_workspace_size(B, T, C, Hq, Hkv, D, rotated, rope_half)
+        if n == 0:
+            raise ValueError("unsupported shape")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    flags = (QK_ROTATED if rotated else 0) | (ROPE_HALF if rope_half else 0)
+    _check("ne_attn_qkv_rmsnorm", lib().ne_attn_qkv_rmsnorm(
+        _ptr(x), _ptr(norm_w), _ptr(w_qkv), _ptr(q), _ptr(k), _ptr(v), _ptr(rstd), B, T, C, Hq, Hkv, D,
+        float(eps), float(rope_base), flags, _ptr(workspace), workspace.numel(), _stream(stream)))
+    return q, k, v, rstd, workspace
+
+
+def rotated_qk(workspace, B, T, Hq, Hkv, D):
+    """Views of the rotated fp16 q [B,T,Hq,D] and k [B,T,Hkv,D] at the start of a
+    forward / backward / projection workspace (NE_ATTN_QK_ROTATED layout)."""
+    def up(n):
+        return (n + 255) // 256 * 256
+    nq, nk = 2 * B * T * Hq * D, 2 * B * T * Hkv * D
+    qr = workspace[:nq].view(torch.float16).view(B, T, Hq, D)
+    kr = workspace[up(nq):up(nq) + nk].view(torch.float16).view(B, T, Hkv, D)
+    return qr, kr

@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libneattn.so")
-SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_decode.cu"]
+SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_decode.cu", "qkv_proj.cu"]
 HEADERS = ["ptx.cuh", "rope.cuh", "internal.h"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

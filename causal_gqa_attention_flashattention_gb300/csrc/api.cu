@@ -250,6 +250,32 @@ int make_map_acc(CUtensorMap* m, void* ptr, long long rows, int D) {
   return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
 }
 
+// 2-D map over a row-major bf16 matrix [rows, cols]; box = 64 columns (128
+// bytes) x box_rows rows, 128-byte swizzle (the UMMA K-major operand layout).
+int make_map_rows(CUtensorMap* m, const void* ptr, long long rows, int cols, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
+}
+
+// 4-D store map over a row-major [rows, H, D] tensor of 2-byte values (as
+// {D, H, rows, 1}); box = 32 values of one head x 128 rows, 64-byte swizzle.
+int make_map_out_box(CUtensorMap* m, void* ptr, long long rows, int H, int D, CUtensorMapDataType dt) {
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)rows * H * D * 2};
+  cuuint32_t box[4] = {32, 1, 128, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, dt, 4, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
+}
+
 int check_shape(int B, int T, int Hq, int Hkv, int D) {
   if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return NE_ERR_ARG;
   if (D != 32 && D != 64) return NE_ERR_UNSUPPORTED;
@@ -302,6 +328,25 @@ int check_decode_shape(int B, int Tq, int Tkv, int Tcap, int Hq, int Hkv, int D)
   return NE_OK;
 }
 
+
+// RMSNorm + projection: the attention shape rules, C % 8 == 0 (16-byte rows),
+// and every row-major index within 2^31 elements.
+int check_qkv_shape(int B, int T, int C, int Hq, int Hkv, int D) {
+  int st = check_shape(B, T, Hq, Hkv, D);
+  if (st != NE_OK) return st;
+  if (C < 8 || C % 8 != 0) return NE_ERR_ARG;
+  const long long M = (long long)B * T, N = (long long)(Hq + 2 * Hkv) * D;
+  if ((M + 127) * C >= (1LL << 31) || N * C >= (1LL << 31) || M * N >= (1LL << 31)) return NE_ERR_UNSUPPORTED;
+  return NE_OK;
+}
+// Workspace: [rotated q | rotated k] (the forward's workspace, with
+// NE_ATTN_QK_ROTATED) then the folded projection matrix [N, C] bf16.
+size_t qkv_wf_offset(int B, int T, int Hq, int Hkv, int D, int flags) {
+  return (flags & kFlagQKRotated) ? fwd_ws_bytes(B, T, Hq, Hkv, D) : 0;
+}
+size_t qkv_ws_bytes(int B, int T, int C, int Hq, int Hkv, int D, int flags) {
+  return qkv_wf_offset(B, T, Hq, Hkv, D, flags) + ws_up((size_t)(Hq + 2 * Hkv) * D * C * 2);
+}
 
 WsLayout ws_layout(int B, int T, int Hq, int Hkv, int D, bool precise) {
   auto up = ws_up;
@@ -398,24 +443,30 @@ using namespace ne;
 extern "C" {
 
 size_t ne_attn_fwd_workspace_size(int B, int T, int Hq, int Hkv, int D, int flags) {
-  if (check_shape(B, T, Hq, Hkv, D) != NE_OK || (flags & ~(kFlagOFp32 | kFlagPreciseQK | kFlagRopeHalf)) != 0) return 0;
-  if (half_with_precise(flags)) return 0;
+  if (check_shape(B, T, Hq, Hkv, D) != NE_OK ||
+      (flags & ~(kFlagOFp32 | kFlagPreciseQK | kFlagRopeHalf | kFlagQKRotated)) != 0)
+    return 0;
+  if (half_with_precise(flags) || ((flags & kFlagQKRotated) && (flags & kFlagPreciseQK))) return 0;
   return (flags & kFlagPreciseQK) ? 0 : fwd_ws_bytes(B, T, Hq, Hkv, D);
 }
 
 int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int Hq,
                    int Hkv, int D, float rope_base, int flags, void* workspace, size_t workspace_bytes,
                    void* stream) {
-  if (!q || !k || !v || !o || !lse) return NE_ERR_ARG;
+  const bool rotated = (flags & kFlagQKRotated) != 0;  // the workspace already holds the rotated q, k
+  if ((!rotated && (!q || !k)) || !v || !o || !lse) return NE_ERR_ARG;
   if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
-  if ((flags & ~(kFlagOFp32 | kFlagPreciseQK | kFlagRopeHalf)) != 0) return NE_ERR_ARG;
+  if ((flags & ~(kFlagOFp32 | kFlagPreciseQK | kFlagRopeHalf | kFlagQKRotated)) != 0) return NE_ERR_ARG;
+  if (rotated && (flags & kFlagPreciseQK)) return NE_ERR_ARG;
   if (half_with_precise(flags)) return NE_ERR_UNSUPPORTED;
   int st = check_shape(B, T, Hq, Hkv, D);
   if (st != NE_OK) return st;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return NE_ERR_ALIGN;
+  if ((q && !aligned16(q)) || (k && !aligned16(k)) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return NE_ERR_ALIGN;
   const bool precise = (flags & kFlagPreciseQK) != 0;
   const size_t ws_need = precise ? 0 : fwd_ws_bytes(B, T, Hq, Hkv, D);
-  if (workspace && (workspace_bytes < ws_need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+  if ((rotated && !workspace) ||
+      (workspace && (workspace_bytes < ws_need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)))
     return NE_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lock(g_mu);
@@ -449,8 +500,10 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
     ra.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
     if ((st = make_map_bthd(&a.map_q, ra.qr, B, T, Hq, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != NE_OK) return st;
     if ((st = make_map_bthd(&a.map_k, ra.kr, B, T, Hkv, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != NE_OK) return st;
-    ProfScope prof(NE_ATTN_KERNEL_FWD_ROPE, s);
-    if (launch_rope_qk(ra, D, s) != cudaSuccess) return NE_ERR_CUDA;
+    if (!rotated) {
+      ProfScope prof(NE_ATTN_KERNEL_FWD_ROPE, s);
+      if (launch_rope_qk(ra, D, s) != cudaSuccess) return NE_ERR_CUDA;
+    }
   }
   if ((st = make_map_bthd(&a.map_v, v, B, T, Hkv, D)) != NE_OK) return st;
   if (!precise && (st = make_map_grad(&a.map_o, o, B, T, Hq, D, (flags & kFlagOFp32) != 0)) != NE_OK) return st;
@@ -488,16 +541,18 @@ size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D, int flag
 int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                 void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D, float rope_base, int flags,
                 void* workspace, size_t workspace_bytes, void* stream) {
-  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return NE_ERR_ARG;
+  // with the rotated q, k in the workspace the kernels never read q and k
+  const bool rotated = (flags & kFlagQKRotated) != 0;
+  if ((!rotated && (!q || !k)) || !v || !o || !lse || !dout || !dq || !dk || !dv) return NE_ERR_ARG;
   if ((flags & ~kBwdFlags) != 0) return NE_ERR_ARG;
   // the forward leaves rotated copies only in default precision
-  if ((flags & kFlagQKRotated) && (flags & kFlagPreciseQK)) return NE_ERR_ARG;
+  if (rotated && (flags & kFlagPreciseQK)) return NE_ERR_ARG;
   if (half_with_precise(flags)) return NE_ERR_UNSUPPORTED;
   if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
   int st = check_shape(B, T, Hq, Hkv, D);
   if (st != NE_OK) return st;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+  if ((q && !aligned16(q)) || (k && !aligned16(k)) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return NE_ERR_ALIGN;
   const bool precise = (flags & kFlagPreciseQK) != 0;
   const int grad_fp32 = (flags & kFlagGradFp32) ? 1 : 0;
@@ -618,6 +673,83 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
     if (launch_bwd_dq(qa, s) != cudaSuccess) return NE_ERR_CUDA;
   }
   return NE_OK;
+}
+
+size_t ne_attn_qkv_workspace_size(int B, int T, int C, int Hq, int Hkv, int D, int flags) {
+  if (check_qkv_shape(B, T, C, Hq, Hkv, D) != NE_OK || (flags & ~(kFlagQKRotated | kFlagRopeHalf)) != 0) return 0;
+  return qkv_ws_bytes(B, T, C, Hq, Hkv, D, flags);
+}
+
+int ne_attn_qkv_rmsnorm(const void* x, const void* norm_w, const void* w_qkv, void* q, void* k, void* v,
+                        float* rstd, int B, int T, int C, int Hq, int Hkv, int D, float eps, float rope_base,
+                        int flags, void* workspace, size_t workspace_bytes, void* stream) {
+  const bool rotated = (flags & kFlagQKRotated) != 0;
+  if (!x || !norm_w || !w_qkv || !v || !rstd || (!rotated && (!q || !k))) return NE_ERR_ARG;
+  if ((flags & ~(kFlagQKRotated | kFlagRopeHalf)) != 0) return NE_ERR_ARG;
+  if (!(eps > 0.0f) || !std::isfinite(eps)) return NE_ERR_ARG;
+  if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
+  int st = check_qkv_shape(B, T, C, Hq, Hkv, D);
+  if (st != NE_OK) return st;
+  if (!aligned16(x) || !aligned16(norm_w) || !aligned16(w_qkv) || !aligned16(v) || !aligned16(rstd) ||
+      (q && !aligned16(q)) || (k && !aligned16(k)))
+    return NE_ERR_ALIGN;
+  const size_t ws_need = qkv_ws_bytes(B, T, C, Hq, Hkv, D, flags);
+  if ((rotated && !workspace) ||
+      (workspace && (workspace_bytes < ws_need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)))
+    return NE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev, nsm = 0;
+  if ((st = current_device(&dev)) != NE_OK) return st;
+  DeviceState* d;
+  if ((st = device_state(dev, &d)) != NE_OK) return st;
+  if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm < 1) return NE_ERR_CUDA;
+  void* ws = workspace;
+  if (!ws && (st = fwd_scratch(*d, s, ws_need, &ws)) != NE_OK) return st;
+  QkvArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (rotated && (st = rope_table(*d, D, (double)rope_base, T, s, &a.rope)) != NE_OK) return st;
+  unsigned char* wsb = static_cast<unsigned char*>(ws);
+  a.M = B * T;
+  a.C = C;
+  a.N = (Hq + 2 * Hkv) * D;
+  a.T = T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.eps = eps;
+  a.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.norm_w = static_cast<const __nv_bfloat16*>(norm_w);
+  a.w = static_cast<const __nv_bfloat16*>(w_qkv);
+  a.wf = reinterpret_cast<__nv_bfloat16*>(wsb + qkv_wf_offset(B, T, Hq, Hkv, D, flags));
+  a.rstd = rstd;
+  a.q = static_cast<__nv_bfloat16*>(q);
+  a.k = static_cast<__nv_bfloat16*>(k);
+  a.v = static_cast<__nv_bfloat16*>(v);
+  if (rotated) {
+    a.qr = reinterpret_cast<__half*>(wsb);
+    a.kr = reinterpret_cast<__half*>(wsb + ws_up(2 * (size_t)B * T * Hq * D));
+  }
+  a.status = d->status;
+  int grid = 1;
+  const int BN = qkv_pick_bn(a.M, a.N, nsm, &grid);
+  a.nkb = (C + 63) / 64;
+  a.ntn = (a.N + BN - 1) / BN;
+  a.tiles = ((a.M + 127) / 128) * a.ntn;
+  if ((st = make_map_rows(&a.map_x, x, a.M, C, 128)) != NE_OK) return st;
+  if ((st = make_map_rows(&a.map_w, a.wf, a.N, C, BN)) != NE_OK) return st;
+  if ((st = make_map_out_box(&a.map_vst, v, a.M, Hkv, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)) != NE_OK) return st;
+  if (rotated) {
+    if ((st = make_map_out_box(&a.map_qr, a.qr, a.M, Hq, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != NE_OK) return st;
+    if ((st = make_map_out_box(&a.map_kr, a.kr, a.M, Hkv, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != NE_OK) return st;
+  }
+  {
+    ProfScope prof(NE_ATTN_KERNEL_QKV_PREP, s);
+    if (launch_qkv_prep(a, s) != cudaSuccess) return NE_ERR_CUDA;
+  }
+  ProfScope prof(NE_ATTN_KERNEL_QKV, s);
+  return launch_qkv_gemm(a, BN, grid, s) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
 }
 
 int ne_attn_check_status(void* stream) {

@@ -142,6 +142,32 @@ struct DecodeArgs {
   float scale_log2;
 };
 
+// RMSNorm + fused Q/K/V projection (see qkv_proj.cu).  Rows r = b * T + t of
+// x [M, C]; projection features n of w_qkv [N, C], N = (Hq + 2 Hkv) D.
+struct QkvArgs {
+  CUtensorMap map_x;              // x [M, C] bf16, box 64 x 128, 128-byte swizzle
+  CUtensorMap map_w;              // folded weight [N, C] bf16, box 64 x BN, 128-byte swizzle
+  CUtensorMap map_qr, map_kr;     // store maps over the rotated fp16 q [M, Hq, D], k [M, Hkv, D]
+  CUtensorMap map_vst;            // store map over v [M, Hkv, D] bf16 (boxes 32 x 1 x 128, 64-byte swizzle)
+  const __nv_bfloat16* x;         // [M, C]
+  const __nv_bfloat16* norm_w;    // [C]
+  const __nv_bfloat16* w;         // [N, C]
+  __nv_bfloat16* wf;              // [N, C] w_qkv[n', c] * norm_w[c], rows permuted for half-split q, k
+  float* rstd;                    // [M]
+  __nv_bfloat16 *q, *k, *v;       // [M, Hq, D], [M, Hkv, D], [M, Hkv, D] (q and k may be null)
+  __half *qr, *kr;                // rotated fp16 q and k (null: not written)
+  const float2* rope;
+  int* status;
+  int M, C, N, T, Hq, Hkv, D;
+  int nkb, ntn, tiles;            // 64-wide K blocks, BN-wide column tiles, 128 x BN tiles
+  int rope_half;
+  float eps;
+};
+
+cudaError_t launch_qkv_prep(const QkvArgs& a, cudaStream_t s);
+cudaError_t launch_qkv_gemm(const QkvArgs& a, int BN, int grid, cudaStream_t s);
+int qkv_pick_bn(int M, int N, int nsm, int* grid);
+
 cudaError_t launch_fwd(const FwdArgs& a, bool precise, cudaStream_t s);
 cudaError_t launch_kv_append(const KvAppendArgs& a, int D, cudaStream_t s);
 cudaError_t launch_decode_q(const DecodeArgs& a, cudaStream_t s);

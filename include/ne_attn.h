@@ -70,12 +70,15 @@ typedef enum {
                                 remainder [B,Hq,T] (LSE = hi + lo), which the backward uses to
                                 rebuild P where one fp32 ulp of the LSE is already ~1e-3.
                                 Use the same setting for the forward and the backward. */
-#define NE_ATTN_QK_ROTATED 8 /* backward only, default precision: the first
-                                ne_attn_fwd_workspace_size bytes of `workspace` still hold the
-                                rotated q and k that ne_attn_fwd_ex wrote there for these q, k and
-                                rope_base, so the backward does not rotate them again (the
-                                forward's workspace is laid out as the start of the backward's).
-                                Rejected with NE_ATTN_PRECISE_QK and by ne_attn_bwd_noalloc. */
+#define NE_ATTN_QK_ROTATED 8 /* default precision: the first ne_attn_fwd_workspace_size bytes
+                                of `workspace` hold the rotated q and k (fp16) for these q, k and
+                                rope_base, so the call does not rotate them again.  The forward's
+                                workspace is laid out as the start of the backward's.
+                                ne_attn_fwd_ex: ne_attn_qkv_rmsnorm wrote them there (same flag);
+                                the workspace is then required and q, k may be NULL.
+                                ne_attn_bwd: ne_attn_fwd_ex or ne_attn_qkv_rmsnorm wrote them.
+                                ne_attn_qkv_rmsnorm: write them.  Rejected with
+                                NE_ATTN_PRECISE_QK and by ne_attn_bwd_noalloc. */
 #define NE_ATTN_ROPE_HALF 16 /* rotary pairs (x[i], x[i + D/2]) (the half-split layout) instead
                                 of the interleaved (x[2i], x[2i+1]); same angles t * base^(-2i/D)
                                 for pair i.  The pages name no pair layout.  Accepted by the
@@ -109,8 +112,8 @@ int ne_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse
 size_t ne_attn_fwd_workspace_size(int B, int T, int Hq, int Hkv, int D, int flags);
 
 /*
- * Forward pass with flags (NE_ATTN_O_FP32, NE_ATTN_PRECISE_QK; others
- * rejected) and an optional caller workspace (256-byte aligned, at least
+ * Forward pass with flags (NE_ATTN_O_FP32, NE_ATTN_PRECISE_QK, NE_ATTN_ROPE_HALF,
+ * NE_ATTN_QK_ROTATED; others rejected) and an optional caller workspace (256-byte aligned, at least
  * ne_attn_fwd_workspace_size bytes, else NE_ERR_WORKSPACE; the caller owns it
  * and must not touch it until the call's work on `stream` is done).  With
  * workspace = NULL the library uses a buffer of its own per stream, grown
@@ -229,6 +232,38 @@ int ne_attn_decode(const void* q, const void* k_cache, const void* v_cache, void
                    size_t workspace_bytes, void* stream);
 
 /*
+ * The step in front of attention: pre-norm RMSNorm and the fused Q/K/V
+ * projection without bias (socker-news README, "Architecture" and the block
+ * order x = x + attn(rmsnorm(x)); mynewscn README).  For row r = b * T + t:
+ *
+ *   rstd[r] = 1 / sqrt(mean_c x[r, c]^2 + eps)
+ *   qkv[r, n] = sum_c x[r, c] * rstd[r] * norm_w[c] * w_qkv[n, c]
+ *   q[b,t,h,:] = qkv[r, h*D ..],  k[b,t,g,:] = qkv[r, Hq*D + g*D ..],
+ *   v[b,t,g,:] = qkv[r, (Hq+Hkv)*D + g*D ..]
+ *
+ * x [B, T, C], norm_w [C] and w_qkv [(Hq + 2 Hkv) D, C] (output by input) are
+ * bfloat16; q [B,T,Hq,D], k and v [B,T,Hkv,D] are bfloat16 outputs; rstd
+ * [B*T] float32 is an output (the RMSNorm backward needs it).  Requires
+ * C % 8 == 0 and the attention shape rules above.  eps > 0.
+ * flags: NE_ATTN_QK_ROTATED also writes the rotated q and k (rotary embedding
+ * at position t, as ne_attn_fwd applies it) as fp16 into the first
+ * ne_attn_fwd_workspace_size bytes of `workspace`, where ne_attn_fwd_ex and
+ * ne_attn_bwd with NE_ATTN_QK_ROTATED (and the same workspace, rope_base and
+ * rotary layout) take them; q and k may then be NULL.  NE_ATTN_ROPE_HALF
+ * selects the half-split rotary pairs for those.  The workspace
+ * (ne_attn_qkv_workspace_size bytes, 256-byte aligned) is required with
+ * NE_ATTN_QK_ROTATED; with workspace = NULL otherwise the library uses its
+ * per-stream buffer as ne_attn_fwd_ex does.
+ * Two kernels: per-row rstd together with the projection matrix scaled by
+ * norm_w (bf16, in the workspace); then a persistent tensor-core GEMM over
+ * 128-row tiles whose epilogue applies rstd and the rotation and stores.
+ */
+size_t ne_attn_qkv_workspace_size(int B, int T, int C, int Hq, int Hkv, int D, int flags);
+int ne_attn_qkv_rmsnorm(const void* x, const void* norm_w, const void* w_qkv, void* q, void* k, void* v,
+                        float* rstd, int B, int T, int C, int Hq, int Hkv, int D, float eps, float rope_base,
+                        int flags, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: NE_OK, NE_ERR_DEVICE_TIMEOUT, or NE_ERR_CUDA if the
  * synchronisation itself failed.
@@ -240,8 +275,8 @@ const char* ne_attn_status_string(int status);
 
 /*
  * Kernel timing.  Between ne_attn_profile_start(capacity) and
- * ne_attn_profile_stop(), each kernel that ne_attn_fwd/_ex and ne_attn_bwd
- * launch is bracketed by a pair of CUDA timing events recorded on the launch
+ * ne_attn_profile_stop(), each kernel that the library's calls launch is
+ * bracketed by a pair of CUDA timing events recorded on the launch
  * stream (at most `capacity` launches; later ones are not timed but still
  * counted).  ne_attn_profile_stop synchronises those events and fills, per
  * kernel kind (NE_ATTN_KERNEL_*), the summed device time in milliseconds and
@@ -264,7 +299,9 @@ const char* ne_attn_status_string(int status);
 #define NE_ATTN_KERNEL_KV_APPEND 5
 #define NE_ATTN_KERNEL_DECODE 6     /* the split sweep over the cache */
 #define NE_ATTN_KERNEL_DECODE_AUX 7 /* query packing and the combine of the splits */
-#define NE_ATTN_NUM_KERNEL_KINDS 8
+#define NE_ATTN_KERNEL_QKV_PREP 8   /* RMSNorm row statistics and the weight fold */
+#define NE_ATTN_KERNEL_QKV 9        /* the projection GEMM with the rotary epilogue */
+#define NE_ATTN_NUM_KERNEL_KINDS 10
 int ne_attn_profile_start(int capacity);
 int ne_attn_profile_stop(double* total_ms, long long* launches);
 int ne_attn_profile_detach(void);

@@ -138,3 +138,52 @@ def test_half_split_flag_rules(libne):
     libne.ne_attn_bwd_noalloc.restype = i
     assert libne.ne_attn_bwd_noalloc(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 16 | 4, null) == -3
 
+
+
+def test_qkv_workspace_size(libne):
+    B, T, C, Hq, Hkv, D = 16, 512, 768, 12, 4, 64
+    N = (Hq + 2 * Hkv) * D
+    n = libne.ne_attn_qkv_workspace_size(B, T, C, Hq, Hkv, D, 0)
+    assert n == N * C * 2  # the folded projection matrix (already a 256-byte multiple)
+    fwd = libne.ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, 0)
+    assert libne.ne_attn_qkv_workspace_size(B, T, C, Hq, Hkv, D, 8) == fwd + n  # rotated q, k first
+    assert libne.ne_attn_qkv_workspace_size(B, T, C, Hq, Hkv, D, 8 | 16) == fwd + n
+    assert libne.ne_attn_qkv_workspace_size(B, T, 100, Hq, Hkv, D, 0) == 0  # rows must be 16-byte multiples
+    assert libne.ne_attn_qkv_workspace_size(B, T, C, Hq, Hkv, D, 1) == 0  # output-dtype flag is not accepted
+    assert libne.ne_attn_qkv_workspace_size(B, T, C, 12, 5, D, 0) == 0  # Hq % Hkv
+    # the forward accepts the reuse flag now (it changes nothing in the size)
+    assert libne.ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, 8) == fwd
+    assert libne.ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, 8 | 4) == 0
+
+
+def test_qkv_host_argument_checks(libne):
+    buf = ctypes.create_string_buffer(4096 + 512)
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    p = ctypes.c_void_p(base)
+    mis = ctypes.c_void_p(base + 2)
+    null = None
+    ok = (1, 4, 64, 4, 2, 32)  # B, T, C, Hq, Hkv, D
+    # ne_attn_qkv_rmsnorm(x, norm_w, w_qkv, q, k, v, rstd, B, T, C, Hq, Hkv, D, eps, base, flags, ws, bytes, stream)
+    f = libne.ne_attn_qkv_rmsnorm
+    assert f(null, p, p, p, p, p, p, *ok, 1e-5, 10000.0, 0, p, 1 << 20, null) == -1
+    assert f(p, p, p, p, p, p, null, *ok, 1e-5, 10000.0, 0, p, 1 << 20, null) == -1  # rstd is an output
+    assert f(p, p, p, null, p, p, p, *ok, 1e-5, 10000.0, 0, p, 1 << 20, null) == -1  # q needed without the flag
+    assert f(p, p, p, p, p, p, p, *ok, 0.0, 10000.0, 0, p, 1 << 20, null) == -1      # eps > 0
+    assert f(p, p, p, p, p, p, p, *ok, 1e-5, 1.0, 0, p, 1 << 20, null) == -1         # rope base
+    assert f(p, p, p, p, p, p, p, *ok, 1e-5, 10000.0, 4, p, 1 << 20, null) == -1     # precise flag
+    assert f(p, p, p, p, p, p, p, 1, 4, 60, 4, 2, 32, 1e-5, 10000.0, 0, p, 1 << 20, null) == -1  # C % 8
+    assert f(p, p, p, p, p, p, p, 1, 4, 64, 4, 2, 48, 1e-5, 10000.0, 0, p, 1 << 20, null) == -3  # D
+    assert f(p, mis, p, p, p, p, p, *ok, 1e-5, 10000.0, 0, p, 1 << 20, null) == -2
+    assert f(p, p, p, p, p, p, p, *ok, 1e-5, 10000.0, 8, null, 0, null) == -5  # rotated q, k need a workspace
+    assert f(p, p, p, null, null, p, p, *ok, 1e-5, 10000.0, 8, p, 64, null) == -5  # too small (q, k optional)
+    assert f(p, p, p, p, p, p, p, *ok, 1e-5, 10000.0, 0, mis, 1 << 20, null) == -5
+    # forward and backward: q, k may be NULL only with the reuse flag, which needs the workspace
+    # ne_attn_fwd_ex(q, k, v, o, lse, B, T, Hq, Hkv, D, base, flags, ws, bytes, stream)
+    fx = libne.ne_attn_fwd_ex
+    assert fx(null, null, p, p, p, 1, 4, 4, 2, 32, 10000.0, 0, p, 1 << 20, null) == -1
+    assert fx(null, null, p, p, p, 1, 4, 4, 2, 32, 10000.0, 8, null, 0, null) == -5
+    assert fx(null, null, p, p, p, 1, 4, 4, 2, 32, 10000.0, 8 | 4, p, 1 << 20, null) == -1
+    # ne_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, T, Hq, Hkv, D, base, flags, ws, bytes, stream)
+    bx = libne.ne_attn_bwd
+    assert bx(null, null, p, p, p, p, p, p, p, 1, 4, 4, 2, 32, 10000.0, 0, p, 1 << 20, null) == -1
+    assert bx(null, null, p, p, p, p, p, p, p, 1, 4, 4, 2, 32, 10000.0, 8, p, 64, null) == -5

@@ -594,6 +594,97 @@ def run_prologue(args):
     return 0
 
 
+def run_fp8(args):
+    """One JSON line for the FP8 forward (NE_ATTN_FP8, an inference variant) on
+    the 116M model's attention shape: forward TFLOP/s with e4m3 rotated q, k.
+    The default (fp16 q, k) forward is timed the same way beside it.  Input
+    sets rotate so that their total exceeds L2; graph replay as in the main line.
+    """
+    import torch
+    from causal_gqa_attention_flashattention_gb300 import binding
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(dev)
+    B, T, Hq, Hkv, D = inputs.WORKLOADS[WORKLOAD][:5]
+    flops = algo_flops(B, T, Hq, D)["fwd"]
+    set_bytes = 2 * B * T * (2 * Hq + 2 * Hkv) * D + B * T * (Hq + Hkv) * D
+    nsets = max(2, min(16, -(-2 * 129 * 2 ** 20 // set_bytes)))
+    g = torch.Generator(device=dev).manual_seed(9)
+    sets = []
+    for _ in range(nsets):
+        q = torch.randn((B, T, Hq, D), device=dev, generator=g).bfloat16()
+        k = torch.randn((B, T, Hkv, D), device=dev, generator=g).bfloat16()
+        v = torch.randn((B, T, Hkv, D), device=dev, generator=g).bfloat16()
+        sets.append(dict(q=q, k=k, v=v, o=torch.empty_like(q),
+                         lse=torch.empty((B, Hq, T), dtype=torch.float32, device=dev),
+                         ws8=torch.empty(binding.fwd_workspace_size(B, T, Hq, Hkv, D, fp8=True), dtype=torch.uint8,
+                                         device=dev),
+                         ws=torch.empty(binding.fwd_workspace_size(B, T, Hq, Hkv, D), dtype=torch.uint8, device=dev)))
+
+    def timed(fp8):
+        def call(st):
+            binding.attn_fwd(st["q"], st["k"], st["v"], o=st["o"], lse=st["lse"], fp8=fp8,
+                             workspace=st["ws8"] if fp8 else st["ws"], stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                for st in sets:
+                    call(st)
+        binding.check_status(stream)
+        binding.profile_start(4 * nsets + 4)
+        g_prof = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_prof, stream=stream):
+            for st in sets:
+                call(st)
+        cap = binding.profile_stop_deferred()
+        g_all = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_all, stream=stream):
+            for st in sets:
+                call(st)
+        reps = max(1, args.steps // nsets)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g_all.replay()
+            torch.cuda.synchronize(dev)
+            clocks = ClockSampler(0)
+            clocks.start()
+            e0.record(stream)
+            for _ in range(reps):
+                g_all.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            clk = clocks.stop()
+            binding.check_status(stream)
+            for _ in range(3):
+                g_prof.replay()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / (reps * nsets), binding.profile_read(cap), reps * nsets, clk
+
+    ms8, prof8, n8, clk = timed(True)
+    ms16, prof16, _, _ = timed(False)
+    ms_attn = prof8["fwd"][0] / max(1, prof8["fwd"][1])
+    achieved = flops / (ms_attn * 1e-3) / 1e12
+    line = dict(metric="FP8 forward: causal GQA attention TFLOP/s, e4m3 rotated q and k (inference variant)",
+                value=flops / (ms8 * 1e-3) / 1e12, unit="TFLOP/s", n_gpus=1, steps=n8, warmup=args.warmup,
+                ms_per_step=ms8, higher_is_better=True, scaling="weak", vs_baseline=None,
+                dtype="e4m3 q/k, bf16 v and P, fp32 accumulate", data="synthetic",
+                config=dict(workload=WORKLOAD, B=B, T=T, Hq=Hq, Hkv=Hkv, D=D, input_sets=nsets,
+                            l2="%d rotating input sets of %.1f MB" % (nsets, set_bytes / 1e6),
+                            launch="CUDA graph replay (max pass, quantising pass, attention kernel)"),
+                default_forward=dict(ms_per_step=ms16, value=flops / (ms16 * 1e-3) / 1e12, unit="TFLOP/s",
+                                     kernels={k: dict(us_per_launch=v[0] / v[1] * 1e3, launches=v[1])
+                                              for k, v in prof16.items() if v[1]}),
+                roofline=dict(bound="tensor", achieved=achieved, peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                              frac=achieved / peaks["bf16_tflops"], kernel="fwd",
+                              traffic=None, peak_source="%s bf16 (burst); S runs at the 8-bit rate, P V at bf16"
+                              % peaks["source"], per_launch_us=ms_attn * 1e3,
+                              kernels={k: dict(us_per_launch=v[0] / v[1] * 1e3, launches=v[1])
+                                       for k, v in prof8.items() if v[1]}),
+                gpu_launches=3 * n8, clocks=clk)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -608,6 +699,8 @@ def main():
                     help="with --decode: only this workload")
     ap.add_argument("--prologue", action="store_true",
                     help="measure RMSNorm + the fused Q/K/V projection (one JSON line) instead")
+    ap.add_argument("--fp8", action="store_true",
+                    help="measure the FP8 forward (one JSON line) instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -615,6 +708,8 @@ def main():
         return run_decode(args)
     if args.prologue:
         return run_prologue(args)
+    if args.fp8:
+        return run_fp8(args)
     world, rank, local = dist_init()
     if args.impl == "reference":
         return run_reference(args, world, rank)

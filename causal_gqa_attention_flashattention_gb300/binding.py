@@ -19,6 +19,7 @@ GRAD_FP32 = 2
 PRECISE_QK = 4
 QK_ROTATED = 8
 ROPE_HALF = 16
+FP8 = 32
 _lib = None
 
 
@@ -95,12 +96,13 @@ def _shape(q, k):
     return B, T, Hq, Hkv, D
 
 
-def fwd_workspace_size(B, T, Hq, Hkv, D, precise=False):
-    return int(lib().ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, PRECISE_QK if precise else 0))
+def fwd_workspace_size(B, T, Hq, Hkv, D, precise=False, fp8=False):
+    flags = (PRECISE_QK if precise else 0) | (FP8 if fp8 else 0)
+    return int(lib().ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, flags))
 
 
 def attn_fwd(q, k, v, rope_base=10000.0, o=None, lse=None, o_dtype=torch.bfloat16, precise=False,
-             workspace=None, rope_half=False, qk_rotated=False, Hq=None, stream=None):
+             workspace=None, rope_half=False, qk_rotated=False, Hq=None, fp8=False, stream=None):
     """o, lse = causal GQA attention of q [B,T,Hq,D], k/v [B,T,Hkv,D] (bf16, CUDA).
 
     o_dtype: bfloat16 or float32.  precise: hi+lo split of the rotated q, k
@@ -108,7 +110,8 @@ def attn_fwd(q, k, v, rope_base=10000.0, o=None, lse=None, o_dtype=torch.bfloat1
     least fwd_workspace_size bytes (the rotated fp16 q, k land there); if None
     one is allocated for the call.  qk_rotated: `workspace` already holds the
     rotated q and k (written by qkv_rmsnorm with rotated=True); q and k may
-    then be None, with the number of query heads given as Hq.
+    then be None, with the number of query heads given as Hq.  fp8: the
+    e4m3 forward (NE_ATTN_FP8; D = 64, about 3e-2 relative error in o).
     """
     if qk_rotated and workspace is None:
         raise ValueError("qk_rotated needs the workspace that holds the rotated q and k")
@@ -130,9 +133,9 @@ def attn_fwd(q, k, v, rope_base=10000.0, o=None, lse=None, o_dtype=torch.bfloat1
     assert o.dtype in (torch.bfloat16, torch.float32) and o.is_contiguous()
     assert lse.dtype == torch.float32 and lse.is_contiguous()
     flags = ((O_FP32 if o.dtype == torch.float32 else 0) | (PRECISE_QK if precise else 0)
-             | (ROPE_HALF if rope_half else 0) | (QK_ROTATED if qk_rotated else 0))
+             | (ROPE_HALF if rope_half else 0) | (QK_ROTATED if qk_rotated else 0) | (FP8 if fp8 else 0))
     if workspace is None:
-        n = fwd_workspace_size(B, T, Hq, Hkv, D, precise)
+        n = fwd_workspace_size(B, T, Hq, Hkv, D, precise, fp8)
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=v.device)
     assert workspace.dtype == torch.uint8 and workspace.is_cuda
     _check("ne_attn_fwd_ex", lib().ne_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),

@@ -207,6 +207,19 @@ int make_map_bthd(CUtensorMap* m, const void* ptr, int B, int T, int H, int D,
   return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
 }
 
+// 4-D map over a [B, T, H, D] e4m3 tensor (one byte per value); box = one head,
+// 128 rows, all D (64 bytes per row for D = 64, 64-byte swizzle).
+int make_map_bthd8(CUtensorMap* m, const void* ptr, int B, int T, int H, int D) {
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D, (cuuint64_t)H * D, (cuuint64_t)T * H * D};
+  cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)kTile, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NE_OK : NE_ERR_CUDA;
+}
+
 // 4-D map over a head-major key/value cache [B, H, Tcap, D] of which positions
 // 0..Tkv-1 are valid: rows at or past Tkv read as zeros.  Box = 128 rows of one
 // head, all D (one contiguous stretch).
@@ -302,6 +315,20 @@ struct WsLayout {
 size_t ws_up(size_t x) { return (x + 255) / 256 * 256; }
 size_t fwd_ws_bytes(int B, int T, int Hq, int Hkv, int D) {
   return ws_up(2 * (size_t)B * T * Hq * D) + ws_up(2 * (size_t)B * T * Hkv * D);
+}
+// FP8 forward workspace: e4m3 rotated q [B,T,Hq,D] and k [B,T,Hkv,D], then the
+// per-head maxima [Hq + Hkv] (fp32).
+size_t fwd8_ws_bytes(int B, int T, int Hq, int Hkv, int D) {
+  return ws_up((size_t)B * T * Hq * D) + ws_up((size_t)B * T * Hkv * D) + ws_up(4 * (size_t)(Hq + Hkv));
+}
+constexpr int kFwdFlags = kFlagOFp32 | kFlagPreciseQK | kFlagRopeHalf | kFlagQKRotated | kFlagFp8;
+// The FP8 forward: default precision, q and k rotated by the library, D = 64,
+// at most 256 heads in all (per-head maxima of its first pass).
+int fp8_rules(int flags, int Hq, int Hkv, int D) {
+  if (!(flags & kFlagFp8)) return NE_OK;
+  if (flags & (kFlagPreciseQK | kFlagQKRotated)) return NE_ERR_ARG;
+  if (D != 64 || Hq + Hkv > 256) return NE_ERR_UNSUPPORTED;
+  return NE_OK;
 }
 
 // Decode workspace: packed rotated queries, then the splits' partial O and (max, sum).
@@ -443,10 +470,10 @@ using namespace ne;
 extern "C" {
 
 size_t ne_attn_fwd_workspace_size(int B, int T, int Hq, int Hkv, int D, int flags) {
-  if (check_shape(B, T, Hq, Hkv, D) != NE_OK ||
-      (flags & ~(kFlagOFp32 | kFlagPreciseQK | kFlagRopeHalf | kFlagQKRotated)) != 0)
-    return 0;
+  if (check_shape(B, T, Hq, Hkv, D) != NE_OK || (flags & ~kFwdFlags) != 0) return 0;
   if (half_with_precise(flags) || ((flags & kFlagQKRotated) && (flags & kFlagPreciseQK))) return 0;
+  if (fp8_rules(flags, Hq, Hkv, D) != NE_OK) return 0;
+  if (flags & kFlagFp8) return fwd8_ws_bytes(B, T, Hq, Hkv, D);
   return (flags & kFlagPreciseQK) ? 0 : fwd_ws_bytes(B, T, Hq, Hkv, D);
 }
 
@@ -456,15 +483,17 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
   const bool rotated = (flags & kFlagQKRotated) != 0;  // the workspace already holds the rotated q, k
   if ((!rotated && (!q || !k)) || !v || !o || !lse) return NE_ERR_ARG;
   if (!(rope_base > 1.0f) || !std::isfinite(rope_base)) return NE_ERR_ARG;
-  if ((flags & ~(kFlagOFp32 | kFlagPreciseQK | kFlagRopeHalf | kFlagQKRotated)) != 0) return NE_ERR_ARG;
+  if ((flags & ~kFwdFlags) != 0) return NE_ERR_ARG;
   if (rotated && (flags & kFlagPreciseQK)) return NE_ERR_ARG;
   if (half_with_precise(flags)) return NE_ERR_UNSUPPORTED;
   int st = check_shape(B, T, Hq, Hkv, D);
   if (st != NE_OK) return st;
+  if ((st = fp8_rules(flags, Hq, Hkv, D)) != NE_OK) return st;
+  const bool fp8 = (flags & kFlagFp8) != 0;
   if ((q && !aligned16(q)) || (k && !aligned16(k)) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return NE_ERR_ALIGN;
   const bool precise = (flags & kFlagPreciseQK) != 0;
-  const size_t ws_need = precise ? 0 : fwd_ws_bytes(B, T, Hq, Hkv, D);
+  const size_t ws_need = precise ? 0 : (fp8 ? fwd8_ws_bytes(B, T, Hq, Hkv, D) : fwd_ws_bytes(B, T, Hq, Hkv, D));
   if ((rotated && !workspace) ||
       (workspace && (workspace_bytes < ws_need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)))
     return NE_ERR_WORKSPACE;
@@ -481,6 +510,32 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
   if (precise) {
     if ((st = make_map_bthd(&a.map_q, q, B, T, Hq, D)) != NE_OK) return st;
     if ((st = make_map_bthd(&a.map_k, k, B, T, Hkv, D)) != NE_OK) return st;
+  } else if (fp8) {
+    void* ws = workspace;
+    if (!ws && (st = fwd_scratch(*d, s, ws_need, &ws)) != NE_OK) return st;
+    unsigned char* wb = static_cast<unsigned char*>(ws);
+    RopeArgs ra;
+    std::memset(&ra, 0, sizeof(ra));
+    ra.q = static_cast<const __nv_bfloat16*>(q);
+    ra.k = static_cast<const __nv_bfloat16*>(k);
+    ra.q8 = wb;
+    ra.k8 = wb + ws_up((size_t)B * T * Hq * D);
+    ra.amax = reinterpret_cast<float*>(wb + ws_up((size_t)B * T * Hq * D) + ws_up((size_t)B * T * Hkv * D));
+    ra.rope = a.rope;
+    ra.B = B;
+    ra.T = T;
+    ra.Hq = Hq;
+    ra.Hkv = Hkv;
+    ra.div_hq = make_fastdiv((uint32_t)Hq);
+    ra.div_hkv = make_fastdiv((uint32_t)Hkv);
+    ra.div_t = make_fastdiv((uint32_t)T);
+    ra.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
+    if ((st = make_map_bthd8(&a.map_q, ra.q8, B, T, Hq, D)) != NE_OK) return st;
+    if ((st = make_map_bthd8(&a.map_k, ra.k8, B, T, Hkv, D)) != NE_OK) return st;
+    a.qk_amax = ra.amax;
+    ProfScope prof(NE_ATTN_KERNEL_FWD_ROPE, s);
+    if (cudaMemsetAsync(ra.amax, 0, sizeof(float) * (size_t)(Hq + Hkv), s) != cudaSuccess) return NE_ERR_CUDA;
+    if (launch_rope_amax(ra, s) != cudaSuccess || launch_rope_q8(ra, s) != cudaSuccess) return NE_ERR_CUDA;
   } else {
     void* ws = workspace;
     if (!ws && (st = fwd_scratch(*d, s, ws_need, &ws)) != NE_OK) return st;
@@ -523,7 +578,7 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
   a.scale_log2_lo = (float)(sl2 - (double)a.scale_log2);
   a.lse_lo = precise ? lse + (size_t)B * Hq * T : nullptr;
   ProfScope prof(NE_ATTN_KERNEL_FWD, s);
-  return launch_fwd(a, precise, s) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+  return (fp8 ? launch_fwd_fp8(a, s) : launch_fwd(a, precise, s)) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
 }
 
 int ne_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int Hq, int Hkv,

@@ -502,6 +502,73 @@ __global__ void __launch_bounds__(256) k_rope_qk(const RopeArgs a) {
   }
 }
 
+// ====================================================================== FP8 pre-passes (D = 64)
+// The FP8 forward takes the rotated q and k as e4m3 with one scale per head:
+// value = e4m3 code * max_h / 448, max_h the largest |rotated value| of head h
+// over all batches and positions.  Pass 1 finds max_h, pass 2 rotates again and
+// rounds (round to nearest even, saturating at 448).
+constexpr int kMaxHeadsF8 = 256;  // Hq + Hkv at most (shared-memory maxima of pass 1)
+
+__global__ void __launch_bounds__(256) k_rope_amax(const RopeArgs a) {
+  constexpr int D = 64, kCPR = D / 8;
+  __shared__ unsigned smax[kMaxHeadsF8];
+  const int nh = a.Hq + a.Hkv;
+  for (int i = threadIdx.x; i < nh; i += blockDim.x) smax[i] = 0u;
+  __syncthreads();
+  const uint32_t nq = (uint32_t)a.B * a.T * a.Hq * kCPR;
+  const uint32_t n = nq + (uint32_t)a.B * a.T * a.Hkv * kCPR;
+  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < n; it += gridDim.x * blockDim.x) {
+    const bool isq = it < nq;
+    const uint32_t x = isq ? it : it - nq;
+    const uint32_t row = x / kCPR;  // (b, t, h)
+    const uint32_t bt = fdiv(row, isq ? a.div_hq : a.div_hkv);
+    const uint32_t h = row - bt * (isq ? a.Hq : a.Hkv);
+    const uint32_t t = bt - fdiv(bt, a.div_t) * a.T;
+    const uint4 v = load_rope_chunk<D>((isq ? a.q : a.k) + (size_t)row * D, (int)(x % kCPR), a.rope_half != 0);
+    float4 c0, c1;
+    rope_coeffs<D>(a.rope, (int)t, (int)(x % kCPR), c0, c1);
+    float y[8];
+    rope_chunk_f32(v, c0, c1, y);
+    float m = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; e++) m = fmaxf(m, fabsf(y[e]));
+    atomicMax(&smax[isq ? h : a.Hq + h], __float_as_uint(m));  // non-negative floats order as integers
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < nh; i += blockDim.x)
+    if (smax[i]) atomicMax(reinterpret_cast<unsigned*>(a.amax) + i, smax[i]);
+}
+
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__global__ void __launch_bounds__(256) k_rope_q8(const RopeArgs a) {
+  constexpr int D = 64, kCPR = D / 8;
+  const uint32_t nq = (uint32_t)a.B * a.T * a.Hq * kCPR;
+  const uint32_t n = nq + (uint32_t)a.B * a.T * a.Hkv * kCPR;
+  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < n; it += gridDim.x * blockDim.x) {
+    const bool isq = it < nq;
+    const uint32_t x = isq ? it : it - nq;
+    const uint32_t row = x / kCPR;
+    const uint32_t bt = fdiv(row, isq ? a.div_hq : a.div_hkv);
+    const uint32_t h = row - bt * (isq ? a.Hq : a.Hkv);
+    const uint32_t t = bt - fdiv(bt, a.div_t) * a.T;
+    const float mx = __ldg(a.amax + (isq ? h : a.Hq + h));
+    const float inv = mx > 0.f ? 448.f / mx : 1.f;
+    const uint4 v = load_rope_chunk<D>((isq ? a.q : a.k) + (size_t)row * D, (int)(x % kCPR), a.rope_half != 0);
+    float4 c0, c1;
+    rope_coeffs<D>(a.rope, (int)t, (int)(x % kCPR), c0, c1);
+    float y[8];
+    rope_chunk_f32(v, c0, c1, y);
+    const uint32_t w0 = (uint32_t)e4m3x2(y[0] * inv, y[1] * inv) | ((uint32_t)e4m3x2(y[2] * inv, y[3] * inv) << 16);
+    const uint32_t w1 = (uint32_t)e4m3x2(y[4] * inv, y[5] * inv) | ((uint32_t)e4m3x2(y[6] * inv, y[7] * inv) << 16);
+    reinterpret_cast<uint2*>(isq ? a.q8 : a.k8)[x] = make_uint2(w0, w1);
+  }
+}
+
 // ====================================================================== persistent forward, one head per item
 // Default-precision forward over the pre-rotated fp16 q, k.  One CTA per SM
 // loops over work items (query tile i, batch, query head), largest first in a
@@ -543,19 +610,25 @@ __device__ __forceinline__ void stage_rows(const float (&x)[D], uint8_t* stg, in
   }
 }
 
-template <int D>
+// F8: q and k tiles hold e4m3 (one byte per value; 64-byte rows, 64-byte
+// swizzle for D = 64); v, P and O keep their formats.
+template <int D, bool F8 = false>
 struct Fwd3Cfg {
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr uint32_t kSpan = D * 2;
   static constexpr uint32_t kSwz = D == 64 ? kSw128 : kSw64;
   static constexpr uint32_t kSBO = 8 * kSpan;
+  static constexpr int kQKTileBytes = kTile * D * (F8 ? 1 : 2);
+  static constexpr uint32_t kQKSpan = D * (F8 ? 1 : 2);
+  static constexpr uint32_t kQKSwz = kQKSpan == 128 ? kSw128 : (kQKSpan == 64 ? kSw64 : kSw32);
+  static constexpr uint32_t kQKSBO = 8 * kQKSpan;
   static constexpr int kStages = 4;  // K/V ring
   static constexpr uint32_t kColO = 0, kColS = 128, kColP = 384;  // S buffers at 128, 256; P buffers at 384, 448
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kThreads = 352;
   static constexpr int kOffQ = 0;  // [2]
-  static constexpr int kOffK = 2 * kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffK = 2 * kQKTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kQKTileBytes;
   static constexpr int kOstBytes = kTile * D * 4;                // O staging per warpgroup (fp32 rows at most)
   static constexpr int kOffOst = kOffV + kStages * kTileBytes;    // [2]
   static constexpr int kOffStat = kOffOst + 2 * kOstBytes;         // m[128], l[128]
@@ -580,14 +653,15 @@ __device__ __forceinline__ bool fwd3_item(const FwdArgs& a, int tl, Fwd3Item& it
   return true;
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ FwdArgs a) {
-  using C = Fwd3Cfg<D>;
+  using C = Fwd3Cfg<D, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   constexpr int S = C::kStages;
   constexpr int TB = C::kTileBytes;
+  constexpr int TQK = C::kQKTileBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars;         // [2]
   uint64_t* q_empty = bars + 2;    // [2]
@@ -650,14 +724,14 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
       for (int tl = 0; ok && fwd3_item(a, tl, it); tl++) {
         const int qb = tl & 1, kvh = it.h / a.G;
         if (tl >= 2 && !(ok = mbar_wait(q_empty + qb, ((tl >> 1) - 1) & 1, abort))) break;
-        mbar_arrive_expect_tx(q_full + qb, TB);
-        tma_load_4d(smem + C::kOffQ + qb * TB, &a.map_q, q_full + qb, 0, it.h, it.i * kTile, it.b);
+        mbar_arrive_expect_tx(q_full + qb, TQK);
+        tma_load_4d(smem + C::kOffQ + qb * TQK, &a.map_q, q_full + qb, 0, it.h, it.i * kTile, it.b);
         loaded_items = tl + 1;
         for (int j = 0; j <= it.i; j++, g++) {
           const int st = g % S, use = g / S;
           if (use > 0 && !(ok = mbar_wait(kv_empty + st, (use - 1) & 1, abort))) break;
-          mbar_arrive_expect_tx(kv_full + st, 2 * TB);
-          tma_load_4d(smem + C::kOffK + st * TB, &a.map_k, kv_full + st, 0, kvh, j * kTile, it.b);
+          mbar_arrive_expect_tx(kv_full + st, TQK + TB);
+          tma_load_4d(smem + C::kOffK + st * TQK, &a.map_k, kv_full + st, 0, kvh, j * kTile, it.b);
           tma_load_4d(smem + C::kOffV + st * TB, &a.map_v, kv_full + st, 0, kvh, j * kTile, it.b);
         }
       }
@@ -670,11 +744,11 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
   } else if (warp == 1) {
     // ------------------------------------------------------------ S = Q K^T issuer
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_fp16(128, 128, false, false);
-      constexpr uint32_t kStepK = 32 >> 4;
-      constexpr uint32_t tstep = (uint32_t)TB >> 4;
-      const uint64_t dQ0 = smem_desc(smem_u32(smem + C::kOffQ), 16, C::kSBO, C::kSwz);
-      const uint64_t dK0 = smem_desc(smem_u32(smem + C::kOffK), 16, C::kSBO, C::kSwz);
+      constexpr uint32_t idS = F8 ? idesc_e4m3(128, 128, false, false) : idesc_fp16(128, 128, false, false);
+      constexpr uint32_t kStepK = 32 >> 4;  // 16 fp16 or 32 e4m3 values of K
+      constexpr uint32_t tstep = (uint32_t)TQK >> 4;
+      const uint64_t dQ0 = smem_desc(smem_u32(smem + C::kOffQ), 16, C::kQKSBO, C::kQKSwz);
+      const uint64_t dK0 = smem_desc(smem_u32(smem + C::kOffK), 16, C::kQKSBO, C::kQKSwz);
       bool ok = true;
       int g = 0;
       Fwd3Item it;
@@ -687,8 +761,12 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
           // the score buffer's previous step (g - 2) has read its scores
           if (g >= 2 && !(ok = mbar_wait(s_read + (g & 1), ((g >> 1) - 1) & 1, abort))) break;
           tc_fence_after();
-          mma_ss_chain<D / 16>(tmem + C::kColS + (g & 1) * 128, dQ0 + (uint64_t)(qb * tstep), kStepK,
-                               dK0 + (uint64_t)(st * tstep), kStepK, idS, 0u);
+          if constexpr (F8)
+            mma_ss_chain2_f8(tmem + C::kColS + (g & 1) * 128, dQ0 + (uint64_t)(qb * tstep), kStepK,
+                             dK0 + (uint64_t)(st * tstep), kStepK, idS, 0u);
+          else
+            mma_ss_chain<D / 16>(tmem + C::kColS + (g & 1) * 128, dQ0 + (uint64_t)(qb * tstep), kStepK,
+                                 dK0 + (uint64_t)(st * tstep), kStepK, idS, 0u);
           mma_commit(s_full + (g & 1));
           if (j == it.i) mma_commit(q_empty + qb);
         }
@@ -733,12 +811,16 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
     const uint32_t sbuf = trow + C::kColS + wg * 128;
     const uint32_t pbuf = trow + C::kColP + wg * 64;
     uint8_t* ost = smem + C::kOffOst + wg * C::kOstBytes;
-    const float sl2 = a.scale_log2;
+    float sl2 = a.scale_log2;
     bool ok = true;
     int g = 0, ne = 0;  // ne: this warpgroup's epilogues so far
     Fwd3Item it;
     for (int tl = 0; ok && fwd3_item(a, tl, it); tl++) {
       const int t = it.i * kTile + r;
+      if constexpr (F8) {  // scores are in e4m3 code units: fold in the two heads' scales
+        const float sq = __ldg(a.qk_amax + it.h), sk = __ldg(a.qk_amax + a.Hq + it.h / a.G);
+        sl2 = a.scale_log2 * ((sq > 0.f ? sq : 448.f) * (1.f / 448.f)) * ((sk > 0.f ? sk : 448.f) * (1.f / 448.f));
+      }
       for (int j = 0; j <= it.i; j++, g++) {
         if ((g & 1) != wg) continue;
         const bool diag = (j == it.i);
@@ -933,21 +1015,22 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
   }
 }
 
-template <int D>
+template <int D, bool F8 = false>
 cudaError_t launch_fwd3_t(const FwdArgs& a, cudaStream_t s) {
-  using C = Fwd3Cfg<D>;
+  using C = Fwd3Cfg<D, F8>;
   static bool attr_set[64] = {};
   int dev = 0, nsm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_fwd3<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    cudaError_t e =
+        cudaFuncSetAttribute(k_attn_fwd3<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   cudaError_t e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int items = a.nt * a.B * a.Hq;
-  k_attn_fwd3<D><<<items < nsm ? items : nsm, C::kThreads, C::kSmemBytes, s>>>(a);
+  k_attn_fwd3<D, F8><<<items < nsm ? items : nsm, C::kThreads, C::kSmemBytes, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -973,6 +1056,24 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
 cudaError_t launch_fwd(const FwdArgs& a, bool precise, cudaStream_t s) {
   if (a.D == 64) return precise ? launch_fwd_t<64, true>(a, s) : launch_fwd3_t<64>(a, s);
   return precise ? launch_fwd_t<32, true>(a, s) : launch_fwd3_t<32>(a, s);
+}
+
+cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t s) { return launch_fwd3_t<64, true>(a, s); }
+
+cudaError_t launch_rope_amax(const RopeArgs& a, cudaStream_t s) {
+  const long long n = (long long)a.B * a.T * (a.Hq + a.Hkv) * 8;
+  const long long want = (n + 4 * 256 - 1) / (4 * 256);
+  const int blocks = (int)(want < 4096 ? want : 4096);  // few blocks: each merges its maxima once
+  k_rope_amax<<<blocks, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_q8(const RopeArgs& a, cudaStream_t s) {
+  const long long n = (long long)a.B * a.T * (a.Hq + a.Hkv) * 8;
+  const long long want = (n + 255) / 256;
+  const int blocks = (int)(want < 65536 ? want : 65536);
+  k_rope_q8<<<blocks, 256, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_rope_qk(const RopeArgs& a, int D, cudaStream_t s) {

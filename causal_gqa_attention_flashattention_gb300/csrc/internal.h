@@ -20,6 +20,7 @@ constexpr int kFlagGradFp32 = 2;   // dq, dk, dv are float32
 constexpr int kFlagPreciseQK = 4;  // logits from hi + lo fp16 parts of rotated q and k
 constexpr int kFlagQKRotated = 8;  // backward: the workspace already holds the forward's rotated q and k
 constexpr int kFlagRopeHalf = 16;  // RoPE pairs (x[i], x[i + D/2]) instead of (x[2i], x[2i+1])
+constexpr int kFlagFp8 = 32;       // forward: rotated q, k as e4m3 with per-head scales
 
 // Largest number of query heads one forward CTA handles (TMEM/smem budget).
 inline int fwd_max_heads(int D, bool precise) { return D == 64 ? (precise ? 3 : 4) : 8; }
@@ -40,6 +41,7 @@ struct FwdArgs {
   int o_fp32;
   float scale_log2;                 // log2(e) / sqrt(D), rounded to fp32
   float scale_log2_lo;              // remainder log2(e)/sqrt(D) - scale_log2
+  const float* qk_amax;             // FP8 forward: per-head max |rotated value|, [Hq] for q then [Hkv] for k
 };
 
 // Division of a non-negative 32-bit n < 2^31 by a runtime divisor d >= 1 with
@@ -67,6 +69,8 @@ struct RopeArgs {
   int B, T, Hq, Hkv;
   int rope_half;  // half-split pair layout of q and k
   FastDiv div_hq, div_hkv, div_t;
+  uint8_t *q8, *k8;  // FP8 forward: rotated q, k as e4m3 scaled by 448 / max |value| of their head
+  float* amax;       // FP8 forward: [Hq + Hkv] per-head max |rotated value| (zeroed before the max pass)
 };
 
 struct BwdArgs {
@@ -174,6 +178,9 @@ cudaError_t launch_decode_q(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int nsm, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_rope_qk(const RopeArgs& a, int D, cudaStream_t s);
+cudaError_t launch_rope_amax(const RopeArgs& a, cudaStream_t s);  // D = 64
+cudaError_t launch_rope_q8(const RopeArgs& a, cudaStream_t s);    // D = 64
+cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t s);      // D = 64
 cudaError_t launch_bwd_prep(const PrepArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, bool precise, cudaStream_t s);
 cudaError_t launch_bwd_dq(const DqArgs& a, cudaStream_t s);

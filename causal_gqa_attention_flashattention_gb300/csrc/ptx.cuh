@@ -273,6 +273,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
 __host__ __device__ constexpr uint32_t idesc_fp16(int M, int N, bool a_mn, bool b_mn) {
   return idesc_f16kind(M, N, a_mn, b_mn, false);
 }
+// kind::f8f6f4 with both operands e4m3 (format code 0 in the same A / B fields)
+// and fp32 accumulation: the same bit pattern as fp16 under kind::f16.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_f16kind(M, N, a_mn, b_mn, false);
+}
 
 // D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -342,6 +347,18 @@ __device__ __forceinline__ void mma_ss_chain(uint32_t d, uint64_t a, uint32_t a_
         "r"(acc), "r"(idesc)
         : "memory");
   }
+}
+
+// Two MMAs of kind::f8f6f4 (8-bit operands, 32 values of K each) into one
+// accumulator; operand k at base + k * step (16-byte units).
+__device__ __forceinline__ void mma_ss_chain2_f8(uint32_t d, uint64_t a, uint32_t a_step, uint64_t b, uint32_t b_step,
+                                                 uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 q, %5, %5;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %3, %6, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %2, %4, %6, q;\n\t}" ::"r"(d),
+      "l"(a), "l"(a + (uint64_t)a_step), "l"(b), "l"(b + (uint64_t)b_step), "r"(acc), "r"(idesc)
+      : "memory");
 }
 
 // Same with the A operand in tensor memory: A_k at TMEM column a + 8k (16

@@ -48,6 +48,19 @@ __device__ __forceinline__ uint4 rope_chunk_f16(uint4 x, const float4 cs01, cons
   return make_uint4(hi[0], hi[1], hi[2], hi[3]);
 }
 
+// The same rotation left in fp32: y[0..7] for the four pairs of the chunk.
+__device__ __forceinline__ void rope_chunk_f32(uint4 x, const float4 cs01, const float4 cs23, float (&y)[8]) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  const float c[4] = {cs01.x, cs01.z, cs23.x, cs23.z};
+  const float s[4] = {cs01.y, cs01.w, cs23.y, cs23.w};
+#pragma unroll
+  for (int p = 0; p < 4; p++) {
+    const float x0 = bf_lo(w[p]), x1 = bf_hi(w[p]);
+    y[2 * p] = fmaf(x0, c[p], -x1 * s[p]);
+    y[2 * p + 1] = fmaf(x0, s[p], x1 * c[p]);
+  }
+}
+
 // Chunk c (pairs 4c..4c+3) of a bf16 row of D values, in the interleaved order
 // the rotation works on.  Interleaved rows store it as is.  In the half-split
 // layout pair i is (x[i], x[i + D/2]): the chunk gathers x[4c..4c+3] and

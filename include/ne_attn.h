@@ -86,6 +86,16 @@ typedef enum {
                                 NE_ATTN_QK_ROTATED), ne_attn_kv_append and ne_attn_decode (the
                                 cache and the queries must agree); not with NE_ATTN_PRECISE_QK
                                 (NE_ERR_UNSUPPORTED). */
+#define NE_ATTN_FP8 32       /* forward only (an inference variant), D = 64, Hq + Hkv <= 256:
+                                the rotated q and k are rounded to e4m3 with one scale per head
+                                (code = value * 448 / max |value| of the head over the whole
+                                batch, round to nearest even) and S = Q K^T runs on the tensor
+                                cores' 8-bit path (kind::f8f6f4); v, P and O keep their formats.
+                                Expect about 3e-2 relative error in o (the e4m3 rounding of q, k
+                                alone); not with NE_ATTN_PRECISE_QK or NE_ATTN_QK_ROTATED
+                                (NE_ERR_ARG), other D (NE_ERR_UNSUPPORTED).  The workspace
+                                holds the e4m3 q, k and the maxima (ne_attn_fwd_workspace_size
+                                with this flag). */
 
 /*
  * Forward pass: writes o (bfloat16) and lse.  Same as ne_attn_fwd_ex with
@@ -113,7 +123,7 @@ size_t ne_attn_fwd_workspace_size(int B, int T, int Hq, int Hkv, int D, int flag
 
 /*
  * Forward pass with flags (NE_ATTN_O_FP32, NE_ATTN_PRECISE_QK, NE_ATTN_ROPE_HALF,
- * NE_ATTN_QK_ROTATED; others rejected) and an optional caller workspace (256-byte aligned, at least
+ * NE_ATTN_QK_ROTATED, NE_ATTN_FP8; others rejected) and an optional caller workspace (256-byte aligned, at least
  * ne_attn_fwd_workspace_size bytes, else NE_ERR_WORKSPACE; the caller owns it
  * and must not touch it until the call's work on `stream` is done).  With
  * workspace = NULL the library uses a buffer of its own per stream, grown

@@ -52,3 +52,50 @@ def gather_lse(x, qsel):    # x [B,Hq,T]
 
 def make(B, T, Hq, Hkv, D, seed, recipe="normal"):
     return inputs.make_shape_inputs(B, T, Hq, Hkv, D, seed, recipe)
+
+
+# ------------------------------------------------------------------ the FP8 forward
+# The bound for NE_ATTN_FP8 (derived in tests/test_fp8_tolerance.py) is the error
+# that the e4m3 rounding of the rotated q, k alone causes on the same inputs (the
+# "floor": exact attention on the rounded values against exact attention), with a
+# 1.5x margin, plus the default path's own bounds for everything after the rounding.
+# On unit-normal inputs the floor is about 3e-2 relative in O.
+FP8_FLOOR_MARGIN = 1.5
+
+
+def fp8_bounds(floor):
+    """floor = (O rel L2, O max abs, LSE max abs) of the e4m3 emulation -> bounds."""
+    rel, mx, lse = floor
+    return (FP8_FLOOR_MARGIN * rel + REL_L2_TOL, FP8_FLOOR_MARGIN * mx + MAX_ABS_TOL,
+            FP8_FLOOR_MARGIN * lse + LSE_ABS_TOL)
+
+
+def e4m3_round(x):
+    """Round to the OCP FP8 E4M3 grid: 1 sign, 4 exponent bits (bias 7), 3
+    mantissa bits, subnormal step 2^-9, largest finite 448; round to nearest
+    even, saturating at 448 (values stay finite)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    e = np.clip(np.floor(np.log2(np.maximum(a, 2.0 ** -9))), -6, 8)
+    step = 2.0 ** (e - 3)
+    return np.sign(x) * np.minimum(np.round(a / step) * step, 448.0)
+
+
+def e4m3_per_head(xr):
+    """xr [B,T,H,D] rotated values -> their e4m3 rounding with one scale per head
+    (code = value * 448 / max |value| over the head's batches, positions and
+    features), returned as values (code * max / 448)."""
+    amax = np.max(np.abs(xr), axis=(0, 1, 3), keepdims=True)
+    s = np.where(amax > 0, amax / 448.0, 1.0)
+    return e4m3_round(xr / s) * s
+
+
+def fp8_floor(oracle_mod, x, base, half=False):
+    """Exact attention on e4m3-rounded rotated q, k (per-head scales) against
+    exact attention: returns ((rel, max abs, LSE max abs), ref_o, ref_lse)."""
+    ref_o, ref_l = oracle_mod.attn_fwd(x["q"], x["k"], x["v"], base, half=half)
+    q8 = oracle_mod.rope(e4m3_per_head(oracle_mod.rope(x["q"], base, half=half)), base, inverse=True, half=half)
+    k8 = oracle_mod.rope(e4m3_per_head(oracle_mod.rope(x["k"], base, half=half)), base, inverse=True, half=half)
+    o8, l8 = oracle_mod.attn_fwd(q8, k8, x["v"], base, half=half)
+    rel, mx = errors(o8, ref_o)
+    return (rel, mx, float(np.max(np.abs(l8 - ref_l)))), ref_o, ref_l

@@ -187,3 +187,23 @@ def test_qkv_host_argument_checks(libne):
     bx = libne.ne_attn_bwd
     assert bx(null, null, p, p, p, p, p, p, p, 1, 4, 4, 2, 32, 10000.0, 0, p, 1 << 20, null) == -1
     assert bx(null, null, p, p, p, p, p, p, p, 1, 4, 4, 2, 32, 10000.0, 8, p, 64, null) == -5
+
+
+def test_fp8_flag_rules_on_the_host(libne):
+    B, T, Hq, Hkv, D = 16, 512, 12, 4, 64
+    n8 = libne.ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, 32)
+    assert n8 == B * T * (Hq + Hkv) * D + 256  # e4m3 q and k, then the per-head maxima
+    assert libne.ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, 32 | 16) == n8  # either rotary layout
+    assert libne.ne_attn_fwd_workspace_size(B, T, Hq, Hkv, 32, 32) == 0       # D = 64 only
+    assert libne.ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, 32 | 4) == 0    # not with precise logits
+    assert libne.ne_attn_fwd_workspace_size(B, T, Hq, Hkv, D, 32 | 8) == 0    # the library rotates
+    assert libne.ne_attn_fwd_workspace_size(1, 16, 256, 1, D, 32) == 0        # at most 256 heads in all
+    assert libne.ne_attn_bwd_workspace_size(B, T, Hq, Hkv, D, 32) == 0        # forward only
+    buf = ctypes.create_string_buffer(4096 + 512)
+    p = ctypes.c_void_p((ctypes.addressof(buf) + 255) // 256 * 256)
+    null = None
+    fx = libne.ne_attn_fwd_ex
+    assert fx(p, p, p, p, p, 1, 16, 2, 1, 32, 10000.0, 32, null, 0, null) == -3
+    assert fx(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 32 | 4, null, 0, null) == -1
+    assert fx(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 32, p, 64, null) == -5  # workspace too small
+    assert fx(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 64, null, 0, null) == -1  # unknown flag

@@ -469,6 +469,7 @@ def run_decode(args):
         prof = binding.profile_read(prof_cap)
         ms_call = e0.elapsed_time(e1) / (reps * nsets)
         ms_sweep = prof["decode"][0] / max(1, prof["decode"][1])
+        dec_tr = traffic_record("k_decode")
         achieved = cache_bytes / (ms_sweep * 1e-3) / 1e9
         line = dict(metric="decode: KV-cache bytes read per second (one decode step, all sequences)",
                     value=cache_bytes / (ms_call * 1e-3) / 1e9, unit="GB/s", n_gpus=1, steps=reps * nsets,
@@ -479,7 +480,10 @@ def run_decode(args):
                                 launch="CUDA graph replay (3 library kernels per decode call)"),
                     tokens_per_s=B * Tq / (ms_call * 1e-3),
                     roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
-                                  frac=achieved / peaks["hbm_gbs"], kernel="decode", traffic=None,
+                                  frac=achieved / peaks["hbm_gbs"], kernel="decode",
+                                  # the committed capture is of the 8192-position workload
+                                  traffic=(dec_tr["dram_bytes_per_launch"]
+                                           if dec_tr and name == "decode_116m_ctx8192" else None),
                                   peak_source="%s hbm" % peaks["source"], per_launch_us=ms_sweep * 1e3,
                                   kernels={k: dict(us_per_launch=v[0] / v[1] * 1e3, launches=v[1])
                                            for k, v in prof.items() if v[1]}),
@@ -676,7 +680,9 @@ def run_fp8(args):
                                               for k, v in prof16.items() if v[1]}),
                 roofline=dict(bound="tensor", achieved=achieved, peak=peaks["bf16_tflops"], unit="TFLOP/s",
                               frac=achieved / peaks["bf16_tflops"], kernel="fwd",
-                              traffic=None, peak_source="%s bf16 (burst); S runs at the 8-bit rate, P V at bf16"
+                              traffic=(lambda tr: tr["dram_bytes_per_launch"] if tr else None)(
+                                  traffic_record("k_attn_fwd3_fp8")),
+                              peak_source="%s bf16 (burst); S runs at the 8-bit rate, P V at bf16"
                               % peaks["source"], per_launch_us=ms_attn * 1e3,
                               kernels={k: dict(us_per_launch=v[0] / v[1] * 1e3, launches=v[1])
                                        for k, v in prof8.items() if v[1]}),

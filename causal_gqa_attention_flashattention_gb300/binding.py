@@ -360,3 +360,69 @@ def rotated_qk(workspace, B, T, Hq, Hkv, D):
     qr = workspace[:nq].view(torch.float16).view(B, T, Hq, D)
     kr = workspace[up(nq):up(nq) + nk].view(torch.float16).view(B, T, Hkv, D)
     return qr, kr
+
+
+class HostStepPipeline:
+    """Forward + backward steps on host tensors, with the copies of one step
+    overlapping the compute of the others.
+
+    Inputs go up on one stream, the library's kernels run on a second, results
+    come down on a third; `depth` device buffer sets rotate, and CUDA events
+    order each set's reuse (a set is refilled only after its previous results
+    have come down).  Host tensors should be pinned so the copies run
+    asynchronously.  submit() only enqueues work; synchronize() waits for all
+    of it and raises if a kernel reported a device-side timeout.
+    """
+
+    def __init__(self, B, T, Hq, Hkv, D, rope_base=10000.0, depth=3, grad_dtype=torch.float32,
+                 o_dtype=torch.bfloat16, device="cuda"):
+        self.shape = (B, T, Hq, Hkv, D)
+        self.rope_base = float(rope_base)
+        self.grad_dtype = grad_dtype
+        self.device = torch.device(device)
+        self.up = torch.cuda.Stream(self.device)
+        self.comp = torch.cuda.Stream(self.device)
+        self.down = torch.cuda.Stream(self.device)
+        self.sets = []
+        for _ in range(depth):
+            def bf(h):
+                return torch.empty((B, T, h, D), dtype=torch.bfloat16, device=self.device)
+            self.sets.append(dict(
+                q=bf(Hq), k=bf(Hkv), v=bf(Hkv), do=bf(Hq),
+                o=torch.empty((B, T, Hq, D), dtype=o_dtype, device=self.device),
+                lse=torch.empty((B, Hq, T), dtype=torch.float32, device=self.device),
+                dq=torch.empty((B, T, Hq, D), dtype=grad_dtype, device=self.device),
+                dk=torch.empty((B, T, Hkv, D), dtype=grad_dtype, device=self.device),
+                dv=torch.empty((B, T, Hkv, D), dtype=grad_dtype, device=self.device),
+                ws=alloc_workspace(B, T, Hq, Hkv, D, device=self.device),
+                up_done=torch.cuda.Event(), comp_done=torch.cuda.Event(), down_done=torch.cuda.Event(),
+                used=False))
+        self.n = 0
+
+    def submit(self, q, k, v, dout, out):
+        """Enqueue one step: q, k, v, dout are host bf16 tensors; `out` maps
+        o, lse, dq, dk, dv to host tensors that receive the results."""
+        s = self.sets[self.n % len(self.sets)]
+        self.n += 1
+        if s["used"]:
+            self.up.wait_event(s["down_done"])  # the set's last results have come down
+        with torch.cuda.stream(self.up):
+            for name, src in (("q", q), ("k", k), ("v", v), ("do", dout)):
+                s[name].copy_(src, non_blocking=True)
+            s["up_done"].record(self.up)
+        self.comp.wait_event(s["up_done"])
+        attn_fwd(s["q"], s["k"], s["v"], self.rope_base, o=s["o"], lse=s["lse"], workspace=s["ws"],
+                 stream=self.comp)
+        attn_bwd(s["q"], s["k"], s["v"], s["o"], s["lse"], s["do"], self.rope_base, grad_dtype=self.grad_dtype,
+                 dq=s["dq"], dk=s["dk"], dv=s["dv"], workspace=s["ws"], qk_rotated=True, stream=self.comp)
+        s["comp_done"].record(self.comp)
+        self.down.wait_event(s["comp_done"])
+        with torch.cuda.stream(self.down):
+            for name in ("o", "lse", "dq", "dk", "dv"):
+                out[name].copy_(s[name], non_blocking=True)
+            s["down_done"].record(self.down)
+        s["used"] = True
+
+    def synchronize(self):
+        self.down.synchronize()
+        check_status(self.comp)

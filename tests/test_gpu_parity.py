@@ -362,3 +362,33 @@ def test_half_split_layout_changes_the_result(nb):
 def test_decode_half_split_layout(nb, oracle_mod, shape):
     decode_case(nb, oracle_mod, shape, half=True)
 
+
+
+def test_host_step_pipeline(nb, oracle_mod):
+    """Five pipelined steps on three different inputs through two rotating device
+    buffer sets: every step's results match the oracle for its own inputs."""
+    B, T, Hq, Hkv, D = 2, 300, 4, 2, 64
+    xs = [H.make(B, T, Hq, Hkv, D, seed=900 + i) for i in range(3)]
+
+    def host(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+
+    hosts = [[host(x[n + "_bits"]) for n in ("q", "k", "v", "dout")] for x in xs]
+    pipe = nb.HostStepPipeline(B, T, Hq, Hkv, D, inputs.ROPE_BASE, depth=2)
+    outs = []
+    for i in range(5):
+        out = dict(o=torch.empty((B, T, Hq, D), dtype=torch.bfloat16).pin_memory(),
+                   lse=torch.empty((B, Hq, T), dtype=torch.float32).pin_memory(),
+                   dq=torch.empty((B, T, Hq, D), dtype=torch.float32).pin_memory(),
+                   dk=torch.empty((B, T, Hkv, D), dtype=torch.float32).pin_memory(),
+                   dv=torch.empty((B, T, Hkv, D), dtype=torch.float32).pin_memory())
+        pipe.submit(*hosts[i % 3], out)
+        outs.append(out)
+    pipe.synchronize()
+    refs = [oracle_mod.attn_bwd(x["q"], x["k"], x["v"], x["dout"], inputs.ROPE_BASE) for x in xs]
+    for i, out in enumerate(outs):
+        ref = refs[i % 3]
+        for n in ("o", "dq", "dk", "dv"):
+            rel, mx = H.errors(out[n].float().numpy().astype(np.float64), ref[n])
+            assert rel <= H.REL_L2_TOL and mx <= H.MAX_ABS_TOL, (i, n, rel, mx)
+        assert np.max(np.abs(out["lse"].numpy() - ref["lse"])) <= H.LSE_ABS_TOL

@@ -477,7 +477,7 @@ def run_decode(args):
                     vs_baseline=None, dtype="fp16 keys, bf16 values, fp32 accumulate", data="synthetic",
                     config=dict(workload=name, B=B, Tkv=Tkv, Tq=Tq, Hq=Hq, Hkv=Hkv, D=D, cache_sets=nsets,
                                 l2="%d rotating cache sets of %.1f MB" % (nsets, cache_bytes / 1e6),
-                                launch="CUDA graph replay (3 library kernels per decode call)"),
+                                launch="CUDA graph replay (2 library kernels per decode call)"),
                     tokens_per_s=B * Tq / (ms_call * 1e-3),
                     roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
                                   frac=achieved / peaks["hbm_gbs"], kernel="decode",

@@ -333,7 +333,7 @@ int fp8_rules(int flags, int Hq, int Hkv, int D) {
 
 // Decode workspace: packed rotated queries, then the splits' partial O and (max, sum).
 struct DecodeWs {
-  size_t qpk, part_o, part_ml, total;
+  size_t qpk, part_o, part_ml, done, total;
 };
 int decode_copies(int R) { return R <= 32 ? 4 : (R <= 64 ? 2 : 1); }
 DecodeWs decode_ws(int B, int Tq, int Tkv, int Hq, int Hkv, int D) {
@@ -343,7 +343,8 @@ DecodeWs decode_ws(int B, int Tq, int Tkv, int Hq, int Hkv, int D) {
   w.qpk = 0;
   w.part_o = ws_up((size_t)B * Hkv * kTile * D * 2);
   w.part_ml = w.part_o + ws_up((size_t)B * Hkv * ntk * F * R * D * 4);
-  w.total = w.part_ml + ws_up((size_t)B * Hkv * ntk * F * R * 8);
+  w.done = w.part_ml + ws_up((size_t)B * Hkv * ntk * F * R * 8);
+  w.total = w.done + ws_up((size_t)B * Hkv * 4);
   return w;
 }
 
@@ -977,6 +978,7 @@ int ne_attn_decode(const void* q, const void* k_cache, const void* v_cache, void
   a.qpk = reinterpret_cast<__half*>(ws + w.qpk);
   a.part_o = reinterpret_cast<float*>(ws + w.part_o);
   a.part_ml = reinterpret_cast<float*>(ws + w.part_ml);
+  a.done = reinterpret_cast<unsigned*>(ws + w.done);
   a.o = o;
   a.lse = lse;
   a.status = d->status;
@@ -996,7 +998,7 @@ int ne_attn_decode(const void* q, const void* k_cache, const void* v_cache, void
   // Splits of each (batch, key/value head)'s key tiles: the count whose slowest
   // CTA (work items per CTA x tiles per item, plus about one tile of fixed cost
   // per item) is shortest; among equals the smaller count, which leaves fewer
-  // partial results for the combine to merge.
+  // partial results to merge.
   const long long bh = (long long)B * Hkv;
   long long best = -1;
   for (int ns = 1; ns <= a.ntk && ns <= 64; ns++) {
@@ -1016,12 +1018,8 @@ int ne_attn_decode(const void* q, const void* k_cache, const void* v_cache, void
     ProfScope prof(NE_ATTN_KERNEL_DECODE_AUX, s);
     if (launch_decode_q(a, s) != cudaSuccess) return NE_ERR_CUDA;
   }
-  {
-    ProfScope prof(NE_ATTN_KERNEL_DECODE, s);
-    if (launch_decode(a, nsm, s) != cudaSuccess) return NE_ERR_CUDA;
-  }
-  ProfScope prof(NE_ATTN_KERNEL_DECODE_AUX, s);
-  return launch_decode_combine(a, s) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+  ProfScope prof(NE_ATTN_KERNEL_DECODE, s);
+  return launch_decode(a, nsm, s) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
 }
 
 int ne_attn_debug_timeout_probe(int limit_us, void* stream) {

@@ -17,8 +17,9 @@
 //                     items (batch, key/value head, split of the key tiles);
 //                     S = Q K^T and O += P V on the tensor cores, an online softmax
 //                     in between; each item leaves its unnormalised O and its
-//                     running max and sum for the rows of the tile
-//   k_decode_combine  the splits of a row merged: O = sum 2^(m_s - m) O_s / l
+//                     running max and sum for the rows of the tile, and the CTA
+//                     that finishes a group's last split merges the group's
+//                     partials: O = sum 2^(m_s - m) O_s / l
 //
 // Decode streams the cache once and does little arithmetic per byte, so the
 // sweep is bound by HBM; the G query heads of a key/value head (and the Tq
@@ -65,6 +66,44 @@ __global__ void __launch_bounds__(256) k_kv_append(const KvAppendArgs a) {
   }
 }
 
+// ====================================================================== merging the partials
+// Row r (token r / G, head g * G + r % G) of group bk = b * Hkv + g, one warp:
+// O = sum_s 2^(m_s - m) O_s / l with l = sum_s 2^(m_s - m) l_s over the
+// nsplit x F partials (splits of the cache, copies of the query rows).
+template <int D>
+__device__ __forceinline__ void merge_row(const DecodeArgs& a, int bk, int r, int lane) {
+  constexpr int kPer = D / 32;
+  const int b = bk / a.Hkv, g = bk - b * a.Hkv;
+  const int t = r / a.G, h = g * a.G + (r - t * a.G);
+  const int npart = a.nsplit * a.F;
+  const size_t base = (size_t)bk * npart;
+  const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
+  float m = -INFINITY;
+  for (int p = 0; p < npart; p++) m = fmaxf(m, __ldcg(&ml[(base + p) * a.R + r].x));
+  float acc[kPer], L = 0.f;
+#pragma unroll
+  for (int e = 0; e < kPer; e++) acc[e] = 0.f;
+  for (int p = 0; p < npart; p++) {
+    const size_t pr = (base + p) * a.R + r;
+    const float2 v = __ldcg(&ml[pr]);
+    if (v.y == 0.f) continue;  // no visible key in this part
+    const float w = ex2(v.x - m);
+    L += w * v.y;
+#pragma unroll
+    for (int e = 0; e < kPer; e++) acc[e] += w * __ldcg(a.part_o + pr * D + lane + 32 * e);
+  }
+  const float inv = 1.f / L;
+  const size_t orow = (((size_t)b * a.Tq + t) * a.Hq + h) * D;
+#pragma unroll
+  for (int e = 0; e < kPer; e++) {
+    if (a.o_fp32)
+      static_cast<float*>(a.o)[orow + lane + 32 * e] = acc[e] * inv;
+    else
+      static_cast<__nv_bfloat16*>(a.o)[orow + lane + 32 * e] = __float2bfloat16_rn(acc[e] * inv);
+  }
+  if (lane == 0) a.lse[((size_t)b * a.Hq + h) * a.Tq + t] = (m + __log2f(L)) * kLn2;
+}
+
 // ====================================================================== packed queries
 template <int D>
 __global__ void __launch_bounds__(256) k_decode_q(const DecodeArgs a) {
@@ -87,6 +126,9 @@ __global__ void __launch_bounds__(256) k_decode_q(const DecodeArgs a) {
     }
     reinterpret_cast<uint4*>(a.qpk)[it] = out;
   }
+  // the sweep counts finished splits per (batch, kv head) group from zero
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < (uint32_t)(a.B * a.Hkv); i += gridDim.x * blockDim.x)
+    a.done[i] = 0u;
 }
 
 // ====================================================================== split sweep
@@ -128,7 +170,8 @@ __device__ __forceinline__ bool dec_item(const DecodeArgs& a, int tl, DecItem& i
 template <int D, int W>
 __device__ __forceinline__ bool decode_softmax(const DecodeArgs& a, uint32_t tmem, int warp, int lane, uint64_t* s_full,
                                                uint64_t* s_read, uint64_t* p_ready, uint64_t* pv_done,
-                                               uint64_t* o_free, volatile int* abort) {
+                                               uint64_t* o_free, uint64_t* part_done, uint64_t* merge_go,
+                                               volatile int* merge_flag, int nact, volatile int* abort) {
   using C = DecCfg<D>;
   const int q4 = warp & 3;        // TMEM lane quarter
   const int rr = q4 * 32 + lane;  // row of the packed tile
@@ -258,6 +301,31 @@ __device__ __forceinline__ bool decode_softmax(const DecodeArgs& a, uint32_t tme
       reinterpret_cast<float2*>(a.part_ml)[prow] = make_float2(r_max == -INFINITY ? -INFINITY : __fmul_rn(r_max, sl2), l);
     tc_fence_before();
     warp_arrive(o_free);  // the next item's first P V may overwrite O
+    // The CTA that completes a group's last split merges the group's partials
+    // (a count of finished splits per group; fences order the partials before it).
+    __threadfence();
+    warp_arrive(part_done);
+    if (q4 == 0) {  // quarter 0 always holds query rows
+      bool good = true;
+      if (lane == 0) {
+        good = mbar_wait(part_done, tl & 1, abort);
+        if (good) {
+          __threadfence();
+          *merge_flag = atomicAdd(a.done + it.bk, 1u) == (unsigned)(a.nsplit - 1) ? 1 : 0;
+          __threadfence();
+          mbar_arrive(merge_go);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+      if (!ok) break;
+    }
+    ok = __all_sync(0xffffffffu, mbar_wait(merge_go, tl & 1, abort));
+    if (!ok) break;
+    if (*merge_flag) {
+      __threadfence();
+      for (int row = (rr >> 5) % nact; row < a.R; row += nact)  // one warp per row
+        merge_row<D>(a, it.bk, row, lane);
+    }
   }
   return ok;
 }
@@ -281,8 +349,11 @@ __global__ void __launch_bounds__(224, 1) k_decode(const __grid_constant__ Decod
   uint64_t* pv_done = s_full + 3;
   uint64_t* o_free = s_full + 4;      // an item's O has been read out
   uint64_t* drain = s_full + 5;       // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 7);
-  volatile int* abort = reinterpret_cast<volatile int*>(s_full + 7) + 1;
+  uint64_t* part_done = s_full + 7;   // the item's partials are written (one arrival per active softmax warp)
+  uint64_t* merge_go = s_full + 8;    // merge_flag says whether this CTA merges the group
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 9);
+  volatile int* abort = reinterpret_cast<volatile int*>(s_full + 9) + 1;
+  volatile int* merge_flag = reinterpret_cast<volatile int*>(s_full + 9) + 2;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // softmax warps whose TMEM lane quarter holds query rows (the others sit out)
   int nact = 0;
@@ -304,6 +375,8 @@ __global__ void __launch_bounds__(224, 1) k_decode(const __grid_constant__ Decod
     mbar_init(p_ready, nact);
     mbar_init(pv_done, 1);
     mbar_init(o_free, nact);
+    mbar_init(part_done, nact);
+    mbar_init(merge_go, 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_slot, C::kTmemCols);
@@ -402,11 +475,14 @@ __global__ void __launch_bounds__(224, 1) k_decode(const __grid_constant__ Decod
     // ------------------------------------------------------------ softmax, one row per thread
     bool ok;
     if (a.F == 4)
-      ok = decode_softmax<D, 32>(a, tmem, warp, lane, s_full, s_read, p_ready, pv_done, o_free, abort);
+      ok = decode_softmax<D, 32>(a, tmem, warp, lane, s_full, s_read, p_ready, pv_done, o_free, part_done, merge_go,
+                                 merge_flag, nact, abort);
     else if (a.F == 2)
-      ok = decode_softmax<D, 64>(a, tmem, warp, lane, s_full, s_read, p_ready, pv_done, o_free, abort);
+      ok = decode_softmax<D, 64>(a, tmem, warp, lane, s_full, s_read, p_ready, pv_done, o_free, part_done, merge_go,
+                                 merge_flag, nact, abort);
     else
-      ok = decode_softmax<D, 128>(a, tmem, warp, lane, s_full, s_read, p_ready, pv_done, o_free, abort);
+      ok = decode_softmax<D, 128>(a, tmem, warp, lane, s_full, s_read, p_ready, pv_done, o_free, part_done, merge_go,
+                                  merge_flag, nact, abort);
     if (!ok) record_timeout(a.status, abort);
   }
 
@@ -416,49 +492,6 @@ __global__ void __launch_bounds__(224, 1) k_decode(const __grid_constant__ Decod
   if (warp == 0) {
     tmem_relinquish();
     tmem_dealloc(tmem, C::kTmemCols);
-  }
-}
-
-// ====================================================================== combine
-// One warp per (b, t, h) row: O = sum_s 2^(m_s - m) O_s / l, l = sum_s 2^(m_s - m) l_s.
-template <int D>
-__global__ void __launch_bounds__(256) k_decode_combine(const DecodeArgs a) {
-  constexpr int kPer = D / 32;
-  const int lane = threadIdx.x & 31;
-  const uint32_t nrows = (uint32_t)a.B * a.Tq * a.Hq;
-  for (uint32_t row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < nrows;
-       row += (gridDim.x * blockDim.x) >> 5) {
-    const uint32_t bt = row / a.Hq, h = row - bt * a.Hq;
-    const uint32_t b = bt / a.Tq, t = bt - b * a.Tq;
-    const uint32_t g = h / a.G, gg = h - g * a.G;
-    const int r = (int)(t * a.G + gg);
-    const int npart = a.nsplit * a.F;  // splits x copies of the query rows
-    const size_t base = ((size_t)b * a.Hkv + g) * npart;
-    const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
-    float m = -INFINITY;
-    for (int s = 0; s < npart; s++) m = fmaxf(m, ml[(base + s) * a.R + r].x);
-    float acc[kPer], L = 0.f;
-#pragma unroll
-    for (int e = 0; e < kPer; e++) acc[e] = 0.f;
-    for (int s = 0; s < npart; s++) {
-      const size_t pr = (base + s) * a.R + r;
-      const float2 v = ml[pr];
-      if (v.y == 0.f) continue;  // no visible key in this split
-      const float w = ex2(v.x - m);
-      L += w * v.y;
-#pragma unroll
-      for (int e = 0; e < kPer; e++) acc[e] += w * a.part_o[pr * D + lane + 32 * e];
-    }
-    const float inv = 1.f / L;
-    const size_t orow = (((size_t)b * a.Tq + t) * a.Hq + h) * D;
-#pragma unroll
-    for (int e = 0; e < kPer; e++) {
-      if (a.o_fp32)
-        static_cast<float*>(a.o)[orow + lane + 32 * e] = acc[e] * inv;
-      else
-        static_cast<__nv_bfloat16*>(a.o)[orow + lane + 32 * e] = __float2bfloat16_rn(acc[e] * inv);
-    }
-    if (lane == 0) a.lse[((size_t)b * a.Hq + h) * a.Tq + t] = (m + __log2f(L)) * kLn2;
   }
 }
 
@@ -507,15 +540,6 @@ cudaError_t launch_decode_q(const DecodeArgs& a, cudaStream_t s) {
 
 cudaError_t launch_decode(const DecodeArgs& a, int nsm, cudaStream_t s) {
   return a.D == 64 ? launch_decode_t<64>(a, s, nsm) : launch_decode_t<32>(a, s, nsm);
-}
-
-cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s) {
-  const long long rows = (long long)a.B * a.Tq * a.Hq;
-  if (a.D == 64)
-    k_decode_combine<64><<<grid_for(rows * 32, 256), 256, 0, s>>>(a);
-  else
-    k_decode_combine<32><<<grid_for(rows * 32, 256), 256, 0, s>>>(a);
-  return cudaGetLastError();
 }
 
 }  // namespace ne

@@ -136,6 +136,7 @@ struct DecodeArgs {
   __half* qpk;               // [B, Hkv, 128, D] packed rotated queries (workspace)
   float* part_o;             // [B, Hkv, nsplit, F, R, D] unnormalised O per split and copy (workspace)
   float* part_ml;            // [B, Hkv, nsplit, F, R] (max in log2 units, sum) pairs (workspace)
+  unsigned* done;            // [B * Hkv] finished splits per group (workspace; zeroed by the query pass)
   void* o;                   // [B, Tq, Hq, D] bf16 or fp32
   float* lse;                // [B, Hq, Tq]
   const float2* rope;
@@ -176,7 +177,6 @@ cudaError_t launch_fwd(const FwdArgs& a, bool precise, cudaStream_t s);
 cudaError_t launch_kv_append(const KvAppendArgs& a, int D, cudaStream_t s);
 cudaError_t launch_decode_q(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int nsm, cudaStream_t s);
-cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_rope_qk(const RopeArgs& a, int D, cudaStream_t s);
 cudaError_t launch_rope_amax(const RopeArgs& a, cudaStream_t s);  // D = 64
 cudaError_t launch_rope_q8(const RopeArgs& a, cudaStream_t s);    // D = 64

@@ -232,10 +232,11 @@ size_t ne_attn_decode_workspace_size(int B, int Tq, int Tkv, int Hq, int Hkv, in
  * (Hq / Hkv) * Tq <= 128: the queries of one key/value head fill at most one
  * 128-row tile, which every K/V tile of the cache serves at once.  The
  * workspace is required.
- * Three kernels: query rotation and packing; a sweep over the cache in which
+ * Two kernels: query rotation and packing; a sweep over the cache in which
  * one CTA per SM takes work items (batch, key/value head, split of the key
  * tiles) and runs S = Q K^T and O += P V on the tensor cores with an online
- * softmax; and a combine of the splits.  The result is bitwise reproducible.
+ * softmax, where the CTA that finishes the last split of a (batch, key/value
+ * head) merges that group's splits.  The result is bitwise reproducible.
  */
 int ne_attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B, int Tq,
                    int Tkv, int Tcap, int Hq, int Hkv, int D, float rope_base, int flags, void* workspace,
@@ -308,7 +309,7 @@ const char* ne_attn_status_string(int status);
 #define NE_ATTN_KERNEL_FWD_ROPE 4 /* the forward's RoPE pre-pass */
 #define NE_ATTN_KERNEL_KV_APPEND 5
 #define NE_ATTN_KERNEL_DECODE 6     /* the split sweep over the cache */
-#define NE_ATTN_KERNEL_DECODE_AUX 7 /* query packing and the combine of the splits */
+#define NE_ATTN_KERNEL_DECODE_AUX 7 /* query rotation and packing */
 #define NE_ATTN_KERNEL_QKV_PREP 8   /* RMSNorm row statistics and the weight fold */
 #define NE_ATTN_KERNEL_QKV 9        /* the projection GEMM with the rotary epilogue */
 #define NE_ATTN_NUM_KERNEL_KINDS 10

@@ -406,7 +406,7 @@ def run_decode(args):
     The caches (rotated fp16 keys, bf16 values) are filled through the public
     append call from seeded N(0,1) data; enough cache sets rotate through the
     timed graph that their total exceeds L2 twice over.  The timed region
-    replays a CUDA graph of decode calls (query packing, split sweep, combine).
+    replays a CUDA graph of decode calls (query packing, then the split sweep with its merge).
     """
     import torch
     from causal_gqa_attention_flashattention_gb300 import binding

@@ -49,14 +49,20 @@ __global__ void __launch_bounds__(256) k_qkv_prep(const QkvArgs a, int row_block
     if (row >= a.M) return;
     const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)row * a.C);
     float ss = 0.f;
-    for (int c = lane; c < cpr; c += 32) {
-      const uint4 u = __ldg(xr + c);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    // four chunks per lane in flight at once (a 768-wide row is three)
+    for (int c0 = lane; c0 < cpr; c0 += 128) {
+      uint4 u[4];
 #pragma unroll
-      for (int p = 0; p < 4; p++) {
-        const float lo = __uint_as_float(w[p] << 16), hi = __uint_as_float(w[p] & 0xFFFF0000u);
-        ss = fmaf(lo, lo, ss);
-        ss = fmaf(hi, hi, ss);
+      for (int k = 0; k < 4; k++) u[k] = c0 + 32 * k < cpr ? __ldg(xr + c0 + 32 * k) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const uint32_t w[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+#pragma unroll
+        for (int p = 0; p < 4; p++) {
+          const float lo = __uint_as_float(w[p] << 16), hi = __uint_as_float(w[p] & 0xFFFF0000u);
+          ss = fmaf(lo, lo, ss);
+          ss = fmaf(hi, hi, ss);
+        }
       }
     }
 #pragma unroll

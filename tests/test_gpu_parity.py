@@ -392,3 +392,21 @@ def test_host_step_pipeline(nb, oracle_mod):
             rel, mx = H.errors(out[n].float().numpy().astype(np.float64), ref[n])
             assert rel <= H.REL_L2_TOL and mx <= H.MAX_ABS_TOL, (i, n, rel, mx)
         assert np.max(np.abs(out["lse"].numpy() - ref["lse"])) <= H.LSE_ABS_TOL
+
+
+def test_decode_is_bitwise_reproducible(nb):
+    """The splits of a group are merged by whichever CTA finishes last, in a
+    fixed order: repeated calls (and calls after other shapes have used the
+    workspace's counters) give the same bits."""
+    B, Tkv, Tq, Hq, Hkv, D = 4, 6000, 2, 12, 4, 64
+    x = H.make(B, Tkv, Hq, Hkv, D, seed=77)
+    k, v = (H.to_device(x[n + "_bits"]) for n in ("k", "v"))
+    q = H.to_device(x["q_bits"])[:, Tkv - Tq:].contiguous()
+    kc, vc = nb.kv_cache(B, Tkv, Hkv, D, "cuda")
+    nb.kv_append(k, v, kc, vc, 0)
+    ws = torch.empty(nb.decode_workspace_size(B, Tq, Tkv, Hq, Hkv, D), dtype=torch.uint8, device="cuda")
+    o1, l1 = nb.attn_decode(q, kc, vc, Tkv, workspace=ws)
+    nb.attn_decode(q[:, :1].contiguous(), kc, vc, 300, workspace=ws)  # another shape through the same workspace
+    o2, l2 = nb.attn_decode(q, kc, vc, Tkv, workspace=ws)
+    nb.check_status()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)

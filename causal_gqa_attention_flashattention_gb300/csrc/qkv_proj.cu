@@ -18,10 +18,12 @@
 //                stages, 64-wide K blocks go to the tensor cores as four
 //                128 x BN x 16 MMAs into one of two TMEM accumulators, and four
 //                epilogue warps read the other accumulator (one output row per
-//                thread), scale it by rstd, rotate query and key features
-//                (the rotary embedding, socker-news README "Architecture") and
-//                store q, k, v (bf16) and the rotated q, k (fp16, the operand
-//                format of the attention forward and backward)
+//                thread), scale it by rstd and rotate query and key features
+//                (the rotary embedding, socker-news README "Architecture");
+//                v (bf16) and the rotated q, k (fp16, the operand format of the
+//                attention forward and backward) leave through shared-memory
+//                boxes that a seventh warp stores with TMA, plain q, k (bf16,
+//                optional) straight from registers
 //
 // The rotated fp16 q and k land in the layout of the attention forward's
 // workspace, so the forward can skip its own rotation pass.
@@ -105,9 +107,11 @@ struct QkvCfg {
   static constexpr int kNStg = 8;             // staging boxes in flight
   static constexpr int kStgLag = 4;           // stores the store warp keeps unread before freeing a box
   static constexpr int kBudget = 226 * 1024;
-  static_assert(2 * 6 + 4 + 2 * 8 + 1 <= 62, "barriers, slot and flag fit in 512 bytes");
   static constexpr int kFit = (kBudget - kNStg * kStgBytes) / kStageBytes;
   static constexpr int kStages = kFit < 6 ? kFit : 6;
+  // full / empty per stage, two accumulators' full / empty, staging full / free,
+  // drain, then the TMEM slot and the abort flag: all within 512 bytes
+  static_assert((2 * kStages + 4 + 2 * kNStg + 1) * 8 + 8 <= 512, "barrier area");
   static constexpr int kOffStg = kStages * kStageBytes;
   static constexpr int kOffBar = kOffStg + kNStg * kStgBytes;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // barriers, slot, flag; alignment slack
@@ -115,7 +119,7 @@ struct QkvCfg {
   static constexpr int kThreads = 224;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warp 6 stores
 };
 
-// Eight fp32 values -> one 16-byte chunk of four bf16 or fp16 pairs.
+// Eight fp32 values -> one 16-byte chunk of four bf16 pairs.
 __device__ __forceinline__ uint4 pack8_bf16(const float* y) {
   return make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
 }

@@ -162,3 +162,20 @@ def test_qkv_bad_arguments(nb):
     with pytest.raises(ValueError):
         nb.qkv_rmsnorm(dx, dw, dW, 2, 1, 32, write_qk=False)  # nothing would hold q and k
     nb.check_status()
+
+
+@pytest.mark.parametrize("shape,base", [((4, 1, 64, 2, 1, 32), inputs.ROPE_BASE), ((2, 150, 128, 4, 2, 64), 500000.0)],
+                         ids=["one_position", "base_500000"])
+def test_qkv_other_sizes_and_base(nb, oracle_mod, shape, base):
+    """Sequences of one position (four rows in all) and another rotary base."""
+    B, T, C, Hq, Hkv, D = shape
+    x = inputs.make_prologue_inputs(B, T, C, Hq, Hkv, D, seed=31 + T)
+    dx, dw, dW = (H.to_device(x[n + "_bits"]) for n in ("x", "norm_w", "w_qkv"))
+    q, k, v, rstd, ws = nb.qkv_rmsnorm(dx, dw, dW, Hq, Hkv, D, eps=EPS, rope_base=base, rotated=True)
+    nb.check_status()
+    rq, rk, rv, rr = oracle_mod.qkv_rmsnorm(x["x"], x["norm_w"], x["w_qkv"], Hq, Hkv, D, eps=EPS)
+    check("q", H.to_f64(q), rq)
+    check("v", H.to_f64(v), rv)
+    qr, kr = nb.rotated_qk(ws, B, T, Hq, Hkv, D)
+    check("q rotated", H.to_f64(qr), oracle_mod.rope(rq, base))
+    check("k rotated", H.to_f64(kr), oracle_mod.rope(rk, base))

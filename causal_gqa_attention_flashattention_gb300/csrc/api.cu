@@ -8,6 +8,8 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <queue>
+#include <utility>
 #include <vector>
 
 #include "../../include/ne_attn.h"
@@ -83,6 +85,12 @@ struct RopeTable {
   float2* ptr;
 };
 
+// Work items of the persistent forward, per CTA: see fwd_schedule.
+struct FwdSchedule {
+  int nt, per_i, grid, K;
+  int* ptr;  // [grid, K] device
+};
+
 // Library-owned forward workspace of one stream (calls that pass none).
 struct FwdScratch {
   cudaStream_t stream;
@@ -95,6 +103,7 @@ struct DeviceState {
   bool supported = false;
   int* status = nullptr;
   std::vector<RopeTable> tables;
+  std::vector<FwdSchedule> scheds;
   std::vector<FwdScratch> fwd_scratch;
   unsigned char* static_scratch = nullptr;  // device address of g_static_scratch (set on first use)
 };
@@ -154,6 +163,49 @@ int rope_table(DeviceState& d, int D, double base, int Tneed, cudaStream_t s, co
   // Older, smaller tables stay allocated: kernels queued on other streams may still read them.
   d.tables.push_back(RopeTable{D, base, Tcap, p});
   *out = p;
+  return NE_OK;
+}
+
+// The persistent forward's work items, assigned on the host once per
+// (query tiles, batch x heads, grid): items in largest-first order (query tile
+// nt - 1 first; an item of tile i has i + 1 key tiles) each go to the CTA with
+// the least work so far, counting a key tile as 2 and an item's epilogue as 1.
+// Against a fixed round-robin order this shortens the busiest CTA (at the
+// 116M-model shape from 14 to 13 key tiles).  The table is uploaded with a
+// synchronous copy: make one call per shape before capturing calls in a graph.
+// Requires g_mu held.
+int fwd_schedule(DeviceState& d, int nt, int per_i, int grid, const int** out, int* K) {
+  for (auto& x : d.scheds)
+    if (x.nt == nt && x.per_i == per_i && x.grid == grid) {
+      *out = x.ptr;
+      *K = x.K;
+      return NE_OK;
+    }
+  const long long n = (long long)nt * per_i;
+  std::vector<std::vector<int>> lists(grid);
+  using Load = std::pair<long long, int>;  // (work so far, CTA): ties go to the lower CTA
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int c = 0; c < grid; c++) heap.push(Load(0, c));
+  for (long long w = 0; w < n; w++) {
+    const Load l = heap.top();
+    heap.pop();
+    lists[l.second].push_back((int)w);
+    heap.push(Load(l.first + 2 * (nt - w / per_i) + 1, l.second));
+  }
+  int k = 0;
+  for (auto& v : lists) k = (int)v.size() > k ? (int)v.size() : k;
+  std::vector<int> table((size_t)grid * k, -1);
+  for (int c = 0; c < grid; c++)
+    for (size_t j = 0; j < lists[c].size(); j++) table[(size_t)c * k + j] = lists[c][j];
+  int* p = nullptr;
+  if (cudaMalloc(&p, sizeof(int) * table.size()) != cudaSuccess) return NE_ERR_CUDA;
+  if (cudaMemcpy(p, table.data(), sizeof(int) * table.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(p);
+    return NE_ERR_CUDA;
+  }
+  d.scheds.push_back(FwdSchedule{nt, per_i, grid, k, p});
+  *out = p;
+  *K = k;
   return NE_OK;
 }
 
@@ -508,6 +560,13 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
   std::memset(&a, 0, sizeof(a));
   a.nt = (T + kTile - 1) / kTile;
   if ((st = rope_table(*d, D, (double)rope_base, a.nt * kTile, s, &a.rope)) != NE_OK) return st;
+  if (!precise) {
+    int nsm = 0;
+    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm < 1) return NE_ERR_CUDA;
+    const long long items = (long long)a.nt * B * Hq;
+    const int grid = (int)(items < nsm ? items : nsm);
+    if ((st = fwd_schedule(*d, a.nt, B * Hq, grid, &a.sched, &a.sched_k)) != NE_OK) return st;
+  }
   if (precise) {
     if ((st = make_map_bthd(&a.map_q, q, B, T, Hq, D)) != NE_OK) return st;
     if ((st = make_map_bthd(&a.map_k, k, B, T, Hkv, D)) != NE_OK) return st;

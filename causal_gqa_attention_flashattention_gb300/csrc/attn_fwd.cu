@@ -641,11 +641,14 @@ struct Fwd3Item {
   int i, b, h;
 };
 
+// Item tl of this CTA from the host-built schedule: w indexes the largest-first
+// order of (query tile, batch, head), items given out longest first to the CTA
+// with the least work so far.
 __device__ __forceinline__ bool fwd3_item(const FwdArgs& a, int tl, Fwd3Item& it) {
-  const int G = (int)gridDim.x, c = (int)blockIdx.x;
-  const int w = (tl & 1) ? (tl + 1) * G - 1 - c : tl * G + c;  // snake over the largest-first order
+  if (tl >= a.sched_k) return false;
+  const int w = __ldg(a.sched + (size_t)blockIdx.x * a.sched_k + tl);
+  if (w < 0) return false;
   const int per_i = a.B * a.Hq;
-  if (w >= a.nt * per_i) return false;
   it.i = a.nt - 1 - w / per_i;
   const int rem = w % per_i;
   it.h = rem % a.Hq;  // the heads of one kv group sit next to each other: their K/V tiles meet in L2

@@ -42,6 +42,8 @@ struct FwdArgs {
   float scale_log2;                 // log2(e) / sqrt(D), rounded to fp32
   float scale_log2_lo;              // remainder log2(e)/sqrt(D) - scale_log2
   const float* qk_amax;             // FP8 forward: per-head max |rotated value|, [Hq] for q then [Hkv] for k
+  const int* sched;                 // [grid, sched_k] work items of each CTA (-1: none), see fwd_schedule
+  int sched_k;
 };
 
 // Division of a non-negative 32-bit n < 2^31 by a runtime divisor d >= 1 with

@@ -68,6 +68,8 @@ def lib():
         L.ne_attn_decode_workspace_size.restype = sz
         L.ne_attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, sz, vp]
         L.ne_attn_decode.restype = i
+        L.ne_attn_debug_fwd_schedule.argtypes = [i, i, i, ctypes.POINTER(ctypes.c_int), i, ctypes.POINTER(ctypes.c_int)]
+        L.ne_attn_debug_fwd_schedule.restype = i
         L.ne_attn_qkv_workspace_size.argtypes = [i, i, i, i, i, i, i]
         L.ne_attn_qkv_workspace_size.restype = sz
         L.ne_attn_qkv_rmsnorm.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, i, vp, sz, vp]
@@ -426,3 +428,14 @@ class HostStepPipeline:
     def synchronize(self):
         self.down.synchronize()
         check_status(self.comp)
+
+
+def fwd_schedule(nt, per_i, grid):
+    """The persistent forward's work items per CTA (host computation, no GPU):
+    a list of `grid` lists of item indices in largest-first order."""
+    k = ctypes.c_int(0)
+    lib().ne_attn_debug_fwd_schedule(nt, per_i, grid, None, 0, ctypes.byref(k))
+    buf = (ctypes.c_int * max(1, grid * k.value))()
+    _check("ne_attn_debug_fwd_schedule",
+           lib().ne_attn_debug_fwd_schedule(nt, per_i, grid, buf, grid * k.value, ctypes.byref(k)))
+    return [[w for w in buf[c * k.value:(c + 1) * k.value] if w >= 0] for c in range(grid)]

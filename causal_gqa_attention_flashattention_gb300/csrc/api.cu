@@ -173,14 +173,7 @@ int rope_table(DeviceState& d, int D, double base, int Tneed, cudaStream_t s, co
 // Against a fixed round-robin order this shortens the busiest CTA (at the
 // 116M-model shape from 14 to 13 key tiles).  The table is uploaded with a
 // synchronous copy: make one call per shape before capturing calls in a graph.
-// Requires g_mu held.
-int fwd_schedule(DeviceState& d, int nt, int per_i, int grid, const int** out, int* K) {
-  for (auto& x : d.scheds)
-    if (x.nt == nt && x.per_i == per_i && x.grid == grid) {
-      *out = x.ptr;
-      *K = x.K;
-      return NE_OK;
-    }
+std::vector<int> fwd_schedule_table(int nt, int per_i, int grid, int* K) {
   const long long n = (long long)nt * per_i;
   std::vector<std::vector<int>> lists(grid);
   using Load = std::pair<long long, int>;  // (work so far, CTA): ties go to the lower CTA
@@ -197,6 +190,20 @@ int fwd_schedule(DeviceState& d, int nt, int per_i, int grid, const int** out, i
   std::vector<int> table((size_t)grid * k, -1);
   for (int c = 0; c < grid; c++)
     for (size_t j = 0; j < lists[c].size(); j++) table[(size_t)c * k + j] = lists[c][j];
+  *K = k;
+  return table;
+}
+
+// Requires g_mu held.
+int fwd_schedule(DeviceState& d, int nt, int per_i, int grid, const int** out, int* K) {
+  for (auto& x : d.scheds)
+    if (x.nt == nt && x.per_i == per_i && x.grid == grid) {
+      *out = x.ptr;
+      *K = x.K;
+      return NE_OK;
+    }
+  int k = 0;
+  const std::vector<int> table = fwd_schedule_table(nt, per_i, grid, &k);
   int* p = nullptr;
   if (cudaMalloc(&p, sizeof(int) * table.size()) != cudaSuccess) return NE_ERR_CUDA;
   if (cudaMemcpy(p, table.data(), sizeof(int) * table.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
@@ -1079,6 +1086,14 @@ int ne_attn_decode(const void* q, const void* k_cache, const void* v_cache, void
   }
   ProfScope prof(NE_ATTN_KERNEL_DECODE, s);
   return launch_decode(a, nsm, s) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
+}
+
+int ne_attn_debug_fwd_schedule(int nt, int per_i, int grid, int* table, int capacity, int* K) {
+  if (nt < 1 || per_i < 1 || grid < 1 || !K || (long long)nt * per_i >= (1LL << 31)) return NE_ERR_ARG;
+  const std::vector<int> t = fwd_schedule_table(nt, per_i, grid, K);
+  if (!table || capacity < (long long)t.size()) return NE_ERR_ARG;
+  std::memcpy(table, t.data(), sizeof(int) * t.size());
+  return NE_OK;
 }
 
 int ne_attn_debug_timeout_probe(int limit_us, void* stream) {

@@ -326,6 +326,15 @@ int ne_attn_profile_read(double* total_ms, long long* launches);
  */
 int ne_attn_debug_timeout_probe(int limit_us, void* stream);
 
+/*
+ * Host-only view of the persistent forward's work schedule (no device call):
+ * for nt query tiles, per_i = B * Hq items per tile and `grid` CTAs, writes
+ * the [grid, K] table of item indices w (largest-first order: query tile
+ * nt - 1 - w / per_i; -1 pads a CTA's row) into `table` and K into *K.
+ * NE_ERR_ARG (with *K set) if capacity < grid * K.
+ */
+int ne_attn_debug_fwd_schedule(int nt, int per_i, int grid, int* table, int capacity, int* K);
+
 #ifdef __cplusplus
 }
 #endif

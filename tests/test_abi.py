@@ -207,3 +207,25 @@ def test_fp8_flag_rules_on_the_host(libne):
     assert fx(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 32 | 4, null, 0, null) == -1
     assert fx(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 32, p, 64, null) == -5  # workspace too small
     assert fx(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 64, null, 0, null) == -1  # unknown flag
+
+
+@pytest.mark.parametrize("nt,per_i,grid", [(4, 192, 152), (1, 7, 7), (64, 24, 152), (3, 5, 152), (5, 33, 10)])
+def test_forward_schedule(libne, nt, per_i, grid):
+    """The forward's work table (host logic): every item exactly once, each CTA's
+    items longest first, and the busiest CTA no busier than with the fixed
+    snake order over the same largest-first list."""
+    from causal_gqa_attention_flashattention_gb300 import binding
+    lists = binding.fwd_schedule(nt, per_i, grid)
+    n = nt * per_i
+    assert len(lists) == grid and sorted(w for l in lists for w in l) == list(range(n))
+    size = lambda w: nt - w // per_i  # key tiles of item w
+    for l in lists:
+        assert [size(w) for w in l] == sorted((size(w) for w in l), reverse=True)
+    busiest = max(sum(size(w) for w in l) for l in lists)
+    snake = [0] * grid
+    for w in range(n):
+        tl, c = divmod(w, grid)
+        snake[c if tl % 2 == 0 else grid - 1 - c] += size(w)
+    assert busiest <= max(snake)
+    if (nt, per_i, grid) == (4, 192, 152):  # the 116M-model forward: 13 key tiles instead of 14
+        assert busiest == 13 and max(snake) == 14

@@ -34,9 +34,12 @@
  *
  * The library keeps one small table per (device, D, rope_base): fp32
  * cos/sin of t * theta_i for t below the largest T seen so far, built on the
- * device in double precision.  The first call that needs a new or larger
- * table allocates it with cudaMalloc, so make one call with the largest T
- * before capturing calls in a CUDA graph.  Nothing else is allocated.
+ * device in double precision; and, per forward shape, the table of work items
+ * of each CTA of the persistent forward kernel (built on the host, copied once).
+ * The first call that needs a new or larger table allocates it with
+ * cudaMalloc, so make one call per shape (with the largest T) before capturing
+ * calls in a CUDA graph.  Calls that pass no workspace use a buffer of the
+ * library's per stream (see ne_attn_fwd_ex).  Nothing else is allocated.
  */
 #ifndef NE_ATTN_H
 #define NE_ATTN_H

@@ -159,6 +159,11 @@ def test_decode_is_the_last_rows(oracle_mod, shape):
     o, lse = oracle_mod.decode_fwd(q[:, T - Tq:], k, v, 10000.0)
     close(o, o_ref[:, T - Tq:], 1e-12)
     close(lse, lse_ref[:, :, T - Tq:], 1e-12)
+    # the same with the half-split pair layout
+    o_ref, lse_ref, _, _, _ = bruteforce(q, k, v, do, 10000.0, half=True)
+    o, lse = oracle_mod.decode_fwd(q[:, T - Tq:], k, v, 10000.0, half=True)
+    close(o, o_ref[:, T - Tq:], 1e-12)
+    close(lse, lse_ref[:, :, T - Tq:], 1e-12)
 
 
 @pytest.mark.parametrize("shape", [(1, 5, 2, 1, 4), (2, 7, 4, 2, 8), (1, 9, 3, 3, 6)])

@@ -6,16 +6,19 @@ CPU-baseline leg of ``bench.py`` may import this package; the product path
 (the CUDA library and its Python binding) never does, and this package never
 imports the product package.
 
-The attention arithmetic lives in ``attn_oracle.c`` (plain C, double
-precision, OpenMP over rows); this module compiles it with gcc and marshals
+The e4m3 rounding with one scale per head, the oracle of the FP8 forward,
+is in ``fp8.py``.  The attention arithmetic lives in ``attn_oracle.c``
+(plain C, double precision, OpenMP over rows); this module compiles it with gcc and marshals
 numpy arrays.  The RMSNorm + projection step (``qkv_rmsnorm``) is written here
 in float64 numpy, with one library matrix product.  The header of
 ``attn_oracle.c`` and the docstrings below name the passages of the NanoEuler
 pages each step follows and the readings taken where the pages are silent.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` (brute force in a
-second formulation, closed forms, invariants and central finite differences);
-no function here is "parity unpinned".
+second formulation, closed forms, invariants and central finite differences)
+and the e4m3 emulation by ``tests/test_fp8_tolerance.py`` (values worked by
+hand from the format and the per-head scale); no function here is "parity
+unpinned".
 """
 import ctypes
 import os

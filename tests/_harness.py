@@ -2,6 +2,7 @@
 import numpy as np
 
 from causal_gqa_attention_flashattention_gb300 import inputs
+from oracle.fp8 import e4m3_per_head, e4m3_round  # noqa: F401  (the FP8 oracle)
 
 # Tolerances for O, dQ, dK, dV against the fp64 oracle on the same bf16 inputs.
 REL_L2_TOL = 5e-3
@@ -68,26 +69,6 @@ def fp8_bounds(floor):
     rel, mx, lse = floor
     return (FP8_FLOOR_MARGIN * rel + REL_L2_TOL, FP8_FLOOR_MARGIN * mx + MAX_ABS_TOL,
             FP8_FLOOR_MARGIN * lse + LSE_ABS_TOL)
-
-
-def e4m3_round(x):
-    """Round to the OCP FP8 E4M3 grid: 1 sign, 4 exponent bits (bias 7), 3
-    mantissa bits, subnormal step 2^-9, largest finite 448; round to nearest
-    even, saturating at 448 (values stay finite)."""
-    x = np.asarray(x, dtype=np.float64)
-    a = np.abs(x)
-    e = np.clip(np.floor(np.log2(np.maximum(a, 2.0 ** -9))), -6, 8)
-    step = 2.0 ** (e - 3)
-    return np.sign(x) * np.minimum(np.round(a / step) * step, 448.0)
-
-
-def e4m3_per_head(xr):
-    """xr [B,T,H,D] rotated values -> their e4m3 rounding with one scale per head
-    (code = value * 448 / max |value| over the head's batches, positions and
-    features), returned as values (code * max / 448)."""
-    amax = np.max(np.abs(xr), axis=(0, 1, 3), keepdims=True)
-    s = np.where(amax > 0, amax / 448.0, 1.0)
-    return e4m3_round(xr / s) * s
 
 
 def fp8_floor(oracle_mod, x, base, half=False):

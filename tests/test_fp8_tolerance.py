@@ -11,7 +11,8 @@ bound in _harness.fp8_bounds is the floor of the same inputs with a 1.5x
 margin plus the default path's own bounds (a floor measured on one small case
 would be too tight for larger ones: the maximum error grows with the number
 of outputs).  The e4m3 rounding
-itself is pinned to values worked out from the format's definition.
+itself is pinned to values worked out from the format's definition, and the
+per-head scale to a tensor worked by hand (oracle/fp8.py holds the emulation).
 """
 import numpy as np
 
@@ -30,6 +31,57 @@ def test_e4m3_rounding_pins():
     grid = np.array([g for g in grid if g <= 448.0])
     np.testing.assert_array_equal(H.e4m3_round(grid), grid)
     assert len(np.unique(grid)) == 127  # 0, 7 subnormals and 15 x 8 normals less 480 (codes 0x00..0x7e)
+
+
+# A [B=2, T=2, H=2, D=2] tensor worked by hand.  Head 0 takes its largest
+# |value| (3.5) at batch 1, position 0; head 1 its largest (0.7) at batch 0,
+# position 1 (and -0.7 at batch 1).  Scales: 3.5 / 448 = 2^-7 (codes = value *
+# 128) and 0.7 / 448 = 1 / 640 (codes = value * 640).  Codes on the e4m3 grid:
+#   0.3 * 128 = 38.4   in [32, 64), step 4          -> 40    -> 0.3125
+#   -1.1 * 128 = -140.8 in [128, 256), step 16      -> -144  -> -1.125
+#   0.01 * 128 = 1.28  in [1, 2), step 1/8          -> 1.25  -> 0.009765625
+#   3.5 * 128 = 448, 1.0 * 128 = 128, 2.0 * 128 = 256 (on the grid)
+#   0.123 * 640 = 78.72 in [64, 128), step 8         -> 80    -> 0.125
+#   3e-4 * 640 = 0.192 in [1/8, 1/4), step 1/64      -> 0.1875 -> 2.9296875e-4
+#   0.1 * 640 = 64, -0.05 * 640 = -32, 0.7 * 640 = 448 (on the grid)
+PER_HEAD_X = np.array([
+    [[[0.3, -1.1], [0.1, 3e-4]],      # b=0, t=0: head 0, head 1
+     [[0.01, 0.0], [0.7, -0.05]]],    # b=0, t=1
+    [[[1.0, 3.5], [0.123, 0.0]],      # b=1, t=0
+     [[-0.3, 2.0], [-0.7, 0.0]]],     # b=1, t=1
+])
+PER_HEAD_CODES = np.array([
+    [[[40.0, -144.0], [64.0, 0.1875]],
+     [[1.25, 0.0], [448.0, -32.0]]],
+    [[[128.0, 448.0], [80.0, 0.0]],
+     [[-40.0, 256.0], [-448.0, 0.0]]],
+])
+PER_HEAD_VALUES = np.array([
+    [[[0.3125, -1.125], [0.1, 2.9296875e-4]],
+     [[0.009765625, 0.0], [0.7, -0.05]]],
+    [[[1.0, 3.5], [0.125, 0.0]],
+     [[-0.3125, 2.0], [-0.7, 0.0]]],
+])
+
+
+def test_e4m3_per_head_scale_pins():
+    from oracle import fp8
+    np.testing.assert_array_equal(fp8.head_scales(PER_HEAD_X), [3.5, 0.7])
+    vals, codes = fp8.e4m3_per_head(PER_HEAD_X, return_codes=True)
+    np.testing.assert_allclose(codes, PER_HEAD_CODES, rtol=1e-12, atol=0)
+    np.testing.assert_allclose(vals, PER_HEAD_VALUES, rtol=1e-12, atol=1e-18)
+    # a scale per (batch, head) or per row rounds this tensor differently: the
+    # reduction axes are pinned, not just the element rounding
+    for axes in ((1, 3), (3,)):
+        amax = np.max(np.abs(PER_HEAD_X), axis=axes, keepdims=True)
+        s = np.where(amax > 0, amax / 448.0, 1.0)
+        other = fp8.e4m3_round(PER_HEAD_X / s) * s
+        assert np.max(np.abs(other - PER_HEAD_VALUES)) > 1e-3, axes
+    # a head of zeros keeps zero codes
+    z = np.zeros((1, 3, 2, 4))
+    z[0, 1, 0, 2] = 0.5
+    v, c = fp8.e4m3_per_head(z, return_codes=True)
+    assert c[0, 1, 0, 2] == 448.0 and v[0, 1, 0, 2] == 0.5 and not np.any(c[:, :, 1])
 
 
 def test_fp8_floor_level(oracle_mod):

@@ -3,9 +3,9 @@ scale per head, S on the 8-bit tensor-core path, v / P / O as in the default
 forward.  Checked against the fp64 oracle on the same bf16 inputs with the
 bound derived in test_fp8_tolerance.py (the e4m3 floor of the same inputs
 with a 1.5x margin, plus the default path's bounds), and against the CPU
-emulation of the
-same e4m3 rounding (written in the tests from the format's definition), which
-it must follow far more closely than the exact oracle.
+emulation of the same e4m3 rounding (oracle/fp8.py, written from the format's
+definition and pinned by hand-worked values), which it must follow far more
+closely than the exact oracle.
 """
 import numpy as np
 import pytest

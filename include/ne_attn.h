@@ -139,7 +139,11 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
 
 /*
  * Bytes of device workspace ne_attn_bwd needs for this shape and flags
- * (pass a 256-byte aligned pointer).  Holds: the rotated q and k (fp16, plus
+ * (pass a 256-byte aligned pointer).  The pages' backward keeps the softmax
+ * statistics of the forward and recomputes the probabilities from them
+ * (socker-news README, "Verified backward" and "GPU engine": FlashAttention
+ * never stores the T x T matrix); this buffer holds what that recomputation
+ * and the dQ accumulation need between the backward's kernels.  Holds: the rotated q and k (fp16, plus
  * their fp16 remainders with NE_ATTN_PRECISE_QK), per-row
  * Delta_t = dO_t . O_t and lse * log2(e) (fp32, rows padded to a multiple of
  * 128), and the fp32 dQ accumulator [B, Hq, Tpad, D].  Returns 0 for
@@ -151,7 +155,13 @@ size_t ne_attn_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D, int flag
  * Backward pass: given q, k, v, the forward's o and lse, and the upstream
  * gradient dout (bfloat16), writes dq, dk, dv: the gradients with respect to
  * the un-rotated inputs (the inverse rotation R_t^T is applied on the way
- * out).  flags: NE_ATTN_O_FP32 (o is float32), NE_ATTN_GRAD_FP32 (float32
+ * out).  The pages hand-write this backward, RoPE and the GQA head sharing
+ * included, and check it against central finite differences (socker-news
+ * README, "Verified backward"; openai-hub article, hand-written forward and
+ * backward):
+ *   dV = P^T dO,  dP = dO V^T,  Delta_t = dO_t . O_t,  dS = P o (dP - Delta),
+ *   dq = R_t^T (dS k^) / sqrt(D),  dk = R_j^T (dS^T q^) / sqrt(D) summed over
+ *   the query heads of each key/value head, with P rebuilt from lse.  flags: NE_ATTN_O_FP32 (o is float32), NE_ATTN_GRAD_FP32 (float32
  * gradients, else bfloat16), NE_ATTN_PRECISE_QK.
  * Three kernels: a pre-pass (Delta = rowsum(dO * O), rotated q/k, zeroed dQ
  * accumulator), a key-tile sweep (dK and dV summed over the query heads of
@@ -167,12 +177,15 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
 
 /*
  * Backward pass for callers that cannot allocate device memory: the same
- * result as ne_attn_bwd (same kernels, same flags) with no workspace argument.
+ * result as ne_attn_bwd (same kernels) with no workspace argument.  Flags:
+ * NE_ATTN_O_FP32, NE_ATTN_GRAD_FP32, NE_ATTN_PRECISE_QK, NE_ATTN_ROPE_HALF;
+ * NE_ATTN_QK_ROTATED is rejected with NE_ERR_ARG, because the fixed array never
+ * holds a forward's rotated q and k (the call always rotates them itself).
  * The NanoEuler pages have no counterpart to this entry point; it exists for
- * callers such as code that runs while a stream is being captured into a CUDA
- * graph (no cudaMalloc allowed there), plugins whose host process owns every
- * device allocation, or fixed-memory deployments that forbid allocating after
- * start-up.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ * callers such as plugins whose host process owns every device allocation,
+ * or fixed-memory deployments that forbid allocating after start-up, where a
+ * call that grows device memory would fail or break the host's accounting.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
  *
  * Scratch (the workspace of ne_attn_bwd plus the rotary table) comes from one
  * fixed device array of NE_ATTN_STATIC_SCRATCH_BYTES that the library defines;
@@ -280,7 +293,9 @@ int ne_attn_qkv_rmsnorm(const void* x, const void* norm_w, const void* w_qkv, vo
 /*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: NE_OK, NE_ERR_DEVICE_TIMEOUT, or NE_ERR_CUDA if the
- * synchronisation itself failed.
+ * synchronisation itself failed.  The pages have no counterpart to this
+ * call; it reports the one failure the kernels detect themselves, a pipeline
+ * wait that gave up, while the GPU context stays usable.
  */
 int ne_attn_check_status(void* stream);
 

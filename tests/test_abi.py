@@ -137,6 +137,8 @@ def test_half_split_flag_rules(libne):
     libne.ne_attn_bwd_noalloc.argtypes = [vp] * 9 + [i] * 5 + [f, i, vp]
     libne.ne_attn_bwd_noalloc.restype = i
     assert libne.ne_attn_bwd_noalloc(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 16 | 4, null) == -3
+    # the fixed scratch never holds a forward's rotated q, k: the reuse flag is refused
+    assert libne.ne_attn_bwd_noalloc(p, p, p, p, p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 8, null) == -1
 
 
 

@@ -1,8 +1,8 @@
 """ne_attn_bwd_noalloc: the backward pass for callers that cannot allocate.
 
 Some callers of this library cannot call cudaMalloc when they need the
-backward pass, for example code running while a stream is captured into a
-CUDA graph, or a plugin whose host process owns all device memory.  For them
+backward pass, for example a plugin whose host process owns all device memory,
+or a deployment that fixes its memory at start-up.  For them
 the library has an entry point that takes no workspace and allocates nothing:
 its scratch is one fixed device array inside the library.  These tests call it
 through the C ABI and check that it returns what ne_attn_bwd (with a caller

@@ -68,7 +68,8 @@ def lib():
         L.ne_attn_decode_workspace_size.restype = sz
         L.ne_attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, sz, vp]
         L.ne_attn_decode.restype = i
-        L.ne_attn_debug_fwd_schedule.argtypes = [i, i, i, ctypes.POINTER(ctypes.c_int), i, ctypes.POINTER(ctypes.c_int)]
+        ip = ctypes.POINTER(ctypes.c_int)
+        L.ne_attn_debug_fwd_schedule.argtypes = [i, i, i, i, i, ip, i, ip, ip]
         L.ne_attn_debug_fwd_schedule.restype = i
         L.ne_attn_qkv_workspace_size.argtypes = [i, i, i, i, i, i, i]
         L.ne_attn_qkv_workspace_size.restype = sz
@@ -430,12 +431,24 @@ class HostStepPipeline:
         check_status(self.comp)
 
 
-def fwd_schedule(nt, per_i, grid):
+def fwd_schedule(B, Hkv, G, nt, nsm):
     """The persistent forward's work items per CTA (host computation, no GPU):
-    a list of `grid` lists of item indices in largest-first order."""
-    k = ctypes.c_int(0)
-    lib().ne_attn_debug_fwd_schedule(nt, per_i, grid, None, 0, ctypes.byref(k))
-    buf = (ctypes.c_int * max(1, grid * k.value))()
+    a list of `grid` lists of items (b, (h0, i0), (h1, i1) or None), each CTA's
+    items in the order it runs them."""
+    k, grid = ctypes.c_int(0), ctypes.c_int(0)
+    lib().ne_attn_debug_fwd_schedule(B, Hkv, G, nt, nsm, None, 0, ctypes.byref(grid), ctypes.byref(k))
+    n = max(1, 4 * grid.value * k.value)
+    buf = (ctypes.c_int * n)()
     _check("ne_attn_debug_fwd_schedule",
-           lib().ne_attn_debug_fwd_schedule(nt, per_i, grid, buf, grid * k.value, ctypes.byref(k)))
-    return [[w for w in buf[c * k.value:(c + 1) * k.value] if w >= 0] for c in range(grid)]
+           lib().ne_attn_debug_fwd_schedule(B, Hkv, G, nt, nsm, buf, n, ctypes.byref(grid), ctypes.byref(k)))
+    out = []
+    for c in range(grid.value):
+        row = []
+        for j in range(k.value):
+            b, hh, i0, i1 = buf[4 * (c * k.value + j):4 * (c * k.value + j) + 4]
+            if b < 0:
+                continue
+            h0, h1 = hh & 0xFFFF, (hh >> 16) - 1
+            row.append((b, (h0, i0), (h1, i1) if h1 >= 0 else None))
+        out.append(row)
+    return out

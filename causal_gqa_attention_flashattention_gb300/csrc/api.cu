@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -85,10 +86,10 @@ struct RopeTable {
   float2* ptr;
 };
 
-// Work items of the persistent forward, per CTA: see fwd_schedule.
+// Work items of the persistent forward, per CTA: see fwd_pair_schedule.
 struct FwdSchedule {
-  int nt, per_i, grid, K;
-  int* ptr;  // [grid, K] device
+  int B, Hkv, G, nt, nsm, grid, K;
+  int* ptr;  // [grid, K] int4 entries, device
 };
 
 // Library-owned forward workspace of one stream (calls that pass none).
@@ -166,15 +167,42 @@ int rope_table(DeviceState& d, int D, double base, int Tneed, cudaStream_t s, co
   return NE_OK;
 }
 
-// The persistent forward's work items, assigned on the host once per
-// (query tiles, batch x heads, grid): items in largest-first order (query tile
-// nt - 1 first; an item of tile i has i + 1 key tiles) each go to the CTA with
-// the least work so far, counting a key tile as 2 and an item's epilogue as 1.
-// Against a fixed round-robin order this shortens the busiest CTA (at the
-// 116M-model shape from 14 to 13 key tiles).  The table is uploaded with a
-// synchronous copy: make one call per shape before capturing calls in a graph.
-std::vector<int> fwd_schedule_table(int nt, int per_i, int grid, int* K) {
-  const long long n = (long long)nt * per_i;
+// The persistent forward's work items, built on the host once per shape.  A
+// unit is one query head's 128-row query tile; an item pairs two units of one
+// (batch, key/value head), which share its K/V stream (key tiles
+// 0 .. max(i0, i1)), one softmax warpgroup per unit.  Pairs: heads 2k and 2k+1
+// of the group at the same query tile; with an odd group size the last head of
+// the group pairs its own adjacent tiles (nt-1, nt-2), (nt-3, nt-4), ..., and a
+// leftover tile 0 goes alone.  An item costs 2 per unit key tile plus 1 per
+// unit epilogue; items in decreasing cost (ties: larger tile, then batch, then
+// key/value head, so a group's items go out together and meet in L2) each go
+// to the CTA with the least work so far.  Entries are int4
+// (b, h0 | (h1 + 1) << 16, i0, i1) with i0 >= i1 (h1 + 1 = 0: one unit);
+// rows are padded with b = -1.  grid = min(items, nsm).
+struct PairItem {
+  int b, kvh, h0, h1, i0, i1;
+  long long cost;
+};
+std::vector<int> fwd_pair_schedule(int B, int Hkv, int G, int nt, int nsm, int* grid_out, int* K) {
+  std::vector<PairItem> items;
+  for (int b = 0; b < B; b++)
+    for (int g = 0; g < Hkv; g++) {
+      const int h = g * G;
+      for (int i = nt - 1; i >= 0; i--)
+        for (int k = 0; k + 1 < G; k += 2) items.push_back(PairItem{b, g, h + k, h + k + 1, i, i, 0});
+      if (G % 2 == 1)
+        for (int i = nt - 1; i >= 0; i -= 2)
+          items.push_back(PairItem{b, g, h + G - 1, i >= 1 ? h + G - 1 : -1, i, i >= 1 ? i - 1 : -1, 0});
+    }
+  for (auto& x : items) x.cost = 2LL * (x.i0 + 1) + 1 + (x.h1 >= 0 ? 2LL * (x.i1 + 1) + 1 : 0);
+  std::stable_sort(items.begin(), items.end(), [](const PairItem& p, const PairItem& q) {
+    if (p.cost != q.cost) return p.cost > q.cost;
+    if (p.i0 != q.i0) return p.i0 > q.i0;
+    if (p.b != q.b) return p.b < q.b;
+    return p.kvh < q.kvh;
+  });
+  const long long n = (long long)items.size();
+  const int grid = (int)(n < nsm ? n : nsm);
   std::vector<std::vector<int>> lists(grid);
   using Load = std::pair<long long, int>;  // (work so far, CTA): ties go to the lower CTA
   std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
@@ -183,35 +211,46 @@ std::vector<int> fwd_schedule_table(int nt, int per_i, int grid, int* K) {
     const Load l = heap.top();
     heap.pop();
     lists[l.second].push_back((int)w);
-    heap.push(Load(l.first + 2 * (nt - w / per_i) + 1, l.second));
+    heap.push(Load(l.first + items[w].cost, l.second));
   }
   int k = 0;
   for (auto& v : lists) k = (int)v.size() > k ? (int)v.size() : k;
-  std::vector<int> table((size_t)grid * k, -1);
+  std::vector<int> table((size_t)grid * k * 4, -1);
   for (int c = 0; c < grid; c++)
-    for (size_t j = 0; j < lists[c].size(); j++) table[(size_t)c * k + j] = lists[c][j];
+    for (size_t j = 0; j < lists[c].size(); j++) {
+      const PairItem& x = items[lists[c][j]];
+      int* e = &table[((size_t)c * k + j) * 4];
+      e[0] = x.b;
+      e[1] = x.h0 | ((x.h1 + 1) << 16);
+      e[2] = x.i0;
+      e[3] = x.h1 >= 0 ? x.i1 : 0;
+    }
+  *grid_out = grid;
   *K = k;
   return table;
 }
 
-// Requires g_mu held.
-int fwd_schedule(DeviceState& d, int nt, int per_i, int grid, const int** out, int* K) {
+// Requires g_mu held.  The table is uploaded with a synchronous copy: make one
+// call per shape before capturing calls in a graph.
+int fwd_schedule(DeviceState& d, int B, int Hkv, int G, int nt, int nsm, const int** out, int* grid, int* K) {
   for (auto& x : d.scheds)
-    if (x.nt == nt && x.per_i == per_i && x.grid == grid) {
+    if (x.B == B && x.Hkv == Hkv && x.G == G && x.nt == nt && x.nsm == nsm) {
       *out = x.ptr;
+      *grid = x.grid;
       *K = x.K;
       return NE_OK;
     }
-  int k = 0;
-  const std::vector<int> table = fwd_schedule_table(nt, per_i, grid, &k);
+  int k = 0, gr = 0;
+  const std::vector<int> table = fwd_pair_schedule(B, Hkv, G, nt, nsm, &gr, &k);
   int* p = nullptr;
   if (cudaMalloc(&p, sizeof(int) * table.size()) != cudaSuccess) return NE_ERR_CUDA;
   if (cudaMemcpy(p, table.data(), sizeof(int) * table.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
     cudaFree(p);
     return NE_ERR_CUDA;
   }
-  d.scheds.push_back(FwdSchedule{nt, per_i, grid, k, p});
+  d.scheds.push_back(FwdSchedule{B, Hkv, G, nt, nsm, gr, k, p});
   *out = p;
+  *grid = gr;
   *K = k;
   return NE_OK;
 }
@@ -294,14 +333,14 @@ int make_map_cache(CUtensorMap* m, const void* ptr, int B, int Tkv, int Tcap, in
 }
 
 // 4-D store map over a gradient [B, T, H, D] (fp32 or bf16); box = 128 bytes of
-// columns (64 bytes when a row is that short) x 1 head x 128 rows x 1, with the
-// swizzle of that span.
-int make_map_grad(CUtensorMap* m, void* ptr, int B, int T, int H, int D, bool fp32) {
+// columns (64 bytes when a row is that short) x 1 head x box_rows rows x 1, with
+// the swizzle of that span.
+int make_map_grad(CUtensorMap* m, void* ptr, int B, int T, int H, int D, bool fp32, int box_rows = kTile) {
   const int es = fp32 ? 4 : 2;
   const int span = D * es < 128 ? D * es : 128;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)D * es, (cuuint64_t)H * D * es, (cuuint64_t)T * H * D * es};
-  cuuint32_t box[4] = {(cuuint32_t)(span / es), 1, (cuuint32_t)kTile, 1};
+  cuuint32_t box[4] = {(cuuint32_t)(span / es), 1, (cuuint32_t)box_rows, 1};
   cuuint32_t e1[4] = {1, 1, 1, 1};
   CUresult r = g_encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims,
                         strides, box, e1, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -356,6 +395,7 @@ int check_shape(int B, int T, int Hq, int Hkv, int D) {
   if ((long long)B * Tp * maxH * D >= (1LL << 31)) return NE_ERR_UNSUPPORTED;
   const long long ntiles = Tp / kTile;
   if (ntiles * B * Hq >= (1LL << 31) - 1) return NE_ERR_UNSUPPORTED;
+  if (Hq > 32767) return NE_ERR_UNSUPPORTED;  // the forward's work table packs two heads in 32 bits
   return NE_OK;
 }
 
@@ -570,9 +610,7 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
   if (!precise) {
     int nsm = 0;
     if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm < 1) return NE_ERR_CUDA;
-    const long long items = (long long)a.nt * B * Hq;
-    const int grid = (int)(items < nsm ? items : nsm);
-    if ((st = fwd_schedule(*d, a.nt, B * Hq, grid, &a.sched, &a.sched_k)) != NE_OK) return st;
+    if ((st = fwd_schedule(*d, B, Hkv, Hq / Hkv, a.nt, nsm, &a.sched, &a.grid, &a.sched_k)) != NE_OK) return st;
   }
   if (precise) {
     if ((st = make_map_bthd(&a.map_q, q, B, T, Hq, D)) != NE_OK) return st;
@@ -628,7 +666,8 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
     }
   }
   if ((st = make_map_bthd(&a.map_v, v, B, T, Hkv, D)) != NE_OK) return st;
-  if (!precise && (st = make_map_grad(&a.map_o, o, B, T, Hq, D, (flags & kFlagOFp32) != 0)) != NE_OK) return st;
+  // the forward's warps store O 32 rows at a time
+  if (!precise && (st = make_map_grad(&a.map_o, o, B, T, Hq, D, (flags & kFlagOFp32) != 0, 32)) != NE_OK) return st;
   a.o = o;
   a.lse = lse;
   a.status = d->status;
@@ -1088,9 +1127,11 @@ int ne_attn_decode(const void* q, const void* k_cache, const void* v_cache, void
   return launch_decode(a, nsm, s) == cudaSuccess ? NE_OK : NE_ERR_CUDA;
 }
 
-int ne_attn_debug_fwd_schedule(int nt, int per_i, int grid, int* table, int capacity, int* K) {
-  if (nt < 1 || per_i < 1 || grid < 1 || !K || (long long)nt * per_i >= (1LL << 31)) return NE_ERR_ARG;
-  const std::vector<int> t = fwd_schedule_table(nt, per_i, grid, K);
+int ne_attn_debug_fwd_schedule(int B, int Hkv, int G, int nt, int nsm, int* table, int capacity, int* grid,
+                               int* K) {
+  if (B < 1 || Hkv < 1 || G < 1 || nt < 1 || nsm < 1 || !K || !grid) return NE_ERR_ARG;
+  if ((long long)B * Hkv * G * nt >= (1LL << 31) || (long long)Hkv * G > 32767) return NE_ERR_ARG;
+  const std::vector<int> t = fwd_pair_schedule(B, Hkv, G, nt, nsm, grid, K);
   if (!table || capacity < (long long)t.size()) return NE_ERR_ARG;
   std::memcpy(table, t.data(), sizeof(int) * t.size());
   return NE_OK;

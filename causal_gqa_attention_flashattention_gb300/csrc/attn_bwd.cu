@@ -377,12 +377,13 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
           mma_ss(tmem + col, smem_desc(sa + ks * 32, 16, C::kSBO, C::kSwz),
                  smem_desc(sb + ks * 32, 16, C::kSBO, C::kSwz), id, (acc || ks > 0) ? 1u : 0u);
       };
-      // S^T = Khi Qhi^T (+ Klo Qhi^T + Khi Qlo^T)
+      // S^T = Khi Qhi^T (+ Khi Qlo^T + Klo Qhi^T): the forward's products in the
+      // forward's order, so the recomputed logits round as the forward's did
       auto issue_s = [&](int stq) {
         issue_kmajor(C::kColS, sK, sQ + stq * C::kTileBytes, idS, 0);
         if (PRECISE) {
-          issue_kmajor(C::kColS, sKlo, sQ + stq * C::kTileBytes, idS, 1);
           issue_kmajor(C::kColS, sK, sQlo + stq * C::kTileBytes, idS, 1);
+          issue_kmajor(C::kColS, sKlo, sQ + stq * C::kTileBytes, idS, 1);
         }
       };
       // dK += dS^T Q (A = dS^T tile read K-major), dQ = dS K (A = dS^T tile read MN-major)

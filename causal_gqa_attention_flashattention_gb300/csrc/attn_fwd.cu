@@ -4,29 +4,23 @@
 // and never forms the T x T score matrix (socker-news README, "GPU engine" /
 // "Kernels and acceleration"; ojeo summary); its causal mask skips the upper
 // triangle instead of masking it (openai-hub article, softmax-kernel section).
-// This kernel computes the same result with the GB300 tensor cores:
+// The kernels here compute the same result with the GB300 tensor cores:
 //
-//   CTA = (query tile i of 128 rows, batch b, key/value head g, chunk of HC
-//         query heads of g's group).  Tiles are issued largest-i first.
-//   warp 0      TMA producer: the HC query tiles once, then K_j / V_j for
-//               j = 0..i through a ring of kStages stages.  Each K/V tile is
-//               read once and used by all HC heads (GQA sharing).
-//   warp 1      tcgen05 MMA issuer: S = Q_h K_j^T into one of two TMEM score
-//               buffers, then O_h += P V_j with P read from TMEM.
-//   warps 2-3   RoPE: rotate the Q tiles and each K tile in shared memory
-//               (in place, through the swizzled layout) before the MMA reads
-//               them; rotated values never go to HBM.  Rotated operands are
-//               fp16 (three more mantissa bits than bf16).  With PRECISE the
-//               fp16 remainder (rotated - hi) goes to a second buffer and
-//               S = Qhi Khi^T + Qlo Khi^T + Qhi Klo^T, so the logits carry
-//               ~2^-22 relative error even when |s| reaches 10^3.
-//   warps 4-7   softmax, one thread per query row: row max, lazy rescale of
-//               the TMEM accumulator (only when the max grows by > 2^8),
-//               exp2, P (bf16) back into TMEM, row sum of the rounded P (so
-//               O is an exact convex combination of V rows with the weights
-//               the MMA used; with PRECISE, P = hi + lo in two bf16 parts and
-//               O += Phi V + Plo V); epilogue O / l (bf16 or fp32) and
-//               LSE = ln(sum exp).
+//   k_rope_qk     streaming pre-pass: q, k -> rotated fp16 copies in the
+//                 workspace (the backward reads them too).
+//   k_attn_fwd4   default precision, persistent: work items of two (query head,
+//                 128-row query tile) units of one key/value head that share
+//                 the K/V stream; S = Q K^T and O += P V on tcgen05 with the
+//                 accumulators in TMEM; one softmax warpgroup per unit keeps the
+//                 unit's row maximum and sum in registers (lazy rescale, only
+//                 when the maximum grows by more than 2^8); epilogue O / l and
+//                 LSE = ln(sum exp).  With F8 the rotated q, k are e4m3.
+//   k_attn_fwd    split precision (NE_ATTN_PRECISE_QK), one CTA per (query
+//                 tile, batch, key/value head, chunk of query heads): rotates
+//                 the bf16 Q and K tiles in shared memory into fp16 hi + lo
+//                 parts, S = Qhi Khi^T + Qlo Khi^T + Qhi Klo^T so the logits
+//                 carry ~2^-22 relative error when |s| reaches 10^3, P = hi + lo
+//                 in two bf16 parts, and a two-part LSE.
 // Only the diagonal tile (j == i) is masked; tiles above it are never visited.
 #include <cuda_bf16.h>
 
@@ -569,26 +563,32 @@ __global__ void __launch_bounds__(256) k_rope_q8(const RopeArgs a) {
   }
 }
 
-// ====================================================================== persistent forward, one head per item
-// Default-precision forward over the pre-rotated fp16 q, k.  One CTA per SM
-// loops over work items (query tile i, batch, query head), largest first in a
-// snake order.  Key tile j of an item is step n of the CTA (n counts across
-// items); step n computes S into TMEM score buffer n & 1, is handled by softmax
-// warpgroup n & 1 (warps 2-5 or 6-9, one thread per query row) and writes its
-// P into TMEM P buffer n & 1, from which O += P V reads it.  With separate S
-// and P buffers, S of step n + 2 goes out as soon as step n's scores have been
-// read, and P of step n + 2 waits only for the PV of step n (issued a full
-// step earlier): the warpgroups never wait for the tensor core in the steady
-// state.  The row statistics pass from one step to the next through shared
-// memory: the running maximum after the first pass over the scores (m_ready),
-// the running sum after the second (l_ready).  The warpgroup of an item's last
-// key tile writes O and the LSE.
-// Warps: 0 TMA producer, 1 S = Q K^T issuer, 10 O += P V issuer.
-// Writes row r of a 128-row tile (D values, fp32 when ES == 4, else bf16) into a
-// staging area of column boxes: `span` = min(D * ES, 128) bytes per row, box after
-// box, each with the TMA / UMMA swizzle of that span.
+// ====================================================================== persistent forward, two query tiles per item
+// Default-precision forward over the rotated fp16 (or, with F8, e4m3) q, k that
+// the RoPE pre-pass (or the projection's epilogue) left in the workspace.  A work
+// item is a pair of units of one (batch, key/value head); a unit is one query
+// head's 128-row query tile.  The two units share the item's K/V stream (key
+// tiles 0 .. max(i0, i1)), and each softmax warpgroup owns one unit's rows for
+// the whole item: its row maximum and row sum stay in registers, so the two
+// warpgroups never wait for each other.  Unit u has its own TMEM score buffer
+// S_u, P buffer P_u and accumulator O_u (2 x (128 + 64 + 64) = 512 columns), so
+// S_u of the next key tile goes out as soon as the scores of this one have been
+// read.  O_u += P_u V goes out in two halves of 64 keys, the first while the
+// warpgroup still exponentiates the second, so that P_u of the next key tile
+// rarely waits for it.
+// Items come from a host-built table (fwd_pair_schedule in api.cu): pairs of
+// heads of one group at the same query tile; with an odd group size the
+// group's last head pairs adjacent query tiles (i, i - 1) of itself.
+// Warps: 0 TMA producer (a ring of four Q slots, a K/V ring), 1 S = Q K^T
+// issuer for both units, 2 and 3 O += P V issuers for units 0 and 1, 4-7 and
+// 8-11 the softmax warpgroups of units 0 and 1 (one thread per query row).
+// Each softmax warp stores its 32 rows of O itself (TMA boxes of 32 rows).
+
+// Writes row r (0..31) of a 32-row slice of O (D values, fp32 when ES == 4, else
+// bf16) into a staging area of column boxes of 32 rows: `span` = min(D * ES, 128)
+// bytes per row, box after box, each with the TMA / UMMA swizzle of that span.
 template <int D, int ES>
-__device__ __forceinline__ void stage_rows(const float (&x)[D], uint8_t* stg, int r) {
+__device__ __forceinline__ void stage_rows32(const float (&x)[D], uint8_t* stg, int r) {
   constexpr int kSpan = D * ES < 128 ? D * ES : 128;
   constexpr int kCols = kSpan / ES;
 #pragma unroll
@@ -605,16 +605,14 @@ __device__ __forceinline__ void stage_rows(const float (&x)[D], uint8_t* stg, in
         w = make_uint4(pack_bf16(x[i], x[i + 1]), pack_bf16(x[i + 2], x[i + 3]), pack_bf16(x[i + 4], x[i + 5]),
                        pack_bf16(x[i + 6], x[i + 7]));
       }
-      *reinterpret_cast<uint4*>(stg + bx * kTile * kSpan + swz(r, ch, kSpan)) = w;
+      *reinterpret_cast<uint4*>(stg + bx * 32 * kSpan + swz(r, ch, kSpan)) = w;
     }
   }
 }
 
-// F8: q and k tiles hold e4m3 (one byte per value; 64-byte rows, 64-byte
-// swizzle for D = 64); v, P and O keep their formats.
 template <int D, bool F8 = false>
-struct Fwd3Cfg {
-  static constexpr int kTileBytes = kTile * D * 2;
+struct Fwd4Cfg {
+  static constexpr int kTileBytes = kTile * D * 2;  // V tile (bf16)
   static constexpr uint32_t kSpan = D * 2;
   static constexpr uint32_t kSwz = D == 64 ? kSw128 : kSw64;
   static constexpr uint32_t kSBO = 8 * kSpan;
@@ -622,90 +620,91 @@ struct Fwd3Cfg {
   static constexpr uint32_t kQKSpan = D * (F8 ? 1 : 2);
   static constexpr uint32_t kQKSwz = kQKSpan == 128 ? kSw128 : (kQKSpan == 64 ? kSw64 : kSw32);
   static constexpr uint32_t kQKSBO = 8 * kQKSpan;
-  static constexpr int kStages = 4;  // K/V ring
-  static constexpr uint32_t kColO = 0, kColS = 128, kColP = 384;  // S buffers at 128, 256; P buffers at 384, 448
+  static constexpr int kQSlots = 4;                      // two items' worth of query tiles
+  static constexpr int kStages = (D == 64 && !F8) ? 3 : 4;  // K/V ring
+  static constexpr uint32_t kColO = 0, kColS = 128, kColP = 384;  // unit u: O at 64u, S at 128 + 128u, P at 384 + 64u
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kThreads = 352;
-  static constexpr int kOffQ = 0;  // [2]
-  static constexpr int kOffK = 2 * kQKTileBytes;
+  static constexpr int kThreads = 384;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQSlots * kQKTileBytes;
   static constexpr int kOffV = kOffK + kStages * kQKTileBytes;
-  static constexpr int kOstBytes = kTile * D * 4;                // O staging per warpgroup (fp32 rows at most)
-  static constexpr int kOffOst = kOffV + kStages * kTileBytes;    // [2]
-  static constexpr int kOffStat = kOffOst + 2 * kOstBytes;         // m[128], l[128]
-  static constexpr int kOffBar = kOffStat + 2 * kTile * 4;
-  static constexpr int kSmemBytes = kOffBar + 40 * 8 + 16 + 1024;
+  static constexpr int kOstBytes = kTile * D * 4;  // O staging per unit (fp32 rows at most)
+  static constexpr int kOffOst = kOffV + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffOst + 2 * kOstBytes;
+  static constexpr int kNumBars = 2 * kQSlots + 2 * kStages + 14 + 3;
+  static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16;  // the dynamic area is 1024-aligned
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-struct Fwd3Item {
-  int i, b, h;
+struct Fwd4Item {
+  int b, nu;       // batch; number of units (1 or 2)
+  int h0, h1, i0, i1;  // query head and query tile of each unit; i0 >= i1
+  __device__ __forceinline__ int h(int u) const { return u ? h1 : h0; }
+  __device__ __forceinline__ int i(int u) const { return u ? i1 : i0; }
 };
 
-// Item tl of this CTA from the host-built schedule: w indexes the largest-first
-// order of (query tile, batch, head), items given out longest first to the CTA
-// with the least work so far.
-__device__ __forceinline__ bool fwd3_item(const FwdArgs& a, int tl, Fwd3Item& it) {
+// Item tl of this CTA: entries (b, h0 | (h1 + 1) << 16, i0, i1), b = -1 past the end.
+__device__ __forceinline__ bool fwd4_item(const FwdArgs& a, int tl, Fwd4Item& it) {
   if (tl >= a.sched_k) return false;
-  const int w = __ldg(a.sched + (size_t)blockIdx.x * a.sched_k + tl);
-  if (w < 0) return false;
-  const int per_i = a.B * a.Hq;
-  it.i = a.nt - 1 - w / per_i;
-  const int rem = w % per_i;
-  it.h = rem % a.Hq;  // the heads of one kv group sit next to each other: their K/V tiles meet in L2
-  it.b = rem / a.Hq;
+  const int4 w = __ldg(reinterpret_cast<const int4*>(a.sched) + (size_t)blockIdx.x * a.sched_k + tl);
+  if (w.x < 0) return false;
+  it.b = w.x;
+  it.h0 = w.y & 0xffff;
+  it.h1 = (int)((uint32_t)w.y >> 16) - 1;
+  it.nu = it.h1 >= 0 ? 2 : 1;
+  it.i0 = w.z;
+  it.i1 = it.nu == 2 ? w.w : -1;
   return true;
 }
 
 template <int D, bool F8>
-__global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ FwdArgs a) {
-  using C = Fwd3Cfg<D, F8>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+__global__ void __launch_bounds__(384, 1) k_attn_fwd4(const __grid_constant__ FwdArgs a) {
+  using C = Fwd4Cfg<D, F8>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  // the swizzled tiles need a 1024-byte aligned base; the declaration asks for it
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicCAS(a.status, 0, kStatusTimeout);
+    return;
+  }
   constexpr int S = C::kStages;
   constexpr int TB = C::kTileBytes;
   constexpr int TQK = C::kQKTileBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* q_full = bars;         // [2]
-  uint64_t* q_empty = bars + 2;    // [2]
-  uint64_t* kv_full = bars + 4;    // [S]
-  uint64_t* kv_empty = bars + 8;   // [S]
-  uint64_t* s_full = bars + 12;    // [2]
-  uint64_t* s_read = bars + 14;    // [2] the step's warpgroup has read its scores
-  uint64_t* p_ready = bars + 16;   // [2]
-  uint64_t* pv_done = bars + 18;   // [2] PV of the P buffer's last step completed
-  uint64_t* m_ready = bars + 20;   // running maximum of the latest step stored
-  uint64_t* l_ready = bars + 21;   // running sum of the latest step stored
-  uint64_t* o_free = bars + 22;    // the item's O has been read out
-  uint64_t* drain = bars + 23;     // [2] one per issuing thread
-  uint64_t* ost_full = bars + 26;  // [2] a warpgroup's rows of O are staged
-  uint64_t* ost_free = bars + 28;  // [2] the previous store from a warpgroup's staging tile has read it
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 30);
-  volatile int* abort = reinterpret_cast<volatile int*>(bars + 30) + 1;
-  float* sm_m = reinterpret_cast<float*>(smem + C::kOffStat);
-  float* sm_l = sm_m + kTile;
+  uint64_t* q_full = bars;                  // [4] Q slots
+  uint64_t* q_empty = q_full + 4;           // [4] the slot's last S has completed
+  uint64_t* kv_full = q_empty + 4;          // [S]
+  uint64_t* kv_empty = kv_full + S;         // [S] both O += P V issuers are done with the stage
+  uint64_t* s_full = kv_empty + S;          // [2] per unit
+  uint64_t* s_read = s_full + 2;            // [2] the unit's warpgroup holds its scores in registers
+  uint64_t* p_ready = s_read + 2;           // [2][2] per unit and key half: the half of P is in TMEM
+  uint64_t* pv_done = p_ready + 4;          // [2][2] per unit and key half: that half of O += P V has completed
+  uint64_t* o_free = pv_done + 4;           // [2] the unit's O has been read out
+  uint64_t* drain = o_free + 2;             // [3] one per issuing thread
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* abort = reinterpret_cast<volatile int*>(bars + C::kNumBars) + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
     *abort = 0;
-    for (int k = 0; k < 2; k++) {
+    for (int k = 0; k < C::kQSlots; k++) {
       mbar_init(q_full + k, 1);
       mbar_init(q_empty + k, 1);
-      mbar_init(s_full + k, 1);
-      mbar_init(s_read + k, 4);  // one arrival per warp of the warpgroup
-      mbar_init(p_ready + k, 4);
-      mbar_init(pv_done + k, 1);
-      mbar_init(drain + k, 1);
-      mbar_init(ost_full + k, 4);
-      mbar_init(ost_free + k, 1);
     }
     for (int k = 0; k < S; k++) {
       mbar_init(kv_full + k, 1);
-      mbar_init(kv_empty + k, 1);
+      mbar_init(kv_empty + k, 2);
     }
-    mbar_init(m_ready, 4);
-    mbar_init(l_ready, 4);
-    mbar_init(o_free, 4);
+    for (int u = 0; u < 2; u++) {
+      mbar_init(s_full + u, 1);
+      mbar_init(s_read + u, 4);  // one arrival per warp of the warpgroup
+      mbar_init(p_ready + 2 * u, 4);
+      mbar_init(p_ready + 2 * u + 1, 4);
+      mbar_init(pv_done + 2 * u, 1);
+      mbar_init(pv_done + 2 * u + 1, 1);
+      mbar_init(o_free + u, 4);
+    }
+    for (int k = 0; k < 3; k++) mbar_init(drain + k, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
@@ -714,7 +713,10 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const volatile int never = 0;
-
+  // registers per thread: 64 for the producer and issuer warps (warps 0-3) and
+  // 216 for the softmax warpgroups: 128 x 64 + 256 x 216 = 63,488 of the
+  // 384 x 168 = 64,512 the block is launched with
+  if (warp < 4) regs_dec<64>();  // warpgroup 0: TMA producer and MMA issuers
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -722,15 +724,19 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
       prefetch_tmap(&a.map_k);
       prefetch_tmap(&a.map_v);
       bool ok = true;
-      int g = 0, loaded_items = 0;
-      Fwd3Item it;
-      for (int tl = 0; ok && fwd3_item(a, tl, it); tl++) {
-        const int qb = tl & 1, kvh = it.h / a.G;
-        if (tl >= 2 && !(ok = mbar_wait(q_empty + qb, ((tl >> 1) - 1) & 1, abort))) break;
-        mbar_arrive_expect_tx(q_full + qb, TQK);
-        tma_load_4d(smem + C::kOffQ + qb * TQK, &a.map_q, q_full + qb, 0, it.h, it.i * kTile, it.b);
-        loaded_items = tl + 1;
-        for (int j = 0; j <= it.i; j++, g++) {
+      int g = 0, c = 0;  // K/V stages and Q slots handed out so far
+      Fwd4Item it, nx;
+      bool have = fwd4_item(a, 0, it);
+      for (int tl = 0; ok && have; tl++, it = nx) {
+        have = fwd4_item(a, tl + 1, nx);  // the next entry loads while this item runs
+        const int kvh = it.h0 / a.G;
+        for (int u = 0; u < it.nu; u++, c++) {
+          const int sl = c & 3, use = c >> 2;
+          if (use > 0 && !(ok = mbar_wait(q_empty + sl, (use - 1) & 1, abort))) break;
+          mbar_arrive_expect_tx(q_full + sl, TQK);
+          tma_load_4d(smem + C::kOffQ + sl * TQK, &a.map_q, q_full + sl, 0, it.h(u), it.i(u) * kTile, it.b);
+        }
+        for (int j = 0; ok && j <= it.i0; j++, g++) {
           const int st = g % S, use = g / S;
           if (use > 0 && !(ok = mbar_wait(kv_empty + st, (use - 1) & 1, abort))) break;
           mbar_arrive_expect_tx(kv_full + st, TQK + TB);
@@ -740,12 +746,11 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
       }
       if (!ok) record_timeout(a.status, abort);
       // let every copy issued above land before the CTA can exit
-      for (int tl = loaded_items - 2 < 0 ? 0 : loaded_items - 2; tl < loaded_items; tl++)
-        mbar_wait(q_full + (tl & 1), (tl >> 1) & 1, &never);
+      for (int x = c - 4 < 0 ? 0 : c - 4; x < c; x++) mbar_wait(q_full + (x & 3), (x >> 2) & 1, &never);
       for (int x = g - S < 0 ? 0 : g - S; x < g; x++) mbar_wait(kv_full + x % S, (x / S) & 1, &never);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ S = Q K^T issuer
+    // ------------------------------------------------------------ S = Q K^T issuer (both units)
     if (lane == 0) {
       constexpr uint32_t idS = F8 ? idesc_e4m3(128, 128, false, false) : idesc_fp16(128, 128, false, false);
       constexpr uint32_t kStepK = 32 >> 4;  // 16 fp16 or 32 e4m3 values of K
@@ -753,81 +758,111 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
       const uint64_t dQ0 = smem_desc(smem_u32(smem + C::kOffQ), 16, C::kQKSBO, C::kQKSwz);
       const uint64_t dK0 = smem_desc(smem_u32(smem + C::kOffK), 16, C::kQKSBO, C::kQKSwz);
       bool ok = true;
-      int g = 0;
-      Fwd3Item it;
-      for (int tl = 0; ok && fwd3_item(a, tl, it); tl++) {
-        const int qb = tl & 1;
-        if (!(ok = mbar_wait(q_full + qb, (tl >> 1) & 1, abort))) break;
-        for (int j = 0; j <= it.i; j++, g++) {
+      int g = 0, c = 0, n[2] = {0, 0};  // K/V stages, Q slots, S issued per unit
+      Fwd4Item it, nx;
+      bool have = fwd4_item(a, 0, it);
+      for (int tl = 0; ok && have; tl++, it = nx) {
+        have = fwd4_item(a, tl + 1, nx);
+        for (int j = 0; ok && j <= it.i0; j++, g++) {
           const int st = g % S;
           if (!(ok = mbar_wait(kv_full + st, (g / S) & 1, abort))) break;
-          // the score buffer's previous step (g - 2) has read its scores
-          if (g >= 2 && !(ok = mbar_wait(s_read + (g & 1), ((g >> 1) - 1) & 1, abort))) break;
-          tc_fence_after();
-          if constexpr (F8)
-            mma_ss_chain2_f8(tmem + C::kColS + (g & 1) * 128, dQ0 + (uint64_t)(qb * tstep), kStepK,
-                             dK0 + (uint64_t)(st * tstep), kStepK, idS, 0u);
-          else
-            mma_ss_chain<D / 16>(tmem + C::kColS + (g & 1) * 128, dQ0 + (uint64_t)(qb * tstep), kStepK,
-                                 dK0 + (uint64_t)(st * tstep), kStepK, idS, 0u);
-          mma_commit(s_full + (g & 1));
-          if (j == it.i) mma_commit(q_empty + qb);
+          for (int u = 0; u < it.nu; u++) {
+            if (j > it.i(u)) continue;
+            const int q = c + u, sl = q & 3;
+            if (j == 0 && !(ok = mbar_wait(q_full + sl, (q >> 2) & 1, abort))) break;
+            // the unit's previous scores are in its warpgroup's registers
+            if (n[u] > 0 && !(ok = mbar_wait(s_read + u, (n[u] - 1) & 1, abort))) break;
+            tc_fence_after();
+            if constexpr (F8)
+              mma_ss_chain2_f8(tmem + C::kColS + 128u * u, dQ0 + (uint64_t)(sl * tstep), kStepK,
+                               dK0 + (uint64_t)(st * tstep), kStepK, idS, 0u);
+            else
+              mma_ss_chain<D / 16>(tmem + C::kColS + 128u * u, dQ0 + (uint64_t)(sl * tstep), kStepK,
+                                   dK0 + (uint64_t)(st * tstep), kStepK, idS, 0u);
+            mma_commit(s_full + u);
+            if (j == it.i(u)) mma_commit(q_empty + sl);
+            n[u]++;
+          }
         }
+        c += it.nu;
       }
       if (!ok) record_timeout(a.status, abort);
       mma_commit(drain);
       mbar_wait(drain, 0, &never);
     }
-  } else if (warp == 10) {
-    // ------------------------------------------------------------ O += P V issuer
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ O_u += P_u V issuers
     if (lane == 0) {
+      const int u = warp - 2;
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
       constexpr uint32_t kStepMN = (16 * C::kSpan) >> 4;
       constexpr uint32_t tstep = (uint32_t)TB >> 4;
       const uint64_t dV0 = smem_desc(smem_u32(smem + C::kOffV), 16, C::kSBO, C::kSwz);
       bool ok = true;
-      int g = 0;
-      Fwd3Item it;
-      for (int tl = 0; ok && fwd3_item(a, tl, it); tl++) {
-        for (int j = 0; j <= it.i; j++, g++) {
+      int g = 0, n = 0, e = 0;  // K/V stages, this unit's steps, this unit's items
+      Fwd4Item it, nx;
+      bool have = fwd4_item(a, 0, it);
+      for (int tl = 0; ok && have; tl++, it = nx) {
+        have = fwd4_item(a, tl + 1, nx);
+        const bool act = u < it.nu;
+        for (int j = 0; ok && j <= it.i0; j++, g++) {
           const int st = g % S;
-          if (!(ok = mbar_wait(p_ready + (g & 1), (g >> 1) & 1, abort))) break;
-          if (j == 0 && tl > 0 && !(ok = mbar_wait(o_free, (tl - 1) & 1, abort))) break;
-          tc_fence_after();
-          mma_ts_chain<8, false>(tmem + C::kColO, tmem + C::kColP + (g & 1) * 64, dV0 + (uint64_t)(st * tstep),
-                                 kStepMN, idPV, j > 0 ? 1u : 0u);
-          mma_commit(pv_done + (g & 1));
-          // K was read by S(g), which completed before this step's softmax began
-          mma_commit(kv_empty + st);
+          if (act && j <= it.i(u)) {
+            // keys 0..63 of P go out while the warpgroup still computes keys 64..127
+            if (!(ok = mbar_wait(p_ready + 2 * u, n & 1, abort))) break;
+            if (j == 0 && e > 0 && !(ok = mbar_wait(o_free + u, (e - 1) & 1, abort))) break;
+            tc_fence_after();
+            const uint64_t dv = dV0 + (uint64_t)(st * tstep);
+            mma_ts_chain<4, false>(tmem + C::kColO + 64u * u, tmem + C::kColP + 64u * u, dv, kStepMN, idPV,
+                                   j > 0 ? 1u : 0u);
+            mma_commit(pv_done + 2 * u);
+            if (!(ok = mbar_wait(p_ready + 2 * u + 1, n & 1, abort))) break;
+            tc_fence_after();
+            mma_ts_chain<4, false>(tmem + C::kColO + 64u * u, tmem + C::kColP + 64u * u + 32u,
+                                   dv + (uint64_t)(4 * kStepMN), kStepMN, idPV, 1u);
+            mma_commit(pv_done + 2 * u + 1);
+            mma_commit(kv_empty + st);  // V by this PV; K by this unit's S, complete before its P existed
+            n++;
+          } else {
+            mbar_arrive(kv_empty + st);  // this unit does not use the stage
+          }
         }
+        if (act) e++;
       }
       if (!ok) record_timeout(a.status, abort);
-      mma_commit(drain + 1);
-      mbar_wait(drain + 1, 0, &never);
+      mma_commit(drain + 1 + u);
+      mbar_wait(drain + 1 + u, 0, &never);
     }
   } else {
-    // ------------------------------------------------------------ softmax warpgroups
-    const int wg = (warp - 2) >> 2;  // 0: warps 2-5, 1: warps 6-9
-    const int q4 = warp & 3;         // TMEM lane quarter
-    const int r = q4 * 32 + lane;    // query row within the tile
+    // ------------------------------------------------------------ softmax warpgroup of unit u
+    regs_inc<216>();
+    const int u = (warp - 4) >> 2;  // 0: warps 4-7, 1: warps 8-11
+    const int q4 = warp & 3;        // TMEM lane quarter
+    const int r = q4 * 32 + lane;   // query row within the tile
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-    const uint32_t sbuf = trow + C::kColS + wg * 128;
-    const uint32_t pbuf = trow + C::kColP + wg * 64;
-    uint8_t* ost = smem + C::kOffOst + wg * C::kOstBytes;
-    float sl2 = a.scale_log2;
+    const uint32_t sbuf = trow + C::kColS + 128u * u;
+    const uint32_t pbuf = trow + C::kColP + 64u * u;
+    const uint32_t obuf = trow + C::kColO + 64u * u;
+    // this warp's staging area for its 32 rows of O (boxes of 32 rows x 128 bytes)
+    uint8_t* ost = smem + C::kOffOst + u * C::kOstBytes + q4 * (C::kOstBytes / 4);
     bool ok = true;
-    int g = 0, ne = 0;  // ne: this warpgroup's epilogues so far
-    Fwd3Item it;
-    for (int tl = 0; ok && fwd3_item(a, tl, it); tl++) {
-      const int t = it.i * kTile + r;
+    int n = 0, ne = 0;  // this unit's steps and epilogues so far
+    Fwd4Item it, nx;
+    bool have = fwd4_item(a, 0, it);
+    for (int tl = 0; ok && have; tl++, it = nx) {
+      have = fwd4_item(a, tl + 1, nx);
+      if (u >= it.nu) continue;
+      const int iu = it.i(u), hu = it.h(u);
+      const int t = iu * kTile + r;
+      float sl2 = a.scale_log2;
       if constexpr (F8) {  // scores are in e4m3 code units: fold in the two heads' scales
-        const float sq = __ldg(a.qk_amax + it.h), sk = __ldg(a.qk_amax + a.Hq + it.h / a.G);
+        const float sq = __ldg(a.qk_amax + hu), sk = __ldg(a.qk_amax + a.Hq + hu / a.G);
         sl2 = a.scale_log2 * ((sq > 0.f ? sq : 448.f) * (1.f / 448.f)) * ((sk > 0.f ? sk : 448.f) * (1.f / 448.f));
       }
-      for (int j = 0; j <= it.i; j++, g++) {
-        if ((g & 1) != wg) continue;
-        const bool diag = (j == it.i);
-        ok = __all_sync(0xffffffffu, mbar_wait(s_full + wg, (g >> 1) & 1, abort));
+      float r_run = 0.f, l_run = 0.f;  // running maximum (raw logit units) and sum of the row
+      for (int j = 0; j <= iu; j++, n++) {
+        const bool diag = (j == iu);
+        ok = __all_sync(0xffffffffu, mbar_wait(s_full + u, n & 1, abort));
         if (!ok) break;
         tc_fence_after();
         // pass 1: row maximum over the 128 keys (masked past the diagonal); the
@@ -839,38 +874,31 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
 #pragma unroll
         for (int h2 = 0; h2 < 2; h2++) {
           uint32_t lo[64];
-          uint32_t(&u)[64] = h2 ? hi : lo;
-          tmem_ld32(sbuf + h2 * 64, *reinterpret_cast<uint32_t(*)[32]>(u));
-          tmem_ld32(sbuf + h2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+          uint32_t(&w)[64] = h2 ? hi : lo;
+          tmem_ld32(sbuf + h2 * 64, *reinterpret_cast<uint32_t(*)[32]>(w));
+          tmem_ld32(sbuf + h2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(w + 32));
           tmem_wait_ld();
           if (diag) {
 #pragma unroll
             for (int e = 0; e < 64; e++)
-              if (h2 * 64 + e > r) u[e] = 0xff800000u;  // -inf: key after the query
+              if (h2 * 64 + e > r) w[e] = 0xff800000u;  // -inf: key after the query
           }
 #pragma unroll
           for (int e = 0; e < 64; e += 2)
-            mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(u[e]), __uint_as_float(u[e + 1]));
+            mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(w[e]), __uint_as_float(w[e + 1]));
         }
         const float mxr = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        // running maximum (raw logit units) after the previous key tile, from the other
-        // warpgroup; at an item's first tile the wait only orders the two writes of sm_m
         float r_use = mxr, alpha = 1.f;
-        if (g > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(m_ready, (g - 1) & 1, abort));
-          if (!ok) break;
-        }
         if (j > 0) {
-          const float r_old = sm_m[r];
-          r_use = r_old;
-          const float m_old = __fmul_rn(r_old, sl2);
-          const float r_new = fmaxf(r_old, mxr);
+          r_use = r_run;
+          const float m_old = __fmul_rn(r_run, sl2);
+          const float r_new = fmaxf(r_run, mxr);
           const float m_new = __fmul_rn(r_new, sl2);
           // lazy rescale: only when some row's maximum grew by more than 2^8; O must
-          // then hold every earlier P V (the latest is step g - 1's)
+          // then hold every earlier P V (the latest is this unit's previous step)
           if (__any_sync(0xffffffffu, m_new > m_old + 8.0f)) {
-            ok = __all_sync(0xffffffffu, mbar_wait(pv_done + ((g - 1) & 1), ((g - 1) >> 1) & 1, abort));
+            ok = __all_sync(0xffffffffu, mbar_wait(pv_done + 2 * u + 1, (n - 1) & 1, abort));
             if (!ok) break;
             tc_fence_after();
             r_use = r_new;
@@ -878,26 +906,26 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
             uint32_t w[32];
 #pragma unroll
             for (int c = 0; c < D / 32; c++) {
-              tmem_ld32(trow + C::kColO + c * 32, w);
+              tmem_ld32(obuf + c * 32, w);
               tmem_wait_ld();
 #pragma unroll
               for (int e = 0; e < 32; e++) w[e] = __float_as_uint(__uint_as_float(w[e]) * alpha);
-              tmem_st32(trow + C::kColO + c * 32, w);
+              tmem_st32(obuf + c * 32, w);
             }
             tmem_wait_st();
             tc_fence_before();
           }
         }
-        sm_m[r] = r_use;
-        warp_arrive(m_ready);
+        r_run = r_use;
         const float m_use = __fmul_rn(r_use, sl2);
-        // P's buffer is free once the PV of step g - 2 has completed
-        if (g >= 2) {
-          ok = __all_sync(0xffffffffu, mbar_wait(pv_done + wg, ((g >> 1) - 1) & 1, abort));
+        // keys 0..63 of the P buffer are free once the first half of the unit's previous
+        // O += P V has completed (keys 64..127: its second half, waited for below)
+        if (n > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(pv_done + 2 * u, (n - 1) & 1, abort));
           if (!ok) break;
         }
         tc_fence_after();
-        // pass 2: P = exp2(s * scale_log2 - m) as bf16 into this warpgroup's P buffer.
+        // pass 2: P = exp2(s * scale_log2 - m) as bf16 into the unit's P buffer.
         // Keys 0..63 are read again, 16 at a time (the next chunk loads while this
         // one is exponentiated); keys 64..127 come from pass 1's registers.
         // (the row sum adds the fp32 values of P; the MMA multiplies their bf16 roundings)
@@ -916,6 +944,18 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
             for (int e = 0; e < 16; e++)
               if (16 * c + e > r) cur[e] = 0xff800000u;  // exp2(-inf) = 0
           }
+          if (c == 4) {
+            // keys 0..63 of P are stored: the first half of O += P V may start; keys
+            // 64..127 wait for the second half of the previous one
+            tmem_wait_st();
+            tc_fence_before();
+            warp_arrive(p_ready + 2 * u);
+            if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(pv_done + 2 * u + 1, (n - 1) & 1, abort))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           uint32_t pk[8];
 #pragma unroll
           for (int e = 0; e < 8; e++) {
@@ -928,84 +968,67 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
           tmem_st8(pbuf + c * 8, pk);
           if (c < 3) tmem_wait_ld();
           if (c == 2) {
-            // every score is in registers: S of step g + 2 may overwrite them
+            // every score is in registers: the unit's next S may overwrite them
             tc_fence_before();
-            warp_arrive(s_read + wg);
+            warp_arrive(s_read + u);
           }
         }
+        if (!ok) break;
         tmem_wait_st();
         tc_fence_before();
-        warp_arrive(p_ready + wg);
-        float l;
+        warp_arrive(p_ready + 2 * u + 1);
         {
           float s0, s1, s2, s3, s4, s5, s6, s7;
           f2_split(sum4[0], s0, s1);
           f2_split(sum4[1], s2, s3);
           f2_split(sum4[2], s4, s5);
           f2_split(sum4[3], s6, s7);
-          l = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+          const float l = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+          l_run = j > 0 ? fmaf(l_run, alpha, l) : l;
         }
-        // running sum after the previous key tile; at an item's first tile the wait only
-        // orders this step's write of sm_l after the previous step's read
-        if (g > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(l_ready, (g - 1) & 1, abort));
-          if (!ok) break;
-        }
-        if (j > 0) l += sm_l[r] * alpha;
-        if (!diag) sm_l[r] = l;
-        warp_arrive(l_ready);
         if (!diag) continue;
-        // last key tile of the item: O / l and the LSE
-        ok = __all_sync(0xffffffffu, mbar_wait(pv_done + wg, (g >> 1) & 1, abort));
+        // last key tile of the unit: O / l and the LSE
+        ok = __all_sync(0xffffffffu, mbar_wait(pv_done + 2 * u + 1, n & 1, abort));
         if (!ok) break;
         tc_fence_after();
-        const float inv = 1.f / l;
+        const float inv = 1.f / l_run;
         float x[D];
 #pragma unroll
         for (int c = 0; c < D / 32; c++) {
           uint32_t w[32];
-          tmem_ld32(trow + C::kColO + c * 32, w);
+          tmem_ld32(obuf + c * 32, w);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; e++) x[c * 32 + e] = __uint_as_float(w[e]) * inv;
         }
         tc_fence_before();
-        warp_arrive(o_free);  // O is in registers: the next item's first PV may overwrite it
-        // O leaves through the warpgroup's staging tile and a TMA store (rows past T
-        // are not written); the tile is reused once the previous store has read it
+        warp_arrive(o_free + u);  // O is in registers: the unit's next first O += P V may overwrite it
+        // each warp's 32 rows of O leave through its staging area and TMA stores (rows
+        // past T are not written); the area is reused once the previous store has read it
         if (ne > 0) {
-          if (r == 0) {
-            bulk_wait_read<0>();
-            mbar_arrive(ost_free + wg);
-          }
-          ok = __all_sync(0xffffffffu, mbar_wait(ost_free + wg, (ne - 1) & 1, abort));
-          if (!ok) break;
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
         }
         if (a.o_fp32) {
-          stage_rows<D, 4>(x, ost, r);
+          stage_rows32<D, 4>(x, ost, lane);
         } else {
-          stage_rows<D, 2>(x, ost, r);
+          stage_rows32<D, 2>(x, ost, lane);
         }
         fence_proxy_async_smem();
-        warp_arrive(ost_full + wg);
-        if (r == 0) {
-          if (!(ok = mbar_wait(ost_full + wg, ne & 1, abort))) {
-            record_timeout(a.status, abort);
-          } else {
-            const int span = D * (a.o_fp32 ? 4 : 2) < 128 ? D * (a.o_fp32 ? 4 : 2) : 128;
-            const int cols = span / (a.o_fp32 ? 4 : 2);
-            for (int c0 = 0, bx = 0; c0 < D; c0 += cols, bx++)
-              tma_store_4d(&a.map_o, ost + bx * kTile * span, c0, it.h, it.i * kTile, it.b);
-            bulk_commit();
-          }
+        __syncwarp();
+        if (lane == 0) {
+          const int span = D * (a.o_fp32 ? 4 : 2) < 128 ? D * (a.o_fp32 ? 4 : 2) : 128;
+          const int cols = span / (a.o_fp32 ? 4 : 2);
+          for (int c0 = 0, bx = 0; c0 < D; c0 += cols, bx++)
+            tma_store_4d(&a.map_o, ost + bx * 32 * span, c0, hu, iu * kTile + q4 * 32, it.b);
+          bulk_commit();
         }
         ne++;
-        if (!__all_sync(0xffffffffu, ok)) break;
         if (t < a.T)
-          a.lse[((size_t)it.b * a.Hq + it.h) * a.T + t] = (__fmul_rn(r_use, sl2) + __log2f(l)) * 0.69314718055994531f;
+          a.lse[((size_t)it.b * a.Hq + hu) * a.T + t] = (m_use + __log2f(l_run)) * 0.69314718055994531f;
       }
     }
-    if (r == 0) bulk_wait<0>();  // the O stores are done with the staging tiles
+    if (lane == 0) bulk_wait<0>();  // the O stores are done with the staging areas
     if (!ok) record_timeout(a.status, abort);
   }
 
@@ -1019,21 +1042,18 @@ __global__ void __launch_bounds__(352, 1) k_attn_fwd3(const __grid_constant__ Fw
 }
 
 template <int D, bool F8 = false>
-cudaError_t launch_fwd3_t(const FwdArgs& a, cudaStream_t s) {
-  using C = Fwd3Cfg<D, F8>;
+cudaError_t launch_fwd4_t(const FwdArgs& a, int grid, cudaStream_t s) {
+  using C = Fwd4Cfg<D, F8>;
   static bool attr_set[64] = {};
-  int dev = 0, nsm = 0;
+  int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
     cudaError_t e =
-        cudaFuncSetAttribute(k_attn_fwd3<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        cudaFuncSetAttribute(k_attn_fwd4<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  cudaError_t e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  const int items = a.nt * a.B * a.Hq;
-  k_attn_fwd3<D, F8><<<items < nsm ? items : nsm, C::kThreads, C::kSmemBytes, s>>>(a);
+  k_attn_fwd4<D, F8><<<grid, C::kThreads, C::kSmemBytes, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -1057,11 +1077,11 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, bool precise, cudaStream_t s) {
-  if (a.D == 64) return precise ? launch_fwd_t<64, true>(a, s) : launch_fwd3_t<64>(a, s);
-  return precise ? launch_fwd_t<32, true>(a, s) : launch_fwd3_t<32>(a, s);
+  if (precise) return a.D == 64 ? launch_fwd_t<64, true>(a, s) : launch_fwd_t<32, true>(a, s);
+  return a.D == 64 ? launch_fwd4_t<64>(a, a.grid, s) : launch_fwd4_t<32>(a, a.grid, s);
 }
 
-cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t s) { return launch_fwd3_t<64, true>(a, s); }
+cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t s) { return launch_fwd4_t<64, true>(a, a.grid, s); }
 
 cudaError_t launch_rope_amax(const RopeArgs& a, cudaStream_t s) {
   const long long n = (long long)a.B * a.T * (a.Hq + a.Hkv) * 8;

@@ -27,10 +27,10 @@ inline int fwd_max_heads(int D, bool precise) { return D == 64 ? (precise ? 3 : 
 
 struct FwdArgs {
   // 4-D tiled maps over [B, T, H, D], box D x 1 x 128 x 1.  Default precision:
-  // map_q / map_k cover the rotated fp16 copies made by the RoPE pre-pass;
-  // precise logits: the bf16 inputs (the kernel rotates them itself).
+  // map_q / map_k cover the rotated fp16 copies in the workspace (e4m3 with
+  // FP8); precise logits: the bf16 inputs (the kernel rotates them itself).
   CUtensorMap map_q, map_k, map_v;
-  CUtensorMap map_o;                // store map over o (default precision): 128-byte (or 64-byte) column boxes x 128 rows
+  CUtensorMap map_o;                // store map over o (default precision): 128-byte (or 64-byte) column boxes x 32 rows
   void* o;                          // [B, T, Hq, D] bf16 or fp32
   float* lse;                       // [B, Hq, T]
   float* lse_lo;                    // [B, Hq, T] fp32 remainder of lse (precise logits only)
@@ -42,8 +42,9 @@ struct FwdArgs {
   float scale_log2;                 // log2(e) / sqrt(D), rounded to fp32
   float scale_log2_lo;              // remainder log2(e)/sqrt(D) - scale_log2
   const float* qk_amax;             // FP8 forward: per-head max |rotated value|, [Hq] for q then [Hkv] for k
-  const int* sched;                 // [grid, sched_k] work items of each CTA (-1: none), see fwd_schedule
+  const int* sched;                 // [grid, sched_k] int4 work items of each CTA (b = -1: none), see fwd_pair_schedule
   int sched_k;
+  int grid;                         // CTAs of the persistent forward
 };
 
 // Division of a non-negative 32-bit n < 2^31 by a runtime divisor d >= 1 with

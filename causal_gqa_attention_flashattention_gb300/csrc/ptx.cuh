@@ -418,6 +418,20 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
+// ------------------------------------------------------------------ register budget
+// Per-warpgroup register limits (all four warps of a warpgroup execute these):
+// dec returns registers to the block's pool, inc takes them from it and waits
+// until enough are free.  The warpgroups' shares must add up to at most the
+// block's launch total (threads x registers per thread at launch).
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ misc math
 __device__ __forceinline__ float ex2(float x) {
   float y;

@@ -64,7 +64,10 @@ typedef enum {
 /* Flag bits for ne_attn_fwd_ex, ne_attn_bwd and the workspace-size queries. */
 #define NE_ATTN_O_FP32 1     /* o is float32 [B,T,Hq,D] (forward output, backward input) */
 #define NE_ATTN_GRAD_FP32 2  /* dq, dk, dv are float32 */
-#define NE_ATTN_PRECISE_QK 4 /* split precision for inputs whose logits reach |s| ~ 10^2..10^4:
+#define NE_ATTN_PRECISE_QK 4 /* split precision for inputs whose logits reach |s| ~ 10^2..10^4
+                                (default precision rounds the rotated q, k to fp16, 2^-11
+                                relative, which there moves a logit by whole units: on such
+                                inputs its dq and dk are several percent off):
                                 S = qhi.khi + qlo.khi + qhi.klo from fp16 hi + lo parts of the
                                 rotated q and k (three tensor-core products instead of one);
                                 P = Phi + Plo (two bf16 parts) in O += P V and dV += P^T dO;
@@ -345,13 +348,18 @@ int ne_attn_profile_read(double* total_ms, long long* launches);
 int ne_attn_debug_timeout_probe(int limit_us, void* stream);
 
 /*
- * Host-only view of the persistent forward's work schedule (no device call):
- * for nt query tiles, per_i = B * Hq items per tile and `grid` CTAs, writes
- * the [grid, K] table of item indices w (largest-first order: query tile
- * nt - 1 - w / per_i; -1 pads a CTA's row) into `table` and K into *K.
- * NE_ERR_ARG (with *K set) if capacity < grid * K.
+ * Host-only view of the persistent forward's work schedule (no device call)
+ * for B batches, Hkv key/value heads of G query heads each, nt query tiles and
+ * nsm SMs.  A work item pairs two units (query head, 128-row query tile) of one
+ * (batch, key/value head) that share the item's key/value tiles; each of the
+ * kernel's two softmax warpgroups owns one unit.  Writes *grid = min(items,
+ * nsm), *K (items of the busiest CTA) and the [grid, K] table of int4 entries
+ * (b, h0 | (h1 + 1) << 16, i0, i1) into `table` (4 ints per entry; h1 + 1 = 0
+ * for an item of one unit; b = -1 pads a CTA's row).  NE_ERR_ARG (with *grid
+ * and *K set) if capacity < 4 * grid * K.
  */
-int ne_attn_debug_fwd_schedule(int nt, int per_i, int grid, int* table, int capacity, int* K);
+int ne_attn_debug_fwd_schedule(int B, int Hkv, int G, int nt, int nsm, int* table, int capacity, int* grid,
+                               int* K);
 
 #ifdef __cplusplus
 }

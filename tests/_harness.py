@@ -11,6 +11,20 @@ MAX_ABS_TOL = 2e-2
 # within a few fp32 ulps of ln(sum exp) times the row's dynamic range.
 LSE_ABS_TOL = 1e-2
 
+# The long-context stress workload in split precision (NE_ATTN_PRECISE_QK).  Its
+# outlier rows reach logits |s| ~ 1.7e4.  The split-precision logits carry the
+# rotated q, k as fp16 hi + lo (22 mantissa bits: 2^-22 relative per operand)
+# and accumulate in fp32 (2^-24 per step at |s|), so a logit is off by up to
+# ~2^-21 |s|, about 1e-2 at 1.7e4 (the LSE, measured: 1.1e-2).  A row's P then
+# moves by that much relative, and dq = scale sum_j dS_tj k_j, dk (and the LSE)
+# with it: on the few rows whose gradients reach 1e2 .. 3e2 the error is about
+# 1e-3 of the value, above the absolute 2e-2 (measured 1.1e-3 relative at
+# worst).  For dq and dk on that workload each element is held to
+# 2e-2 + 2e-3 |value|; the LSE to 1e-2 + 2^-20 |lse|.  O and dv, and the
+# relative L2 of every tensor, keep the stated bounds.
+STRESS_GRAD_REL = 2e-3
+STRESS_LSE_REL = 2.0 ** -20
+
 
 def to_device(bits):
     import torch

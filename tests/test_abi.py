@@ -211,23 +211,31 @@ def test_fp8_flag_rules_on_the_host(libne):
     assert fx(p, p, p, p, p, 1, 16, 2, 1, 64, 10000.0, 64, null, 0, null) == -1  # unknown flag
 
 
-@pytest.mark.parametrize("nt,per_i,grid", [(4, 192, 152), (1, 7, 7), (64, 24, 152), (3, 5, 152), (5, 33, 10)])
-def test_forward_schedule(libne, nt, per_i, grid):
-    """The forward's work table (host logic): every item exactly once, each CTA's
-    items longest first, and the busiest CTA no busier than with the fixed
-    snake order over the same largest-first list."""
+@pytest.mark.parametrize("B,Hkv,G,nt,nsm", [(16, 4, 3, 4, 152), (8, 4, 4, 8, 152), (2, 4, 3, 64, 152),
+                                             (8, 2, 2, 4, 152), (1, 1, 8, 3, 152), (3, 2, 5, 5, 10),
+                                             (1, 1, 1, 1, 152), (2, 3, 1, 7, 4)])
+def test_forward_schedule(libne, B, Hkv, G, nt, nsm):
+    """The forward's work table (host logic): every (batch, head, query tile)
+    unit exactly once; the two units of an item share batch and key/value head
+    and their first unit has the larger tile; head pairs sit at one tile and
+    tile pairs of one head are adjacent; each CTA's items longest first; and
+    the busiest CTA within one item of the average."""
     from causal_gqa_attention_flashattention_gb300 import binding
-    lists = binding.fwd_schedule(nt, per_i, grid)
-    n = nt * per_i
-    assert len(lists) == grid and sorted(w for l in lists for w in l) == list(range(n))
-    size = lambda w: nt - w // per_i  # key tiles of item w
+    lists = binding.fwd_schedule(B, Hkv, G, nt, nsm)
+    units = []
+    cost = lambda it: 2 * (it[1][1] + 1) + 1 + (2 * (it[2][1] + 1) + 1 if it[2] else 0)
     for l in lists:
-        assert [size(w) for w in l] == sorted((size(w) for w in l), reverse=True)
-    busiest = max(sum(size(w) for w in l) for l in lists)
-    snake = [0] * grid
-    for w in range(n):
-        tl, c = divmod(w, grid)
-        snake[c if tl % 2 == 0 else grid - 1 - c] += size(w)
-    assert busiest <= max(snake)
-    if (nt, per_i, grid) == (4, 192, 152):  # the 116M-model forward: 13 key tiles instead of 14
-        assert busiest == 13 and max(snake) == 14
+        for b, u0, u1 in l:
+            units.append((b, u0[0], u0[1]))
+            if u1 is not None:
+                units.append((b, u1[0], u1[1]))
+                assert u0[0] // G == u1[0] // G and u0[1] >= u1[1]
+                assert (u0[1] == u1[1] and u1[0] == u0[0] + 1) or (u0[0] == u1[0] and u1[1] == u0[1] - 1)
+        assert [cost(it) for it in l] == sorted((cost(it) for it in l), reverse=True)
+    want = sorted((b, h, i) for b in range(B) for h in range(Hkv * G) for i in range(nt))
+    assert sorted(units) == want
+    n_items = sum(len(l) for l in lists)
+    assert len(lists) == min(n_items, nsm)
+    loads = [sum(cost(it) for it in l) for l in lists]
+    biggest = max(cost(it) for l in lists for it in l)
+    assert max(loads) <= sum(loads) / len(lists) + biggest

@@ -42,31 +42,45 @@ def run_gpu(nb, x, base=inputs.ROPE_BASE, grad_dtype=None, o_dtype=None, precise
                 dk=H.to_f64(dk), dv=H.to_f64(dv))
 
 
-def compare(oracle_mod, x, gpu, shape, groups, base=inputs.ROPE_BASE, tol_abs=H.MAX_ABS_TOL):
+def compare(oracle_mod, x, gpu, shape, groups, base=inputs.ROPE_BASE, tol_abs=H.MAX_ABS_TOL, ref=None,
+            check=True, grad_rel=0.0, lse_rel=0.0):
+    """grad_rel / lse_rel: per-element allowances proportional to the value, for
+    dq, dk and the LSE (the stress workload's split-precision bound, _harness)."""
     B, T, Hq, Hkv, D = shape
-    ref = oracle_mod.attn_bwd(x["q"], x["k"], x["v"], x["dout"], base, groups=groups)
+    if ref is None:
+        ref = oracle_mod.attn_bwd(x["q"], x["k"], x["v"], x["dout"], base, groups=groups)
     qsel, ksel = H.group_slices(B, Hq, Hkv, groups)
-    report = {}
+    report, over = {}, {}
     for name, gat, sel in (("o", H.gather_q, qsel), ("dq", H.gather_q, qsel),
                            ("dk", H.gather_k, ksel), ("dv", H.gather_k, ksel)):
         g, r = gat(gpu[name], sel), gat(ref[name], sel)
         assert np.isfinite(g).all(), name
         report[name] = H.errors(g, r)
+        rel = grad_rel if name in ("dq", "dk") else 0.0
+        over[name] = int(np.sum(np.abs(g - r) > tol_abs + rel * np.abs(r)))
     g, r = H.gather_lse(gpu["lse"], qsel), H.gather_lse(ref["lse"], qsel)
     report["lse"] = H.errors(g, r)
-    bad = [n for n in ("o", "dq", "dk", "dv") if report[n][0] > H.REL_L2_TOL or report[n][1] > tol_abs]
+    over["lse"] = int(np.sum(np.abs(g - r) > H.LSE_ABS_TOL + lse_rel * np.abs(r)))
+    bad = [n for n in ("o", "dq", "dk", "dv") if report[n][0] > H.REL_L2_TOL or over[n]]
     print("PARITY", shape, {k: ("%.2e" % v[0], "%.2e" % v[1]) for k, v in report.items()})
-    assert not bad and report["lse"][1] <= H.LSE_ABS_TOL, report
+    if check:
+        assert not bad and not over["lse"], (report, over)
     return report
 
 
-WORKLOAD_GROUPS = {
-    "tiny_cpu_model": None,
-    "cpu_small_model_ctx512": None,
-    "gpu_116m_model": None,
-    "scaled_270m_synthetic": [(0, 0), (3, 1), (5, 2), (7, 3)],
-    "long_context_stress": [(1, 2)],
-}
+# Every workload is compared on all of its (batch, kv-head) groups: the stress
+# workload's outlier rows sit anywhere, and the oracle does all of it in seconds.
+WORKLOAD_GROUPS = {name: None for name in inputs.WORKLOAD_ORDER}
+
+_ORACLE_CACHE = {}
+
+
+def workload_oracle(oracle_mod, name, x):
+    """The oracle's forward + backward of a whole workload, computed once per session."""
+    if name not in _ORACLE_CACHE:
+        _ORACLE_CACHE[name] = oracle_mod.attn_bwd(x["q"], x["k"], x["v"], x["dout"], inputs.ROPE_BASE,
+                                                  groups=WORKLOAD_GROUPS[name])
+    return _ORACLE_CACHE[name]
 
 # Output precision per workload.  Gradients are fp32: a bf16 gradient of
 # magnitude >= 4 is already 1/64 away from its neighbours, most of the
@@ -91,8 +105,25 @@ def test_workload_parity(nb, oracle_mod, name):
     kw = mode_kwargs(name)
     # default precision: one workspace for forward and backward, as bench.py runs it
     gpu = run_gpu(nb, x, qk_rotated=not kw["precise"], **kw)
-    rep = compare(oracle_mod, x, gpu, shape, WORKLOAD_GROUPS[name])
+    stress = name == "long_context_stress"
+    rep = compare(oracle_mod, x, gpu, shape, WORKLOAD_GROUPS[name], ref=workload_oracle(oracle_mod, name, x),
+                  grad_rel=H.STRESS_GRAD_REL if stress else 0.0, lse_rel=H.STRESS_LSE_REL if stress else 0.0)
     print(name, rep)
+
+
+def test_stress_workload_in_default_precision(nb, oracle_mod):
+    """What the default precision returns on the stress workload (logits up to
+    ~1.7e4, near one-hot rows): finite outputs, but fp16 rotated operands give
+    the logits ~2^-11 relative error, units of the logit itself there, so dq and
+    dk miss the bounds by far (measured rel-L2 5e-2 and 1.1e-1).  Inputs like
+    these need NE_ATTN_PRECISE_QK; this test keeps that statement true."""
+    name = "long_context_stress"
+    x = inputs.make_workload_inputs(name)
+    shape = tuple(inputs.WORKLOADS[name][:5])
+    gpu = run_gpu(nb, x, grad_dtype=torch.float32, o_dtype=torch.float32, precise=False, qk_rotated=True)
+    rep = compare(oracle_mod, x, gpu, shape, None, ref=workload_oracle(oracle_mod, name, x), check=False)
+    print("STRESS_DEFAULT", {k: ("%.3e" % v[0], "%.3e" % v[1]) for k, v in rep.items()})
+    assert rep["dq"][0] > H.REL_L2_TOL and rep["dk"][0] > H.REL_L2_TOL
 
 
 def test_bf16_gradient_outputs(nb, oracle_mod):

@@ -7,7 +7,10 @@ inputs, seeded).  The metric is algorithmic TFLOP/s: 14 * B * Hq * D *
 T(T+1)/2 matmul flops per fwd+bwd (QK^T and PV forward; recomputed QK^T,
 dP, dV, dK, dQ backward), over the device time of the step.
 
-  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
+
+--workload times another of the workload shapes the same way (the long-context
+stress workload in split precision with fp32 o, the mode its parity needs).
 
 With N > 1 (launched by torchrun, one process per GPU) every rank runs its
 own replica of the workload (the attention has no exchange step) and the
@@ -34,6 +37,7 @@ METRIC = "causal GQA attn fwd+bwd TFLOP/s on 1 GB300 (% of bf16 tensor peak)"
 UNIT = "TFLOP/s"
 WORKLOAD = "gpu_116m_model"
 NUM_SETS = 4  # rotating input/output sets so consecutive steps do not hit a warm L2
+LOAD_S = 0.4  # seconds of graph replays before and after the timed region while clocks are sampled
 
 
 def algo_flops(B, T, Hq, D):
@@ -146,7 +150,7 @@ def traffic_record(kernel):
     return rec
 
 
-def cpu_oracle_sample(budget_s, shape, x):
+def cpu_oracle_sample(budget_s, shape, x, workload=WORKLOAD):
     """Times the fp64 oracle (fwd + bwd) on whole (batch, kv-head) groups of the
     workload until about budget_s seconds of CPU work have been done."""
     import oracle
@@ -163,7 +167,7 @@ def cpu_oracle_sample(budget_s, shape, x):
     G = Hq // Hkv
     fl = algo_flops(1, T, G, D)["total"] * n
     return dict(value=fl / dt / 1e12, unit=UNIT, cores=oracle.num_threads(), kind="oracle",
-                sample="%d of %d (batch, kv-head) groups of %s (fp64 fwd+bwd, %.1f s)" % (n, len(order), WORKLOAD, dt),
+                sample="%d of %d (batch, kv-head) groups of %s (fp64 fwd+bwd, %.1f s)" % (n, len(order), workload, dt),
                 seconds=dt)
 
 
@@ -214,12 +218,16 @@ def run_ours(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
-    shape = tuple(inputs.WORKLOADS[WORKLOAD][:5])
+    workload = args.workload
+    shape = tuple(inputs.WORKLOADS[workload][:5])
     B, T, Hq, Hkv, D = shape
     fl = algo_flops(B, T, Hq, D)
-    x = inputs.make_workload_inputs(WORKLOAD)
+    x = inputs.make_workload_inputs(workload)
     base = inputs.ROPE_BASE
     grad_dtype = torch.float32
+    # the stress workload's logits reach ~1.7e4: it runs in split precision with an fp32 o
+    precise = workload == "long_context_stress"
+    o_dtype = torch.float32 if precise else torch.bfloat16
 
     def host_bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).view(torch.bfloat16)
@@ -228,12 +236,12 @@ def run_ours(args, world, rank, local):
     sets = []
     for _ in range(NUM_SETS):
         q, k, v, do = (t.to(dev) for t in (hq, hk, hv, hdo))
-        sets.append(dict(q=q, k=k, v=v, do=do, o=torch.empty_like(q),
-                         lse=torch.empty((B, Hq, T), dtype=torch.float32, device=dev),
+        sets.append(dict(q=q, k=k, v=v, do=do, o=torch.empty(q.shape, dtype=o_dtype, device=dev),
+                         lse=torch.empty(((2 if precise else 1) * B, Hq, T), dtype=torch.float32, device=dev),
                          dq=torch.empty(q.shape, dtype=grad_dtype, device=dev),
                          dk=torch.empty(k.shape, dtype=grad_dtype, device=dev),
                          dv=torch.empty(k.shape, dtype=grad_dtype, device=dev),
-                         ws=binding.alloc_workspace(B, T, Hq, Hkv, D, device=dev)))
+                         ws=binding.alloc_workspace(B, T, Hq, Hkv, D, precise=precise, device=dev)))
     set_bytes = sum(t.numel() * t.element_size() for t in sets[0].values())
     torch.cuda.synchronize(dev)
     # a side stream: CUDA graphs are captured on a non-default stream
@@ -243,9 +251,11 @@ def run_ours(args, world, rank, local):
     def step(i):
         s = sets[i % NUM_SETS]
         # the forward's workspace (rotated q, k) is the first part of the backward's
-        binding.attn_fwd(s["q"], s["k"], s["v"], base, o=s["o"], lse=s["lse"], workspace=s["ws"], stream=stream)
+        binding.attn_fwd(s["q"], s["k"], s["v"], base, o=s["o"], lse=s["lse"], workspace=s["ws"], o_dtype=o_dtype,
+                         precise=precise, stream=stream)
         binding.attn_bwd(s["q"], s["k"], s["v"], s["o"], s["lse"], s["do"], base, grad_dtype=grad_dtype,
-                         dq=s["dq"], dk=s["dk"], dv=s["dv"], workspace=s["ws"], qk_rotated=True, stream=stream)
+                         dq=s["dq"], dk=s["dk"], dv=s["dv"], workspace=s["ws"], qk_rotated=not precise,
+                         precise=precise, stream=stream)
 
     def barrier():
         if world > 1:
@@ -285,8 +295,23 @@ def run_ours(args, world, rank, local):
     barrier()
     torch.cuda.synchronize(dev)
 
+    # Clocks: the sampler runs while the same graph replays for about LOAD_S seconds
+    # before the timed region and again after it, so that the samples (every 50 ms)
+    # see the load the timed steps run under; the timed region itself is exactly
+    # the K steps between the two events.
+    g_all.replay()
+    torch.cuda.synchronize(dev)
+    t_rep = time.perf_counter()
+    g_all.replay()
+    torch.cuda.synchronize(dev)
+    load_reps = max(1, int(LOAD_S / max(time.perf_counter() - t_rep, 1e-5)))
     clocks = ClockSampler(local)
     clocks.start()
+    for _ in range(load_reps):
+        g_all.replay()
+    torch.cuda.synchronize(dev)
+    barrier()
+    torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     full, rest = divmod(args.steps, NUM_SETS)
     e0.record(stream)
@@ -296,7 +321,14 @@ def run_ours(args, world, rank, local):
         g_one[i].replay()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    barrier()
+    for _ in range(load_reps):
+        g_all.replay()
+    torch.cuda.synchronize(dev)
     clk = clocks.stop()
+    if clk is not None:
+        clk["how"] = "sampled every 50 ms over %.1f s of the same graph replaying around the timed region" % (
+            2 * LOAD_S)
     binding.check_status(stream)
     # per-kernel device time: the profiled graph (NUM_SETS steps), warm, then read once
     for _ in range(3):
@@ -321,7 +353,8 @@ def run_ours(args, world, rank, local):
     # the public pipelined call: inputs go up on one stream, the kernels run on a
     # second, results come down on a third, three device buffer sets rotate; the
     # timed region opens before the first copy up and closes after the last copy down
-    pipe = binding.HostStepPipeline(B, T, Hq, Hkv, D, base, depth=3, grad_dtype=grad_dtype, device=dev)
+    pipe = binding.HostStepPipeline(B, T, Hq, Hkv, D, base, depth=3, grad_dtype=grad_dtype, device=dev,
+                                    precise=precise)
     for i in range(3):
         pipe.submit(*pin, outs)
     pipe.synchronize()
@@ -355,31 +388,49 @@ def run_ours(args, world, rank, local):
     else:
         work = None
         roof = dict(bound="hbm", achieved=None, peak=peaks["hbm_gbs"], unit="GB/s", frac=None)
-    kernel_names = dict(fwd="k_attn_fwd3", fwd_rope="k_rope_qk", bwd_prep="k_bwd_prep", bwd_dkdv="k_bwd_dkdv3",
-                        bwd_dq="k_bwd_dq")
+    kernel_names = dict(fwd="k_attn_fwd" if precise else "k_attn_fwd4", fwd_rope="k_rope_qk", bwd_prep="k_bwd_prep",
+                        bwd_dkdv="k_bwd_dkdv" if precise else "k_bwd_dkdv3", bwd_dq="k_bwd_dq")
     tr = traffic_record(kernel_names.get(dom, dom))
     roof.update(kernel=dom, traffic=(tr["dram_bytes_per_launch"] if tr else None),
                 peak_source="%s bf16 burst" % peaks["source"] if roof["bound"] == "tensor" else
                 "%s hbm" % peaks["source"], per_launch_us=per_launch_ms * 1e3,
                 kernels={k: dict(us_per_launch=v[0] / v[1] * 1e3, launches=v[1])
                          for k, v in prof.items() if v[1]})
+    # the streaming kernels against the measured copy rate: algorithmic bytes per
+    # launch (each tensor read or written once) over the launch's event time
+    Tp = -(-T // 128) * 128
+    oe = 4 if precise else 2
+    stream_bytes = dict(
+        fwd_rope=(2 * B * T * (Hq + Hkv) * D * 2) * (2 if precise else 1),  # q, k in; rotated fp16 (hi, lo) out
+        bwd_prep=B * T * Hq * D * (oe + 2) + B * Hq * T * 4 * (2 if precise else 1)   # o, dO, lse in
+        + B * Hq * Tp * 4 * (3 if precise else 2) + B * Hq * Tp * D * 4,             # Delta, lse2 out; dQacc zeroed
+        bwd_dq=B * Hq * Tp * D * 4 + B * T * Hq * D * 4)                             # dQacc in, fp32 dq out
+    streaming = {}
+    for k, nbytes in stream_bytes.items():
+        if k in prof and prof[k][1]:
+            us = prof[k][0] / prof[k][1] * 1e3
+            gbs = nbytes / (us * 1e-6) / 1e9
+            streaming[k] = dict(kernel=kernel_names[k], algorithmic_bytes=nbytes, us_per_launch=us, achieved_gbs=gbs,
+                                peak_gbs=peaks["hbm_gbs"], frac=gbs / peaks["hbm_gbs"])
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_sample(args.cpu_seconds, shape, x)
+        cpu = cpu_oracle_sample(args.cpu_seconds, shape, x, workload)
         cpu.pop("seconds", None)
     line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
                 ms_per_step=ms_step, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
                 data="synthetic",
-                config=dict(workload=WORKLOAD, B=B, T=T, Hq=Hq, Hkv=Hkv, D=D, rope_base=base,
+                config=dict(workload=workload, B=B, T=T, Hq=Hq, Hkv=Hkv, D=D, rope_base=base,
                             gflop_per_step=fl["total"] / 1e9,
-                            precision="fp16 rotated q/k, bf16 P/V/dO, fp32 accumulate, bf16 o, fp32 dq/dk/dv",
+                            precision=("split precision (NE_ATTN_PRECISE_QK): fp16 hi + lo rotated q/k, bf16 hi + lo "
+                                       "P, fp32 accumulate, fp32 o and dq/dk/dv") if precise else
+                            "fp16 rotated q/k, bf16 P/V/dO, fp32 accumulate, bf16 o, fp32 dq/dk/dv",
                             l2="%d rotating buffer sets of %.0f MB (%.0f MB > L2)" % (
                                 NUM_SETS, set_bytes / 1e6, NUM_SETS * set_bytes / 1e6),
                             parallelism="replicas" if world > 1 else "single GPU",
                             launch="CUDA graph replay of %d-step graphs (%d library kernels per step)" % (
                                 NUM_SETS, launches_per_step)),
                 pct_of_bf16_peak=100.0 * value / world / peaks["bf16_tflops"],
-                roofline=roof, cpu_baseline=cpu,
+                roofline=roof, prepass=streaming.get("bwd_prep"), streaming=streaming, cpu_baseline=cpu,
                 e2e=dict(value=whole_job_tflops(world, fl["total"], e2e_ms), unit=UNIT, h2d_bytes_per_step=h2d,
                          d2h_bytes_per_step=d2h, ms_per_step=e2e_ms,
                          how="binding.HostStepPipeline: pinned host inputs up, forward + backward, every output "
@@ -710,6 +761,8 @@ def main():
                     help="measure RMSNorm + the fused Q/K/V projection (one JSON line) instead")
     ap.add_argument("--fp8", action="store_true",
                     help="measure the FP8 forward (one JSON line) instead")
+    ap.add_argument("--workload", default=WORKLOAD, choices=list(inputs.WORKLOAD_ORDER),
+                    help="the training step's workload shape (default: the 116M model's)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -374,14 +374,19 @@ class HostStepPipeline:
     order each set's reuse (a set is refilled only after its previous results
     have come down).  Host tensors should be pinned so the copies run
     asynchronously.  submit() only enqueues work; synchronize() waits for all
-    of it and raises if a kernel reported a device-side timeout.
+    of it and raises if a kernel reported a device-side timeout.  precise:
+    split precision (NE_ATTN_PRECISE_QK) with an fp32 o, for inputs with very
+    large logits; lse then holds the LSE and its remainder ([2 B, Hq, T]).
     """
 
     def __init__(self, B, T, Hq, Hkv, D, rope_base=10000.0, depth=3, grad_dtype=torch.float32,
-                 o_dtype=torch.bfloat16, device="cuda"):
+                 o_dtype=torch.bfloat16, device="cuda", precise=False):
         self.shape = (B, T, Hq, Hkv, D)
         self.rope_base = float(rope_base)
         self.grad_dtype = grad_dtype
+        self.precise = bool(precise)
+        if self.precise:
+            o_dtype = torch.float32
         self.device = torch.device(device)
         self.up = torch.cuda.Stream(self.device)
         self.comp = torch.cuda.Stream(self.device)
@@ -393,11 +398,11 @@ class HostStepPipeline:
             self.sets.append(dict(
                 q=bf(Hq), k=bf(Hkv), v=bf(Hkv), do=bf(Hq),
                 o=torch.empty((B, T, Hq, D), dtype=o_dtype, device=self.device),
-                lse=torch.empty((B, Hq, T), dtype=torch.float32, device=self.device),
+                lse=torch.empty(((2 if self.precise else 1) * B, Hq, T), dtype=torch.float32, device=self.device),
                 dq=torch.empty((B, T, Hq, D), dtype=grad_dtype, device=self.device),
                 dk=torch.empty((B, T, Hkv, D), dtype=grad_dtype, device=self.device),
                 dv=torch.empty((B, T, Hkv, D), dtype=grad_dtype, device=self.device),
-                ws=alloc_workspace(B, T, Hq, Hkv, D, device=self.device),
+                ws=alloc_workspace(B, T, Hq, Hkv, D, precise=self.precise, device=self.device),
                 up_done=torch.cuda.Event(), comp_done=torch.cuda.Event(), down_done=torch.cuda.Event(),
                 used=False))
         self.n = 0
@@ -415,9 +420,10 @@ class HostStepPipeline:
             s["up_done"].record(self.up)
         self.comp.wait_event(s["up_done"])
         attn_fwd(s["q"], s["k"], s["v"], self.rope_base, o=s["o"], lse=s["lse"], workspace=s["ws"],
-                 stream=self.comp)
+                 o_dtype=s["o"].dtype, precise=self.precise, stream=self.comp)
         attn_bwd(s["q"], s["k"], s["v"], s["o"], s["lse"], s["do"], self.rope_base, grad_dtype=self.grad_dtype,
-                 dq=s["dq"], dk=s["dk"], dv=s["dv"], workspace=s["ws"], qk_rotated=True, stream=self.comp)
+                 dq=s["dq"], dk=s["dk"], dv=s["dv"], workspace=s["ws"], qk_rotated=not self.precise,
+                 precise=self.precise, stream=self.comp)
         s["comp_done"].record(self.comp)
         self.down.wait_event(s["comp_done"])
         with torch.cuda.stream(self.down):

@@ -769,27 +769,23 @@ __device__ __forceinline__ bool bwd_item(const BwdArgs& a, int tl, BwdItem& it) 
   return true;
 }
 
-// Stores one 128-row tile of a gradient (row r per thread of a 128-thread
-// group, values x) through shared memory: 128-byte-wide boxes (64 when a row is
-// shorter), swizzled.  Per box: every warp writes its rows and arrives on
-// `full` (4 arrivals); thread 0 stores the box with TMA (rows past T are not written), waits
-// until the store has read the box and arrives on `free_`; every thread waits
-// for that before the next box.  `e` counts the boxes (barrier phases).
-// Returns false if a wait gave up.
+// Writes row r of a 128-row tile of a gradient (values x, fp32 when ES == 4,
+// else bf16) into staging boxes of 128 rows by min(D * ES, 128) bytes with the
+// TMA / UMMA swizzle of that span: box 0 at stg0, box 1 (fp32 rows of D = 64
+// only) at stg1.  Returns the number of boxes.  HALF: x holds the rotated
+// (interleaved) order of a half-split row, whose column j is x[2j] (j < D/2)
+// or x[2(j - D/2) + 1].
 template <int D, int ES, bool HALF = false>
-__device__ __forceinline__ bool stage_store(const float (&x)[D], uint8_t* stg, const CUtensorMap* map, int r,
-                                            uint64_t* full, uint64_t* free_, int& e, int h, int row0, int b,
-                                            const volatile int* abort) {
+__device__ __forceinline__ int stage_grad(const float (&x)[D], uint8_t* stg0, uint8_t* stg1, int r) {
   constexpr int kSpan = D * ES < 128 ? D * ES : 128;
   constexpr int kCols = kSpan / ES;
+  auto col = [&](int j) { return HALF ? x[j < D / 2 ? 2 * j : 2 * (j - D / 2) + 1] : x[j]; };
 #pragma unroll
-  for (int c0 = 0; c0 < D; c0 += kCols) {
+  for (int c0 = 0, bx = 0; c0 < D; c0 += kCols, bx++) {
+    uint8_t* stg = bx == 0 ? stg0 : stg1;
 #pragma unroll
     for (int ch = 0; ch < kSpan / 16; ch++) {
       uint4 w;
-      // column j of the row; with HALF, x holds the rotated (interleaved) order of
-      // a half-split row, whose column j is x[2j] (j < D/2) or x[2(j - D/2) + 1]
-      auto col = [&](int j) { return HALF ? x[j < D / 2 ? 2 * j : 2 * (j - D / 2) + 1] : x[j]; };
       if constexpr (ES == 4) {
         const int i = c0 + ch * 4;
         w = make_uint4(__float_as_uint(col(i)), __float_as_uint(col(i + 1)), __float_as_uint(col(i + 2)),
@@ -801,21 +797,8 @@ __device__ __forceinline__ bool stage_store(const float (&x)[D], uint8_t* stg, c
       }
       *reinterpret_cast<uint4*>(stg + swz(r, ch, kSpan)) = w;
     }
-    fence_proxy_async_smem();
-    warp_arrive(full);
-    if (r == 0) {
-      if (mbar_wait(full, e & 1, abort)) {
-        tma_store_4d(map, stg, c0, h, row0, b);
-        bulk_commit();
-        bulk_wait_read<0>();
-        mbar_arrive(free_);
-      }
-    }
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(free_, e & 1, abort));
-    e++;
-    if (!ok) return false;
   }
-  return true;
+  return D / kCols;
 }
 
 template <int D>
@@ -826,7 +809,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* kv_full = bars;        // [2]
-  uint64_t* kv_empty = bars + 2;   // [2] released by the three issuers
+  uint64_t* kv_empty = bars + 2;   // [2] released by the three issuers and the item's gradient stores
   uint64_t* qd_full = bars + 4;    // [kStages]
   uint64_t* qd_empty = bars + 7;   // [kStages] released by issuers 1 and 2
   uint64_t* s_full = bars + 10;
@@ -841,8 +824,8 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
   uint64_t* acc_done = bars + 19;  // an item's last dV and dK complete
   uint64_t* acc_free = bars + 20;  // the compute warps read dK and dV
   uint64_t* drain = bars + 21;     // [3]
-  uint64_t* stg_full = bars + 24;  // [2] per compute warpgroup: its rows of a gradient box are staged
-  uint64_t* stg_free = bars + 26;  // [2] the TMA store has read the box
+  uint64_t* stg_full = bars + 24;  // [2] per compute warpgroup: its rows of the item's gradient are staged
+  uint64_t* stg_free = bars + 26;  // [2] the gradient's TMA stores have read the staging
   uint64_t* dp_read = bars + 28;   // the compute warps hold dP^T(g): dP^T(g+1) may overwrite it
   uint64_t* dk_done = bars + 29;   // dK(g) read dS^T(g) from the P^T columns
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -854,7 +837,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
     *abort = 0;
     for (int s = 0; s < 2; s++) {
       mbar_init(kv_full + s, 1);
-      mbar_init(kv_empty + s, 3);
+      mbar_init(kv_empty + s, 5);  // the three issuers, and both compute warpgroups' gradient stores
     }
     for (int s = 0; s < C::kStages; s++) {
       mbar_init(qd_full + s, 1);
@@ -1086,7 +1069,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
     const uint32_t x7 = (uint32_t)(r & 7);  // swizzle of this key row in the dS tile
     uint8_t* atom = smem + C::kOffDS + wg * 16384;
     bool ok = true;
-    int g = 0, boxes = 0;
+    int g = 0, epi = 0;  // steps and item epilogues of this warpgroup so far
     BwdItem it;
     for (int tl = 0; ok && bwd_item(a, tl, it); tl++) {
       for (int n = 0; n < it.N; n++, g++) {
@@ -1141,6 +1124,16 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
 
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(dp_full, g & 1, abort)))) break;
         if (g > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (g - 1) & 1, abort)))) break;
+        if (n == 0 && epi > 0) {
+          // the previous item's gradient stores read this warpgroup's half of the dS
+          // tile (and its K or V buffer): dS may go there once they have
+          if (r == 0) {
+            bulk_wait_read<0>();
+            mbar_arrive(stg_free + wg);
+            mbar_arrive(kv_empty + ((tl - 1) & 1));
+          }
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(stg_free + wg, (epi - 1) & 1, abort)))) break;
+        }
         tc_fence_after();
         // dS = P * (dP - Delta), 16 columns at a time; the next chunk of dP^T loads
         // while this one is computed (its columns are never the ones being stored)
@@ -1193,6 +1186,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
       }
       if (!ok) break;
       // item epilogue: warps 4-7 store dK (scale, inverse rotation), warps 8-11 store dV
+      const int t = it.j * kTile + r;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(acc_done, tl & 1, abort)))) break;
       tc_fence_after();
       float x[D];
@@ -1206,7 +1200,6 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
       }
       tc_fence_before();
       warp_arrive(acc_free);  // the next item's first dV / dK may overwrite the accumulators
-      const int t = it.j * kTile + r;
       if (wg == 0) {
         // dK = scale * (inverse rotation of the accumulated dK^)
 #pragma unroll
@@ -1222,24 +1215,35 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
           }
         }
       }
-      // Coalesced store: each warpgroup stages its tile (128 rows) in its half of
-      // the dS tile, one 128-byte-wide box at a time, and one thread stores the
-      // box with TMA (rows past T are not written).  The dS tile is free once
-      // the item's last dQ has read it.
+      // Coalesced store: each warpgroup stages its 128 rows, 128-byte-wide boxes,
+      // swizzled: the first box in its half of the dS tile, a second (fp32 rows of
+      // D = 64) in this item's K (dK) or V (dV) buffer; one thread then stores
+      // them with TMA (rows past T are not written).  Both are free once the
+      // item's last dQ has read the dS tile and K (the last S^T and dP^T, which
+      // read K and V, completed before acc_done).  The wait for the stores to read
+      // them comes at the next item's first dS, which also releases the K/V
+      // buffer to the producer.
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (g - 1) & 1, abort)))) break;
-      // (the next item writes dS into this tile only after the stores have read it)
       const CUtensorMap* map = wg == 0 ? &a.map_dk : &a.map_dv;
-      // dK in the half-split layout: rotated pair i goes back to columns i, i + D/2
+      uint8_t* stg1 = smem + C::kOffKV + (2 * (tl & 1) + wg) * C::kTileBytes;
+      int nbox;
       if (wg == 0 && a.rope_half)
-        ok = a.grad_fp32 ? stage_store<D, 4, true>(x, atom, map, r, stg_full + wg, stg_free + wg, boxes, it.kvh,
-                                                   it.j * kTile, it.b, abort)
-                         : stage_store<D, 2, true>(x, atom, map, r, stg_full + wg, stg_free + wg, boxes, it.kvh,
-                                                   it.j * kTile, it.b, abort);
+        nbox = a.grad_fp32 ? stage_grad<D, 4, true>(x, atom, stg1, r) : stage_grad<D, 2, true>(x, atom, stg1, r);
       else
-        ok = a.grad_fp32 ? stage_store<D, 4>(x, atom, map, r, stg_full + wg, stg_free + wg, boxes, it.kvh,
-                                             it.j * kTile, it.b, abort)
-                         : stage_store<D, 2>(x, atom, map, r, stg_full + wg, stg_free + wg, boxes, it.kvh,
-                                             it.j * kTile, it.b, abort);
+        nbox = a.grad_fp32 ? stage_grad<D, 4>(x, atom, stg1, r) : stage_grad<D, 2>(x, atom, stg1, r);
+      fence_proxy_async_smem();
+      warp_arrive(stg_full + wg);
+      if (r == 0) {
+        if ((ok = mbar_wait(stg_full + wg, epi & 1, abort))) {
+          const int span = nbox == 2 ? 128 : D * (a.grad_fp32 ? 4 : 2);
+          const int cols = span / (a.grad_fp32 ? 4 : 2);
+          tma_store_4d(map, atom, 0, it.kvh, it.j * kTile, it.b);
+          if (nbox == 2) tma_store_4d(map, stg1, cols, it.kvh, it.j * kTile, it.b);
+          bulk_commit();
+        }
+      }
+      epi++;
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
     }
     if (ok && r == 0) bulk_wait<0>();
     if (!ok) record_timeout(a.status, abort);

@@ -655,6 +655,7 @@ int ne_attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* 
     ra.Hq = Hq;
     ra.Hkv = Hkv;
     ra.div_hq = make_fastdiv((uint32_t)Hq);
+    ra.div_hg = make_fastdiv((uint32_t)(Hq + Hkv + 3) / 4);
     ra.div_hkv = make_fastdiv((uint32_t)Hkv);
     ra.div_t = make_fastdiv((uint32_t)T);
     ra.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
@@ -828,6 +829,7 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   qa.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
   qa.scale = (float)scale;
   qa.div_hq = make_fastdiv((uint32_t)Hq);
+  qa.div_hg = make_fastdiv((uint32_t)(Hq + 3) / 4);
   qa.div_t = make_fastdiv((uint32_t)T);
   {
     ProfScope prof(NE_ATTN_KERNEL_BWD_DQ, s);
@@ -1282,6 +1284,7 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
   qa.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
   qa.scale = (float)scale;
   qa.div_hq = make_fastdiv((uint32_t)Hq);
+  qa.div_hg = make_fastdiv((uint32_t)(Hq + 3) / 4);
   qa.div_t = make_fastdiv((uint32_t)T);
   if (launch_bwd_dq(qa, s) != cudaSuccess) return NE_ERR_CUDA;
   return NE_OK;

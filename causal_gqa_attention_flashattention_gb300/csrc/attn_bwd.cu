@@ -147,49 +147,70 @@ __global__ void __launch_bounds__(256) k_bwd_prep(const PrepArgs a) {
 }
 
 // ====================================================================== dq epilogue
+// dq = scale R_t^T dQacc.  A thread takes one 32-byte chunk c (four pairs) of
+// one position (b, t) for a group of four query heads, so the chunk's
+// (cos, sin) entries are read once for the four, whose loads are in flight
+// together.
 template <int D>
 __global__ void __launch_bounds__(256) k_bwd_dq(const DqArgs a) {
   constexpr int kCPR = D / 8;
-  constexpr int kShift = D == 64 ? 3 : 2;
-  const uint32_t n = (uint32_t)a.B * a.T * a.Hq * kCPR;
+  constexpr int kU = 4;  // heads per thread
+  const uint32_t ngr = (uint32_t)(a.Hq + kU - 1) / kU;
+  const uint32_t n = (uint32_t)a.B * a.T * ngr * kCPR;
   for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < n; it += gridDim.x * blockDim.x) {
-    const uint32_t row = it >> kShift;  // (b, t, h)
-    const int c = (int)(it & (kCPR - 1));
-    const uint32_t bt = fdiv(row, a.div_hq);
-    const uint32_t h = row - bt * a.Hq;
+    const int c = (int)(it % kCPR);
+    const uint32_t rest = it / kCPR;  // (b * T + t) * ngr + head group
+    const uint32_t bt = fdiv(rest, a.div_hg);
+    const int h0 = (int)(rest - bt * ngr) * kU;
     const uint32_t b = fdiv(bt, a.div_t);
     const uint32_t t = bt - b * a.T;
-    const float4* src = reinterpret_cast<const float4*>(a.dqacc + (((size_t)b * a.Hq + h) * a.Tp + t) * D + c * 8);
-    const float4 x0 = src[0], x1 = src[1];
     float4 c0, c1;
     rope_coeffs<D>(a.rope, (int)t, c, c0, c1);
-    const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
     const float cs[4] = {c0.x, c0.z, c1.x, c1.z}, sn[4] = {c0.y, c0.w, c1.y, c1.w};
-    float y[8];
+    {
+      float4 x0[kU], x1[kU];
 #pragma unroll
-    for (int p = 0; p < 4; p++) {
-      y[2 * p] = a.scale * (xs[2 * p] * cs[p] + xs[2 * p + 1] * sn[p]);
-      y[2 * p + 1] = a.scale * (xs[2 * p + 1] * cs[p] - xs[2 * p] * sn[p]);
-    }
-    if (a.rope_half) {
-      // pair p of the chunk is (x[4c + p], x[D/2 + 4c + p]) of the row
-      const size_t r0 = (size_t)row * D + 4 * c, r1 = r0 + D / 2;
-      if (a.grad_fp32) {
-        *reinterpret_cast<float4*>(static_cast<float*>(a.dq) + r0) = make_float4(y[0], y[2], y[4], y[6]);
-        *reinterpret_cast<float4*>(static_cast<float*>(a.dq) + r1) = make_float4(y[1], y[3], y[5], y[7]);
-      } else {
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.dq) + r0) =
-            make_uint2(pack_bf16(y[0], y[2]), pack_bf16(y[4], y[6]));
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.dq) + r1) =
-            make_uint2(pack_bf16(y[1], y[3]), pack_bf16(y[5], y[7]));
+      for (int u = 0; u < kU; u++) {
+        if (h0 + u < a.Hq) {
+          const float4* src = reinterpret_cast<const float4*>(
+              a.dqacc + (((size_t)b * a.Hq + h0 + u) * a.Tp + t) * D + c * 8);
+          x0[u] = src[0];
+          x1[u] = src[1];
+        }
       }
-    } else if (a.grad_fp32) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.dq) + (size_t)it * 8);
-      dst[0] = make_float4(y[0], y[1], y[2], y[3]);
-      dst[1] = make_float4(y[4], y[5], y[6], y[7]);
-    } else {
-      reinterpret_cast<uint4*>(a.dq)[it] =
-          make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+#pragma unroll
+      for (int u = 0; u < kU; u++) {
+        const int h = h0 + u;
+        if (h >= a.Hq) continue;
+        const float xs[8] = {x0[u].x, x0[u].y, x0[u].z, x0[u].w, x1[u].x, x1[u].y, x1[u].z, x1[u].w};
+        float y[8];
+#pragma unroll
+        for (int p = 0; p < 4; p++) {
+          y[2 * p] = a.scale * (xs[2 * p] * cs[p] + xs[2 * p + 1] * sn[p]);
+          y[2 * p + 1] = a.scale * (xs[2 * p + 1] * cs[p] - xs[2 * p] * sn[p]);
+        }
+        const size_t row = (size_t)bt * a.Hq + h;  // (b, t, h)
+        if (a.rope_half) {
+          // pair p of the chunk is (x[4c + p], x[D/2 + 4c + p]) of the row
+          const size_t r0 = row * D + 4 * c, r1 = r0 + D / 2;
+          if (a.grad_fp32) {
+            *reinterpret_cast<float4*>(static_cast<float*>(a.dq) + r0) = make_float4(y[0], y[2], y[4], y[6]);
+            *reinterpret_cast<float4*>(static_cast<float*>(a.dq) + r1) = make_float4(y[1], y[3], y[5], y[7]);
+          } else {
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.dq) + r0) =
+                make_uint2(pack_bf16(y[0], y[2]), pack_bf16(y[4], y[6]));
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.dq) + r1) =
+                make_uint2(pack_bf16(y[1], y[3]), pack_bf16(y[5], y[7]));
+          }
+        } else if (a.grad_fp32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.dq) + row * D + c * 8);
+          dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+          dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+        } else {
+          reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) + row * D)[c] =
+              make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+        }
+      }
     }
   }
 }
@@ -1327,7 +1348,8 @@ cudaError_t launch_bwd_prep(const PrepArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_bwd_dq(const DqArgs& a, cudaStream_t s) {
-  const long long items = (long long)a.B * a.T * a.Hq * a.D / 8;
+  // one thread per (position, group of four heads, chunk)
+  const long long items = (long long)a.B * a.T * ((a.Hq + 3) / 4) * (a.D / 8);
   const int blocks = elementwise_blocks(items);
   if (a.D == 64)
     k_bwd_dq<64><<<blocks, 256, 0, s>>>(a);

@@ -459,38 +459,46 @@ __global__ void __launch_bounds__(256, 1) k_attn_fwd(const __grid_constant__ Fwd
 
 // ====================================================================== RoPE pre-pass
 // q [B,T,Hq,D] and k [B,T,Hkv,D] (bf16) -> rotated fp16 copies of the same
-// layout, one 16-byte chunk (four pairs) per thread.  Streaming work: every
-// byte is read and written once, the cos/sin table stays in L2.
+// layout.  Every head at position t turns by the same angles, so a thread takes
+// one 16-byte chunk c (four pairs) of one position (b, t) for a group of four
+// heads (of the Hq query heads followed by the Hkv key heads): the chunk's
+// (cos, sin) entries are read once for the four, and the four loads are in
+// flight together.  Streaming work: every byte is read and written once.
 template <int D>
 __global__ void __launch_bounds__(256) k_rope_qk(const RopeArgs a) {
   constexpr int kCPR = D / 8;  // 16-byte chunks per row
-  constexpr int kShift = D == 64 ? 3 : 2;
-  constexpr int kPer = 4;      // chunks per thread, loaded together
-  const uint32_t nq = (uint32_t)a.B * a.T * a.Hq * kCPR;
-  const uint32_t n = nq + (uint32_t)a.B * a.T * a.Hkv * kCPR;
-  const uint32_t stride = gridDim.x * blockDim.x;
-  for (uint32_t base = blockIdx.x * blockDim.x + threadIdx.x; base < n; base += kPer * stride) {
-    uint4 v[kPer];
-    float4 c0[kPer], c1[kPer];
+  constexpr int kU = 4;        // heads per thread
+  const int H = a.Hq + a.Hkv;
+  const uint32_t ngr = (uint32_t)(H + kU - 1) / kU;
+  const uint32_t n = (uint32_t)a.B * a.T * ngr * kCPR;
+  const bool half = a.rope_half != 0;
+  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < n; it += gridDim.x * blockDim.x) {
+    const int c = (int)(it % kCPR);
+    const uint32_t rest = it / kCPR;  // (b * T + t) * ngr + head group
+    const uint32_t bt = fdiv(rest, a.div_hg);
+    const int h0 = (int)(rest - bt * ngr) * kU;
+    const uint32_t t = bt - fdiv(bt, a.div_t) * a.T;
+    float4 c0, c1;
+    rope_coeffs<D>(a.rope, (int)t, c, c0, c1);
+    {
+      uint4 v[kU];
 #pragma unroll
-    for (int u = 0; u < kPer; u++) {
-      const uint32_t it = base + u * stride;
-      if (it < n) {
-        const bool isq = it < nq;
-        const uint32_t x = isq ? it : it - nq;
-        const uint32_t row = x >> kShift;  // (b, t, h)
-        const uint32_t bt = fdiv(row, isq ? a.div_hq : a.div_hkv);
-        const uint32_t t = bt - fdiv(bt, a.div_t) * a.T;
-        v[u] = load_rope_chunk<D>((isq ? a.q : a.k) + (size_t)row * D, (int)(x & (kCPR - 1)), a.rope_half != 0);
-        rope_coeffs<D>(a.rope, (int)t, (int)(x & (kCPR - 1)), c0[u], c1[u]);
+      for (int u = 0; u < kU; u++) {
+        const int h = h0 + u;
+        if (h < H) {
+          const bool isq = h < a.Hq;
+          const __nv_bfloat16* row = isq ? a.q + ((size_t)bt * a.Hq + h) * D : a.k + ((size_t)bt * a.Hkv + h - a.Hq) * D;
+          v[u] = load_rope_chunk<D>(row, c, half);
+        }
       }
-    }
 #pragma unroll
-    for (int u = 0; u < kPer; u++) {
-      const uint32_t it = base + u * stride;
-      if (it < n) {
-        const bool isq = it < nq;
-        reinterpret_cast<uint4*>(isq ? a.qr : a.kr)[isq ? it : it - nq] = rope_chunk_f16(v[u], c0[u], c1[u], nullptr);
+      for (int u = 0; u < kU; u++) {
+        const int h = h0 + u;
+        if (h < H) {
+          const bool isq = h < a.Hq;
+          __half* dst = isq ? a.qr + ((size_t)bt * a.Hq + h) * D : a.kr + ((size_t)bt * a.Hkv + h - a.Hq) * D;
+          reinterpret_cast<uint4*>(dst)[c] = rope_chunk_f16(v[u], c0, c1, nullptr);
+        }
       }
     }
   }
@@ -1100,8 +1108,9 @@ cudaError_t launch_rope_q8(const RopeArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_rope_qk(const RopeArgs& a, int D, cudaStream_t s) {
-  const long long n = (long long)a.B * a.T * (a.Hq + a.Hkv) * (D / 8);
-  const long long want = (n + 4 * 256 - 1) / (4 * 256);  // four chunks per thread
+  // one thread per (position, group of four heads, chunk)
+  const long long n = (long long)a.B * a.T * ((a.Hq + a.Hkv + 3) / 4) * (D / 8);
+  const long long want = (n + 255) / 256;
   const int blocks = (int)(want < 65536 ? want : 65536);
   if (D == 64)
     k_rope_qk<64><<<blocks, 256, 0, s>>>(a);

@@ -72,6 +72,7 @@ struct RopeArgs {
   int B, T, Hq, Hkv;
   int rope_half;  // half-split pair layout of q and k
   FastDiv div_hq, div_hkv, div_t;
+  FastDiv div_hg;    // by the groups of four heads (Hq + Hkv, four per thread) of k_rope_qk
   uint8_t *q8, *k8;  // FP8 forward: rotated q, k as e4m3 scaled by 448 / max |value| of their head
   float* amax;       // FP8 forward: [Hq + Hkv] per-head max |rotated value| (zeroed before the max pass)
 };
@@ -118,6 +119,7 @@ struct DqArgs {
   int rope_half;  // dq leaves in the half-split pair layout
   float scale;
   FastDiv div_hq, div_t;
+  FastDiv div_hg;  // by the groups of four query heads (four per thread)
 };
 
 // Key/value cache append: rotated keys (fp16) and values (bf16) of Tn new positions.

@@ -37,7 +37,6 @@ METRIC = "causal GQA attn fwd+bwd TFLOP/s on 1 GB300 (% of bf16 tensor peak)"
 UNIT = "TFLOP/s"
 WORKLOAD = "gpu_116m_model"
 NUM_SETS = 4  # rotating input/output sets so consecutive steps do not hit a warm L2
-LOAD_S = 0.4  # seconds of graph replays before and after the timed region while clocks are sampled
 
 
 def algo_flops(B, T, Hq, D):
@@ -295,7 +294,7 @@ def run_ours(args, world, rank, local):
     barrier()
     torch.cuda.synchronize(dev)
 
-    # Clocks: the sampler runs while the same graph replays for about LOAD_S seconds
+    # Clocks: the sampler runs while the same graph replays for --clock-seconds seconds
     # before the timed region and again after it, so that the samples (every 50 ms)
     # see the load the timed steps run under; the timed region itself is exactly
     # the K steps between the two events.
@@ -304,7 +303,7 @@ def run_ours(args, world, rank, local):
     t_rep = time.perf_counter()
     g_all.replay()
     torch.cuda.synchronize(dev)
-    load_reps = max(1, int(LOAD_S / max(time.perf_counter() - t_rep, 1e-5)))
+    load_reps = int(args.clock_seconds / max(time.perf_counter() - t_rep, 1e-5))
     clocks = ClockSampler(local)
     clocks.start()
     for _ in range(load_reps):
@@ -328,7 +327,7 @@ def run_ours(args, world, rank, local):
     clk = clocks.stop()
     if clk is not None:
         clk["how"] = "sampled every 50 ms over %.1f s of the same graph replaying around the timed region" % (
-            2 * LOAD_S)
+            2 * args.clock_seconds)
     binding.check_status(stream)
     # per-kernel device time: the profiled graph (NUM_SETS steps), warm, then read once
     for _ in range(3):
@@ -735,7 +734,7 @@ def run_fp8(args):
                 roofline=dict(bound="tensor", achieved=achieved, peak=peaks["bf16_tflops"], unit="TFLOP/s",
                               frac=achieved / peaks["bf16_tflops"], kernel="fwd",
                               traffic=(lambda tr: tr["dram_bytes_per_launch"] if tr else None)(
-                                  traffic_record("k_attn_fwd3_fp8")),
+                                  traffic_record("k_attn_fwd4_fp8")),
                               peak_source="%s bf16 (burst); S runs at the 8-bit rate, P V at bf16"
                               % peaks["source"], per_launch_us=ms_attn * 1e3,
                               kernels={k: dict(us_per_launch=v[0] / v[1] * 1e3, launches=v[1])
@@ -761,6 +760,8 @@ def main():
                     help="measure RMSNorm + the fused Q/K/V projection (one JSON line) instead")
     ap.add_argument("--fp8", action="store_true",
                     help="measure the FP8 forward (one JSON line) instead")
+    ap.add_argument("--clock-seconds", type=float, default=0.4,
+                    help="seconds of graph replays before and after the timed region while clocks are sampled")
     ap.add_argument("--workload", default=WORKLOAD, choices=list(inputs.WORKLOAD_ORDER),
                     help="the training step's workload shape (default: the 116M model's)")
     args = ap.parse_args()

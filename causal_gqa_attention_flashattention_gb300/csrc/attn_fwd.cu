@@ -580,8 +580,9 @@ __global__ void __launch_bounds__(256) k_rope_q8(const RopeArgs a) {
 // the whole item: its row maximum and row sum stay in registers, so the two
 // warpgroups never wait for each other.  Unit u has its own TMEM score buffer
 // S_u, P buffer P_u and accumulator O_u (2 x (128 + 64 + 64) = 512 columns), so
-// S_u of the next key tile goes out as soon as the scores of this one have been
-// read.  O_u += P_u V goes out in two halves of 64 keys, the first while the
+// S_u of the next key tile goes out as soon as the scores of this one are in
+// the warpgroup's registers (all 128 per row, one TMEM round trip, before the
+// row maximum).  O_u += P_u V goes out in two halves of 64 keys, the first while the
 // warpgroup still exponentiates the second, so that P_u of the next key tile
 // rarely waits for it.
 // Items come from a host-built table (fwd_pair_schedule in api.cu): pairs of
@@ -873,28 +874,26 @@ __global__ void __launch_bounds__(384, 1) k_attn_fwd4(const __grid_constant__ Fw
         ok = __all_sync(0xffffffffu, mbar_wait(s_full + u, n & 1, abort));
         if (!ok) break;
         tc_fence_after();
-        // pass 1: row maximum over the 128 keys (masked past the diagonal); the
-        // scores of keys 64..127 stay in registers for pass 2
+        // pass 1: all 128 scores of the row into registers (one TMEM round trip; the
+        // unit's next S may then overwrite the score buffer), the row maximum over
+        // them (masked past the diagonal)
+        uint32_t sc[128];
+#pragma unroll
+        for (int c = 0; c < 4; c++) tmem_ld32(sbuf + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sc + 32 * c));
+        tmem_wait_ld();
+        tc_fence_before();
+        warp_arrive(s_read + u);
+        if (diag) {
+#pragma unroll
+          for (int e = 0; e < 128; e++)
+            if (e > r) sc[e] = 0xff800000u;  // -inf: key after the query (exp2(-inf) = 0)
+        }
         float mx8[8];
 #pragma unroll
         for (int e = 0; e < 8; e++) mx8[e] = -INFINITY;
-        uint32_t hi[64];
 #pragma unroll
-        for (int h2 = 0; h2 < 2; h2++) {
-          uint32_t lo[64];
-          uint32_t(&w)[64] = h2 ? hi : lo;
-          tmem_ld32(sbuf + h2 * 64, *reinterpret_cast<uint32_t(*)[32]>(w));
-          tmem_ld32(sbuf + h2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(w + 32));
-          tmem_wait_ld();
-          if (diag) {
-#pragma unroll
-            for (int e = 0; e < 64; e++)
-              if (h2 * 64 + e > r) w[e] = 0xff800000u;  // -inf: key after the query
-          }
-#pragma unroll
-          for (int e = 0; e < 64; e += 2)
-            mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(w[e]), __uint_as_float(w[e + 1]));
-        }
+        for (int e = 0; e < 128; e += 2)
+          mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], __uint_as_float(sc[e]), __uint_as_float(sc[e + 1]));
         const float mxr = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         float r_use = mxr, alpha = 1.f;
@@ -933,25 +932,13 @@ __global__ void __launch_bounds__(384, 1) k_attn_fwd4(const __grid_constant__ Fw
           if (!ok) break;
         }
         tc_fence_after();
-        // pass 2: P = exp2(s * scale_log2 - m) as bf16 into the unit's P buffer.
-        // Keys 0..63 are read again, 16 at a time (the next chunk loads while this
-        // one is exponentiated); keys 64..127 come from pass 1's registers.
+        // pass 2: P = exp2(s * scale_log2 - m) as bf16 into the unit's P buffer, 16 keys
+        // at a time from pass 1's registers.
         // (the row sum adds the fp32 values of P; the MMA multiplies their bf16 roundings)
         uint64_t sum4[4] = {0ull, 0ull, 0ull, 0ull};
         const uint64_t sl2x2 = f2(sl2, sl2), negm = f2(-m_use, -m_use);
-        uint32_t ua[16], ub[16];
-        tmem_ld16(sbuf, ua);
-        tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 8; c++) {
-          uint32_t(&cur)[16] = c >= 4 ? *reinterpret_cast<uint32_t(*)[16]>(hi + 16 * (c - 4)) : ((c & 1) ? ub : ua);
-          uint32_t(&nxt)[16] = (c & 1) ? ua : ub;
-          if (c < 3) tmem_ld16(sbuf + (c + 1) * 16, nxt);
-          if (diag && c < 4) {
-#pragma unroll
-            for (int e = 0; e < 16; e++)
-              if (16 * c + e > r) cur[e] = 0xff800000u;  // exp2(-inf) = 0
-          }
           if (c == 4) {
             // keys 0..63 of P are stored: the first half of O += P V may start; keys
             // 64..127 wait for the second half of the previous one
@@ -967,19 +954,14 @@ __global__ void __launch_bounds__(384, 1) k_attn_fwd4(const __grid_constant__ Fw
           uint32_t pk[8];
 #pragma unroll
           for (int e = 0; e < 8; e++) {
+            const int k = 16 * c + 2 * e;
             float x0, x1;
-            f2_split(f2_fma(f2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])), sl2x2, negm), x0, x1);
+            f2_split(f2_fma(f2(__uint_as_float(sc[k]), __uint_as_float(sc[k + 1])), sl2x2, negm), x0, x1);
             const float p0 = ex2(x0), p1 = ex2(x1);
             pk[e] = pack_bf16(p0, p1);
             sum4[e & 3] = f2_add(sum4[e & 3], f2(p0, p1));
           }
           tmem_st8(pbuf + c * 8, pk);
-          if (c < 3) tmem_wait_ld();
-          if (c == 2) {
-            // every score is in registers: the unit's next S may overwrite them
-            tc_fence_before();
-            warp_arrive(s_read + u);
-          }
         }
         if (!ok) break;
         tmem_wait_st();

@@ -562,6 +562,124 @@ struct ProfScope {
   ~ProfScope() { prof_end(slot, s); }
 };
 
+// The backward's three launches (pre-pass, dK/dV sweep, dq epilogue) on a
+// workspace `ws` laid out as `w` with the rotary table `rope`; shared by
+// ne_attn_bwd (caller workspace) and ne_attn_bwd_noalloc (the fixed array).
+// Requires g_mu held.
+int bwd_launch(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+               void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D, int flags, uint8_t* ws,
+               const WsLayout& w, const float2* rope, int* status, cudaStream_t s) {
+  int st;
+  const bool precise = (flags & kFlagPreciseQK) != 0;
+  const int grad_fp32 = (flags & kFlagGradFp32) ? 1 : 0;
+  const int nt = (T + kTile - 1) / kTile;
+  const int Tp = nt * kTile;
+  float* dqacc = reinterpret_cast<float*>(ws + w.dqacc);
+  __half* qr = reinterpret_cast<__half*>(ws + w.qr);
+  __half* kr = reinterpret_cast<__half*>(ws + w.kr);
+  __half* qlo = precise ? reinterpret_cast<__half*>(ws + w.qlo) : nullptr;
+  __half* klo = precise ? reinterpret_cast<__half*>(ws + w.klo) : nullptr;
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  float* lse2_lo = precise ? reinterpret_cast<float*>(ws + w.lse2_lo) : nullptr;
+  float* delta = reinterpret_cast<float*>(ws + w.delta);
+  const double scale = 1.0 / std::sqrt((double)D);
+
+  PrepArgs p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.o = o;
+  p.o_fp32 = (flags & kFlagOFp32) ? 1 : 0;
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.lse = lse;
+  p.lse_lo = precise ? lse + (size_t)B * Hq * T : nullptr;
+  p.lse2_lo = lse2_lo;
+  p.qr = qr;
+  p.kr = kr;
+  p.qlo = qlo;
+  p.klo = klo;
+  p.lse2 = lse2;
+  p.delta = delta;
+  p.dqacc = dqacc;
+  p.rope = rope;
+  p.B = B;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.Tp = Tp;
+  p.rotate_qk = (flags & kFlagQKRotated) ? 0 : 1;
+  p.negate = precise ? 0 : 1;
+  p.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
+  p.div_hq = make_fastdiv((uint32_t)Hq);
+  p.div_hkv = make_fastdiv((uint32_t)Hkv);
+  p.div_t = make_fastdiv((uint32_t)T);
+  p.div_pad = make_fastdiv((uint32_t)(Tp > T ? Tp - T : 1));
+  {
+    ProfScope prof(NE_ATTN_KERNEL_BWD_PREP, s);
+    if (launch_bwd_prep(p, s) != cudaSuccess) return NE_ERR_CUDA;
+  }
+
+  BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  constexpr CUtensorMapDataType kF16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if ((st = make_map_bthd(&a.map_qr, qr, B, T, Hq, D, kF16)) != NE_OK) return st;
+  if ((st = make_map_bthd(&a.map_kr, kr, B, T, Hkv, D, kF16)) != NE_OK) return st;
+  if ((st = make_map_bthd(&a.map_v, v, B, T, Hkv, D)) != NE_OK) return st;
+  if ((st = make_map_bthd(&a.map_do, dout, B, T, Hq, D)) != NE_OK) return st;
+  if (precise) {
+    if ((st = make_map_bthd(&a.map_qlo, qlo, B, T, Hq, D, kF16)) != NE_OK) return st;
+    if ((st = make_map_bthd(&a.map_klo, klo, B, T, Hkv, D, kF16)) != NE_OK) return st;
+  }
+  if ((st = make_map_acc(&a.map_dqacc, dqacc, (long long)B * Hq * Tp, D)) != NE_OK) return st;
+  if ((st = make_map_grad(&a.map_dk, dk, B, T, Hkv, D, grad_fp32 != 0)) != NE_OK) return st;
+  if ((st = make_map_grad(&a.map_dv, dv, B, T, Hkv, D, grad_fp32 != 0)) != NE_OK) return st;
+  a.lse2 = lse2;
+  a.lse2_lo = lse2_lo;
+  a.delta = delta;
+  a.dk = dk;
+  a.dv = dv;
+  a.rope = rope;
+  a.status = status;
+  a.B = B;
+  a.T = T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.G = Hq / Hkv;
+  a.nt = nt;
+  a.Tp = Tp;
+  a.grad_fp32 = grad_fp32;
+  a.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
+  a.scale_log2 = (float)(1.4426950408889634 * scale);
+  a.scale_log2_lo = (float)(1.4426950408889634 * scale - (double)a.scale_log2);
+  a.scale = (float)scale;
+  {
+    ProfScope prof(NE_ATTN_KERNEL_BWD_DKDV, s);
+    if (launch_bwd_dkdv(a, precise, s) != cudaSuccess) return NE_ERR_CUDA;
+  }
+
+  DqArgs qa;
+  qa.dqacc = dqacc;
+  qa.dq = dq;
+  qa.rope = rope;
+  qa.B = B;
+  qa.T = T;
+  qa.Hq = Hq;
+  qa.D = D;
+  qa.Tp = Tp;
+  qa.grad_fp32 = grad_fp32;
+  qa.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
+  qa.scale = (float)scale;
+  qa.div_hq = make_fastdiv((uint32_t)Hq);
+  qa.div_hg = make_fastdiv((uint32_t)(Hq + 3) / 4);
+  qa.div_t = make_fastdiv((uint32_t)T);
+  {
+    ProfScope prof(NE_ATTN_KERNEL_BWD_DQ, s);
+    if (launch_bwd_dq(qa, s) != cudaSuccess) return NE_ERR_CUDA;
+  }
+  return NE_OK;
+}
+
 }  // namespace
 }  // namespace ne
 
@@ -717,7 +835,6 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return NE_ERR_ALIGN;
   const bool precise = (flags & kFlagPreciseQK) != 0;
-  const int grad_fp32 = (flags & kFlagGradFp32) ? 1 : 0;
   const WsLayout w = ws_layout(B, T, Hq, Hkv, D, precise);
   if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return NE_ERR_WORKSPACE;
@@ -732,110 +849,7 @@ int ne_attn_bwd(const void* q, const void* k, const void* v, const void* o, cons
   const float2* rope = nullptr;
   if ((st = rope_table(*d, D, (double)rope_base, Tp, s, &rope)) != NE_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* dqacc = reinterpret_cast<float*>(ws + w.dqacc);
-  __half* qr = reinterpret_cast<__half*>(ws + w.qr);
-  __half* kr = reinterpret_cast<__half*>(ws + w.kr);
-  __half* qlo = precise ? reinterpret_cast<__half*>(ws + w.qlo) : nullptr;
-  __half* klo = precise ? reinterpret_cast<__half*>(ws + w.klo) : nullptr;
-  float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
-  float* lse2_lo = precise ? reinterpret_cast<float*>(ws + w.lse2_lo) : nullptr;
-  float* delta = reinterpret_cast<float*>(ws + w.delta);
-  const double scale = 1.0 / std::sqrt((double)D);
-
-  PrepArgs p;
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k = static_cast<const __nv_bfloat16*>(k);
-  p.o = o;
-  p.o_fp32 = (flags & kFlagOFp32) ? 1 : 0;
-  p.dout = static_cast<const __nv_bfloat16*>(dout);
-  p.lse = lse;
-  p.lse_lo = precise ? lse + (size_t)B * Hq * T : nullptr;
-  p.lse2_lo = lse2_lo;
-  p.qr = qr;
-  p.kr = kr;
-  p.qlo = qlo;
-  p.klo = klo;
-  p.lse2 = lse2;
-  p.delta = delta;
-  p.dqacc = dqacc;
-  p.rope = rope;
-  p.B = B;
-  p.T = T;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.D = D;
-  p.Tp = Tp;
-  p.rotate_qk = (flags & kFlagQKRotated) ? 0 : 1;
-  p.negate = precise ? 0 : 1;
-  p.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
-  p.div_hq = make_fastdiv((uint32_t)Hq);
-  p.div_hkv = make_fastdiv((uint32_t)Hkv);
-  p.div_t = make_fastdiv((uint32_t)T);
-  p.div_pad = make_fastdiv((uint32_t)(Tp > T ? Tp - T : 1));
-  {
-    ProfScope prof(NE_ATTN_KERNEL_BWD_PREP, s);
-    if (launch_bwd_prep(p, s) != cudaSuccess) return NE_ERR_CUDA;
-  }
-
-  BwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  constexpr CUtensorMapDataType kF16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if ((st = make_map_bthd(&a.map_qr, qr, B, T, Hq, D, kF16)) != NE_OK) return st;
-  if ((st = make_map_bthd(&a.map_kr, kr, B, T, Hkv, D, kF16)) != NE_OK) return st;
-  if ((st = make_map_bthd(&a.map_v, v, B, T, Hkv, D)) != NE_OK) return st;
-  if ((st = make_map_bthd(&a.map_do, dout, B, T, Hq, D)) != NE_OK) return st;
-  if (precise) {
-    if ((st = make_map_bthd(&a.map_qlo, qlo, B, T, Hq, D, kF16)) != NE_OK) return st;
-    if ((st = make_map_bthd(&a.map_klo, klo, B, T, Hkv, D, kF16)) != NE_OK) return st;
-  }
-  if ((st = make_map_acc(&a.map_dqacc, dqacc, (long long)B * Hq * Tp, D)) != NE_OK) return st;
-  if ((st = make_map_grad(&a.map_dk, dk, B, T, Hkv, D, grad_fp32 != 0)) != NE_OK) return st;
-  if ((st = make_map_grad(&a.map_dv, dv, B, T, Hkv, D, grad_fp32 != 0)) != NE_OK) return st;
-  a.lse2 = lse2;
-  a.lse2_lo = lse2_lo;
-  a.delta = delta;
-  a.dk = dk;
-  a.dv = dv;
-  a.rope = rope;
-  a.status = d->status;
-  a.B = B;
-  a.T = T;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.D = D;
-  a.G = Hq / Hkv;
-  a.nt = nt;
-  a.Tp = Tp;
-  a.grad_fp32 = grad_fp32;
-  a.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
-  a.scale_log2 = (float)(1.4426950408889634 * scale);
-  a.scale_log2_lo = (float)(1.4426950408889634 * scale - (double)a.scale_log2);
-  a.scale = (float)scale;
-  {
-    ProfScope prof(NE_ATTN_KERNEL_BWD_DKDV, s);
-    if (launch_bwd_dkdv(a, precise, s) != cudaSuccess) return NE_ERR_CUDA;
-  }
-
-  DqArgs qa;
-  qa.dqacc = dqacc;
-  qa.dq = dq;
-  qa.rope = rope;
-  qa.B = B;
-  qa.T = T;
-  qa.Hq = Hq;
-  qa.D = D;
-  qa.Tp = Tp;
-  qa.grad_fp32 = grad_fp32;
-  qa.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
-  qa.scale = (float)scale;
-  qa.div_hq = make_fastdiv((uint32_t)Hq);
-  qa.div_hg = make_fastdiv((uint32_t)(Hq + 3) / 4);
-  qa.div_t = make_fastdiv((uint32_t)T);
-  {
-    ProfScope prof(NE_ATTN_KERNEL_BWD_DQ, s);
-    if (launch_bwd_dq(qa, s) != cudaSuccess) return NE_ERR_CUDA;
-  }
-  return NE_OK;
+  return bwd_launch(q, k, v, o, lse, dout, dq, dk, dv, B, T, Hq, Hkv, D, flags, ws, w, rope, d->status, s);
 }
 
 size_t ne_attn_qkv_workspace_size(int B, int T, int C, int Hq, int Hkv, int D, int flags) {
@@ -1170,7 +1184,6 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return NE_ERR_ALIGN;
   const bool precise = (flags & kFlagPreciseQK) != 0;
-  const int grad_fp32 = (flags & kFlagGradFp32) ? 1 : 0;
   const int nt = (T + kTile - 1) / kTile;
   const int Tp = nt * kTile;
   // scratch layout: [rotary table, Tp x D/2 float2][workspace as in ne_attn_bwd]
@@ -1193,101 +1206,7 @@ int ne_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void*
   // The array keeps the previous call's contents: the table is rebuilt here and
   // the pre-pass zeroes the dQ accumulator and writes every other field it uses.
   if (launch_rope_table(rope, Tp, D, (double)rope_base, s) != cudaSuccess) return NE_ERR_CUDA;
-  float* dqacc = reinterpret_cast<float*>(ws + w.dqacc);
-  __half* qr = reinterpret_cast<__half*>(ws + w.qr);
-  __half* kr = reinterpret_cast<__half*>(ws + w.kr);
-  __half* qlo = precise ? reinterpret_cast<__half*>(ws + w.qlo) : nullptr;
-  __half* klo = precise ? reinterpret_cast<__half*>(ws + w.klo) : nullptr;
-  float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
-  float* lse2_lo = precise ? reinterpret_cast<float*>(ws + w.lse2_lo) : nullptr;
-  float* delta = reinterpret_cast<float*>(ws + w.delta);
-  const double scale = 1.0 / std::sqrt((double)D);
-
-  PrepArgs p;
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k = static_cast<const __nv_bfloat16*>(k);
-  p.o = o;
-  p.o_fp32 = (flags & kFlagOFp32) ? 1 : 0;
-  p.dout = static_cast<const __nv_bfloat16*>(dout);
-  p.lse = lse;
-  p.lse_lo = precise ? lse + (size_t)B * Hq * T : nullptr;
-  p.lse2_lo = lse2_lo;
-  p.qr = qr;
-  p.kr = kr;
-  p.qlo = qlo;
-  p.klo = klo;
-  p.lse2 = lse2;
-  p.delta = delta;
-  p.dqacc = dqacc;
-  p.rope = rope;
-  p.B = B;
-  p.T = T;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.D = D;
-  p.Tp = Tp;
-  p.rotate_qk = (flags & kFlagQKRotated) ? 0 : 1;
-  p.negate = precise ? 0 : 1;
-  p.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
-  p.div_hq = make_fastdiv((uint32_t)Hq);
-  p.div_hkv = make_fastdiv((uint32_t)Hkv);
-  p.div_t = make_fastdiv((uint32_t)T);
-  p.div_pad = make_fastdiv((uint32_t)(Tp > T ? Tp - T : 1));
-  if (launch_bwd_prep(p, s) != cudaSuccess) return NE_ERR_CUDA;
-
-  BwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  constexpr CUtensorMapDataType kF16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if ((st = make_map_bthd(&a.map_qr, qr, B, T, Hq, D, kF16)) != NE_OK) return st;
-  if ((st = make_map_bthd(&a.map_kr, kr, B, T, Hkv, D, kF16)) != NE_OK) return st;
-  if ((st = make_map_bthd(&a.map_v, v, B, T, Hkv, D)) != NE_OK) return st;
-  if ((st = make_map_bthd(&a.map_do, dout, B, T, Hq, D)) != NE_OK) return st;
-  if (precise) {
-    if ((st = make_map_bthd(&a.map_qlo, qlo, B, T, Hq, D, kF16)) != NE_OK) return st;
-    if ((st = make_map_bthd(&a.map_klo, klo, B, T, Hkv, D, kF16)) != NE_OK) return st;
-  }
-  if ((st = make_map_acc(&a.map_dqacc, dqacc, (long long)B * Hq * Tp, D)) != NE_OK) return st;
-  if ((st = make_map_grad(&a.map_dk, dk, B, T, Hkv, D, grad_fp32 != 0)) != NE_OK) return st;
-  if ((st = make_map_grad(&a.map_dv, dv, B, T, Hkv, D, grad_fp32 != 0)) != NE_OK) return st;
-  a.lse2 = lse2;
-  a.lse2_lo = lse2_lo;
-  a.delta = delta;
-  a.dk = dk;
-  a.dv = dv;
-  a.rope = rope;
-  a.status = d->status;
-  a.B = B;
-  a.T = T;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.D = D;
-  a.G = Hq / Hkv;
-  a.nt = nt;
-  a.Tp = Tp;
-  a.grad_fp32 = grad_fp32;
-  a.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
-  a.scale_log2 = (float)(1.4426950408889634 * scale);
-  a.scale_log2_lo = (float)(1.4426950408889634 * scale - (double)a.scale_log2);
-  a.scale = (float)scale;
-  if (launch_bwd_dkdv(a, precise, s) != cudaSuccess) return NE_ERR_CUDA;
-
-  DqArgs qa;
-  qa.dqacc = dqacc;
-  qa.dq = dq;
-  qa.rope = rope;
-  qa.B = B;
-  qa.T = T;
-  qa.Hq = Hq;
-  qa.D = D;
-  qa.Tp = Tp;
-  qa.grad_fp32 = grad_fp32;
-  qa.rope_half = (flags & kFlagRopeHalf) ? 1 : 0;
-  qa.scale = (float)scale;
-  qa.div_hq = make_fastdiv((uint32_t)Hq);
-  qa.div_hg = make_fastdiv((uint32_t)(Hq + 3) / 4);
-  qa.div_t = make_fastdiv((uint32_t)T);
-  if (launch_bwd_dq(qa, s) != cudaSuccess) return NE_ERR_CUDA;
-  return NE_OK;
+  return bwd_launch(q, k, v, o, lse, dout, dq, dk, dv, B, T, Hq, Hkv, D, flags, ws, w, rope, d->status, s);
 }
 
 }  // extern "C"

@@ -761,7 +761,16 @@ struct Bwd3Cfg {
   static constexpr int kOffStg = kOffDS + kDsBytes;
   static constexpr int kOffLse = kOffStg + kStgBytes;
   static constexpr int kOffDel = kOffLse + kStages * kVecBytes;
-  static constexpr int kOffBar = kOffDel + kStages * kVecBytes;
+  // (cos, sin) rows of the rotation table for the dK epilogue, position
+  // t = t0 + 16a + b split three ways: the row of each item's t0 = 128 j (one per
+  // K/V buffer), rows 16a (a < 8) and rows b (b < 16, padded so that the 16 rows
+  // one warp reads start in different banks)
+  static constexpr int kRotRow = D * 4;
+  static constexpr int kRotStrideB = kRotRow + 16;
+  static constexpr int kOffRot = kOffDel + kStages * kVecBytes;
+  static constexpr int kOffRotA = kOffRot + 2 * kRotRow;
+  static constexpr int kOffRotB = kOffRotA + 8 * kRotRow;
+  static constexpr int kOffBar = kOffRotB + 16 * kRotStrideB;
   static constexpr int kNumBars = 32;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
@@ -822,7 +831,9 @@ __device__ __forceinline__ int stage_grad(const float (&x)[D], uint8_t* stg0, ui
   return D / kCols;
 }
 
-template <int D>
+// kSplit: fp32 gradients of D = 64 in the interleaved layout, whose item
+// epilogue splits the columns between the two compute warpgroups.
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ BwdArgs a) {
   using C = Bwd3Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -849,6 +860,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
   uint64_t* stg_free = bars + 26;  // [2] the gradient's TMA stores have read the staging
   uint64_t* dp_read = bars + 28;   // the compute warps hold dP^T(g): dP^T(g+1) may overwrite it
   uint64_t* dk_done = bars + 29;   // dK(g) read dS^T(g) from the P^T columns
+  uint64_t* rot_full = bars + 30;  // rows 16a and b of the rotation table are in shared memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -882,6 +894,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
     }
     mbar_init(dp_read, 8);
     mbar_init(dk_done, 1);
+    mbar_init(rot_full, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
@@ -903,13 +916,21 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
       prefetch_tmap(&a.map_v);
       bool ok = true;
       int g = 0, kv_loaded = 0;
+      const uint8_t* rot = reinterpret_cast<const uint8_t*>(a.rope);
+      mbar_arrive_expect_tx(rot_full, 24 * C::kRotRow);
+      for (int x = 0; x < 8; x++)
+        bulk_load(smem + C::kOffRotA + x * C::kRotRow, rot + (size_t)16 * x * C::kRotRow, C::kRotRow, rot_full);
+      for (int x = 0; x < 16; x++)
+        bulk_load(smem + C::kOffRotB + x * C::kRotStrideB, rot + (size_t)x * C::kRotRow, C::kRotRow, rot_full);
       auto load_kv = [&](int k, const BwdItem& x) -> bool {
         const int kb = k & 1;
         if (k >= 2 && !mbar_wait(kv_empty + kb, ((k >> 1) - 1) & 1, abort)) return false;
-        mbar_arrive_expect_tx(kv_full + kb, 2 * C::kTileBytes);
+        mbar_arrive_expect_tx(kv_full + kb, 2 * C::kTileBytes + C::kRotRow);
         tma_load_4d(smem + C::kOffKV + kb * 2 * C::kTileBytes, &a.map_kr, kv_full + kb, 0, x.kvh, x.j * kTile, x.b);
         tma_load_4d(smem + C::kOffKV + (kb * 2 + 1) * C::kTileBytes, &a.map_v, kv_full + kb, 0, x.kvh, x.j * kTile,
                     x.b);
+        bulk_load(smem + C::kOffRot + kb * C::kRotRow, rot + (size_t)x.j * kTile * C::kRotRow, C::kRotRow,
+                  kv_full + kb);
         kv_loaded = k + 1;
         return true;
       };
@@ -937,6 +958,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
         mbar_wait(kv_full + (k & 1), (k >> 1) & 1, &never);
       for (int x = g - C::kStages < 0 ? 0 : g - C::kStages; x < g; x++)
         mbar_wait(qd_full + x % C::kStages, (x / C::kStages) & 1, &never);
+      mbar_wait(rot_full, 0, &never);
     }
   } else if (warp >= 1 && warp <= 3) {
     // ------------------------------------------------------------ MMA issuers
@@ -1206,61 +1228,109 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
         warp_arrive(ds_ready);
       }
       if (!ok) break;
-      // item epilogue: warps 4-7 store dK (scale, inverse rotation), warps 8-11 store dV
-      const int t = it.j * kTile + r;
+      // Item epilogue: dK = scale * (inverse rotation of the accumulated dK^) and
+      // dV, stored with TMA from swizzled staging boxes of 128 rows by 128 bytes.
+      // fp32 gradients of D = 64 in the interleaved layout ("split"): each
+      // warpgroup takes half the columns of both accumulators (dK and dV columns
+      // 32 wg .. 32 wg + 31), so the two share the rotation.  Otherwise warps
+      // 4-7 store dK and warps 8-11 dV, whole rows.
+      constexpr bool split = kSplit;
+      // The angle of pair i at t = t0 + 16a + b is the sum of three table angles,
+      // so its (cos, sin) is the product of three unit complex numbers from
+      // shared memory (each table entry is rounded once; the products add a few
+      // fp32 roundings).  The t0 row came with this item's K and V.
+      auto rotate = [&](float* xr, int p0, auto np_c) {
+        constexpr int np = decltype(np_c)::value;
+        const float2* r0 = reinterpret_cast<const float2*>(smem + C::kOffRot + (tl & 1) * C::kRotRow) + p0;
+        const float2* ra = reinterpret_cast<const float2*>(smem + C::kOffRotA + (r >> 4) * C::kRotRow) + p0;
+        const float2* rb = reinterpret_cast<const float2*>(smem + C::kOffRotB + (r & 15) * C::kRotStrideB) + p0;
+#pragma unroll
+        for (int i = 0; i < np; i++) {
+          const float2 e0 = r0[i], ea = ra[i], eb = rb[i];
+          const float cab = fmaf(ea.x, eb.x, -ea.y * eb.y), sab = fmaf(ea.y, eb.x, ea.x * eb.y);
+          const float cs = fmaf(e0.x, cab, -e0.y * sab), sn = fmaf(e0.y, cab, e0.x * sab);
+          const float x0 = xr[2 * i], x1 = xr[2 * i + 1];
+          xr[2 * i] = a.scale * (x0 * cs + x1 * sn);
+          xr[2 * i + 1] = a.scale * (x1 * cs - x0 * sn);
+        }
+      };
+      if (wg == 0 || split) {  // the rotation table rows used below are in shared memory
+        if (epi == 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(rot_full, 0, abort)))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(kv_full + (tl & 1), (tl >> 1) & 1, abort)))) break;
+      }
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(acc_done, tl & 1, abort)))) break;
       tc_fence_after();
-      float x[D];
-#pragma unroll
-      for (int c = 0; c < D / 16; c++) {
-        uint32_t u[16];
-        tmem_ld16(trow + (wg == 0 ? C::kColDK : C::kColDV) + c * 16, u);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; e++) x[c * 16 + e] = __uint_as_float(u[e]);
-      }
-      tc_fence_before();
-      warp_arrive(acc_free);  // the next item's first dV / dK may overwrite the accumulators
-      if (wg == 0) {
-        // dK = scale * (inverse rotation of the accumulated dK^)
-#pragma unroll
-        for (int c = 0; c < D / 8; c++) {
-          float4 c0, c1;
-          rope_coeffs<D>(a.rope, t, c, c0, c1);
-          const float cs[4] = {c0.x, c0.z, c1.x, c1.z}, sn[4] = {c0.y, c0.w, c1.y, c1.w};
-#pragma unroll
-          for (int p = 0; p < 4; p++) {
-            const float x0 = x[c * 8 + 2 * p], x1 = x[c * 8 + 2 * p + 1];
-            x[c * 8 + 2 * p] = a.scale * (x0 * cs[p] + x1 * sn[p]);
-            x[c * 8 + 2 * p + 1] = a.scale * (x1 * cs[p] - x0 * sn[p]);
-          }
-        }
-      }
-      // Coalesced store: each warpgroup stages its 128 rows, 128-byte-wide boxes,
-      // swizzled: the first box in its half of the dS tile, a second (fp32 rows of
-      // D = 64) in this item's K (dK) or V (dV) buffer; one thread then stores
-      // them with TMA (rows past T are not written).  Both are free once the
+      // Staging: the first box goes to this warpgroup's half of the dS tile, the
+      // second to this item's K (warps 4-7) or V (warps 8-11) buffer; one thread
+      // then stores them (rows past T are not written).  Both are free once the
       // item's last dQ has read the dS tile and K (the last S^T and dP^T, which
       // read K and V, completed before acc_done).  The wait for the stores to read
       // them comes at the next item's first dS, which also releases the K/V
       // buffer to the producer.
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (g - 1) & 1, abort)))) break;
-      const CUtensorMap* map = wg == 0 ? &a.map_dk : &a.map_dv;
       uint8_t* stg1 = smem + C::kOffKV + (2 * (tl & 1) + wg) * C::kTileBytes;
-      int nbox;
-      if (wg == 0 && a.rope_half)
-        nbox = a.grad_fp32 ? stage_grad<D, 4, true>(x, atom, stg1, r) : stage_grad<D, 2, true>(x, atom, stg1, r);
-      else
-        nbox = a.grad_fp32 ? stage_grad<D, 4>(x, atom, stg1, r) : stage_grad<D, 2>(x, atom, stg1, r);
-      fence_proxy_async_smem();
-      warp_arrive(stg_full + wg);
-      if (r == 0) {
-        if ((ok = mbar_wait(stg_full + wg, epi & 1, abort))) {
-          const int span = nbox == 2 ? 128 : D * (a.grad_fp32 ? 4 : 2);
-          const int cols = span / (a.grad_fp32 ? 4 : 2);
-          tma_store_4d(map, atom, 0, it.kvh, it.j * kTile, it.b);
-          if (nbox == 2) tma_store_4d(map, stg1, cols, it.kvh, it.j * kTile, it.b);
-          bulk_commit();
+      if constexpr (split) {
+        // dK columns 32 wg .. 32 wg + 31 in x[0 .. 31], the same dV columns in x[32 .. 63]
+        float x[64];
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+          uint32_t u[16];
+          tmem_ld16(trow + (c < 2 ? C::kColDK : C::kColDV) + wg * 32 + (c & 1) * 16, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; e++) x[c * 16 + e] = __uint_as_float(u[e]);
+        }
+        tc_fence_before();
+        warp_arrive(acc_free);  // the next item's first dV / dK may overwrite the accumulators
+        rotate(x, wg * 16, std::integral_constant<int, 16>());
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (g - 1) & 1, abort)))) break;
+        uint8_t* bk = wg == 0 ? atom : stg1;
+        uint8_t* bv = wg == 0 ? stg1 : atom;
+#pragma unroll
+        for (int ch = 0; ch < 8; ch++) {
+          *reinterpret_cast<float4*>(bk + swz(r, ch, 128)) =
+              make_float4(x[4 * ch], x[4 * ch + 1], x[4 * ch + 2], x[4 * ch + 3]);
+          *reinterpret_cast<float4*>(bv + swz(r, ch, 128)) =
+              make_float4(x[32 + 4 * ch], x[33 + 4 * ch], x[34 + 4 * ch], x[35 + 4 * ch]);
+        }
+        fence_proxy_async_smem();
+        warp_arrive(stg_full + wg);
+        if (r == 0) {
+          if ((ok = mbar_wait(stg_full + wg, epi & 1, abort))) {
+            tma_store_4d(&a.map_dk, bk, wg * 32, it.kvh, it.j * kTile, it.b);
+            tma_store_4d(&a.map_dv, bv, wg * 32, it.kvh, it.j * kTile, it.b);
+            bulk_commit();
+          }
+        }
+      } else {
+        float x[D];
+#pragma unroll
+        for (int c = 0; c < D / 16; c++) {
+          uint32_t u[16];
+          tmem_ld16(trow + (wg == 0 ? C::kColDK : C::kColDV) + c * 16, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; e++) x[c * 16 + e] = __uint_as_float(u[e]);
+        }
+        tc_fence_before();
+        warp_arrive(acc_free);
+        if (wg == 0) rotate(x, 0, std::integral_constant<int, D / 2>());
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (g - 1) & 1, abort)))) break;
+        const CUtensorMap* map = wg == 0 ? &a.map_dk : &a.map_dv;
+        int nbox;
+        if (wg == 0 && a.rope_half)
+          nbox = a.grad_fp32 ? stage_grad<D, 4, true>(x, atom, stg1, r) : stage_grad<D, 2, true>(x, atom, stg1, r);
+        else
+          nbox = a.grad_fp32 ? stage_grad<D, 4>(x, atom, stg1, r) : stage_grad<D, 2>(x, atom, stg1, r);
+        fence_proxy_async_smem();
+        warp_arrive(stg_full + wg);
+        if (r == 0) {
+          if ((ok = mbar_wait(stg_full + wg, epi & 1, abort))) {
+            const int span = nbox == 2 ? 128 : D * (a.grad_fp32 ? 4 : 2);
+            const int cols = span / (a.grad_fp32 ? 4 : 2);
+            tma_store_4d(map, atom, 0, it.kvh, it.j * kTile, it.b);
+            if (nbox == 2) tma_store_4d(map, stg1, cols, it.kvh, it.j * kTile, it.b);
+            bulk_commit();
+          }
         }
       }
       epi++;
@@ -1375,27 +1445,31 @@ cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool kSplit>
 cudaError_t launch_dkdv3_t(const BwdArgs& a, cudaStream_t s) {
   using C = Bwd3Cfg<D>;
   static bool attr_set[64] = {};
   int dev = 0, nsm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_bwd_dkdv3<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    cudaError_t e =
+        cudaFuncSetAttribute(k_bwd_dkdv3<D, kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   cudaError_t e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int items = a.nt * a.B * a.Hkv;
-  k_bwd_dkdv3<D><<<items < nsm ? items : nsm, 512, C::kSmemBytes, s>>>(a);
+  k_bwd_dkdv3<D, kSplit><<<items < nsm ? items : nsm, 512, C::kSmemBytes, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, bool precise, cudaStream_t s) {
-  if (a.D == 64) return precise ? launch_dkdv_t<64, true>(a, s) : launch_dkdv3_t<64>(a, s);
-  return precise ? launch_dkdv_t<32, true>(a, s) : launch_dkdv3_t<32>(a, s);
+  if (a.D == 64) {
+    if (precise) return launch_dkdv_t<64, true>(a, s);
+    return a.grad_fp32 && !a.rope_half ? launch_dkdv3_t<64, true>(a, s) : launch_dkdv3_t<64, false>(a, s);
+  }
+  return precise ? launch_dkdv_t<32, true>(a, s) : launch_dkdv3_t<32, false>(a, s);
 }
 
 }  // namespace ne

@@ -739,8 +739,9 @@ __global__ void __launch_bounds__(384, 1) k_bwd_dkdv(const __grid_constant__ Bwd
 // memory (double-buffered across items, so the next item's K and V load
 // while this one runs); P^T gets TMEM columns of its own, so S^T of the next
 // step may overwrite the score columns as soon as the compute warps have read
-// them, and dS^T replaces P^T there once dV has read it, so dP^T of the next
-// step may overwrite its columns as soon as they are read.  The accumulators pass from one item to the next through acc_done
+// them, and dP^T of the next step may overwrite its columns as soon as they
+// are read.  dS goes to shared memory once, where dK reads it K-major and dQ
+// MN-major.  The accumulators pass from one item to the next through acc_done
 // (MMAs complete) and acc_free (the compute warps have read them).
 // Warps: 0 TMA producer; 1-3 MMA issuers; 4-11 P and dS (two warpgroups, half
 // the query columns each), then each item's dK / dV store; 12-15 dQ drain.
@@ -774,7 +775,7 @@ struct Bwd3Cfg {
   static constexpr int kNumBars = 32;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-  // TMEM: S^T | dP^T | P^T (dS^T over it) | dV | dK | dQ
+  // TMEM: S^T | dP^T | P^T | dV | dK | dQ
   static constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDV = 320, kColDK = 320 + D,
                             kColDQ = 320 + 2 * D;
   static constexpr uint32_t kTmemCols = 512;
@@ -850,7 +851,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
   uint64_t* pbuf_free = bars + 13; // dV read P^T
   uint64_t* dp_full = bars + 14;
   uint64_t* ds_ready = bars + 15;
-  uint64_t* ds_free = bars + 16;   // dQ read the dS tile
+  uint64_t* ds_free = bars + 16;   // dK and dQ read the dS tile
   uint64_t* dq_full = bars + 17;
   uint64_t* dq_free = bars + 18;
   uint64_t* acc_done = bars + 19;  // an item's last dV and dK complete
@@ -859,7 +860,6 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
   uint64_t* stg_full = bars + 24;  // [2] per compute warpgroup: its rows of the item's gradient are staged
   uint64_t* stg_free = bars + 26;  // [2] the gradient's TMA stores have read the staging
   uint64_t* dp_read = bars + 28;   // the compute warps hold dP^T(g): dP^T(g+1) may overwrite it
-  uint64_t* dk_done = bars + 29;   // dK(g) read dS^T(g) from the P^T columns
   uint64_t* rot_full = bars + 30;  // rows 16a and b of the rotation table are in shared memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -882,7 +882,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
     mbar_init(pbuf_free, 1);
     mbar_init(dp_full, 1);
     mbar_init(ds_ready, 8);
-    mbar_init(ds_free, 1);
+    mbar_init(ds_free, 2);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 4);
     mbar_init(acc_done, 2);
@@ -893,7 +893,6 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
       mbar_init(stg_free + s, 1);
     }
     mbar_init(dp_read, 8);
-    mbar_init(dk_done, 1);
     mbar_init(rot_full, 1);
     fence_mbar_init();
   }
@@ -972,7 +971,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
       constexpr uint32_t idS = idesc_fp16(128, 128, false, false);   // K^ x Q^ (both K-major)
       constexpr uint32_t idDP = idesc_bf16(128, 128, false, false);  // V x dO (both K-major)
       constexpr uint32_t idDV = idesc_bf16(128, D, false, true);     // P^T (TMEM) x dO MN-major
-      constexpr uint32_t idDK = idesc_fp16(128, D, false, true);     // dS^T (TMEM) x Q^ MN-major
+      constexpr uint32_t idDK = idesc_fp16(128, D, false, true);     // dS^T (K-major) x Q^ MN-major
       constexpr uint32_t idDQ = idesc_fp16(128, D, true, true);      // dS (MN-major) x K^ MN-major
       constexpr int KD = D / 16;                                     // k-steps over the head dimension
       constexpr uint32_t kStepK = 32 >> 4;                           // K-major: next 16 columns
@@ -981,7 +980,8 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
       const uint64_t dQ0 = smem_desc(sQ, 16, C::kSBO, C::kSwz);
       const uint64_t dDO0 = smem_desc(sDO, 16, C::kSBO, C::kSwz);
       const uint64_t dKV0 = smem_desc(sKV, 16, C::kSBO, C::kSwz);
-      const uint64_t dDS = smem_desc(sDS, 16384, 1024, kSw128);
+      const uint64_t dDS = smem_desc(sDS, 16384, 1024, kSw128);   // dS, MN-major (for dQ)
+      const uint64_t dDSk = smem_desc(sDS, 16, 1024, kSw128);     // dS^T, K-major (for dK)
       auto dK = [&](int kb) { return dKV0 + (uint64_t)(2 * kb * kTileStep); };
       auto dV = [&](int kb) { return dKV0 + (uint64_t)((2 * kb + 1) * kTileStep); };
       auto dQs = [&](int st) { return dQ0 + (uint64_t)(st * kTileStep); };
@@ -1058,8 +1058,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
           for (int n = 0; n < it.N; n++, g++) {
             const int st = g % C::kStages;
             const bool last = (n + 1 == it.N);
-            // dP^T(g+1) as soon as the compute warps hold dP^T(g) (dS^T(g) goes to
-            // the P^T columns, so dK(g) does not have to run first)
+            // dP^T(g+1) as soon as the compute warps hold dP^T(g), ahead of dK(g)
             if (!last || bwd_item(a, tl + 1, nx)) {
               const int g1 = g + 1, st1 = g1 % C::kStages, kb1 = last ? (kb ^ 1) : kb;
               if (!(ok = mbar_wait(dp_read, g & 1, abort))) break;
@@ -1072,9 +1071,11 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
             if (!(ok = mbar_wait(ds_ready, g & 1, abort))) break;
             if (n == 0 && tl > 0 && !(ok = mbar_wait(acc_free, (tl - 1) & 1, abort))) break;
             tc_fence_after();
-            // dK += dS^T Q^ (dS^T in the P^T columns, fp16 pairs)
-            mma_ts_chain<8, false>(tmem + C::kColDK, tmem + C::kColP, dQs(st), kStepMN, idDK, n > 0 ? 1u : 0u);
-            mma_commit(dk_done);
+            // dK += dS^T Q^: the dS tile in shared memory read K-major (queries
+            // along K), one chain of four k-steps per 128-byte swizzle atom of 64 queries
+            mma_ss_chain<4>(tmem + C::kColDK, dDSk, kStepK, dQs(st), kStepMN, idDK, n > 0 ? 1u : 0u);
+            mma_ss_chain<4>(tmem + C::kColDK, dDSk + (16384 >> 4), kStepK, dQs(st) + 4 * kStepMN, kStepMN, idDK, 1u);
+            mma_commit(ds_free);
             mma_commit(qd_empty + st);  // this thread's reads of stage st: dO by dP^T, Q^ by dK
             if (last) {
               mma_commit(acc_done);
@@ -1135,28 +1136,35 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
         tc_fence_before();
         warp_arrive(s_read);  // S^T of the next step may overwrite the score columns
         const uint64_t sl2x2 = f2(sl2, sl2);
+        auto exp_pass = [&](auto masked) {
 #pragma unroll
-        for (int v4 = 0; v4 < 16; v4++) {
-          const float4 t4 = reinterpret_cast<const float4*>(lse2)[v4];
+          for (int v4 = 0; v4 < 16; v4++) {
+            const float4 t4 = reinterpret_cast<const float4*>(lse2)[v4];
 #pragma unroll
-          for (int e = 0; e < 2; e++) {
-            const int q = 4 * v4 + 2 * e;
-            float x0, x1;
-            f2_split(f2_fma(f2(pf[q], pf[q + 1]), sl2x2, e == 0 ? f2(t4.x, t4.y) : f2(t4.z, t4.w)), x0, x1);
-            float p0 = ex2(x0), p1 = ex2(x1);
-            if (diag) {
-              if (cbase + q < r) p0 = 0.f;
-              if (cbase + q + 1 < r) p1 = 0.f;
+            for (int e = 0; e < 2; e++) {
+              const int q = 4 * v4 + 2 * e;
+              float x0, x1;
+              f2_split(f2_fma(f2(pf[q], pf[q + 1]), sl2x2, e == 0 ? f2(t4.x, t4.y) : f2(t4.z, t4.w)), x0, x1);
+              float p0 = ex2(x0), p1 = ex2(x1);
+              if constexpr (decltype(masked)::value) {
+                if (cbase + q < r) p0 = 0.f;
+                if (cbase + q + 1 < r) p1 = 0.f;
+              }
+              pf[q] = p0;
+              pf[q + 1] = p1;
             }
-            pf[q] = p0;
-            pf[q + 1] = p1;
           }
-        }
+        };
+        // the causal mask only on the diagonal tile, in a copy of the pass of its own
+        if (diag)
+          exp_pass(std::true_type());
+        else
+          exp_pass(std::false_type());
         uint32_t pk[32];
 #pragma unroll
         for (int q = 0; q < 32; q++) pk[q] = pack_bf16(pf[2 * q], pf[2 * q + 1]);
-        // the P^T columns are free once dK(g-1) has read dS^T(g-1) from them
-        if (g > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(dk_done, (g - 1) & 1, abort)))) break;
+        // the P^T columns are free once dV(g-1) has read P^T(g-1)
+        if (g > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(pbuf_free, (g - 1) & 1, abort)))) break;
         tc_fence_after();
 #pragma unroll
         for (int hlf = 0; hlf < 4; hlf++)
@@ -1180,7 +1188,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
         tc_fence_after();
         // dS = P * (dP - Delta), 16 columns at a time; the next chunk of dP^T loads
         // while this one is computed (its columns are never the ones being stored)
-        uint32_t va[16], vb[16], dst[32];
+        uint32_t va[16], vb[16];
         tmem_ld16(trow + C::kColDP + cbase, va);
         tmem_wait_ld();
 #pragma unroll
@@ -1203,9 +1211,7 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
               w[q >> 1] = pack_f16(d0, d1);
             }
           }
-          // dS into shared memory (for dQ); dS^T kept for the P^T columns (for dK)
-#pragma unroll
-          for (int q = 0; q < 8; q++) dst[c4 * 8 + q] = w[q];
+          // dS into shared memory, where both dK (K-major) and dQ (MN-major) read it
 #pragma unroll
           for (int q = 0; q < 2; q++)
             *reinterpret_cast<uint4*>(atom + r * 128 + (((uint32_t)(2 * c4 + q) ^ x7) << 4)) =
@@ -1216,13 +1222,6 @@ __global__ void __launch_bounds__(512, 1) k_bwd_dkdv3(const __grid_constant__ Bw
             warp_arrive(dp_read);  // dP^T(g+1) may overwrite the dP^T columns
           }
         }
-        // dS^T over P^T once dV(g) has read P^T
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(pbuf_free, g & 1, abort)))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int q = 0; q < 4; q++)
-          tmem_st8(trow + C::kColP + wg * 32 + q * 8, *reinterpret_cast<const uint32_t(*)[8]>(dst + 8 * q));
-        tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         warp_arrive(ds_ready);

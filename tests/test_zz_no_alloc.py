@@ -51,23 +51,34 @@ def _noalloc_bwd(nb, q, k, v, o, lse, do, flags):
 
 
 def _close(a, b):
+    """a within the parity tolerances of the fp32 result b; a bf16 result also
+    carries the half-ulp its own rounding adds (2^-9 of the value)."""
+    half_ulp = 2.0 ** -9 if a.dtype == torch.bfloat16 else 0.0
     a = a.float().cpu().numpy().astype(np.float64)
     b = b.float().cpu().numpy().astype(np.float64)
     rel, mx = H.errors(a, b)
-    assert rel <= H.REL_L2_TOL and mx <= H.MAX_ABS_TOL, (rel, mx)
+    assert rel <= H.REL_L2_TOL, rel
+    assert np.all(np.abs(a - b) <= H.MAX_ABS_TOL + np.abs(b) * half_ulp), mx
 
 
-@pytest.mark.parametrize("shape,precise", [((2, 300, 6, 2, 64), False), ((1, 200, 4, 2, 32), False),
-                                           ((1, 257, 3, 1, 64), True)])
-def test_noalloc_matches_workspace_entry_point(nb, shape, precise):
+@pytest.mark.parametrize("shape,precise,half,fp32", [
+    ((2, 300, 6, 2, 64), False, False, True), ((1, 200, 4, 2, 32), False, False, True),
+    ((1, 257, 3, 1, 64), True, False, True),
+    ((2, 300, 6, 2, 64), False, True, True),     # half-split rotary layout
+    ((2, 300, 6, 2, 64), False, False, False),   # bf16 gradients
+    ((16, 512, 12, 4, 64), False, False, True),  # the 116M model's attention shape
+])
+def test_noalloc_matches_workspace_entry_point(nb, shape, precise, half, fp32):
     B, T, Hq, Hkv, D = shape
-    flags = nb.GRAD_FP32 | ((nb.PRECISE_QK | nb.O_FP32) if precise else 0)
+    flags = ((nb.GRAD_FP32 if fp32 else 0) | ((nb.PRECISE_QK | nb.O_FP32) if precise else 0)
+             | (nb.ROPE_HALF if half else 0))
     outs = []
     for call in range(2):  # two calls in a row: the fixed scratch keeps the previous call's contents
         x = H.make(*shape, seed=100 + call, recipe="stress" if precise else "normal")
         q, k, v, do = (H.to_device(x[n + "_bits"]) for n in ("q", "k", "v", "dout"))
-        o, lse = nb.attn_fwd(q, k, v, o_dtype=torch.float32 if precise else torch.bfloat16, precise=precise)
-        ref = nb.attn_bwd(q, k, v, o, lse, do, grad_dtype=torch.float32, precise=precise)
+        o, lse = nb.attn_fwd(q, k, v, o_dtype=torch.float32 if precise else torch.bfloat16, precise=precise,
+                             rope_half=half)
+        ref = nb.attn_bwd(q, k, v, o, lse, do, grad_dtype=torch.float32, precise=precise, rope_half=half)
         got = _noalloc_bwd(nb, q, k, v, o, lse, do, flags)
         for r, g in zip(ref, got):
             assert torch.isfinite(g).all()

@@ -163,6 +163,17 @@ def test_edge_shapes(nb, oracle_mod, shape):
     compare(oracle_mod, x, gpu, shape, None)
 
 
+@pytest.mark.parametrize("shape", [(1, 4096, 2, 1, 64), (1, 8100, 1, 1, 32)], ids=lambda s: "x".join(map(str, s)))
+def test_long_sequence_default_precision(nb, oracle_mod, shape):
+    """Positions up to 8099 in default precision with normal-sized logits: the
+    dK epilogue composes each position's (cos, sin) from three table rows
+    (128 j, 16 a, b), the far key tiles exercise the large-angle rows, and
+    the forward's and backward's schedules run many items per CTA."""
+    x = H.make(*shape, seed=sum(shape) + 3)
+    gpu = run_gpu(nb, x, qk_rotated=True)
+    compare(oracle_mod, x, gpu, shape, None)
+
+
 @pytest.mark.parametrize("shape", [(1, 77, 4, 2, 64), (2, 1000, 6, 2, 64), (1, 200, 8, 1, 32), (3, 640, 4, 4, 32)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_backward_reuses_forward_rotation(nb, oracle_mod, shape):
